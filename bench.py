@@ -1,0 +1,514 @@
+"""Benchmark of the GatedDeltaNet hot path on GB300.
+
+A step is one gdn_forward over the decode workload: 64 requests x 1 token,
+Hk=16 key heads, Hv=48 value heads, dk=dv=128, fp16 q/k/v/output, raw FP32
+gates, FP32 V-major state [64, 48, 128, 128] updated in place.  The state is
+rotated over 4 pools of 192 MiB so every step streams it from HBM (the
+working set, 768 MiB, is far larger than the 129 MB L2).
+
+One JSON line is printed by rank 0 (see the keys at the end of main()).
+``--impl reference`` times the FP64 CPU oracle on the same workload instead.
+Under torchrun every rank runs its own 64 requests (weak scaling, no
+collective on the data path); the barrier and the max over ranks are the only
+communication.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import re
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN tokens/s and state HBM GB/s (% of roofline) at decode/prefill, 1×GB300"
+WORKLOAD = "decode step: 64 requests x 1 token, Hk=16, Hv=48, dk=dv=128, fp16 I/O, fp32 state [64,48,128,128]"
+NBUF = 4
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--no-extra", action="store_true", help="skip the prefill / verify+replay sub-measurements")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            import torch
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = torch.device("cuda", self.local) if torch.cuda.is_available() else torch.device("cpu")
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = torch.device("cuda", self.local) if torch.cuda.is_available() else torch.device("cpu")
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def shard_seed(base: int, rank: int) -> int:
+    """Each rank draws its own requests (weak scaling)."""
+    return base + 7919 * rank
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid=None):
+        self.proc = None
+        self.path = None
+        exe = shutil.which("nvidia-smi")
+        if not exe:
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = [exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if device_uuid:
+            cmd += ["-i", device_uuid]
+        self.fh = open(self.path, "w")
+        self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, _, fl in rows for n, f in zip(names, fl) if f.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- profiles
+
+def recorded_traffic(kernel_src: str, name: str):
+    """Per-launch DRAM bytes from the committed ncu summary of this kernel, or
+    None when the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not m_b or not m_h:
+        return None
+    if hashlib.sha256(open(kernel_src, "rb").read()).hexdigest() != m_h.group(1):
+        return None
+    return float(m_b.group(1))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def decode_bytes_per_launch(R, Hk, Hv, dk, dv, io_bytes=2):
+    """Algorithmic HBM bytes of one decode launch: the state read and written
+    once, q, k, v, output in the I/O dtype, raw a and b in FP32."""
+    state = 2 * Hv * dv * dk * 4
+    io = 2 * Hk * dk * io_bytes + 2 * Hv * dv * io_bytes + 2 * Hv * 4
+    return R * (state + io)
+
+
+def run_gdn(a, dist: Dist):
+    import torch
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    from gated_delta_rule_gateddeltanet_gb300 import workloads as wl
+
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    lib = gdn.load_library()
+    stream = torch.cuda.current_stream(dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+
+    # ---- inputs: NBUF rotating input sets and in-place state pools
+    sets = []
+    for i in range(NBUF):
+        inp = wl.decode_step(seed=shard_seed(wl.SEEDS["decode_step"] + 100 * i, dist.rank))
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+        d = dict(q=t(inp.q), k=t(inp.k), v=t(inp.v), a=t(inp.a), b=t(inp.b), A_log=t(inp.A_log),
+                 dt_bias=t(inp.dt_bias), cu=t(inp.cu_seqlens), state=t(inp.initial_state),
+                 out=torch.empty((inp.T, 48, 128), dtype=torch.float16, device=dev), inp=inp)
+        args, _, keep = gdn.build_forward_args(d["q"], d["k"], d["v"], d["a"], d["b"], d["cu"], A_log=d["A_log"],
+                                               dt_bias=d["dt_bias"], initial_state=d["state"],
+                                               final_state=d["state"], output=d["out"])
+        d["args"], d["keep"] = args, keep
+        sets.append(d)
+    R = sets[0]["inp"].B
+    Hk, Hv, dk, dv = sets[0]["inp"].dims
+
+    def step(i):
+        rc = lib.gdn_forward(ctypes.byref(sets[i % NBUF]["args"]), sh)
+        if rc:
+            raise gdn.GdnError(rc, "gdn_forward")
+
+    for i in range(a.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(a.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    ms_local = e0.elapsed_time(e1)
+    ms = dist.max(ms_local)
+    ms_per_step = ms / a.steps
+    tokens = dist.sum(R * a.steps)
+    value = tokens / (ms / 1e3)
+
+    hbm_peak, tc_peak, peak_kind = measured_peaks()
+    bytes_launch = decode_bytes_per_launch(R, Hk, Hv, dk, dv)
+    achieved_gbs = bytes_launch / (ms_local / a.steps / 1e3) / 1e9
+    traffic = recorded_traffic(os.path.join(ROOT, "gated_delta_rule_gateddeltanet_gb300", "csrc", "gdn_recurrent.cu"),
+                               "decode_step.recurrent_kernel.ncu.md")
+    roofline = {"bound": "hbm", "kernel": "recurrent_kernel<half,128,2>", "achieved": round(achieved_gbs, 1),
+                "peak": hbm_peak, "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                "unit": "GB/s", "frac": round(achieved_gbs / hbm_peak, 4), "traffic": traffic,
+                "algorithmic_bytes_per_launch": bytes_launch,
+                "launch_us": round(ms_local / a.steps * 1e3, 2)}
+
+    # ---- e2e: host buffers through the public binding
+    e2e = run_e2e(a, dist, sets, dev, stream)
+
+    extra = {}
+    if not a.no_extra and dist.rank == 0:
+        extra["prefill"] = run_prefill(dev, stream)
+        extra["spec_verify_replay"] = run_spec(dev, stream, lib, sh)
+
+    cpu = None
+    if not a.no_cpu and dist.rank == 0 and dist.world == 1:
+        cpu = run_cpu_baseline(sets[0]["inp"])
+
+    if dist.rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": dist.world,
+                "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_per_step, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic (seeded numpy: q,k,v ~ N(0,1) fp16; a,b ~ N(0,1); A_log=log U(1,16); "
+                        "dt_bias=log expm1 U(1e-3,0.1); state ~ N(0,0.02^2))",
+                "config": {"workload": WORKLOAD, "requests_per_gpu": R, "Hk": Hk, "Hv": Hv, "dk": dk, "dv": dv,
+                           "io_dtype": "fp16", "state_dtype": "fp32", "plan": "auto (recurrent for 1-token spans)",
+                           "l2": f"inputs larger than L2: {NBUF} rotating in-place state pools of 192 MiB",
+                           "parallelism": f"dp{dist.world} (independent requests per GPU)"},
+                "state_gbs": round(2 * R * Hv * dv * dk * 4 / (ms_local / a.steps / 1e3) / 1e9, 1),
+                "roofline": roofline, "e2e": e2e, "gpu_launches": a.steps, "clocks": ck,
+                "cpu_baseline": cpu}
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(a, dist, sets, dev, stream):
+    """Same metric through the public Python binding with host buffers: every
+    step copies that step's q, k, v, a, b and cu_seqlens from pinned host memory,
+    runs gdn_forward and reads the output back to pinned host memory.  The state
+    stays resident in HBM (a fixed-state pool)."""
+    import torch
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    host, devb = [], []
+    for d in sets:
+        hs = {n: d[n].cpu().pin_memory() for n in ("q", "k", "v", "a", "b", "cu")}
+        ho = torch.empty(d["out"].shape, dtype=d["out"].dtype).pin_memory()
+        host.append((hs, ho))
+        devb.append({n: torch.empty_like(d[n]) for n in ("q", "k", "v", "a", "b", "cu")})
+    h2d = sum(x.numel() * x.element_size() for x in host[0][0].values())
+    d2h = host[0][1].numel() * host[0][1].element_size()
+    steps = max(10, min(a.steps // 4, 2000))
+
+    def step(i):
+        j = i % NBUF
+        hs, ho = host[j]
+        db = devb[j]
+        for n in hs:
+            db[n].copy_(hs[n], non_blocking=True)
+        d = sets[j]
+        out, _, _ = gdn.gdn_forward(db["q"], db["k"], db["v"], db["a"], db["b"], db["cu"], A_log=d["A_log"],
+                                    dt_bias=d["dt_bias"], initial_state=d["state"], final_state=d["state"],
+                                    output=d["out"])
+        ho.copy_(out, non_blocking=True)
+
+    for i in range(min(a.warmup, 50)):
+        step(i)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms = dist.max(e0.elapsed_time(e1))
+    tokens = dist.sum(sets[0]["inp"].B * steps)
+    return {"value": round(tokens / (ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 4),
+            "path": "python binding gdn_forward -> C ABI, pinned host inputs/outputs, state resident in HBM"}
+
+
+def _flush_l2(buf):
+    buf.add_(1.0)
+
+
+def run_prefill(dev, stream):
+    """Varlen prefill: 8 packed sequences of U[256, 4096] tokens, Hk=16, Hv=48,
+    d=128, fp16, zero initial state; L2 flushed before each call."""
+    import torch
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    from gated_delta_rule_gateddeltanet_gb300 import workloads as wl
+    inp = wl.varlen_prefill()
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    q, k, v, aa, bb = t(inp.q), t(inp.k), t(inp.v), t(inp.a), t(inp.b)
+    A_log, dt_bias, cu = t(inp.A_log), t(inp.dt_bias), t(inp.cu_seqlens)
+    final = torch.zeros((inp.B, 48, 128, 128), dtype=torch.float32, device=dev)
+    out = torch.empty((inp.T, 48, 128), dtype=torch.float16, device=dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MiB
+    plan = "auto"
+    run = lambda: gdn.gdn_forward(q, k, v, aa, bb, cu, A_log=A_log, dt_bias=dt_bias, final_state=final, output=out,
+                                  plan=plan)
+    for _ in range(2):
+        run()
+    iters = 5
+    times = []
+    for _ in range(iters):
+        _flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    T = inp.T
+    return {"workload": "varlen prefill: 8 sequences, lengths U[256,4096] (seeded), Hk=16, Hv=48, d=128, fp16, "
+                        "zero initial state", "tokens": int(T), "lengths": [int(x) for x in np.diff(inp.cu_seqlens)],
+            "plan": plan, "ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "l2": "flushed (256 MiB write)"}
+
+
+def run_spec(dev, stream, lib, sh):
+    """Speculative verify (16 x 4 tokens with capsules) then replay of the
+    accepted prefixes into the inactive bank; 4 rotating state pools."""
+    import torch
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    from gated_delta_rule_gateddeltanet_gb300 import workloads as wl
+    pools, fargs, rargs = [], [], []
+    for i in range(NBUF):
+        inp = wl.spec_verify(seed=wl.SEEDS["spec_verify"] + 100 * i)
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+        pool = t(inp.initial_state)
+        caps = torch.zeros((16, 4, gdn.capsule_width(16, 48, 128, 128)), dtype=torch.float32, device=dev)
+        scratch = torch.empty_like(pool[:16])
+        d = dict(q=t(inp.q), k=t(inp.k), v=t(inp.v), a=t(inp.a), b=t(inp.b), A_log=t(inp.A_log),
+                 dt_bias=t(inp.dt_bias), cu=t(inp.cu_seqlens), slots=t(inp.state_slots),
+                 out=torch.empty((inp.T, 48, 128), dtype=torch.float16, device=dev), pool=pool, caps=caps,
+                 src=t(inp.extra["src_slots"]), dst=t(inp.extra["dst_slots"]), n=t(inp.extra["accept_len"]),
+                 scratch=scratch)
+        # verify writes the speculative final state to a scratch pool (slots 0..15 of `scratch`)
+        args, _, keep = gdn.build_forward_args(d["q"], d["k"], d["v"], d["a"], d["b"], d["cu"], A_log=d["A_log"],
+                                               dt_bias=d["dt_bias"], initial_state=pool, final_state=scratch,
+                                               state_slots=None, output=d["out"], state_update=caps, capacity=4,
+                                               num_state_slots=16)
+        d["args"], d["keep"], d["acc"] = args, keep, int(inp.extra["accept_len"].sum())
+        pools.append(d)
+
+    def verify(i):
+        rc = lib.gdn_forward(ctypes.byref(pools[i % NBUF]["args"]), sh)
+        if rc:
+            raise gdn.GdnError(rc, "gdn_forward")
+
+    def replay(i):
+        d = pools[i % NBUF]
+        rc = lib.gdn_replay_prefix(ctypes.c_void_p(d["pool"].data_ptr()), 32, 16, 16, 48, 128, 128,
+                                   ctypes.c_void_p(d["src"].data_ptr()), ctypes.c_void_p(d["dst"].data_ptr()),
+                                   ctypes.c_void_p(d["caps"].data_ptr()), 4, ctypes.c_void_p(d["n"].data_ptr()),
+                                   None, sh)
+        if rc:
+            raise gdn.GdnError(rc, "gdn_replay_prefix")
+
+    res = {}
+    for name, fn in (("verify", verify), ("replay", replay)):
+        for i in range(20):
+            fn(i)
+        torch.cuda.synchronize()
+        n = 400
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) / n
+    hbm_peak, _, kind = measured_peaks()
+    state_bytes = 2 * 16 * 48 * 128 * 128 * 4
+    cap_bytes = gdn.capsule_width(16, 48, 128, 128) * 4
+    rep_bytes = state_bytes + statistics.mean(d["acc"] for d in pools) * cap_bytes
+    ver_bytes = state_bytes + 64 * (33152 + cap_bytes)
+    return {"workload": "spec verify + replay: 16 requests x 4 draft tokens, Hk=16, Hv=48, d=128, fp16, "
+                        "capsules for all tokens, replay of U{0..4} accepted into the inactive bank",
+            "verify_us": round(res["verify"] * 1e3, 2), "replay_us": round(res["replay"] * 1e3, 2),
+            "verify_tokens_per_s": round(64 / (res["verify"] / 1e3), 1),
+            "replay_gbs": round(rep_bytes / (res["replay"] / 1e3) / 1e9, 1),
+            "replay_frac_hbm": round(rep_bytes / (res["replay"] / 1e3) / 1e9 / hbm_peak, 4),
+            "verify_gbs": round(ver_bytes / (res["verify"] / 1e3) / 1e9, 1),
+            "l2": f"{NBUF} rotating state pools of 96 MiB"}
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline and reference arm)
+
+def oracle_decode_sample(inp, requests):
+    """The first ``requests`` requests of a decode step, as oracle inputs."""
+    cu = inp.cu_seqlens[:requests + 1]
+    T = int(cu[-1])
+    return dict(q=inp.q[:T], k=inp.k[:T], v=inp.v[:T], a=inp.a[:T], b=inp.b[:T], cu=cu,
+                state=inp.initial_state[:requests], A_log=inp.A_log, dt_bias=inp.dt_bias)
+
+
+def time_oracle_step(s):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.gdn_forward(s["q"], s["k"], s["v"], s["a"], s["b"], s["cu"], A_log=s["A_log"], dt_bias=s["dt_bias"],
+                       initial_state=s["state"])
+    return time.perf_counter() - t0
+
+
+def run_cpu_baseline(inp, budget_s=12.0):
+    import oracle
+    oracle.build()
+    full = oracle_decode_sample(inp, inp.B)
+    t1 = time_oracle_step(full)
+    reps = max(1, int(budget_s / max(t1, 1e-3)))
+    total, n = 0.0, 0
+    for _ in range(reps):
+        total += time_oracle_step(full)
+        n += 1
+    return {"value": round(n * inp.B / total, 2), "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{n} full decode steps (64 requests x 1 token, all 48 heads) in {total:.1f} s, FP64 C oracle "
+                      f"with OpenMP over (request, head) chains"}
+
+
+def run_reference(a, dist: Dist):
+    if dist.rank != 0:
+        return
+    import oracle
+    from gated_delta_rule_gateddeltanet_gb300 import workloads as wl
+    oracle.build()
+    inp = wl.decode_step()
+    full = oracle_decode_sample(inp, inp.B)
+    t_full = time_oracle_step(full)
+    budget = 150.0
+    per_step = budget / max(1, a.steps + a.warmup)
+    req = int(max(1, min(inp.B, math.floor(inp.B * per_step / max(t_full, 1e-6)))))
+    s = oracle_decode_sample(inp, req)
+    for _ in range(a.warmup):
+        time_oracle_step(s)
+    t = sum(time_oracle_step(s) for _ in range(a.steps))
+    value = req * a.steps / t
+    sample = (f"each step: the first {req} of the 64 requests of the decode step (1 token each, all 48 heads), "
+              f"FP64 C oracle, OpenMP over (request, head) chains")
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": a.gpus, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": round(t / a.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "requests_per_step_sampled": req},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": oracle.threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    a = parse()
+    dist = Dist()
+    try:
+        if a.impl == "reference":
+            run_reference(a, dist)
+        else:
+            run_gdn(a, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

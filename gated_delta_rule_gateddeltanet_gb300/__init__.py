@@ -1,0 +1,244 @@
+"""GB300 GatedDeltaNet: Python binding of the libgdn.so C ABI.
+
+This module only marshals arguments: it checks tensor dtypes and devices,
+allocates outputs that the caller did not pass (with torch, on the tensors'
+device), fills the ``gdn_forward_args`` struct of ``include/gdn.h`` and calls
+the library on the current torch stream.  Every step of the computation runs
+in the library's CUDA kernels.  There is no CPU fallback: if ``libgdn.so`` is
+missing or cannot be loaded, importing the entry points raises.
+
+Entry points (same names as the C ABI):
+    gdn_forward(...)        -> (output, final_state, state_update)
+    gdn_replay_prefix(...)  -> state_banks (updated in place)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB as LIB_PATH
+
+__all__ = ["gdn_forward", "gdn_replay_prefix", "GdnError", "load_library", "capsule_width",
+           "STATUS", "DEVERR", "PLAN"]
+
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_DTYPE", 3: "GDN_ERR_SHAPE", 4: "GDN_ERR_ALIGN",
+          5: "GDN_ERR_WORKSPACE", 6: "GDN_ERR_CUDA", 7: "GDN_ERR_UNSUPPORTED", 8: "GDN_ERR_ARG"}
+DEVERR = {"cu_seqlens": 0x1, "state_slot": 0x2, "accept_len": 0x4, "replay_slot": 0x8}
+PLAN = {"auto": 0, "recurrent": 1, "chunked": 2}
+DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+GATE_MODE = {"raw": 0, "precomputed": 1}
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class ForwardArgs(ctypes.Structure):
+    """Mirror of ``gdn_forward_args`` (include/gdn.h)."""
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32), ("num_k_heads", ctypes.c_int32),
+        ("num_v_heads", ctypes.c_int32), ("head_dim_k", ctypes.c_int32), ("head_dim_v", ctypes.c_int32),
+        ("num_state_slots", ctypes.c_int32), ("io_dtype", ctypes.c_int32), ("gate_mode", ctypes.c_int32),
+        ("plan", ctypes.c_int32), ("scale", ctypes.c_float), ("state_update_capacity", ctypes.c_int32),
+        ("q_stride", ctypes.c_int64), ("k_stride", ctypes.c_int64), ("v_stride", ctypes.c_int64),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("cu_seqlens", ctypes.c_void_p), ("state_slots", ctypes.c_void_p),
+        ("initial_state", ctypes.c_void_p), ("final_state", ctypes.c_void_p), ("output", ctypes.c_void_p),
+        ("state_update", ctypes.c_void_p), ("status", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load libgdn.so (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"libgdn.so is not built ({p}); run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(p)
+    P, i32 = ctypes.c_void_p, ctypes.c_int32
+    lib.gdn_forward.restype = i32
+    lib.gdn_forward.argtypes = [ctypes.POINTER(ForwardArgs), P]
+    lib.gdn_forward_workspace_size.restype = i32
+    lib.gdn_forward_workspace_size.argtypes = [ctypes.POINTER(ForwardArgs), ctypes.POINTER(ctypes.c_size_t)]
+    lib.gdn_replay_prefix.restype = i32
+    lib.gdn_replay_prefix.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P, P, i32, P, P, P]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_status_string.argtypes = [i32]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def capsule_width(num_k_heads: int, num_v_heads: int, head_dim_k: int, head_dim_v: int) -> int:
+    """Floats per capsule row: decay per value head, unit key per key head, delta per value head."""
+    return num_v_heads + num_k_heads * head_dim_k + num_v_heads * head_dim_v
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(t, name, dtype=None, device=None, contiguous=True):
+    if t is None:
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _token_stride(t, name, inner):
+    """Elements between consecutive tokens of a [T, H, d] view whose inner two
+    dims are contiguous (allows slices of a fused qkv projection)."""
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be [T, H, d]")
+    if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError(f"{name}: heads and channels must be contiguous inside a token")
+    return t.stride(0) if t.shape[0] > 1 else inner
+
+
+def build_forward_args(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, gate_mode="raw",
+                       initial_state=None, final_state=None, state_slots=None, output=None,
+                       state_update=None, capacity=0, scale=0.0, plan="auto", status=None,
+                       num_state_slots=None, workspace=None):
+    """Fill a ForwardArgs struct from tensors; returns (args, outputs, keepalive)."""
+    dev = q.device
+    T, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    B = cu_seqlens.shape[0] - 1
+    if q.dtype not in DTYPE:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    for name, t in (("k", k), ("v", v)):
+        _check(t, name, dtype=q.dtype, device=dev, contiguous=False)
+    for name, t in (("a", a), ("b", b), ("A_log", A_log), ("dt_bias", dt_bias)):
+        _check(t, name, dtype=torch.float32, device=dev)
+    _check(cu_seqlens, "cu_seqlens", dtype=torch.int32, device=dev)
+    _check(state_slots, "state_slots", dtype=torch.int32, device=dev)
+    _check(status, "status", dtype=torch.int32, device=dev)
+    if num_state_slots is None:
+        if initial_state is not None:
+            num_state_slots = initial_state.shape[0]
+        elif final_state is not None:
+            num_state_slots = final_state.shape[0]
+        else:
+            num_state_slots = B
+    if final_state is None:
+        final_state = (torch.empty if initial_state is not None else torch.zeros)(
+            (num_state_slots, Hv, dv, dk), dtype=torch.float32, device=dev)
+        if initial_state is not None:
+            final_state.copy_(initial_state)
+    _check(initial_state, "initial_state", dtype=torch.float32, device=dev)
+    _check(final_state, "final_state", dtype=torch.float32, device=dev)
+    if output is None:
+        output = torch.empty((T, Hv, dv), dtype=q.dtype, device=dev)
+    _check(output, "output", dtype=q.dtype, device=dev)
+    W = capsule_width(Hk, Hv, dk, dv)
+    if capacity > 0 and state_update is None:
+        state_update = torch.zeros((B, capacity, W), dtype=torch.float32, device=dev)
+    _check(state_update, "state_update", dtype=torch.float32, device=dev)
+
+    args = ForwardArgs()
+    args.num_seqs, args.total_tokens, args.num_k_heads, args.num_v_heads = B, T, Hk, Hv
+    args.head_dim_k, args.head_dim_v, args.num_state_slots = dk, dv, int(num_state_slots)
+    args.io_dtype = DTYPE[q.dtype]
+    args.gate_mode = GATE_MODE[gate_mode]
+    args.plan = PLAN[plan]
+    args.scale = float(scale or 0.0)
+    args.state_update_capacity = int(capacity)
+    args.q_stride = _token_stride(q, "q", Hk * dk)
+    args.k_stride = _token_stride(k, "k", Hk * dk)
+    args.v_stride = _token_stride(v, "v", Hv * dv)
+    args.q, args.k, args.v = _ptr(q), _ptr(k), _ptr(v)
+    args.a, args.b = _ptr(a), _ptr(b)
+    args.A_log, args.dt_bias = _ptr(A_log), _ptr(dt_bias)
+    args.cu_seqlens, args.state_slots = _ptr(cu_seqlens), _ptr(state_slots)
+    # final_state was seeded from initial_state above when the caller passed no output buffer
+    args.initial_state = _ptr(initial_state)
+    args.final_state = _ptr(final_state)
+    args.output = _ptr(output)
+    args.state_update = _ptr(state_update) if capacity > 0 else None
+    args.status = _ptr(status)
+    if workspace is not None:
+        args.workspace, args.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    keep = (q, k, v, a, b, A_log, dt_bias, cu_seqlens, state_slots, initial_state, status, workspace)
+    return args, (output, final_state, state_update), keep
+
+
+def workspace_size(args: ForwardArgs) -> int:
+    n = ctypes.c_size_t(0)
+    rc = load_library().gdn_forward_workspace_size(ctypes.byref(args), ctypes.byref(n))
+    if rc != 0:
+        raise GdnError(rc, "gdn_forward_workspace_size")
+    return int(n.value)
+
+
+def gdn_forward(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, gate_mode="raw",
+                initial_state=None, final_state=None, state_slots=None, output=None,
+                state_update=None, capacity=0, scale=0.0, plan="auto", status=None,
+                num_state_slots=None, workspace=None):
+    """Gated delta rule over a packed varlen batch (C ABI ``gdn_forward``).
+
+    q, k: [T, Hk, dk] fp16/fp32 CUDA; v: [T, Hv, dv]; a, b: [T, Hv] fp32 (raw
+    gate inputs, or g and beta with ``gate_mode="precomputed"``); A_log, dt_bias:
+    [Hv] fp32; cu_seqlens: [B+1] int32.  ``initial_state`` [slots, Hv, dv, dk]
+    fp32 or None (zeros); ``final_state`` may be the same tensor (in place).
+    Returns ``(output, final_state, state_update)``; state_update is
+    [B, capacity, W] fp32 or None.
+    """
+    lib = load_library()
+    args, outs, keep = build_forward_args(q, k, v, a, b, cu_seqlens, A_log=A_log, dt_bias=dt_bias,
+                                          gate_mode=gate_mode, initial_state=initial_state,
+                                          final_state=final_state, state_slots=state_slots, output=output,
+                                          state_update=state_update, capacity=capacity, scale=scale, plan=plan,
+                                          status=status, num_state_slots=num_state_slots, workspace=workspace)
+    need = workspace_size(args)
+    if need > 0 and workspace is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+        args.workspace, args.workspace_bytes = ctypes.c_void_p(ws.data_ptr()), need
+        keep = keep + (ws,)
+    rc = lib.gdn_forward(ctypes.byref(args), _stream_handle(q.device))
+    if rc != 0:
+        raise GdnError(rc, "gdn_forward")
+    return outs
+
+
+def gdn_replay_prefix(state_banks, src_slots, dst_slots, state_update, accept_len, *, num_k_heads,
+                      status=None):
+    """Replay an accepted capsule prefix into the destination banks, in place
+    (C ABI ``gdn_replay_prefix``).  state_banks: [slots, Hv, dv, dk] fp32;
+    state_update: [R, capacity, W] fp32; src/dst/accept_len: [R] int32."""
+    lib = load_library()
+    S, Hv, dv, dk = state_banks.shape
+    R = src_slots.shape[0]
+    cap = state_update.shape[1] if state_update is not None else 0
+    dev = state_banks.device
+    _check(state_banks, "state_banks", dtype=torch.float32, device=dev)
+    for name, t in (("src_slots", src_slots), ("dst_slots", dst_slots), ("accept_len", accept_len),
+                    ("status", status)):
+        _check(t, name, dtype=torch.int32, device=dev)
+    _check(state_update, "state_update", dtype=torch.float32, device=dev)
+    if state_update is not None and state_update.shape[2] != capsule_width(num_k_heads, Hv, dk, dv):
+        raise ValueError("state_update row width does not match the state geometry")
+    rc = lib.gdn_replay_prefix(_ptr(state_banks), S, R, int(num_k_heads), Hv, dk, dv, _ptr(src_slots),
+                               _ptr(dst_slots), _ptr(state_update), cap, _ptr(accept_len), _ptr(status),
+                               _stream_handle(dev))
+    if rc != 0:
+        raise GdnError(rc, "gdn_replay_prefix")
+    return state_banks

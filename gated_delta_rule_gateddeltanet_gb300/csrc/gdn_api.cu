@@ -1,0 +1,153 @@
+// The C ABI of libgdn.so: argument checks, planning and kernel dispatch.
+//
+// Argument rules follow the validation list of "Add GatedDeltaNet evaluation
+// export for Qwen hybrid models" (Dependency: scalar-per-head dt_bias, forced
+// plans, supported dtypes, update-rule inputs, state alias) and the dtype
+// contract of the same page (What changed: FP16 and FP32 I/O, BF16 rejected,
+// FP32 gates and state).  Everything that the host can check is checked
+// here, before any launch; data-dependent checks happen in the kernels.
+#include <math.h>
+#include <stdint.h>
+
+#include "gdn_internal.cuh"
+
+namespace {
+
+bool valid_head_dim(int d) { return d == 32 || d == 64 || d == 128; }
+
+bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// Host-side checks shared by gdn_forward and gdn_forward_workspace_size.
+gdn_status check_sizes(const gdn_forward_args *a) {
+    if (!a) return GDN_ERR_NULL;
+    if (a->io_dtype == GDN_BF16) return GDN_ERR_DTYPE;
+    if (a->io_dtype != GDN_F32 && a->io_dtype != GDN_F16) return GDN_ERR_DTYPE;
+    if (a->gate_mode != GDN_GATES_RAW && a->gate_mode != GDN_GATES_PRECOMPUTED) return GDN_ERR_ARG;
+    if (a->plan != GDN_PLAN_AUTO && a->plan != GDN_PLAN_RECURRENT && a->plan != GDN_PLAN_CHUNKED)
+        return GDN_ERR_ARG;
+    if (a->num_seqs < 0 || a->num_seqs > 65535 || a->total_tokens < 0) return GDN_ERR_SHAPE;
+    if (a->num_k_heads <= 0 || a->num_v_heads <= 0 || a->num_v_heads % a->num_k_heads != 0)
+        return GDN_ERR_SHAPE;
+    if (!valid_head_dim(a->head_dim_k) || !valid_head_dim(a->head_dim_v)) return GDN_ERR_SHAPE;
+    if (a->state_update_capacity < 0) return GDN_ERR_SHAPE;
+    if (a->num_seqs > 0 && a->num_state_slots < 1) return GDN_ERR_SHAPE;
+    if (a->num_seqs > 0 && !a->state_slots && a->num_state_slots < a->num_seqs) return GDN_ERR_SHAPE;
+    const int64_t qk_min = (int64_t)a->num_k_heads * a->head_dim_k;
+    const int64_t v_min = (int64_t)a->num_v_heads * a->head_dim_v;
+    if ((a->q_stride != 0 && a->q_stride < qk_min) || (a->k_stride != 0 && a->k_stride < qk_min) ||
+        (a->v_stride != 0 && a->v_stride < v_min))
+        return GDN_ERR_SHAPE;
+    if (!(a->scale >= 0.f) || isinf(a->scale)) return GDN_ERR_SHAPE;
+    if (a->plan == GDN_PLAN_CHUNKED) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_status_string(gdn_status status) {
+    switch (status) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_NULL: return "a required pointer is NULL";
+        case GDN_ERR_DTYPE: return "unsupported I/O dtype (FP16 and FP32 only; BF16 is rejected)";
+        case GDN_ERR_SHAPE: return "inconsistent or unsupported sizes";
+        case GDN_ERR_ALIGN: return "a state pointer is not 16-byte aligned";
+        case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+        case GDN_ERR_CUDA: return "CUDA launch error";
+        case GDN_ERR_UNSUPPORTED: return "the forced plan does not support these sizes";
+        case GDN_ERR_ARG: return "unknown enum value in the arguments";
+    }
+    return "unknown status";
+}
+
+gdn_status gdn_forward_workspace_size(const gdn_forward_args *args, size_t *bytes) {
+    if (!bytes) return GDN_ERR_NULL;
+    const gdn_status st = check_sizes(args);
+    if (st != GDN_OK) return st;
+    *bytes = 0;
+    return GDN_OK;
+}
+
+gdn_status gdn_forward(const gdn_forward_args *a, gdn_stream_t stream) {
+    const gdn_status st = check_sizes(a);
+    if (st != GDN_OK) return st;
+    if (a->num_seqs == 0) return GDN_OK;
+    if (!a->cu_seqlens || !a->final_state) return GDN_ERR_NULL;
+    if (a->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->a || !a->b || !a->output)) return GDN_ERR_NULL;
+    if (a->gate_mode == GDN_GATES_RAW && (!a->A_log || !a->dt_bias)) return GDN_ERR_NULL;
+    if (a->state_update_capacity > 0 && !a->state_update) return GDN_ERR_NULL;
+    if (!aligned16(a->final_state) || (a->initial_state && !aligned16(a->initial_state))) return GDN_ERR_ALIGN;
+
+    gdn::ForwardParams p{};
+    p.B = a->num_seqs;
+    p.T = a->total_tokens;
+    p.Hk = a->num_k_heads;
+    p.Hv = a->num_v_heads;
+    p.dk = a->head_dim_k;
+    p.dv = a->head_dim_v;
+    p.r = p.Hv / p.Hk;
+    p.num_slots = a->num_state_slots;
+    p.io_f16 = a->io_dtype == GDN_F16;
+    p.gate_raw = a->gate_mode == GDN_GATES_RAW;
+    p.scale = a->scale > 0.f ? a->scale : 1.0f / sqrtf((float)p.dk);
+    p.cap = a->state_update_capacity;
+    p.W = (long long)p.Hv + (long long)p.Hk * p.dk + (long long)p.Hv * p.dv;
+    p.q_stride = a->q_stride ? a->q_stride : (long long)p.Hk * p.dk;
+    p.k_stride = a->k_stride ? a->k_stride : (long long)p.Hk * p.dk;
+    p.v_stride = a->v_stride ? a->v_stride : (long long)p.Hv * p.dv;
+    p.q = a->q;
+    p.k = a->k;
+    p.v = a->v;
+    p.a = a->a;
+    p.b = a->b;
+    p.A_log = a->A_log;
+    p.dt_bias = a->dt_bias;
+    p.cu = a->cu_seqlens;
+    p.slots = a->state_slots;
+    p.init = a->initial_state;
+    p.final_state = a->final_state;
+    p.out = a->output;
+    p.caps = p.cap > 0 ? a->state_update : nullptr;
+    p.status = a->status;
+    p.max_len = 0x7fffffff;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (gdn::launch_recurrent(p, s) != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+gdn_status gdn_replay_prefix(float *state_banks, int32_t num_slots, int32_t num_requests, int32_t num_k_heads,
+                             int32_t num_v_heads, int32_t head_dim_k, int32_t head_dim_v,
+                             const int32_t *src_slots, const int32_t *dst_slots, const float *state_update,
+                             int32_t capacity, const int32_t *accept_len, int32_t *status,
+                             gdn_stream_t stream) {
+    if (num_requests < 0 || num_requests > 65535 || capacity < 0) return GDN_ERR_SHAPE;
+    if (num_k_heads <= 0 || num_v_heads <= 0 || num_v_heads % num_k_heads != 0) return GDN_ERR_SHAPE;
+    if (!valid_head_dim(head_dim_k) || !valid_head_dim(head_dim_v)) return GDN_ERR_SHAPE;
+    if (num_requests == 0) return GDN_OK;
+    if (num_slots < 1) return GDN_ERR_SHAPE;
+    if (!state_banks || !src_slots || !dst_slots || !accept_len) return GDN_ERR_NULL;
+    if (capacity > 0 && !state_update) return GDN_ERR_NULL;
+    if (!aligned16(state_banks)) return GDN_ERR_ALIGN;
+    gdn::ReplayParams p{};
+    p.R = num_requests;
+    p.Hk = num_k_heads;
+    p.Hv = num_v_heads;
+    p.dk = head_dim_k;
+    p.dv = head_dim_v;
+    p.r = num_v_heads / num_k_heads;
+    p.num_slots = num_slots;
+    p.cap = capacity;
+    p.W = (long long)p.Hv + (long long)p.Hk * p.dk + (long long)p.Hv * p.dv;
+    p.banks = state_banks;
+    p.src = src_slots;
+    p.dst = dst_slots;
+    p.n = accept_len;
+    p.caps = state_update;
+    p.status = status;
+    if (gdn::launch_replay(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+}  // extern "C"

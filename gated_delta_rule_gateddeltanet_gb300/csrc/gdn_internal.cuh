@@ -1,0 +1,83 @@
+// Internal launch interface of libgdn.so (not part of the C ABI).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// Everything a forward kernel needs, resolved on the host from gdn_forward_args.
+struct ForwardParams {
+    int B, T, Hk, Hv, dk, dv, r, num_slots;
+    int io_f16;        // 1: q, k, v, output are FP16; 0: FP32
+    int gate_raw;      // 1: raw gate inputs; 0: precomputed g, beta
+    float scale;
+    int cap;           // capsule rows per sequence (0: none)
+    long long W;       // capsule row width in floats
+    long long q_stride, k_stride, v_stride;  // elements between tokens
+    const void *q, *k, *v;
+    const float *a, *b, *A_log, *dt_bias;
+    const int32_t *cu, *slots;
+    const float *init;
+    float *final_state;
+    void *out;
+    float *caps;
+    int32_t *status;
+    // Sequences with more tokens than this are left to the chunked kernel.
+    int max_len;
+};
+
+struct ReplayParams {
+    int R, Hk, Hv, dk, dv, r, num_slots, cap;
+    long long W;
+    float *banks;
+    const int32_t *src, *dst, *n;
+    const float *caps;
+    int32_t *status;
+};
+
+cudaError_t launch_recurrent(const ForwardParams &p, cudaStream_t stream);
+cudaError_t launch_replay(const ReplayParams &p, cudaStream_t stream);
+
+// ---------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+
+__device__ __forceinline__ void flag_error(int32_t *status, int bit) {
+    if (status) atomicOr(status, bit);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// softplus(x) = log(1 + e^x), evaluated without overflow.
+__device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
+
+// Effective decay and beta of one (token, value head).
+__device__ __forceinline__ void gates(const ForwardParams &p, long long t, int h, float &g, float &beta) {
+    const float av = p.a[t * p.Hv + h];
+    const float bv = p.b[t * p.Hv + h];
+    if (p.gate_raw) {
+        g = expf(-expf(p.A_log[h]) * softplus_f(av + p.dt_bias[h]));
+        beta = 1.f / (1.f + expf(-bv));
+    } else {
+        g = av;
+        beta = bv;
+    }
+}
+
+}  // namespace gdn

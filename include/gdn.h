@@ -1,0 +1,196 @@
+/*
+ * gdn.h -- C ABI of libgdn.so, a GB300 (sm_103a) implementation of the
+ * GatedDeltaNet (gated delta rule) recurrence used by the linear-attention
+ * layers of Qwen hybrid models.
+ *
+ * Every entry point takes plain pointers and sizes.  Pointers documented as
+ * "device" must be CUDA device (or managed) memory of the current device.
+ * The caller owns every buffer: the library never allocates, frees or
+ * synchronises, and launches its kernels on the stream it is given, in
+ * stream order.  It keeps no state between calls and may be called from
+ * several host threads at once.
+ *
+ * Errors come in two kinds.
+ *  - Argument errors that the host can see (NULL pointers, bad sizes, BF16,
+ *    misalignment) return a non-zero gdn_status before anything is launched.
+ *  - Errors that depend on device data (the packing in cu_seqlens, a state
+ *    slot out of range, an accepted length out of range) cannot be seen by the
+ *    host without a synchronisation.  The kernels skip the affected unit of
+ *    work (a sequence or a request) and OR a GDN_DEVERR_* bit into the
+ *    optional device word `status`; they never trap.  The caller zeroes that
+ *    word and reads it when it chooses.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (the same type as cudaStream_t); NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_NULL = 1,        /* a required pointer is NULL */
+    GDN_ERR_DTYPE = 2,       /* unsupported I/O dtype; BF16 is always rejected */
+    GDN_ERR_SHAPE = 3,       /* inconsistent or unsupported sizes */
+    GDN_ERR_ALIGN = 4,       /* a state pointer is not 16-byte aligned */
+    GDN_ERR_WORKSPACE = 5,   /* workspace missing or smaller than gdn_forward_workspace_size */
+    GDN_ERR_CUDA = 6,        /* the CUDA runtime reported an error at launch */
+    GDN_ERR_UNSUPPORTED = 7, /* a forced plan that these sizes do not support */
+    GDN_ERR_ARG = 8          /* an enum field holds an unknown value */
+} gdn_status;
+
+/* I/O dtypes of q, k, v and output.  Gates and states are always FP32. */
+enum { GDN_F32 = 0, GDN_F16 = 1, GDN_BF16 = 2 /* rejected */ };
+
+/* How the `a` and `b` inputs are read. */
+enum {
+    GDN_GATES_RAW = 0,         /* raw a, b: g = exp(-exp(A_log) softplus(a + dt_bias)), beta = sigmoid(b) */
+    GDN_GATES_PRECOMPUTED = 1  /* a = effective decay g in [0, 1], b = beta (activation "none") */
+};
+
+/* Which kernel evaluates a sequence. */
+enum {
+    GDN_PLAN_AUTO = 0,       /* per sequence: short spans recurrent, long spans chunked */
+    GDN_PLAN_RECURRENT = 1,  /* every sequence on the token-by-token kernel */
+    GDN_PLAN_CHUNKED = 2     /* every sequence on the tensor-core chunked kernel */
+};
+
+/* Bits of the device status word. */
+#define GDN_DEVERR_CU_SEQLENS 0x1  /* cu_seqlens not 0 = cu[0] <= ... <= cu[B] = T */
+#define GDN_DEVERR_STATE_SLOT 0x2  /* state_slots[b] outside [0, num_state_slots) */
+#define GDN_DEVERR_ACCEPT_LEN 0x4  /* accept_len[j] outside [0, capacity] */
+#define GDN_DEVERR_REPLAY_SLOT 0x8 /* a replay source or destination slot out of range */
+
+/*
+ * Arguments of gdn_forward.
+ *
+ * Source: "[CUDA] Add compact GatedDeltaNet operator" (Description) defines
+ * the operator: packed ragged inputs, fused gate normalisation, native gate
+ * arithmetic from raw A_log, and three outputs [output, final_state,
+ * state_update], where the FP32 state_update capsule packs the decay, the
+ * shared key and the delta of each token.  "Add GatedDeltaNet evaluation
+ * export for Qwen hybrid models" (What changed, Dependency) fixes packed THD
+ * Q/K/V with cumulative sequence lengths, the FP32 V-major state, the
+ * precomputed-gate mode, scalar-per-head dt_bias, FP16/FP32 I/O with BF16
+ * rejected, and an aliased (in-place) state.
+ *
+ * Per token t of sequence b and value head h (key head kh = h / (Hv / Hk)):
+ *   qn = q / max(|q|, 1e-6), kn = k / max(|k|, 1e-6)
+ *   S <- g S;  u = beta (v - S kn);  S <- S + u kn^T;  o = scale S qn
+ * with S the dv x dk FP32 state (row i belongs to value channel i).
+ *
+ * Layouts (T = total_tokens, B = num_seqs, row-major, innermost last):
+ *   q, k          [T, Hk, dk] io_dtype; token stride q_stride / k_stride
+ *                 elements (0 = Hk*dk), heads contiguous inside a token
+ *   v             [T, Hv, dv] io_dtype; token stride v_stride (0 = Hv*dv)
+ *   a, b          [T, Hv] FP32, contiguous
+ *   A_log, dt_bias [Hv] FP32 (RAW mode only; may be NULL in PRECOMPUTED mode)
+ *   cu_seqlens    device [B+1] int32: sequence b owns tokens [cu[b], cu[b+1])
+ *   state_slots   device [B] int32, or NULL for slot b = b
+ *   initial_state device [num_state_slots, Hv, dv, dk] FP32, or NULL for zeros
+ *   final_state   device, same shape; may equal initial_state (in place).
+ *                 Only the slots named by the batch are written.
+ *   output        device [T, Hv, dv] io_dtype, contiguous
+ *   state_update  device [B, capacity, W] FP32 with W = Hv + Hk*dk + Hv*dv, or
+ *                 NULL when capacity = 0.  Row (b, i) describes token i of
+ *                 sequence b for i < min(len_b, capacity):
+ *                 [g for each value head | kn for each key head | u for each
+ *                 value head (dv floats each)].  Rows past the sequence's
+ *                 length are not written.
+ *   status        device int32 or NULL (see above)
+ *   workspace     device scratch of workspace_bytes (may be NULL when
+ *                 gdn_forward_workspace_size reports 0)
+ * Sequences in one call must use distinct state slots.
+ */
+typedef struct gdn_forward_args {
+    int32_t num_seqs;              /* B >= 0 (at most 65535) */
+    int32_t total_tokens;          /* T >= 0 */
+    int32_t num_k_heads;           /* Hk >= 1 */
+    int32_t num_v_heads;           /* Hv, a multiple of Hk */
+    int32_t head_dim_k;            /* dk in {32, 64, 128} */
+    int32_t head_dim_v;            /* dv in {32, 64, 128} */
+    int32_t num_state_slots;       /* leading extent of the state pool */
+    int32_t io_dtype;              /* GDN_F32 or GDN_F16 */
+    int32_t gate_mode;             /* GDN_GATES_* */
+    int32_t plan;                  /* GDN_PLAN_* */
+    float scale;                   /* output scale; 0 means 1/sqrt(dk) */
+    int32_t state_update_capacity; /* capsule rows per sequence; 0 = not emitted */
+    int64_t q_stride;
+    int64_t k_stride;
+    int64_t v_stride;
+    const void *q;
+    const void *k;
+    const void *v;
+    const float *a;
+    const float *b;
+    const float *A_log;
+    const float *dt_bias;
+    const int32_t *cu_seqlens;
+    const int32_t *state_slots;
+    const float *initial_state;
+    float *final_state;
+    void *output;
+    float *state_update;
+    int32_t *status;
+    void *workspace;
+    size_t workspace_bytes;
+} gdn_forward_args;
+
+/*
+ * Bytes of device workspace gdn_forward needs for these arguments (sizes and
+ * plan only are read).  Returns GDN_OK and writes *bytes, or an argument error.
+ */
+gdn_status gdn_forward_workspace_size(const gdn_forward_args *args, size_t *bytes);
+
+/*
+ * Runs the gated delta rule over one packed batch (see gdn_forward_args) and
+ * writes output, final_state and, when capacity > 0, state_update.
+ * Asynchronous on `stream`.
+ */
+gdn_status gdn_forward(const gdn_forward_args *args, gdn_stream_t stream);
+
+/*
+ * Replays an accepted prefix of capsules into an inactive state bank.
+ *
+ * Source: "Replay compact fixed state for hybrid decoding" (Summary, Key
+ * changes): the engine captures packed per-token updates and replays only an
+ * accepted prefix into inactive state banks before publishing them; the
+ * capsule content is the decay, shared key and delta of "[CUDA] Add compact
+ * GatedDeltaNet operator" (Description).
+ *
+ * For request j and every value head h:
+ *   S = state_banks[src_slots[j], h]
+ *   for i < accept_len[j]:  S <- g_i S + u_i kn_i^T   (capsule row (j, i))
+ *   state_banks[dst_slots[j], h] = S
+ * accept_len[j] = 0 copies the source state into the destination.
+ *
+ *   state_banks  device [num_slots, Hv, dv, dk] FP32 (V-major), 16-byte aligned
+ *   src_slots, dst_slots, accept_len  device [num_requests] int32
+ *   state_update device [num_requests, capacity, W] FP32 in the capsule layout
+ *                of gdn_forward (W = Hv + Hk*dk + Hv*dv)
+ *   status       device int32 or NULL: GDN_DEVERR_REPLAY_SLOT,
+ *                GDN_DEVERR_ACCEPT_LEN (the request is skipped)
+ * A destination may equal its own source (in place) but must not be any other
+ * request's source or destination.
+ */
+gdn_status gdn_replay_prefix(float *state_banks, int32_t num_slots, int32_t num_requests,
+                             int32_t num_k_heads, int32_t num_v_heads, int32_t head_dim_k,
+                             int32_t head_dim_v, const int32_t *src_slots, const int32_t *dst_slots,
+                             const float *state_update, int32_t capacity, const int32_t *accept_len,
+                             int32_t *status, gdn_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char *gdn_status_string(gdn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

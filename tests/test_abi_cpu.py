@@ -1,0 +1,131 @@
+"""CPU-side checks of the C ABI: the library builds and loads, exports every
+entry point include/gdn.h declares, the ctypes mirror of gdn_forward_args has
+the C layout, and host-visible argument errors return before any launch.
+No call here reaches a kernel."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_gateddeltanet_gb300 import build
+    build.build()
+    import gated_delta_rule_gateddeltanet_gb300 as g
+    return g.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("gdn_forward", "gdn_forward_workspace_size", "gdn_replay_prefix", "gdn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for n in declared_functions():
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_forward_args_layout_matches_c(tmp_path):
+    import gated_delta_rule_gateddeltanet_gb300 as g
+    fields = [f for f, _ in g.ForwardArgs._fields_]
+    src = tmp_path / "layout.c"
+    body = "\n".join(f'printf("{f} %zu\\n", offsetof(gdn_forward_args, {f}));' for f in fields)
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gdn.h"\nint main(void){\n'
+                   + body + '\nprintf("sizeof %zu\\n", sizeof(gdn_forward_args));\nreturn 0;}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    for f in fields:
+        assert int(got[f]) == getattr(g.ForwardArgs, f).offset, f
+    assert int(got["sizeof"]) == ctypes.sizeof(g.ForwardArgs)
+
+
+def _args(**kw):
+    import gated_delta_rule_gateddeltanet_gb300 as g
+    a = g.ForwardArgs()
+    a.num_seqs, a.total_tokens, a.num_k_heads, a.num_v_heads = 2, 4, 16, 48
+    a.head_dim_k = a.head_dim_v = 128
+    a.num_state_slots, a.io_dtype = 2, 1
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: every case below fails its host check first
+    for f in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "cu_seqlens", "final_state", "output"):
+        setattr(a, f, fake)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(io_dtype=2), 2),                   # BF16 rejected
+    (dict(io_dtype=7), 2),
+    (dict(num_v_heads=40), 3),               # Hv not a multiple of Hk
+    (dict(head_dim_k=96), 3),
+    (dict(head_dim_v=256), 3),
+    (dict(state_update_capacity=-1), 3),
+    (dict(num_state_slots=1), 3),            # identity slots need >= B slots
+    (dict(q_stride=100), 3),                 # shorter than Hk*dk
+    (dict(scale=float("nan")), 3),
+    (dict(gate_mode=5), 8),
+    (dict(plan=9), 8),
+    (dict(A_log=None), 1),                   # raw gates need A_log and dt_bias
+    (dict(cu_seqlens=None), 1),
+    (dict(final_state=None), 1),
+    (dict(state_update_capacity=4), 1),      # capsules requested without a buffer
+    (dict(final_state=ctypes.c_void_p(0x1004)), 4),
+])
+def test_forward_rejects_bad_arguments_before_launch(lib, kw, code):
+    a = _args(**kw)
+    assert lib.gdn_forward(ctypes.byref(a), None) == code
+
+
+def test_forward_null_args_and_workspace_query(lib):
+    assert lib.gdn_forward(None, None) == 1
+    a = _args()
+    n = ctypes.c_size_t(123)
+    assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0
+    assert n.value >= 0
+    assert lib.gdn_forward_workspace_size(ctypes.byref(a), None) == 1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    a = _args(num_seqs=0, total_tokens=0)
+    assert lib.gdn_forward(ctypes.byref(a), None) == 0
+
+
+def test_replay_rejects_bad_arguments(lib):
+    f = lib.gdn_replay_prefix
+    fake = ctypes.c_void_p(0x1000)
+    assert f(fake, 4, 2, 16, 40, 128, 128, fake, fake, fake, 4, fake, None, None) == 3
+    assert f(fake, 4, 2, 16, 48, 128, 100, fake, fake, fake, 4, fake, None, None) == 3
+    assert f(None, 4, 2, 16, 48, 128, 128, fake, fake, fake, 4, fake, None, None) == 1
+    assert f(fake, 4, 2, 16, 48, 128, 128, fake, fake, None, 4, fake, None, None) == 1
+    assert f(ctypes.c_void_p(0x1008), 4, 2, 16, 48, 128, 128, fake, fake, fake, 4, fake, None, None) == 4
+    assert f(fake, 4, 0, 16, 48, 128, 128, None, None, None, 0, None, None, None) == 0
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert lib.gdn_status_string(code)
+    assert lib.gdn_status_string(99) == b"unknown status"
+
+
+def test_capsule_width_matches_pages_geometry():
+    import gated_delta_rule_gateddeltanet_gb300 as g
+    # 48 value heads, 16 key heads, d = 128: 8240 floats = 32,960 bytes per token-layer
+    assert g.capsule_width(16, 48, 128, 128) * 4 == 32960
