@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--no-extra", action="store_true", help="skip the prefill / verify+replay sub-measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     return ap.parse_args()
 
 
@@ -253,7 +254,7 @@ def run_gdn(a, dist: Dist):
                 "launch_us": round(ms_local / a.steps * 1e3, 2)}
 
     # ---- e2e: host buffers through the public binding
-    e2e = run_e2e(a, dist, sets, dev, stream)
+    e2e = None if a.no_e2e else run_e2e(a, dist, sets, dev, stream)
 
     extra = {}
     if not a.no_extra and dist.rank == 0:

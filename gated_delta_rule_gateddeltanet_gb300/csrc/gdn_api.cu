@@ -42,34 +42,9 @@ gdn_status check_sizes(const gdn_forward_args *a) {
     return GDN_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-const char *gdn_status_string(gdn_status status) {
-    switch (status) {
-        case GDN_OK: return "ok";
-        case GDN_ERR_NULL: return "a required pointer is NULL";
-        case GDN_ERR_DTYPE: return "unsupported I/O dtype (FP16 and FP32 only; BF16 is rejected)";
-        case GDN_ERR_SHAPE: return "inconsistent or unsupported sizes";
-        case GDN_ERR_ALIGN: return "a state pointer is not 16-byte aligned";
-        case GDN_ERR_WORKSPACE: return "workspace missing or too small";
-        case GDN_ERR_CUDA: return "CUDA launch error";
-        case GDN_ERR_UNSUPPORTED: return "the forced plan does not support these sizes";
-        case GDN_ERR_ARG: return "unknown enum value in the arguments";
-    }
-    return "unknown status";
-}
-
-gdn_status gdn_forward_workspace_size(const gdn_forward_args *args, size_t *bytes) {
-    if (!bytes) return GDN_ERR_NULL;
-    const gdn_status st = check_sizes(args);
-    if (st != GDN_OK) return st;
-    *bytes = 0;
-    return GDN_OK;
-}
-
-gdn_status gdn_forward(const gdn_forward_args *a, gdn_stream_t stream) {
+// Checks a forward call completely (sizes, pointers, alignment) and resolves
+// it into kernel parameters.  Returns GDN_OK with *out filled, or the error.
+gdn_status resolve_forward(const gdn_forward_args *a, gdn::ForwardParams *out) {
     const gdn_status st = check_sizes(a);
     if (st != GDN_OK) return st;
     if (a->num_seqs == 0) return GDN_OK;
@@ -112,6 +87,41 @@ gdn_status gdn_forward(const gdn_forward_args *a, gdn_stream_t stream) {
     p.status = a->status;
     p.max_len = 0x7fffffff;
 
+    *out = p;
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_status_string(gdn_status status) {
+    switch (status) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_NULL: return "a required pointer is NULL";
+        case GDN_ERR_DTYPE: return "unsupported I/O dtype (FP16 and FP32 only; BF16 is rejected)";
+        case GDN_ERR_SHAPE: return "inconsistent or unsupported sizes";
+        case GDN_ERR_ALIGN: return "a state pointer is not 16-byte aligned";
+        case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+        case GDN_ERR_CUDA: return "CUDA launch error";
+        case GDN_ERR_UNSUPPORTED: return "the forced plan does not support these sizes";
+        case GDN_ERR_ARG: return "unknown enum value in the arguments";
+    }
+    return "unknown status";
+}
+
+gdn_status gdn_forward_workspace_size(const gdn_forward_args *args, size_t *bytes) {
+    if (!bytes) return GDN_ERR_NULL;
+    const gdn_status st = check_sizes(args);
+    if (st != GDN_OK) return st;
+    *bytes = 0;
+    return GDN_OK;
+}
+
+gdn_status gdn_forward(const gdn_forward_args *a, gdn_stream_t stream) {
+    gdn::ForwardParams p{};
+    const gdn_status st = resolve_forward(a, &p);
+    if (st != GDN_OK || a->num_seqs == 0) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (gdn::launch_recurrent(p, s) != cudaSuccess) return GDN_ERR_CUDA;
     return GDN_OK;
