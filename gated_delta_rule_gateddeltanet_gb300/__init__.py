@@ -25,7 +25,7 @@ __all__ = ["gdn_forward", "gdn_replay_prefix", "GdnError", "load_library", "caps
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_DTYPE", 3: "GDN_ERR_SHAPE", 4: "GDN_ERR_ALIGN",
           5: "GDN_ERR_WORKSPACE", 6: "GDN_ERR_CUDA", 7: "GDN_ERR_UNSUPPORTED", 8: "GDN_ERR_ARG"}
-DEVERR = {"cu_seqlens": 0x1, "state_slot": 0x2, "accept_len": 0x4, "replay_slot": 0x8}
+DEVERR = {"cu_seqlens": 0x1, "state_slot": 0x2, "accept_len": 0x4, "replay_slot": 0x8, "timeout": 0x10}
 PLAN = {"auto": 0, "recurrent": 1, "chunked": 2}
 DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 GATE_MODE = {"raw": 0, "precomputed": 1}

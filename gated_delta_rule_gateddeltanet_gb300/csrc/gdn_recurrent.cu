@@ -10,42 +10,55 @@
 //     u_i = beta (v_i - g p)
 //     S_i <- g S_i + u_i kn
 //     o_i = scale (g s + u_i (kn . qn))          (= scale S_i(new) . qn)
-// so both dot products come from the same registers and the state is read
+// so both dot products come from one read of the row, and the state is read
 // once and written once per call however many tokens the span has.
 //
-// Work split: a CTA of 256 threads owns ROWS_CTA rows of one (sequence,
-// value head).  LPR = dk/16 lanes share a row, each holding 16 floats of it as
-// four float4 (coalesced 128-bit loads: the LPR lanes of a row read one
-// contiguous 64*LPR-byte run per instruction).  Reductions are LPR-wide xor
-// shuffles.  The per-token vectors (normalised q and k, gates, v, k.q) are
-// staged in shared memory TB tokens at a time; the state loads are issued
-// before that staging so their latency overlaps it.  State traffic uses
-// streaming (evict-first) loads and stores: it is touched once.
+// Data movement (the kernel is HBM-bound: 0.75 FLOP per state byte): a CTA
+// owns a tile of ROWS = 64 consecutive rows of one (sequence, value head),
+// which is one contiguous 64*dk*4-byte run of the state (32 KiB at dk = 128).
+// One thread moves the whole tile with a single bulk (TMA) copy into shared
+// memory, completion tracked by an mbarrier; the per-token vectors
+// (normalised q and k, k.q, gates, v) are staged meanwhile, so their
+// dependent loads overlap the tile's flight.  After the update the tile goes
+// back with one bulk store.  No state bytes live in registers while in
+// flight, so registers stay low (~63) and 5 CTAs fit per SM: up to 160 KiB of
+// state in flight per SM, enough to cover HBM latency.
+//
+// Compute mapping: LPR = dk/16 lanes share a row, 16 floats each as four
+// float4 (lane l reads float4 j*LPR + l, so the LPR lanes of a row cover one
+// contiguous run and the shared-memory reads are conflict-free); both dot
+// products are LPR-wide xor-shuffle reductions.  Tokens are staged TB at a
+// time; rows stay in registers across the staged tokens.
 #include "gdn_internal.cuh"
+#include "ptx.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int NT = 256;  // threads per CTA
-constexpr int TB = 8;    // tokens staged per round (one warp normalises one token)
+constexpr int NT = 256;    // threads per CTA
+constexpr int TB = 4;      // tokens staged per round (one warp normalises one token)
+constexpr int ROWS = 64;   // state rows per CTA tile
 constexpr float EPS = 1e-6f;
+// Bound on any mbarrier wait (SM cycles, ~2 s); past it the CTA reports
+// GDN_DEVERR_TIMEOUT and leaves its tile unwritten.
+constexpr long long WAIT_LIMIT = 4000000000LL;
 
-template <typename TIO, int DK, int RPT>
-__global__ void __launch_bounds__(NT) recurrent_kernel(const ForwardParams p) {
+template <typename TIO, int DK>
+__global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p) {
     constexpr int LPR = DK / 16;             // lanes per state row
     constexpr int GPW = 32 / LPR;            // rows per warp per pass
     constexpr int ROWS_PASS = (NT / 32) * GPW;
-    constexpr int ROWS_CTA = ROWS_PASS * RPT;
+    constexpr int NPASS = (ROWS + ROWS_PASS - 1) / ROWS_PASS;
     constexpr int EPL = DK / 32;             // q/k elements per lane when normalising
 
+    extern __shared__ __align__(128) float tile[];  // [ROWS][DK]
     __shared__ __align__(16) float kn_s[TB][DK];
     __shared__ __align__(16) float qn_s[TB][DK];
     __shared__ float g_s[TB], beta_s[TB], kq_s[TB];
-    __shared__ float v_s[TB][ROWS_CTA];
-    __shared__ float o_s[TB][ROWS_CTA];
-    __shared__ float u_s[TB][ROWS_CTA];
+    __shared__ float v_s[TB][ROWS], o_s[TB][ROWS], u_s[TB][ROWS];
+    __shared__ __align__(8) uint64_t bar;
 
-    const int nrb = (p.dv + ROWS_CTA - 1) / ROWS_CTA;
+    const int nrb = (p.dv + ROWS - 1) / ROWS;
     const int rb = blockIdx.x % nrb;
     const int h = blockIdx.x / nrb;
     const int b = blockIdx.y;
@@ -66,24 +79,26 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const ForwardParams p) {
         return;
     }
     const int kh = h / p.r;
+    const int rows_here = min(ROWS, p.dv - rb * ROWS);
+    const uint32_t bytes = (uint32_t)rows_here * DK * 4;
+    const size_t off = (((size_t)slot * p.Hv + h) * (size_t)p.dv + (size_t)rb * ROWS) * DK;
 
-    // ---- state rows into registers (issued first)
-    const size_t head_off = ((size_t)slot * p.Hv + h) * (size_t)p.dv * DK;
-    float4 s[RPT][4];
-    int lrow[RPT];
-#pragma unroll
-    for (int k = 0; k < RPT; ++k) {
-        lrow[k] = k * ROWS_PASS + warp * GPW + grp;
-        const int row = rb * ROWS_CTA + lrow[k];
-        if (p.init && row < p.dv) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.init + head_off + (size_t)row * DK);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) s[k][j] = __ldcs(src + j * LPR + l);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) s[k][j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+    // ---- the state tile: one bulk copy in flight while the tokens are staged
+    if (tid == 0) {
+        ptx::mbar_init(&bar, 1);
+        ptx::fence_mbar_init();
     }
+    __syncthreads();
+    if (p.init) {
+        if (tid == 0) {
+            ptx::mbar_arrive_expect_tx(&bar, bytes);
+            ptx::bulk_g2s(tile, p.init + off, bytes, &bar);
+        }
+    } else {
+        float4 *t4 = reinterpret_cast<float4 *>(tile);
+        for (int i = tid; i < rows_here * DK / 4; i += NT) t4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    bool tile_pending = p.init != nullptr;
 
     const TIO *qg = static_cast<const TIO *>(p.q);
     const TIO *kg = static_cast<const TIO *>(p.k);
@@ -128,63 +143,85 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const ForwardParams p) {
                 kq_s[warp] = kq;
             }
         }
-        for (int i = tid; i < nt * ROWS_CTA; i += NT) {
-            const int tt = i / ROWS_CTA, rr = i % ROWS_CTA;
-            const int row = rb * ROWS_CTA + rr;
-            v_s[tt][rr] = row < p.dv ? to_f32(vg[(long long)(t0 + tt) * p.v_stride + (long long)h * p.dv + row]) : 0.f;
+        for (int i = tid; i < nt * ROWS; i += NT) {
+            const int tt = i / ROWS, rr = i % ROWS;
+            v_s[tt][rr] = rr < rows_here
+                              ? to_f32(vg[(long long)(t0 + tt) * p.v_stride + (long long)h * p.dv + rb * ROWS + rr])
+                              : 0.f;
         }
         __syncthreads();
+        if (tile_pending) {
+            const bool ok = ptx::mbar_wait_bounded(&bar, 0, WAIT_LIMIT);
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) {
+                    flag_error(p.status, GDN_DEVERR_TIMEOUT);
+                    ptx::mbar_wait_bounded(&bar, 0, WAIT_LIMIT);  // let the copy land before exit
+                }
+                return;
+            }
+            tile_pending = false;
+        }
 
         // ---- the recurrence, token by token, on register-resident rows
-        for (int tt = 0; tt < nt; ++tt) {
-            const float g = g_s[tt], beta = beta_s[tt], kq = kq_s[tt];
-            float4 kk[4], qq[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                kk[j] = reinterpret_cast<const float4 *>(kn_s[tt])[j * LPR + l];
-                qq[j] = reinterpret_cast<const float4 *>(qn_s[tt])[j * LPR + l];
-            }
+        for (int pass = 0; pass < NPASS; ++pass) {
+            const int lrow = pass * ROWS_PASS + warp * GPW + grp;
+            const bool act = lrow < rows_here;
+            const int srow = act ? lrow : 0;
+            float4 s[4];
+            const float4 *rowp = reinterpret_cast<const float4 *>(tile + (size_t)srow * DK);
 #pragma unroll
-            for (int k = 0; k < RPT; ++k) {
+            for (int j = 0; j < 4; ++j) s[j] = act ? rowp[j * LPR + l] : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int tt = 0; tt < nt; ++tt) {
+                const float g = g_s[tt], beta = beta_s[tt], kq = kq_s[tt];
+                const float4 *kk = reinterpret_cast<const float4 *>(kn_s[tt]);
+                const float4 *qq = reinterpret_cast<const float4 *>(qn_s[tt]);
                 float pk0 = 0.f, pk1 = 0.f, pq0 = 0.f, pq1 = 0.f;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    pk0 = fmaf(s[k][j].x, kk[j].x, pk0);
-                    pk1 = fmaf(s[k][j].y, kk[j].y, pk1);
-                    pk0 = fmaf(s[k][j].z, kk[j].z, pk0);
-                    pk1 = fmaf(s[k][j].w, kk[j].w, pk1);
-                    pq0 = fmaf(s[k][j].x, qq[j].x, pq0);
-                    pq1 = fmaf(s[k][j].y, qq[j].y, pq1);
-                    pq0 = fmaf(s[k][j].z, qq[j].z, pq0);
-                    pq1 = fmaf(s[k][j].w, qq[j].w, pq1);
+                    const float4 k4 = kk[j * LPR + l], q4 = qq[j * LPR + l];
+                    pk0 = fmaf(s[j].x, k4.x, pk0);
+                    pk1 = fmaf(s[j].y, k4.y, pk1);
+                    pk0 = fmaf(s[j].z, k4.z, pk0);
+                    pk1 = fmaf(s[j].w, k4.w, pk1);
+                    pq0 = fmaf(s[j].x, q4.x, pq0);
+                    pq1 = fmaf(s[j].y, q4.y, pq1);
+                    pq0 = fmaf(s[j].z, q4.z, pq0);
+                    pq1 = fmaf(s[j].w, q4.w, pq1);
                 }
                 float pk = pk0 + pk1, pq = pq0 + pq1;
 #pragma unroll
-                for (int off = LPR / 2; off > 0; off >>= 1) {
-                    pk += __shfl_xor_sync(0xffffffffu, pk, off);
-                    pq += __shfl_xor_sync(0xffffffffu, pq, off);
+                for (int o = LPR / 2; o > 0; o >>= 1) {
+                    pk += __shfl_xor_sync(0xffffffffu, pk, o);
+                    pq += __shfl_xor_sync(0xffffffffu, pq, o);
                 }
-                const float u = beta * (v_s[tt][lrow[k]] - g * pk);
+                const float u = beta * (v_s[tt][srow] - g * pk);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    s[k][j].x = fmaf(u, kk[j].x, g * s[k][j].x);
-                    s[k][j].y = fmaf(u, kk[j].y, g * s[k][j].y);
-                    s[k][j].z = fmaf(u, kk[j].z, g * s[k][j].z);
-                    s[k][j].w = fmaf(u, kk[j].w, g * s[k][j].w);
+                    const float4 k4 = kk[j * LPR + l];
+                    s[j].x = fmaf(u, k4.x, g * s[j].x);
+                    s[j].y = fmaf(u, k4.y, g * s[j].y);
+                    s[j].z = fmaf(u, k4.z, g * s[j].z);
+                    s[j].w = fmaf(u, k4.w, g * s[j].w);
                 }
-                if (l == 0) {
-                    o_s[tt][lrow[k]] = p.scale * fmaf(u, kq, g * pq);
-                    u_s[tt][lrow[k]] = u;
+                if (l == 0 && act) {
+                    o_s[tt][lrow] = p.scale * fmaf(u, kq, g * pq);
+                    u_s[tt][lrow] = u;
                 }
+            }
+            if (act) {
+                float4 *roww = reinterpret_cast<float4 *>(tile + (size_t)lrow * DK);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) roww[j * LPR + l] = s[j];
             }
         }
         __syncthreads();
 
         // ---- outputs and capsules of the staged tokens
-        for (int i = tid; i < nt * ROWS_CTA; i += NT) {
-            const int tt = i / ROWS_CTA, rr = i % ROWS_CTA;
-            const int row = rb * ROWS_CTA + rr;
-            if (row >= p.dv) continue;
+        for (int i = tid; i < nt * ROWS; i += NT) {
+            const int tt = i / ROWS, rr = i % ROWS;
+            if (rr >= rows_here) continue;
+            const int row = rb * ROWS + rr;
             const long long t = t0 + tt;
             og[(t * p.Hv + h) * p.dv + row] = from_f32<TIO>(o_s[tt][rr]);
             const int tl = (int)(t - bos);
@@ -206,24 +243,35 @@ __global__ void __launch_bounds__(NT) recurrent_kernel(const ForwardParams p) {
         __syncthreads();
     }
 
-    // ---- state rows out
-#pragma unroll
-    for (int k = 0; k < RPT; ++k) {
-        const int row = rb * ROWS_CTA + lrow[k];
-        if (row >= p.dv) continue;
-        float4 *dst = reinterpret_cast<float4 *>(p.final_state + head_off + (size_t)row * DK);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) __stcs(dst + j * LPR + l, s[k][j]);
+    if (tile_pending) {  // empty sequence: the tile is stored unchanged
+        const bool ok = ptx::mbar_wait_bounded(&bar, 0, WAIT_LIMIT);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                flag_error(p.status, GDN_DEVERR_TIMEOUT);
+                ptx::mbar_wait_bounded(&bar, 0, WAIT_LIMIT);
+            }
+            return;
+        }
+    }
+    // ---- the tile goes back with one bulk store
+    ptx::fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        ptx::bulk_s2g(p.final_state + off, tile, bytes);
+        ptx::bulk_commit();
+        ptx::bulk_wait_read_all();  // the shared-memory source must outlive the copy's reads
     }
 }
 
 template <typename TIO, int DK>
 cudaError_t launch_dk(const ForwardParams &p, cudaStream_t stream) {
-    constexpr int RPT = 2;
-    constexpr int ROWS_CTA = (NT / 32) * (32 / (DK / 16)) * RPT;
-    const int nrb = (p.dv + ROWS_CTA - 1) / ROWS_CTA;
+    const int nrb = (p.dv + ROWS - 1) / ROWS;
     dim3 grid((unsigned)(nrb * p.Hv), (unsigned)p.B);
-    recurrent_kernel<TIO, DK, RPT><<<grid, NT, 0, stream>>>(p);
+    const int smem = ROWS * DK * 4;
+    auto kern = recurrent_kernel<TIO, DK>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, NT, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

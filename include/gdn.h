@@ -67,6 +67,7 @@ enum {
 #define GDN_DEVERR_STATE_SLOT 0x2  /* state_slots[b] outside [0, num_state_slots) */
 #define GDN_DEVERR_ACCEPT_LEN 0x4  /* accept_len[j] outside [0, capacity] */
 #define GDN_DEVERR_REPLAY_SLOT 0x8 /* a replay source or destination slot out of range */
+#define GDN_DEVERR_TIMEOUT 0x10    /* a bounded wait inside a kernel gave up (the unit is not written) */
 
 /*
  * Arguments of gdn_forward.
