@@ -247,7 +247,7 @@ def run_gdn(a, dist: Dist):
     achieved_gbs = bytes_launch / (ms_local / a.steps / 1e3) / 1e9
     traffic = recorded_traffic(os.path.join(ROOT, "gated_delta_rule_gateddeltanet_gb300", "csrc", "gdn_recurrent.cu"),
                                "decode_step.recurrent_kernel.ncu.md")
-    roofline = {"bound": "hbm", "kernel": "recurrent_kernel<half,128,2>", "achieved": round(achieved_gbs, 1),
+    roofline = {"bound": "hbm", "kernel": "recurrent_kernel<__half,128>", "achieved": round(achieved_gbs, 1),
                 "peak": hbm_peak, "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                 "unit": "GB/s", "frac": round(achieved_gbs / hbm_peak, 4), "traffic": traffic,
                 "algorithmic_bytes_per_launch": bytes_launch,
