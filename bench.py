@@ -204,7 +204,7 @@ def run_gdn(a, dist: Dist):
                  out=torch.empty((inp.T, 48, 128), dtype=torch.float16, device=dev), inp=inp)
         args, _, keep = gdn.build_forward_args(d["q"], d["k"], d["v"], d["a"], d["b"], d["cu"], A_log=d["A_log"],
                                                dt_bias=d["dt_bias"], initial_state=d["state"],
-                                               final_state=d["state"], output=d["out"])
+                                               final_state=d["state"], output=d["out"], max_seqlen=1)
         d["args"], d["keep"] = args, keep
         sets.append(d)
     R = sets[0]["inp"].B
@@ -308,7 +308,7 @@ def run_e2e(a, dist, sets, dev, stream):
         d = sets[j]
         out, _, _ = gdn.gdn_forward(db["q"], db["k"], db["v"], db["a"], db["b"], db["cu"], A_log=d["A_log"],
                                     dt_bias=d["dt_bias"], initial_state=d["state"], final_state=d["state"],
-                                    output=d["out"])
+                                    output=d["out"], max_seqlen=1)
         ho.copy_(out, non_blocking=True)
 
     for i in range(min(a.warmup, 50)):
@@ -347,8 +347,10 @@ def run_prefill(dev, stream):
     out = torch.empty((inp.T, 48, 128), dtype=torch.float16, device=dev)
     flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MiB
     plan = "auto"
+    maxlen = int(np.diff(inp.cu_seqlens).max())
+    ws = torch.empty(4096, dtype=torch.uint8, device=dev)
     run = lambda: gdn.gdn_forward(q, k, v, aa, bb, cu, A_log=A_log, dt_bias=dt_bias, final_state=final, output=out,
-                                  plan=plan)
+                                  plan=plan, max_seqlen=maxlen, workspace=ws)
     for _ in range(2):
         run()
     iters = 5
@@ -390,7 +392,7 @@ def run_spec(dev, stream, lib, sh):
         args, _, keep = gdn.build_forward_args(d["q"], d["k"], d["v"], d["a"], d["b"], d["cu"], A_log=d["A_log"],
                                                dt_bias=d["dt_bias"], initial_state=pool, final_state=scratch,
                                                state_slots=None, output=d["out"], state_update=caps, capacity=4,
-                                               num_state_slots=16)
+                                               num_state_slots=16, max_seqlen=4)
         d["args"], d["keep"], d["acc"] = args, keep, int(inp.extra["accept_len"].sum())
         pools.append(d)
 

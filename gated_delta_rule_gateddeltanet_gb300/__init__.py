@@ -44,6 +44,7 @@ class ForwardArgs(ctypes.Structure):
         ("num_v_heads", ctypes.c_int32), ("head_dim_k", ctypes.c_int32), ("head_dim_v", ctypes.c_int32),
         ("num_state_slots", ctypes.c_int32), ("io_dtype", ctypes.c_int32), ("gate_mode", ctypes.c_int32),
         ("plan", ctypes.c_int32), ("scale", ctypes.c_float), ("state_update_capacity", ctypes.c_int32),
+        ("max_seqlen", ctypes.c_int32),
         ("q_stride", ctypes.c_int64), ("k_stride", ctypes.c_int64), ("v_stride", ctypes.c_int64),
         ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
         ("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
@@ -117,7 +118,7 @@ def _token_stride(t, name, inner):
 def build_forward_args(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, gate_mode="raw",
                        initial_state=None, final_state=None, state_slots=None, output=None,
                        state_update=None, capacity=0, scale=0.0, plan="auto", status=None,
-                       num_state_slots=None, workspace=None):
+                       num_state_slots=None, workspace=None, max_seqlen=0):
     """Fill a ForwardArgs struct from tensors; returns (args, outputs, keepalive)."""
     dev = q.device
     T, Hk, dk = q.shape
@@ -162,6 +163,7 @@ def build_forward_args(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, g
     args.plan = PLAN[plan]
     args.scale = float(scale or 0.0)
     args.state_update_capacity = int(capacity)
+    args.max_seqlen = int(max_seqlen or 0)
     args.q_stride = _token_stride(q, "q", Hk * dk)
     args.k_stride = _token_stride(k, "k", Hk * dk)
     args.v_stride = _token_stride(v, "v", Hv * dv)
@@ -192,13 +194,16 @@ def workspace_size(args: ForwardArgs) -> int:
 def gdn_forward(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, gate_mode="raw",
                 initial_state=None, final_state=None, state_slots=None, output=None,
                 state_update=None, capacity=0, scale=0.0, plan="auto", status=None,
-                num_state_slots=None, workspace=None):
+                num_state_slots=None, workspace=None, max_seqlen=0):
     """Gated delta rule over a packed varlen batch (C ABI ``gdn_forward``).
 
     q, k: [T, Hk, dk] fp16/fp32 CUDA; v: [T, Hv, dv]; a, b: [T, Hv] fp32 (raw
     gate inputs, or g and beta with ``gate_mode="precomputed"``); A_log, dt_bias:
     [Hv] fp32; cu_seqlens: [B+1] int32.  ``initial_state`` [slots, Hv, dv, dk]
     fp32 or None (zeros); ``final_state`` may be the same tensor (in place).
+    ``max_seqlen``: an upper bound on the longest sequence (0 = unknown), a
+    hint that lets decode-sized batches skip the chunked kernel.  Workspace is
+    allocated here when the call needs some and none is passed.
     Returns ``(output, final_state, state_update)``; state_update is
     [B, capacity, W] fp32 or None.
     """
@@ -207,7 +212,8 @@ def gdn_forward(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, gate_mod
                                           gate_mode=gate_mode, initial_state=initial_state,
                                           final_state=final_state, state_slots=state_slots, output=output,
                                           state_update=state_update, capacity=capacity, scale=scale, plan=plan,
-                                          status=status, num_state_slots=num_state_slots, workspace=workspace)
+                                          status=status, num_state_slots=num_state_slots, workspace=workspace,
+                                          max_seqlen=max_seqlen)
     need = workspace_size(args)
     if need > 0 and workspace is None:
         ws = torch.empty(need, dtype=torch.uint8, device=q.device)

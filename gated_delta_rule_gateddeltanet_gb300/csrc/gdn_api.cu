@@ -29,7 +29,7 @@ gdn_status check_sizes(const gdn_forward_args *a) {
     if (a->num_k_heads <= 0 || a->num_v_heads <= 0 || a->num_v_heads % a->num_k_heads != 0)
         return GDN_ERR_SHAPE;
     if (!valid_head_dim(a->head_dim_k) || !valid_head_dim(a->head_dim_v)) return GDN_ERR_SHAPE;
-    if (a->state_update_capacity < 0) return GDN_ERR_SHAPE;
+    if (a->state_update_capacity < 0 || a->max_seqlen < 0) return GDN_ERR_SHAPE;
     if (a->num_seqs > 0 && a->num_state_slots < 1) return GDN_ERR_SHAPE;
     if (a->num_seqs > 0 && !a->state_slots && a->num_state_slots < a->num_seqs) return GDN_ERR_SHAPE;
     const int64_t qk_min = (int64_t)a->num_k_heads * a->head_dim_k;
@@ -38,8 +38,24 @@ gdn_status check_sizes(const gdn_forward_args *a) {
         (a->v_stride != 0 && a->v_stride < v_min))
         return GDN_ERR_SHAPE;
     if (!(a->scale >= 0.f) || isinf(a->scale)) return GDN_ERR_SHAPE;
-    if (a->plan == GDN_PLAN_CHUNKED) return GDN_ERR_UNSUPPORTED;
+    if (a->plan == GDN_PLAN_CHUNKED && !gdn::chunked_supported(a->head_dim_k, a->head_dim_v))
+        return GDN_ERR_UNSUPPORTED;
     return GDN_OK;
+}
+
+// Whether these sizes may use the chunked kernel (and so need workspace).
+bool wants_chunked(const gdn_forward_args *a) {
+    if (a->num_seqs == 0 || a->plan == GDN_PLAN_RECURRENT) return false;
+    if (!gdn::chunked_supported(a->head_dim_k, a->head_dim_v)) return false;
+    const int longest = a->max_seqlen > 0 && a->max_seqlen < a->total_tokens ? a->max_seqlen : a->total_tokens;
+    return a->plan == GDN_PLAN_CHUNKED || longest > gdn::RECURRENT_MAX_LEN;
+}
+
+// The chunked kernel reads q, k, v with 8- or 16-byte vector loads.
+bool chunked_aligned(const gdn_forward_args *a, const gdn::ForwardParams &p) {
+    const size_t esz = p.io_f16 ? 2 : 4;
+    return aligned16(a->q) && aligned16(a->k) && aligned16(a->v) && (p.q_stride * esz) % 16 == 0 &&
+           (p.k_stride * esz) % 16 == 0 && (p.v_stride * esz) % 16 == 0;
 }
 
 // Checks a forward call completely (sizes, pointers, alignment) and resolves
@@ -114,7 +130,7 @@ gdn_status gdn_forward_workspace_size(const gdn_forward_args *args, size_t *byte
     if (!bytes) return GDN_ERR_NULL;
     const gdn_status st = check_sizes(args);
     if (st != GDN_OK) return st;
-    *bytes = 0;
+    *bytes = wants_chunked(args) ? gdn::chunked_workspace_bytes(args->num_seqs) : 0;
     return GDN_OK;
 }
 
@@ -123,6 +139,20 @@ gdn_status gdn_forward(const gdn_forward_args *a, gdn_stream_t stream) {
     const gdn_status st = resolve_forward(a, &p);
     if (st != GDN_OK || a->num_seqs == 0) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    bool chunked = wants_chunked(a);
+    if (chunked && !chunked_aligned(a, p)) {
+        if (a->plan == GDN_PLAN_CHUNKED) return GDN_ERR_ALIGN;
+        chunked = false;  // the automatic plan keeps every sequence on the recurrent kernel
+    }
+    if (chunked) {
+        if (!a->workspace || a->workspace_bytes < gdn::chunked_workspace_bytes(a->num_seqs) ||
+            (reinterpret_cast<uintptr_t>(a->workspace) & 15u))
+            return GDN_ERR_WORKSPACE;
+        const int min_len = a->plan == GDN_PLAN_CHUNKED ? -1 : gdn::RECURRENT_MAX_LEN;
+        if (gdn::launch_chunked(p, min_len, a->workspace, s) != cudaSuccess) return GDN_ERR_CUDA;
+        if (a->plan == GDN_PLAN_CHUNKED) return GDN_OK;
+        p.max_len = gdn::RECURRENT_MAX_LEN;
+    }
     if (gdn::launch_recurrent(p, s) != cudaSuccess) return GDN_ERR_CUDA;
     return GDN_OK;
 }

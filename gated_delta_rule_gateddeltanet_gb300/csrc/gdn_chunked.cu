@@ -1,0 +1,621 @@
+// Chunked (WY / UT-transform) gated delta rule on the tcgen05 tensor cores.
+//
+// Operator: "[CUDA] Add compact GatedDeltaNet operator" (Description) -- the
+// tensor-core chunked prefill path of the GatedDeltaNet operator.  Same
+// results as the token-by-token recurrence, evaluated 64 tokens at a time.
+//
+// Algebra (per (sequence, value head) chain, chunk of n <= 64 tokens, S0 the
+// dv x dk state entering the chunk, Gamma_r the within-chunk cumulative log
+// decay, gamma_r = exp(Gamma_r)):
+//   A[r,s] = beta_r exp(Gamma_r - Gamma_s) (k_r . k_s)  (s < r);  T = (I + A)^-1
+//   R^T    = (V - diag(gamma) K S0^T)^T diag(beta)       (dv x n)
+//   U^T    = R^T T^T                                      (the capsule deltas)
+//   O^T    = scale (S0 (diag(gamma) Q)^T + U^T (P o D)^T),  P = Q K^T,
+//            D[r,s] = exp(Gamma_r - Gamma_s) (s <= r)
+//   S1     = gamma_last S0 + (U^T diag(exp(Gamma_last - Gamma))) K
+// This follows from S_r = gamma_r S0 + sum_{s<=r} (gamma_r/gamma_s) u_s k_s^T
+// and u_r = beta_r (v_r - g_r S_{r-1} k_r).  Only differences Gamma_r -
+// Gamma_s with r >= s are exponentiated (never exp(-Gamma)).
+//
+// Every product is an M = 128 tcgen05.mma (kind::f16, fp16 operands, fp32
+// accumulators in tensor memory) with both operands K-major in the 128-byte
+// swizzled layout, the value dimension (dv = 128) as M:
+//   MMA1  [K;Q] K^T            -> G = K K^T, P = Q K^T      (128 x 64, K = dk)
+//   MMA2  S0 [K ; gamma Q]^T   -> X^T = S0 K^T, S0 (gamma Q)^T (128 x 128, K = dk)
+//   MMA3  R^T T^T              -> U^T                        (128 x 64, K = n)
+//   MMA4  U^T (P o D)^T        accumulated onto S0 (gamma Q)^T -> O^T
+//   MMA5  (U^T diag) K         accumulated onto gamma_last S0 -> S1 (128 x 128, K = n)
+// The FP32 state lives in tensor memory for the whole chain (128 columns);
+// its fp16 copy for MMA2 is rebuilt from it every chunk.  The triangular
+// inverse runs on the CUDA cores in FP32 (16 x 16 diagonal blocks by forward
+// substitution, then two levels of block combination).
+//
+// Scheduling: a persistent grid of one CTA per SM (the shared-memory
+// footprint forces one) pulls (sequence, value head) chains from a list that a
+// one-CTA planning kernel sorts longest-first, through an atomic counter in
+// the caller's workspace.
+#include "gdn_internal.cuh"
+#include "ptx.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int NT = 256;
+constexpr int CH = 64;   // chunk length
+constexpr int DH = 128;  // dk = dv on this path
+constexpr float EPS = 1e-6f;
+constexpr float LOG_DECAY_FLOOR = -200.f;  // exp(-200) is 0 in fp32; keeps Gamma well-conditioned
+constexpr long long WAIT_LIMIT = 4000000000LL;
+constexpr int TMEM_COLS = 512;
+
+// Tensor-memory columns (128 lanes each).
+constexpr uint32_t TM_S = 0;     // FP32 state S (dv lanes x dk columns)
+constexpr uint32_t TM_D1 = 128;  // G (lanes 0-63) and P (lanes 64-127), 64 columns
+constexpr uint32_t TM_D3 = 192;  // U^T, 64 columns
+constexpr uint32_t TM_X = 256;   // X^T = S0 K^T, 64 columns
+constexpr uint32_t TM_O = 320;   // S0 (gamma Q)^T + U^T (P o D)^T, 64 columns
+
+// Shared-memory layout (bytes from a 1024-byte aligned base).  fp16 tiles are
+// K-major with the 128-byte swizzle.
+constexpr int OFF_KQ = 0;                  // [128][128]: rows 0-63 K, 64-127 Q        32 KiB
+constexpr int OFF_GQ = OFF_KQ + 32768;     // [64][128]: gamma Q                        16 KiB
+constexpr int OFF_KT = OFF_GQ + 16384;     // [128][64]: K^T (dk rows, token columns)  16 KiB
+constexpr int OFF_S16 = OFF_KT + 16384;    // [128][128]: S0 in fp16                    32 KiB
+constexpr int OFF_A32 = OFF_S16;           //   reused once MMA2 is done: A in fp32 [64][65]
+constexpr int OFF_RT = OFF_S16 + 32768;    // [128][64]: R^T, then U^T                  16 KiB
+constexpr int OFF_UD = OFF_RT + 16384;     // [128][64]: U^T diag(exp(Gamma_last - Gamma)) 16 KiB
+constexpr int OFF_T = OFF_UD + 16384;      // [64][64]: T                               8 KiB
+constexpr int OFF_PD = OFF_T + 8192;       // [64][64]: P o D                           8 KiB
+constexpr int OFF_V = OFF_PD + 8192;       // [64][128] fp32 v                          32 KiB
+constexpr int OFF_T32 = OFF_V;             //   reused once R^T is built: T in fp32 [64][65]
+constexpr int OFF_M = OFF_V + 64 * 65 * 4; //   and the block-combination scratch [32][33]
+constexpr int SMEM_BYTES = OFF_V + 32768;
+constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for the 1024-byte alignment
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+static_assert(64 * 65 * 4 <= 32768, "fp32 A staging fits the fp16 state tile");
+static_assert(OFF_M + 32 * 33 * 4 <= OFF_V + 32768, "fp32 T staging fits the v tile");
+
+// Byte offset of element (row, k) in a K-major, 128-byte swizzled fp16 tile with R rows.
+__device__ __forceinline__ uint32_t sw(int row, int k, int R) {
+    const int kb = k >> 6, kk = k & 63;
+    return (uint32_t)(kb * R * 128 + row * 128 + ((((kk >> 3) ^ (row & 7)) & 7) << 4) + (kk & 7) * 2);
+}
+
+__device__ __forceinline__ void st_h(uint8_t *base, uint32_t off, float x) {
+    *reinterpret_cast<__half *>(base + off) = __float2half_rn(x);
+}
+
+// Four consecutive elements (k % 4 == 0) of one row: one 8-byte store.
+__device__ __forceinline__ void st_h4(uint8_t *base, uint32_t off, float a, float b, float c, float d) {
+    __half2 lo = __floats2half2_rn(a, b), hi = __floats2half2_rn(c, d);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t *>(&lo);
+    v.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(base + off) = v;
+}
+
+template <typename T>
+__device__ __forceinline__ void ld4(const T *p, float (&v)[4]);
+template <>
+__device__ __forceinline__ void ld4<float>(const float *p, float (&v)[4]) {
+    const float4 x = *reinterpret_cast<const float4 *>(p);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+template <>
+__device__ __forceinline__ void ld4<__half>(const __half *p, float (&v)[4]) {
+    const uint2 x = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&x.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&x.y));
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+
+// Unit lower-triangular inverse T = (I + A)^-1 of a 64 x 64 strictly lower A
+// (row stride 65, fp32, shared).  Writes the strictly lower part of T into
+// T32 (row stride 65); the diagonal is 1 and the upper part 0 implicitly.
+__device__ void tri_inverse(const float *A, float *T32, float *M, int tid) {
+    // level 0: the four 16 x 16 diagonal blocks, one column per thread
+    if (tid < 64) {
+        const int blk = tid >> 4, c = tid & 15, o = blk * 16;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int s = 0; s < r; ++s) acc = fmaf(A[(o + r) * 65 + o + s], x[s], acc);
+            x[r] = (r < c) ? 0.f : (r == c ? 1.f : -acc);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            if (r > c) T32[(o + r) * 65 + o + c] = x[r];
+    }
+    __syncthreads();
+    // level 1: 32 x 32 blocks at 0 and 32:  T21 = -T22 A21 T11  (16 x 16 each)
+    {
+        // M = A21 T11 for both pairs: 2 x 256 entries
+        for (int e = tid; e < 512; e += NT) {
+            const int p = e >> 8, r = (e >> 4) & 15, c = e & 15, o = 32 * p;
+            float acc = A[(o + 16 + r) * 65 + o + c];  // s = c term, T11[c][c] = 1
+            for (int s = c + 1; s < 16; ++s) acc = fmaf(A[(o + 16 + r) * 65 + o + s], T32[(o + s) * 65 + o + c], acc);
+            M[p * 272 + r * 17 + c] = acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < 512; e += NT) {
+            const int p = e >> 8, r = (e >> 4) & 15, c = e & 15, o = 32 * p;
+            float acc = M[p * 272 + r * 17 + c];  // s = r term, T22[r][r] = 1
+            for (int s = 0; s < r; ++s) acc = fmaf(T32[(o + 16 + r) * 65 + o + 16 + s], M[p * 272 + s * 17 + c], acc);
+            T32[(o + 16 + r) * 65 + o + c] = -acc;
+        }
+        __syncthreads();
+    }
+    // level 2: T21 = -T22 A21 T11 with 32 x 32 blocks
+    {
+        for (int e = tid; e < 1024; e += NT) {
+            const int r = e >> 5, c = e & 31;
+            float acc = A[(32 + r) * 65 + c];
+            for (int s = c + 1; s < 32; ++s) acc = fmaf(A[(32 + r) * 65 + s], T32[s * 65 + c], acc);
+            M[r * 33 + c] = acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < 1024; e += NT) {
+            const int r = e >> 5, c = e & 31;
+            float acc = M[r * 33 + c];
+            for (int s = 0; s < r; ++s) acc = fmaf(T32[(32 + r) * 65 + 32 + s], M[s * 33 + c], acc);
+            T32[(32 + r) * 65 + c] = -acc;
+        }
+        __syncthreads();
+    }
+}
+
+struct Shared {
+    float Gam[CH], gam[CH], beta[CH], gate[CH];
+    uint64_t bar;
+    uint32_t tmem;
+    int item;
+};
+
+template <typename TIO>
+__global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, int32_t *ws) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ Shared sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;  // the tensor-memory lane this thread reads
+    const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
+
+    float *V_s = reinterpret_cast<float *>(sm + OFF_V);
+    float *A32 = reinterpret_cast<float *>(sm + OFF_A32);
+    float *T32 = reinterpret_cast<float *>(sm + OFF_T32);
+    float *Mws = reinterpret_cast<float *>(sm + OFF_M);
+    const uint32_t a_KQ = ptx::smem_u32(sm + OFF_KQ), a_GQ = ptx::smem_u32(sm + OFF_GQ);
+    const uint32_t a_KT = ptx::smem_u32(sm + OFF_KT), a_S16 = ptx::smem_u32(sm + OFF_S16);
+    const uint32_t a_RT = ptx::smem_u32(sm + OFF_RT), a_UD = ptx::smem_u32(sm + OFF_UD);
+    const uint32_t a_T = ptx::smem_u32(sm + OFF_T), a_PD = ptx::smem_u32(sm + OFF_PD);
+
+    if (warp == 0) {
+        ptx::tmem_alloc(&sh.tmem, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if (tid == 0) {
+        ptx::mbar_init(&sh.bar, 1);
+        ptx::fence_mbar_init();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tm = sh.tmem;
+    uint32_t phase = 0;
+    bool failed = false;
+
+    // waits for the MMAs committed so far; false on time-out (reported, then the CTA stops)
+    auto mma_wait = [&]() -> bool {
+        const bool ok = ptx::mbar_wait_bounded(&sh.bar, phase, WAIT_LIMIT);
+        phase ^= 1u;
+        ptx::tc_fence_after();
+        return __syncthreads_and(ok);
+    };
+    auto mma_ready = [&]() {  // make this thread's smem / tmem writes visible to the next MMA
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+    };
+
+    const int n_items = ws[1] * p.Hv;
+    const TIO *qg = static_cast<const TIO *>(p.q);
+    const TIO *kg = static_cast<const TIO *>(p.k);
+    const TIO *vg = static_cast<const TIO *>(p.v);
+    TIO *og = static_cast<TIO *>(p.out);
+    const long long ubase = (long long)p.Hv + (long long)p.Hk * DH;
+
+    while (!failed) {
+        if (tid == 0) sh.item = atomicAdd(&ws[0], 1);
+        __syncthreads();
+        const int item = sh.item;
+        __syncthreads();
+        if (item >= n_items) break;
+        const int b = ws[2 + item / p.Hv], h = item % p.Hv, kh = h / p.r;
+        const int bos = p.cu[b], eos = p.cu[b + 1];
+        const int slot = p.slots ? p.slots[b] : b;
+        if (slot < 0 || slot >= p.num_slots) {
+            if (tid == 0 && h == 0) flag_error(p.status, GDN_DEVERR_STATE_SLOT);
+            continue;
+        }
+        const size_t head_off = ((size_t)slot * p.Hv + h) * (size_t)DH * DH;
+        const bool has_init = p.init != nullptr;
+
+        // ---- chain start: the initial state into tensor memory
+        if (has_init) {
+            const float *src = p.init + head_off + (size_t)row * DH + half * 64;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(src + c * 32 + j);
+                    v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
+                }
+                ptx::tmem_st32(tm + lane_sel + TM_S + half * 64 + c * 32, v);
+            }
+            ptx::tmem_st_wait();
+        }
+        bool state_live = has_init;  // does TM_S hold the state (else it is zero)?
+
+        for (int t0 = bos; t0 < eos && !failed; t0 += CH) {
+            const int n = min(CH, eos - t0);
+            // ---- A1: gates and the within-chunk cumulative log decay (warp 0)
+            if (warp == 0) {
+                float lg[2], bt[2], gt[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int s = lane + 32 * u;
+                    lg[u] = 0.f; bt[u] = 0.f; gt[u] = 1.f;
+                    if (s < n) {
+                        const long long t = t0 + s;
+                        const float av = p.a[t * p.Hv + h], bv = p.b[t * p.Hv + h];
+                        if (p.gate_raw) {
+                            const float l = -expf(p.A_log[h]) * softplus_f(av + p.dt_bias[h]);
+                            gt[u] = expf(l);
+                            lg[u] = fmaxf(l, LOG_DECAY_FLOOR);
+                            bt[u] = 1.f / (1.f + expf(-bv));
+                        } else {
+                            gt[u] = av;
+                            lg[u] = av > 0.f ? fmaxf(logf(av), LOG_DECAY_FLOOR) : LOG_DECAY_FLOOR;
+                            bt[u] = bv;
+                        }
+                    }
+                }
+                float c0 = lg[0], c1 = lg[1];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y0 = __shfl_up_sync(0xffffffffu, c0, o);
+                    const float y1 = __shfl_up_sync(0xffffffffu, c1, o);
+                    if (lane >= o) { c0 += y0; c1 += y1; }
+                }
+                c1 += __shfl_sync(0xffffffffu, c0, 31);
+                sh.Gam[lane] = c0;
+                sh.Gam[lane + 32] = c1;
+                sh.gam[lane] = expf(c0);
+                sh.gam[lane + 32] = expf(c1);
+                sh.beta[lane] = bt[0];
+                sh.beta[lane + 32] = bt[1];
+                sh.gate[lane] = gt[0];
+                sh.gate[lane + 32] = gt[1];
+                if (p.caps) {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int s = lane + 32 * u, tl = t0 + s - bos;
+                        if (s < n && tl < p.cap) p.caps[((long long)b * p.cap + tl) * p.W + h] = gt[u];
+                    }
+                }
+            }
+            // ---- A2: v rows (fp32) of the chunk
+            for (int e = tid; e < CH * (DH / 4); e += NT) {
+                const int s = e >> 5, c4 = (e & 31) * 4;
+                float v[4] = {0.f, 0.f, 0.f, 0.f};
+                if (s < n) ld4<TIO>(vg + (long long)(t0 + s) * p.v_stride + (long long)h * DH + c4, v);
+                *reinterpret_cast<float4 *>(V_s + s * DH + c4) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+            __syncthreads();
+            // ---- A3: normalised k and q into the operand tiles (one warp per token)
+            for (int s = warp; s < CH; s += NT / 32) {
+                float qv[4] = {0.f, 0.f, 0.f, 0.f}, kv[4] = {0.f, 0.f, 0.f, 0.f};
+                if (s < n) {
+                    const long long t = t0 + s;
+                    ld4<TIO>(qg + t * p.q_stride + (long long)kh * DH + lane * 4, qv);
+                    ld4<TIO>(kg + t * p.k_stride + (long long)kh * DH + lane * 4, kv);
+                }
+                float sq = 0.f, sk = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    sq = fmaf(qv[e], qv[e], sq);
+                    sk = fmaf(kv[e], kv[e], sk);
+                }
+                sq = warp_sum(sq);
+                sk = warp_sum(sk);
+                const float nq = fmaxf(sqrtf(sq), EPS), nk = fmaxf(sqrtf(sk), EPS);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    qv[e] = qv[e] / nq;
+                    kv[e] = kv[e] / nk;
+                }
+                const int c = lane * 4;
+                st_h4(sm + OFF_KQ, sw(s, c, 128), kv[0], kv[1], kv[2], kv[3]);
+                st_h4(sm + OFF_KQ, sw(64 + s, c, 128), qv[0], qv[1], qv[2], qv[3]);
+                const float gm = sh.gam[s];
+                st_h4(sm + OFF_GQ, sw(s, c, 64), gm * qv[0], gm * qv[1], gm * qv[2], gm * qv[3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) st_h(sm + OFF_KT, sw(c + e, s, 128), kv[e]);
+                const int tl = t0 + s - bos;
+                if (p.caps && h % p.r == 0 && s < n && tl < p.cap) {
+                    float *dst = p.caps + ((long long)b * p.cap + tl) * p.W + p.Hv + (long long)kh * DH + c;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dst[e] = kv[e];
+                }
+            }
+            // ---- B: S0 -> fp16 operand tile; the tensor-memory state becomes gamma_last S0
+            {
+                const float gl = sh.gam[n - 1];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int col = half * 64 + c * 32;
+                    float v[32];
+                    if (state_live) {
+                        ptx::tmem_ld32(tm + lane_sel + TM_S + col, v);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) st_h4(sm + OFF_S16, sw(row, col + j, 128), v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    if (state_live) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] *= gl;
+                        ptx::tmem_st32(tm + lane_sel + TM_S + col, v);
+                    }
+                }
+                if (state_live) ptx::tmem_st_wait();
+            }
+            mma_ready();
+            // ---- C: MMA1 and MMA2
+            if (tid == 0) {
+                ptx::tc_fence_after();
+                const uint32_t i64 = ptx::idesc_f16_f32(128, 64);
+                for (int ks = 0; ks < DH / 16; ++ks) {
+                    const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    const uint64_t dKQ = ptx::sdesc_k_sw128(a_KQ + ko);
+                    ptx::mma_f16(tm + TM_D1, dKQ, dKQ, i64, ks > 0);
+                    ptx::mma_f16(tm + TM_X, ptx::sdesc_k_sw128(a_S16 + ko), dKQ, i64, ks > 0);
+                    ptx::mma_f16(tm + TM_O, ptx::sdesc_k_sw128(a_S16 + ko),
+                                 ptx::sdesc_k_sw128(a_GQ + (ks >> 2) * 8192 + (ks & 3) * 32), i64, ks > 0);
+                }
+                ptx::mma_commit(&sh.bar);
+            }
+            if (!mma_wait()) { failed = true; break; }
+            // ---- D1: A (fp32 staging) and P o D (fp16 tile) from G and P; R^T from X^T
+            {
+                float v[32];
+                ptx::tmem_ld32(tm + lane_sel + TM_D1 + half * 32, v);
+                const int r = row & 63;
+                const float Gr = sh.Gam[r];
+                if (quarter < 2) {
+                    const float br = sh.beta[r];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int s = half * 32 + j;
+                        A32[r * 65 + s] = (s < r) ? br * __expf(Gr - sh.Gam[s]) * v[j] : 0.f;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        float w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int s = half * 32 + j + e;
+                            w[e] = (s <= r) ? v[j + e] * __expf(Gr - sh.Gam[s]) : 0.f;
+                        }
+                        st_h4(sm + OFF_PD, sw(r, half * 32 + j, 64), w[0], w[1], w[2], w[3]);
+                    }
+                }
+                ptx::tmem_ld32(tm + lane_sel + TM_X + half * 32, v);
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    float w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = half * 32 + j + e;
+                        w[e] = sh.beta[s] * (V_s[s * DH + row] - sh.gam[s] * v[j + e]);
+                    }
+                    st_h4(sm + OFF_RT, sw(row, half * 32 + j, 128), w[0], w[1], w[2], w[3]);
+                }
+            }
+            __syncthreads();
+            // ---- D2: T = (I + A)^-1 on the CUDA cores, then its fp16 tile
+            tri_inverse(A32, T32, Mws, tid);
+            for (int e = tid; e < CH * CH / 4; e += NT) {
+                const int r = e >> 4, s0 = (e & 15) * 4;
+                float w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int s = s0 + u;
+                    w[u] = s < r ? T32[r * 65 + s] : (s == r ? 1.f : 0.f);
+                }
+                st_h4(sm + OFF_T, sw(r, s0, 64), w[0], w[1], w[2], w[3]);
+            }
+            mma_ready();
+            // ---- E: MMA3  U^T = R^T T^T
+            if (tid == 0) {
+                ptx::tc_fence_after();
+                const uint32_t i64 = ptx::idesc_f16_f32(128, 64);
+                for (int ks = 0; ks < CH / 16; ++ks)
+                    ptx::mma_f16(tm + TM_D3, ptx::sdesc_k_sw128(a_RT + ks * 32), ptx::sdesc_k_sw128(a_T + ks * 32),
+                                 i64, ks > 0);
+                ptx::mma_commit(&sh.bar);
+            }
+            if (!mma_wait()) { failed = true; break; }
+            // ---- F: U^T -> fp16 operands (plain and decayed to the chunk end); capsule deltas
+            {
+                float v[32];
+                ptx::tmem_ld32(tm + lane_sel + TM_D3 + half * 32, v);
+                const float Gl = sh.Gam[n - 1];
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    float w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) w[e] = __expf(Gl - sh.Gam[half * 32 + j + e]) * v[j + e];
+                    st_h4(sm + OFF_RT, sw(row, half * 32 + j, 128), v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    st_h4(sm + OFF_UD, sw(row, half * 32 + j, 128), w[0], w[1], w[2], w[3]);
+                }
+                if (p.caps) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int s = half * 32 + j, tl = t0 + s - bos;
+                        if (s < n && tl < p.cap)
+                            p.caps[((long long)b * p.cap + tl) * p.W + ubase + (long long)h * DH + row] = v[j];
+                    }
+                }
+            }
+            mma_ready();
+            // ---- G: MMA4 (output) and MMA5 (state)
+            if (tid == 0) {
+                ptx::tc_fence_after();
+                const uint32_t i64 = ptx::idesc_f16_f32(128, 64), i128 = ptx::idesc_f16_f32(128, 128);
+                for (int ks = 0; ks < CH / 16; ++ks) {
+                    ptx::mma_f16(tm + TM_O, ptx::sdesc_k_sw128(a_RT + ks * 32), ptx::sdesc_k_sw128(a_PD + ks * 32),
+                                 i64, 1u);
+                    ptx::mma_f16(tm + TM_S, ptx::sdesc_k_sw128(a_UD + ks * 32), ptx::sdesc_k_sw128(a_KT + ks * 32),
+                                 i128, (state_live || ks > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(&sh.bar);
+            }
+            if (!mma_wait()) { failed = true; break; }
+            state_live = true;
+            // ---- H: outputs
+            {
+                float v[32];
+                ptx::tmem_ld32(tm + lane_sel + TM_O + half * 32, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int r = half * 32 + j;
+                    if (r < n) og[((long long)(t0 + r) * p.Hv + h) * DH + row] = from_f32<TIO>(p.scale * v[j]);
+                }
+            }
+            ptx::tc_fence_before();
+            __syncthreads();
+            ptx::tc_fence_after();
+        }
+        if (failed) break;
+        // ---- chain end: the final state
+        {
+            float *dst = p.final_state + head_off + (size_t)row * DH + half * 64;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float v[32];
+                if (state_live) {
+                    ptx::tmem_ld32(tm + lane_sel + TM_S + half * 64 + c * 32, v);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(dst + c * 32 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+        ptx::tc_fence_after();
+    }
+
+    if (failed && tid == 0) {
+        flag_error(p.status, GDN_DEVERR_TIMEOUT);
+        ptx::mbar_wait_bounded(&sh.bar, phase ^ 1u, WAIT_LIMIT);  // let in-flight MMAs drain
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tm, TMEM_COLS);
+    }
+}
+
+// Builds the chain list: ws[0] = 0 (work counter), ws[1] = number of
+// sequences on this path, ws[2..] = those sequences, longest first (counting
+// sort on the number of chunks).  Sequences with a bad packing are left out
+// (the recurrent kernel reports them).
+constexpr int PLAN_BINS = 1024;
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *cu, int B, int T, int min_len, int32_t *ws) {
+    __shared__ int hist[PLAN_BINS];
+    __shared__ int total;
+    const int tid = threadIdx.x;
+    for (int i = tid; i < PLAN_BINS; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    auto key = [&](int b) -> int {
+        const int lo = cu[b], hi = cu[b + 1];
+        if (lo < 0 || hi < lo || hi > T || hi - lo <= min_len) return -1;
+        const int chunks = min((hi - lo + CH - 1) / CH, PLAN_BINS - 1);
+        return PLAN_BINS - 1 - chunks;  // descending length
+    };
+    for (int b = tid; b < B; b += blockDim.x) {
+        const int k = key(b);
+        if (k >= 0) atomicAdd(&hist[k], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {  // exclusive scan (1024 bins, once per call)
+        int run = 0;
+        for (int i = 0; i < PLAN_BINS; ++i) {
+            const int c = hist[i];
+            hist[i] = run;
+            run += c;
+        }
+        total = run;
+    }
+    __syncthreads();
+    for (int b = tid; b < B; b += blockDim.x) {
+        const int k = key(b);
+        if (k >= 0) ws[2 + atomicAdd(&hist[k], 1)] = b;
+    }
+    if (tid == 0) {
+        ws[0] = 0;
+        ws[1] = total;
+    }
+}
+
+int num_sms() {
+    static int cached = 0;
+    if (cached == 0) {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            cached = n;
+        else
+            cached = 148;
+    }
+    return cached;
+}
+
+template <typename TIO>
+cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStream_t stream) {
+    plan_kernel<<<1, 1024, 0, stream>>>(p.cu, p.B, p.T, min_len, ws);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    auto kern = chunked_kernel<TIO>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    const long long chains = (long long)p.B * p.Hv;
+    const int grid = (int)(chains < num_sms() ? chains : num_sms());
+    kern<<<grid, NT, SMEM_ALLOC, stream>>>(p, ws);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t chunked_workspace_bytes(int B) { return ((size_t)(B + 2) * sizeof(int32_t) + 255) & ~size_t(255); }
+
+bool chunked_supported(int dk, int dv) { return dk == DH && dv == DH; }
+
+cudaError_t launch_chunked(const ForwardParams &p, int min_len, void *workspace, cudaStream_t stream) {
+    if (p.B == 0) return cudaSuccess;
+    int32_t *ws = static_cast<int32_t *>(workspace);
+    return p.io_f16 ? launch_io<__half>(p, min_len, ws, stream) : launch_io<float>(p, min_len, ws, stream);
+}
+
+}  // namespace gdn

@@ -42,6 +42,17 @@ struct ReplayParams {
 cudaError_t launch_recurrent(const ForwardParams &p, cudaStream_t stream);
 cudaError_t launch_replay(const ReplayParams &p, cudaStream_t stream);
 
+// Chunked tensor-core path: sequences with more than `min_len` tokens
+// (min_len < 0: every sequence).  Needs chunked_workspace_bytes(B) of
+// device workspace (the chain list and its work counter).
+bool chunked_supported(int dk, int dv);
+size_t chunked_workspace_bytes(int B);
+cudaError_t launch_chunked(const ForwardParams &p, int min_len, void *workspace, cudaStream_t stream);
+
+// Sequences up to this many tokens stay on the recurrent kernel under the
+// automatic plan; longer ones go to the chunked kernel.
+constexpr int RECURRENT_MAX_LEN = 32;
+
 // ---------------------------------------------------------------- device helpers
 
 __device__ __forceinline__ float to_f32(float x) { return x; }

@@ -57,9 +57,11 @@ enum {
 
 /* Which kernel evaluates a sequence. */
 enum {
-    GDN_PLAN_AUTO = 0,       /* per sequence: short spans recurrent, long spans chunked */
+    GDN_PLAN_AUTO = 0,       /* per sequence: up to 32 tokens recurrent, longer ones chunked
+                                (chunked needs dk = dv = 128 and 16-byte aligned q, k, v) */
     GDN_PLAN_RECURRENT = 1,  /* every sequence on the token-by-token kernel */
-    GDN_PLAN_CHUNKED = 2     /* every sequence on the tensor-core chunked kernel */
+    GDN_PLAN_CHUNKED = 2     /* every sequence on the tensor-core chunked kernel
+                                (dk = dv = 128 only, else GDN_ERR_UNSUPPORTED) */
 };
 
 /* Bits of the device status word. */
@@ -123,6 +125,11 @@ typedef struct gdn_forward_args {
     int32_t plan;                  /* GDN_PLAN_* */
     float scale;                   /* output scale; 0 means 1/sqrt(dk) */
     int32_t state_update_capacity; /* capsule rows per sequence; 0 = not emitted */
+    int32_t max_seqlen;            /* upper bound on the longest sequence, 0 = unknown (T).
+                                      A performance hint: under GDN_PLAN_AUTO a bound of
+                                      at most 32 keeps every sequence on the recurrent
+                                      kernel and skips the chunked launches.  Results do
+                                      not depend on it. */
     int64_t q_stride;
     int64_t k_stride;
     int64_t v_stride;
@@ -145,8 +152,12 @@ typedef struct gdn_forward_args {
 } gdn_forward_args;
 
 /*
- * Bytes of device workspace gdn_forward needs for these arguments (sizes and
- * plan only are read).  Returns GDN_OK and writes *bytes, or an argument error.
+ * Bytes of device workspace gdn_forward needs for these arguments (sizes,
+ * plan and max_seqlen only are read).  Non-zero exactly when the chunked
+ * kernel may run; it then holds the chunked kernel's longest-first list of
+ * sequences and its work counter ((B + 2) int32, rounded up to 256 bytes).
+ * The workspace must be 16-byte aligned and not shared by calls that overlap
+ * on the GPU.  Returns GDN_OK and writes *bytes, or an argument error.
  */
 gdn_status gdn_forward_workspace_size(const gdn_forward_args *args, size_t *bytes);
 

@@ -20,7 +20,7 @@ def to_dev(x, dtype=None):
 
 
 def run_gpu(inp, *, plan="auto", capacity=None, gate_mode="raw", a=None, b=None, in_place=True,
-            status=None, final_state=None):
+            status=None, final_state=None, max_seqlen=0):
     """Runs gdn_forward on ``inp`` (a workloads.GdnInputs); returns numpy arrays."""
     import gated_delta_rule_gateddeltanet_gb300 as gdn
     cap = inp.capacity if capacity is None else capacity
@@ -39,7 +39,7 @@ def run_gpu(inp, *, plan="auto", capacity=None, gate_mode="raw", a=None, b=None,
         to_dev(inp.b if b is None else b), to_dev(inp.cu_seqlens), A_log=to_dev(inp.A_log),
         dt_bias=to_dev(inp.dt_bias), gate_mode=gate_mode, initial_state=init, final_state=final_state,
         state_slots=to_dev(inp.state_slots), capacity=cap, plan=plan, status=status,
-        num_state_slots=final_state.shape[0])
+        num_state_slots=final_state.shape[0], max_seqlen=max_seqlen)
     torch.cuda.synchronize()
     return (out.double().cpu().numpy(), final.double().cpu().numpy(),
             None if caps is None else caps.double().cpu().numpy())

@@ -129,3 +129,31 @@ def test_capsule_width_matches_pages_geometry():
     import gated_delta_rule_gateddeltanet_gb300 as g
     # 48 value heads, 16 key heads, d = 128: 8240 floats = 32,960 bytes per token-layer
     assert g.capsule_width(16, 48, 128, 128) * 4 == 32960
+
+
+def test_workspace_size_follows_the_plan(lib):
+    n = ctypes.c_size_t(0)
+    # decode-sized batch (T <= 32): recurrent only, no workspace
+    a = _args(num_seqs=16, total_tokens=16, num_state_slots=16)
+    assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 0
+    # long batch at d = 128: the chunked kernel may run -> (B + 2) int32 rounded to 256 bytes
+    a = _args(num_seqs=8, total_tokens=17000, num_state_slots=8)
+    assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 256
+    a = _args(num_seqs=100, total_tokens=17000, num_state_slots=100)
+    assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 512
+    # a max_seqlen hint of at most 32 keeps the batch recurrent
+    a = _args(num_seqs=64, total_tokens=64, num_state_slots=64, max_seqlen=1)
+    assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 0
+    # forced recurrent plan: none; other head dims: none (recurrent only)
+    a = _args(num_seqs=8, total_tokens=17000, num_state_slots=8, plan=1)
+    assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 0
+    a = _args(num_seqs=8, total_tokens=17000, num_state_slots=8, head_dim_k=64)
+    assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 0
+
+
+def test_forced_chunked_plan_needs_d128_and_workspace(lib):
+    assert lib.gdn_forward(ctypes.byref(_args(plan=2, head_dim_k=64)), None) == 7
+    assert lib.gdn_forward(ctypes.byref(_args(plan=2, head_dim_v=32)), None) == 7
+    assert lib.gdn_forward(ctypes.byref(_args(max_seqlen=-1)), None) == 3
+    # forced chunked plan without workspace
+    assert lib.gdn_forward(ctypes.byref(_args(plan=2)), None) == 5
