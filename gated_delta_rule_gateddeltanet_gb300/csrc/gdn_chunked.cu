@@ -69,9 +69,12 @@ constexpr int OFF_PD = OFF_T + 8192;       // [64][64]: P o D                   
 constexpr int OFF_V = OFF_PD + 8192;       // [64][128] fp32 v                          32 KiB
 constexpr int OFF_T32 = OFF_V;             //   reused once R^T is built: T in fp32 [64][65]
 constexpr int OFF_M = OFF_V + 64 * 65 * 4; //   and the block-combination scratch [32][33]
-constexpr int SMEM_BYTES = OFF_V + 32768;
-constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for the 1024-byte alignment
-static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+constexpr int OFF_STG = OFF_V + 32768;     // fp16 I/O: raw q, k, v rows of the next chunk  48 KiB
+constexpr int STG_BYTES = 3 * CH * DH * 2;
+// fp16 I/O stages the next chunk through shared memory; fp32 I/O loads directly.
+template <typename TIO>
+constexpr int smem_alloc() { return OFF_STG + (sizeof(TIO) == 2 ? STG_BYTES : 0) + 1024; }  // + alignment slack
+static_assert(OFF_STG + STG_BYTES + 1024 + 2048 <= 227 * 1024, "shared memory budget (dynamic + static)");
 static_assert(64 * 65 * 4 <= 32768, "fp32 A staging fits the fp16 state tile");
 static_assert(OFF_M + 32 * 33 * 4 <= OFF_V + 32768, "fp32 T staging fits the v tile");
 
@@ -168,7 +171,8 @@ __device__ void tri_inverse(const float *A, float *T32, float *M, int tid) {
 
 struct Shared {
     float Gam[CH], gam[CH], beta[CH], gate[CH];
-    uint64_t bar;
+    uint64_t bar;   // MMA completion
+    uint64_t lbar;  // staged rows of the next chunk
     uint32_t tmem;
     int item;
 };
@@ -198,14 +202,17 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
     }
     if (tid == 0) {
         ptx::mbar_init(&sh.bar, 1);
+        ptx::mbar_init(&sh.lbar, 1);
         ptx::fence_mbar_init();
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tm = sh.tmem;
-    uint32_t phase = 0;
-    bool failed = false;
+    uint32_t phase = 0, lphase = 0;
+    bool failed = false, load_pending = false;
+    constexpr bool STAGED = sizeof(TIO) == 2;
+    uint8_t *stg = sm + OFF_STG;
 
     // waits for the MMAs committed so far; false on time-out (reported, then the CTA stops)
     auto mma_wait = [&]() -> bool {
@@ -243,6 +250,40 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
         const size_t head_off = ((size_t)slot * p.Hv + h) * (size_t)DH * DH;
         const bool has_init = p.init != nullptr;
 
+        // Bulk copies of the q, k, v rows of the chunk starting at token tc into
+        // the staging area (row s of tensor j at stg + j*16 KiB + s*256 B).
+        auto prefetch = [&](int tc) {
+            const int nn = min(CH, eos - tc);
+            if (tid == 0) ptx::mbar_arrive_expect_tx(&sh.lbar, (uint32_t)(3 * nn * DH * 2));
+            if (tid < 3 * CH) {
+                const int j = tid / CH, s = tid % CH;
+                if (s < nn) {
+                    const long long t = tc + s;
+                    const TIO *src = j == 0 ? qg + t * p.q_stride + (long long)kh * DH
+                                   : j == 1 ? kg + t * p.k_stride + (long long)kh * DH
+                                            : vg + t * p.v_stride + (long long)h * DH;
+                    ptx::bulk_g2s(stg + j * (CH * DH * 2) + s * (DH * 2), src, DH * 2, &sh.lbar);
+                }
+            }
+        };
+        // raw gate inputs of the chunk starting at tc, two tokens per lane of warp 0
+        float ga[2] = {0.f, 0.f}, gb[2] = {0.f, 0.f};
+        auto prefetch_gates = [&](int tc) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const long long t = tc + lane + 32 * u;
+                if (t < eos) {
+                    ga[u] = p.a[t * p.Hv + h];
+                    gb[u] = p.b[t * p.Hv + h];
+                }
+            }
+        };
+        if (STAGED && bos < eos) {
+            prefetch(bos);
+            load_pending = true;
+        }
+        if (warp == 0 && bos < eos) prefetch_gates(bos);
+
         // ---- chain start: the initial state into tensor memory
         if (has_init) {
             const float *src = p.init + head_off + (size_t)row * DH + half * 64;
@@ -270,8 +311,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                     const int s = lane + 32 * u;
                     lg[u] = 0.f; bt[u] = 0.f; gt[u] = 1.f;
                     if (s < n) {
-                        const long long t = t0 + s;
-                        const float av = p.a[t * p.Hv + h], bv = p.b[t * p.Hv + h];
+                        const float av = ga[u], bv = gb[u];
                         if (p.gate_raw) {
                             const float l = -expf(p.A_log[h]) * softplus_f(av + p.dt_bias[h]);
                             gt[u] = expf(l);
@@ -284,6 +324,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                         }
                     }
                 }
+                if (t0 + CH < eos) prefetch_gates(t0 + CH);  // in flight for the rest of the chunk
                 float c0 = lg[0], c1 = lg[1];
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -308,11 +349,22 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                     }
                 }
             }
+            if (STAGED) {
+                const bool ok = ptx::mbar_wait_bounded(&sh.lbar, lphase, WAIT_LIMIT);
+                lphase ^= 1u;
+                load_pending = false;
+                if (!__syncthreads_and(ok)) { failed = true; break; }
+            }
             // ---- A2: v rows (fp32) of the chunk
             for (int e = tid; e < CH * (DH / 4); e += NT) {
                 const int s = e >> 5, c4 = (e & 31) * 4;
                 float v[4] = {0.f, 0.f, 0.f, 0.f};
-                if (s < n) ld4<TIO>(vg + (long long)(t0 + s) * p.v_stride + (long long)h * DH + c4, v);
+                if (s < n) {
+                    if (STAGED)
+                        ld4<TIO>(reinterpret_cast<const TIO *>(stg + 2 * CH * DH * 2 + s * DH * 2) + c4, v);
+                    else
+                        ld4<TIO>(vg + (long long)(t0 + s) * p.v_stride + (long long)h * DH + c4, v);
+                }
                 *reinterpret_cast<float4 *>(V_s + s * DH + c4) = make_float4(v[0], v[1], v[2], v[3]);
             }
             __syncthreads();
@@ -320,9 +372,14 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
             for (int s = warp; s < CH; s += NT / 32) {
                 float qv[4] = {0.f, 0.f, 0.f, 0.f}, kv[4] = {0.f, 0.f, 0.f, 0.f};
                 if (s < n) {
-                    const long long t = t0 + s;
-                    ld4<TIO>(qg + t * p.q_stride + (long long)kh * DH + lane * 4, qv);
-                    ld4<TIO>(kg + t * p.k_stride + (long long)kh * DH + lane * 4, kv);
+                    if (STAGED) {
+                        ld4<TIO>(reinterpret_cast<const TIO *>(stg + s * DH * 2) + lane * 4, qv);
+                        ld4<TIO>(reinterpret_cast<const TIO *>(stg + CH * DH * 2 + s * DH * 2) + lane * 4, kv);
+                    } else {
+                        const long long t = t0 + s;
+                        ld4<TIO>(qg + t * p.q_stride + (long long)kh * DH + lane * 4, qv);
+                        ld4<TIO>(kg + t * p.k_stride + (long long)kh * DH + lane * 4, kv);
+                    }
                 }
                 float sq = 0.f, sk = 0.f;
 #pragma unroll
@@ -389,6 +446,11 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                                  ptx::sdesc_k_sw128(a_GQ + (ks >> 2) * 8192 + (ks & 3) * 32), i64, ks > 0);
                 }
                 ptx::mma_commit(&sh.bar);
+            }
+            // the staging area is consumed: fetch the next chunk while this one computes
+            if (STAGED && t0 + CH < eos) {
+                prefetch(t0 + CH);
+                load_pending = true;
             }
             if (!mma_wait()) { failed = true; break; }
             // ---- D1: A (fp32 staging) and P o D (fp16 tile) from G and P; R^T from X^T
@@ -529,6 +591,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
     if (failed && tid == 0) {
         flag_error(p.status, GDN_DEVERR_TIMEOUT);
         ptx::mbar_wait_bounded(&sh.bar, phase ^ 1u, WAIT_LIMIT);  // let in-flight MMAs drain
+        if (load_pending) ptx::mbar_wait_bounded(&sh.lbar, lphase, WAIT_LIMIT);  // and staged copies
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -598,11 +661,12 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStre
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto kern = chunked_kernel<TIO>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    constexpr int smem = smem_alloc<TIO>();
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long long chains = (long long)p.B * p.Hv;
     const int grid = (int)(chains < num_sms() ? chains : num_sms());
-    kern<<<grid, NT, SMEM_ALLOC, stream>>>(p, ws);
+    kern<<<grid, NT, smem, stream>>>(p, ws);
     return cudaGetLastError();
 }
 
