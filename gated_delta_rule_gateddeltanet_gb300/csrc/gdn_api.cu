@@ -51,10 +51,12 @@ bool wants_chunked(const gdn_forward_args *a) {
     return a->plan == GDN_PLAN_CHUNKED || longest > gdn::RECURRENT_MAX_LEN;
 }
 
-// The chunked kernel reads q, k, v with 8- or 16-byte vector loads.
+// The chunked kernel moves q, k, v rows with bulk copies and writes output
+// rows in 16-byte pieces.
 bool chunked_aligned(const gdn_forward_args *a, const gdn::ForwardParams &p) {
     const size_t esz = p.io_f16 ? 2 : 4;
-    return aligned16(a->q) && aligned16(a->k) && aligned16(a->v) && (p.q_stride * esz) % 16 == 0 &&
+    return aligned16(a->q) && aligned16(a->k) && aligned16(a->v) && aligned16(a->output) &&
+           (p.q_stride * esz) % 16 == 0 &&
            (p.k_stride * esz) % 16 == 0 && (p.v_stride * esz) % 16 == 0;
 }
 

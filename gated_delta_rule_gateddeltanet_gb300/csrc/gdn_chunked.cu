@@ -67,8 +67,8 @@ constexpr int OFF_UD = OFF_RT + 16384;     // [128][64]: U^T diag(exp(Gamma_last
 constexpr int OFF_T = OFF_UD + 16384;      // [64][64]: T                               8 KiB
 constexpr int OFF_PD = OFF_T + 8192;       // [64][64]: P o D                           8 KiB
 constexpr int OFF_V = OFF_PD + 8192;       // [64][128] fp32 v                          32 KiB
-constexpr int OFF_T32 = OFF_V;             //   reused once R^T is built: T in fp32 [64][65]
-constexpr int OFF_M = OFF_V + 64 * 65 * 4; //   and the block-combination scratch [32][33]
+constexpr int OFF_T32 = OFF_V;             //   reused once R^T is built: T in fp32 [64][68]
+constexpr int OFF_M = OFF_V + 64 * 68 * 4; //   and the block-combination scratch [32][36]
 constexpr int OFF_STG = OFF_V + 32768;     // fp16 I/O: raw q, k, v rows of the next chunk  48 KiB
 constexpr int STG_BYTES = 3 * CH * DH * 2;
 // fp16 I/O stages the next chunk through shared memory; fp32 I/O loads directly.
@@ -76,7 +76,7 @@ template <typename TIO>
 constexpr int smem_alloc() { return OFF_STG + (sizeof(TIO) == 2 ? STG_BYTES : 0) + 1024; }  // + alignment slack
 static_assert(OFF_STG + STG_BYTES + 1024 + 2048 <= 227 * 1024, "shared memory budget (dynamic + static)");
 static_assert(64 * 65 * 4 <= 32768, "fp32 A staging fits the fp16 state tile");
-static_assert(OFF_M + 32 * 33 * 4 <= OFF_V + 32768, "fp32 T staging fits the v tile");
+static_assert(OFF_M + 32 * 36 * 4 <= OFF_V + 32768, "fp32 T staging fits the v tile");
 
 // Byte offset of element (row, k) in a K-major, 128-byte swizzled fp16 tile with R rows.
 __device__ __forceinline__ uint32_t sw(int row, int k, int R) {
@@ -113,10 +113,21 @@ __device__ __forceinline__ void ld4<__half>(const __half *p, float (&v)[4]) {
 }
 
 // Unit lower-triangular inverse T = (I + A)^-1 of a 64 x 64 strictly lower A
-// (row stride 65, fp32, shared).  Writes the strictly lower part of T into
-// T32 (row stride 65); the diagonal is 1 and the upper part 0 implicitly.
+// (fp32, row stride AS, shared), written in full (ones on the diagonal, zeros
+// above) into T32 (row stride TS).  The four 16 x 16 diagonal blocks come from
+// forward substitution; the off-diagonal blocks from the block identity
+// [[L11, 0], [L21, L22]]^-1 = [[T11, 0], [-T22 L21 T11, T22]], first for the
+// two 32 x 32 diagonal blocks, then for the whole matrix.  The block products
+// are dense, fully unrolled and register-tiled so their shared-memory loads
+// pipeline.
+constexpr int AS = 65, TS = 68, MS = 36;
 __device__ void tri_inverse(const float *A, float *T32, float *M, int tid) {
-    // level 0: the four 16 x 16 diagonal blocks, one column per thread
+    // entries outside the diagonal 16 x 16 blocks start at zero
+    for (int e = tid; e < 64 * 64; e += NT) {
+        const int r = e >> 6, c = e & 63;
+        if ((r >> 4) != (c >> 4)) T32[r * TS + c] = 0.f;
+    }
+    // level 0: the diagonal 16 x 16 blocks, one column per thread
     if (tid < 64) {
         const int blk = tid >> 4, c = tid & 15, o = blk * 16;
         float x[16];
@@ -124,47 +135,64 @@ __device__ void tri_inverse(const float *A, float *T32, float *M, int tid) {
         for (int r = 0; r < 16; ++r) {
             float acc = 0.f;
 #pragma unroll
-            for (int s = 0; s < r; ++s) acc = fmaf(A[(o + r) * 65 + o + s], x[s], acc);
+            for (int s = 0; s < r; ++s) acc = fmaf(A[(o + r) * AS + o + s], x[s], acc);
             x[r] = (r < c) ? 0.f : (r == c ? 1.f : -acc);
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r)
-            if (r > c) T32[(o + r) * 65 + o + c] = x[r];
+        for (int r = 0; r < 16; ++r) T32[(o + r) * TS + o + c] = x[r];
     }
     __syncthreads();
-    // level 1: 32 x 32 blocks at 0 and 32:  T21 = -T22 A21 T11  (16 x 16 each)
+    // level 1: the two 32 x 32 diagonal blocks (offset o = 0, 32), two outputs per thread
     {
-        // M = A21 T11 for both pairs: 2 x 256 entries
-        for (int e = tid; e < 512; e += NT) {
-            const int p = e >> 8, r = (e >> 4) & 15, c = e & 15, o = 32 * p;
-            float acc = A[(o + 16 + r) * 65 + o + c];  // s = c term, T11[c][c] = 1
-            for (int s = c + 1; s < 16; ++s) acc = fmaf(A[(o + 16 + r) * 65 + o + s], T32[(o + s) * 65 + o + c], acc);
-            M[p * 272 + r * 17 + c] = acc;
+        const int pr = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2, o = 32 * pr;
+        float* Mp = M + pr * 16 * MS;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            const float a = A[(o + 16 + r) * AS + o + s];
+            a0 = fmaf(a, T32[(o + s) * TS + o + c0], a0);
+            a1 = fmaf(a, T32[(o + s) * TS + o + c0 + 1], a1);
         }
+        Mp[r * MS + c0] = a0;
+        Mp[r * MS + c0 + 1] = a1;
         __syncthreads();
-        for (int e = tid; e < 512; e += NT) {
-            const int p = e >> 8, r = (e >> 4) & 15, c = e & 15, o = 32 * p;
-            float acc = M[p * 272 + r * 17 + c];  // s = r term, T22[r][r] = 1
-            for (int s = 0; s < r; ++s) acc = fmaf(T32[(o + 16 + r) * 65 + o + 16 + s], M[p * 272 + s * 17 + c], acc);
-            T32[(o + 16 + r) * 65 + o + c] = -acc;
+        float b0 = 0.f, b1 = 0.f;
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            const float t = T32[(o + 16 + r) * TS + o + 16 + s];
+            b0 = fmaf(t, Mp[s * MS + c0], b0);
+            b1 = fmaf(t, Mp[s * MS + c0 + 1], b1);
         }
+        T32[(o + 16 + r) * TS + o + c0] = -b0;
+        T32[(o + 16 + r) * TS + o + c0 + 1] = -b1;
         __syncthreads();
     }
-    // level 2: T21 = -T22 A21 T11 with 32 x 32 blocks
+    // level 2: the lower-left 32 x 32 block, four consecutive outputs per thread
     {
-        for (int e = tid; e < 1024; e += NT) {
-            const int r = e >> 5, c = e & 31;
-            float acc = A[(32 + r) * 65 + c];
-            for (int s = c + 1; s < 32; ++s) acc = fmaf(A[(32 + r) * 65 + s], T32[s * 65 + c], acc);
-            M[r * 33 + c] = acc;
+        const int r = tid >> 3, c0 = (tid & 7) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < 32; ++s) {
+            const float a = A[(32 + r) * AS + s];
+            const float4 t = *reinterpret_cast<const float4 *>(T32 + s * TS + c0);
+            acc.x = fmaf(a, t.x, acc.x);
+            acc.y = fmaf(a, t.y, acc.y);
+            acc.z = fmaf(a, t.z, acc.z);
+            acc.w = fmaf(a, t.w, acc.w);
         }
+        *reinterpret_cast<float4 *>(M + r * MS + c0) = acc;
         __syncthreads();
-        for (int e = tid; e < 1024; e += NT) {
-            const int r = e >> 5, c = e & 31;
-            float acc = M[r * 33 + c];
-            for (int s = 0; s < r; ++s) acc = fmaf(T32[(32 + r) * 65 + 32 + s], M[s * 33 + c], acc);
-            T32[(32 + r) * 65 + c] = -acc;
+        float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < 32; ++s) {
+            const float t = T32[(32 + r) * TS + 32 + s];
+            const float4 m = *reinterpret_cast<const float4 *>(M + s * MS + c0);
+            out.x = fmaf(t, m.x, out.x);
+            out.y = fmaf(t, m.y, out.y);
+            out.z = fmaf(t, m.z, out.z);
+            out.w = fmaf(t, m.w, out.w);
         }
+        *reinterpret_cast<float4 *>(T32 + (32 + r) * TS + c0) = make_float4(-out.x, -out.y, -out.z, -out.w);
         __syncthreads();
     }
 }
@@ -368,45 +396,82 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                 *reinterpret_cast<float4 *>(V_s + s * DH + c4) = make_float4(v[0], v[1], v[2], v[3]);
             }
             __syncthreads();
-            // ---- A3: normalised k and q into the operand tiles (one warp per token)
-            for (int s = warp; s < CH; s += NT / 32) {
-                float qv[4] = {0.f, 0.f, 0.f, 0.f}, kv[4] = {0.f, 0.f, 0.f, 0.f};
-                if (s < n) {
-                    if (STAGED) {
-                        ld4<TIO>(reinterpret_cast<const TIO *>(stg + s * DH * 2) + lane * 4, qv);
-                        ld4<TIO>(reinterpret_cast<const TIO *>(stg + CH * DH * 2 + s * DH * 2) + lane * 4, kv);
-                    } else {
-                        const long long t = t0 + s;
-                        ld4<TIO>(qg + t * p.q_stride + (long long)kh * DH + lane * 4, qv);
-                        ld4<TIO>(kg + t * p.k_stride + (long long)kh * DH + lane * 4, kv);
+            // ---- A3: normalised k and q into the operand tiles; each warp handles
+            //      its 8 tokens together so their loads and reductions overlap
+            {
+                constexpr int TPW = CH / (NT / 32);  // tokens per warp
+                float qv[TPW][4], kv[TPW][4], sq[TPW], sk[TPW];
+#pragma unroll
+                for (int u = 0; u < TPW; ++u) {
+                    const int s = warp + 8 * u;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) qv[u][e] = kv[u][e] = 0.f;
+                    if (s < n) {
+                        if (STAGED) {
+                            ld4<TIO>(reinterpret_cast<const TIO *>(stg + s * DH * 2) + lane * 4, qv[u]);
+                            ld4<TIO>(reinterpret_cast<const TIO *>(stg + CH * DH * 2 + s * DH * 2) + lane * 4, kv[u]);
+                        } else {
+                            const long long t = t0 + s;
+                            ld4<TIO>(qg + t * p.q_stride + (long long)kh * DH + lane * 4, qv[u]);
+                            ld4<TIO>(kg + t * p.k_stride + (long long)kh * DH + lane * 4, kv[u]);
+                        }
                     }
                 }
-                float sq = 0.f, sk = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    sq = fmaf(qv[e], qv[e], sq);
-                    sk = fmaf(kv[e], kv[e], sk);
+                for (int u = 0; u < TPW; ++u) {
+                    sq[u] = sk[u] = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        sq[u] = fmaf(qv[u][e], qv[u][e], sq[u]);
+                        sk[u] = fmaf(kv[u][e], kv[u][e], sk[u]);
+                    }
                 }
-                sq = warp_sum(sq);
-                sk = warp_sum(sk);
-                const float nq = fmaxf(sqrtf(sq), EPS), nk = fmaxf(sqrtf(sk), EPS);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    qv[e] = qv[e] / nq;
-                    kv[e] = kv[e] / nk;
+                for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+                    for (int u = 0; u < TPW; ++u) {
+                        sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], off);
+                        sk[u] += __shfl_xor_sync(0xffffffffu, sk[u], off);
+                    }
                 }
                 const int c = lane * 4;
-                st_h4(sm + OFF_KQ, sw(s, c, 128), kv[0], kv[1], kv[2], kv[3]);
-                st_h4(sm + OFF_KQ, sw(64 + s, c, 128), qv[0], qv[1], qv[2], qv[3]);
-                const float gm = sh.gam[s];
-                st_h4(sm + OFF_GQ, sw(s, c, 64), gm * qv[0], gm * qv[1], gm * qv[2], gm * qv[3]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) st_h(sm + OFF_KT, sw(c + e, s, 128), kv[e]);
-                const int tl = t0 + s - bos;
-                if (p.caps && h % p.r == 0 && s < n && tl < p.cap) {
-                    float *dst = p.caps + ((long long)b * p.cap + tl) * p.W + p.Hv + (long long)kh * DH + c;
+                for (int u = 0; u < TPW; ++u) {
+                    const int s = warp + 8 * u;
+                    const float nq = fmaxf(sqrtf(sq[u]), EPS), nk = fmaxf(sqrtf(sk[u]), EPS);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) dst[e] = kv[e];
+                    for (int e = 0; e < 4; ++e) {
+                        qv[u][e] = qv[u][e] / nq;
+                        kv[u][e] = kv[u][e] / nk;
+                    }
+                    st_h4(sm + OFF_KQ, sw(s, c, 128), kv[u][0], kv[u][1], kv[u][2], kv[u][3]);
+                    st_h4(sm + OFF_KQ, sw(64 + s, c, 128), qv[u][0], qv[u][1], qv[u][2], qv[u][3]);
+                    const float gm = sh.gam[s];
+                    st_h4(sm + OFF_GQ, sw(s, c, 64), gm * qv[u][0], gm * qv[u][1], gm * qv[u][2], gm * qv[u][3]);
+                    const int tl = t0 + s - bos;
+                    if (p.caps && h % p.r == 0 && s < n && tl < p.cap) {
+                        float *dst = p.caps + ((long long)b * p.cap + tl) * p.W + p.Hv + (long long)kh * DH + c;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) dst[e] = kv[u][e];
+                    }
+                }
+            }
+            __syncthreads();
+            // ---- A4: K^T tile from the K rows (thread: one dk row, 32 tokens)
+            {
+                const int j = tid >> 1, sg = (tid & 1) * 32;
+                const uint8_t *kq = sm + OFF_KQ;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = sg + 8 * m + 2 * e;
+                        const unsigned short lo = *reinterpret_cast<const unsigned short *>(kq + sw(s, j, 128));
+                        const unsigned short hi = *reinterpret_cast<const unsigned short *>(kq + sw(s + 1, j, 128));
+                        w[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + OFF_KT + sw(j, sg + 8 * m, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             // ---- B: S0 -> fp16 operand tile; the tensor-memory state becomes gamma_last S0
@@ -464,7 +529,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int s = half * 32 + j;
-                        A32[r * 65 + s] = (s < r) ? br * __expf(Gr - sh.Gam[s]) * v[j] : 0.f;
+                        A32[r * AS + s] = (s < r) ? br * __expf(Gr - sh.Gam[s]) * v[j] : 0.f;
                     }
                 } else {
 #pragma unroll
@@ -499,7 +564,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int s = s0 + u;
-                    w[u] = s < r ? T32[r * 65 + s] : (s == r ? 1.f : 0.f);
+                    w[u] = T32[r * TS + s];
                 }
                 st_h4(sm + OFF_T, sw(r, s0, 64), w[0], w[1], w[2], w[3]);
             }
@@ -551,14 +616,20 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
             }
             if (!mma_wait()) { failed = true; break; }
             state_live = true;
-            // ---- H: outputs
+            // ---- H: outputs, staged through shared memory (the v tile is free) and
+            //      written as contiguous 16-byte pieces of each token's dv row
             {
                 float v[32];
                 ptx::tmem_ld32(tm + lane_sel + TM_O + half * 32, v);
+                TIO *ost = reinterpret_cast<TIO *>(sm + OFF_V);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int r = half * 32 + j;
-                    if (r < n) og[((long long)(t0 + r) * p.Hv + h) * DH + row] = from_f32<TIO>(p.scale * v[j]);
+                for (int j = 0; j < 32; ++j) ost[(half * 32 + j) * DH + row] = from_f32<TIO>(p.scale * v[j]);
+                __syncthreads();
+                constexpr int VEC = 16 / sizeof(TIO);  // elements per 16-byte piece
+                for (int e = tid; e < n * (DH / VEC); e += NT) {
+                    const int r = e / (DH / VEC), c = (e % (DH / VEC)) * VEC;
+                    *reinterpret_cast<uint4 *>(og + ((long long)(t0 + r) * p.Hv + h) * DH + c) =
+                        *reinterpret_cast<const uint4 *>(ost + r * DH + c);
                 }
             }
             ptx::tc_fence_before();
