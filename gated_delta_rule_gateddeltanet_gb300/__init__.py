@@ -20,7 +20,7 @@ import torch
 
 from .build import LIB as LIB_PATH
 
-__all__ = ["gdn_forward", "gdn_replay_prefix", "GdnError", "load_library", "capsule_width",
+__all__ = ["gdn_forward", "gdn_forward_no_alloc", "gdn_replay_prefix", "GdnError", "load_library", "capsule_width",
            "STATUS", "DEVERR", "PLAN"]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_DTYPE", 3: "GDN_ERR_SHAPE", 4: "GDN_ERR_ALIGN",
@@ -74,6 +74,8 @@ def load_library(path: str | None = None):
     lib.gdn_forward_workspace_size.argtypes = [ctypes.POINTER(ForwardArgs), ctypes.POINTER(ctypes.c_size_t)]
     lib.gdn_replay_prefix.restype = i32
     lib.gdn_replay_prefix.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P, P, i32, P, P, P]
+    lib.gdn_forward_no_alloc.restype = i32
+    lib.gdn_forward_no_alloc.argtypes = [ctypes.POINTER(ForwardArgs), P]
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_status_string.argtypes = [i32]
     if path is None:
@@ -222,6 +224,22 @@ def gdn_forward(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, gate_mod
     rc = lib.gdn_forward(ctypes.byref(args), _stream_handle(q.device))
     if rc != 0:
         raise GdnError(rc, "gdn_forward")
+    return outs
+
+
+def gdn_forward_no_alloc(q, k, v, a, b, cu_seqlens, **kw):
+    """``gdn_forward`` through the C ABI ``gdn_forward_no_alloc``: the chunked
+    kernel's workspace comes from a fixed array inside the library, for hosts
+    that cannot hand the operator extra device memory.  Same arguments and
+    results as ``gdn_forward`` (``workspace`` is ignored); at most
+    ``GDN_NO_ALLOC_MAX_SEQS`` (4094) sequences when the chunked kernel may run.
+    Calls that overlap on the GPU share that array and must not be made."""
+    lib = load_library()
+    kw.pop("workspace", None)
+    args, outs, keep = build_forward_args(q, k, v, a, b, cu_seqlens, **kw)
+    rc = lib.gdn_forward_no_alloc(ctypes.byref(args), _stream_handle(q.device))
+    if rc != 0:
+        raise GdnError(rc, "gdn_forward_no_alloc")
     return outs
 
 

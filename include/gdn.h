@@ -198,6 +198,29 @@ gdn_status gdn_replay_prefix(float *state_banks, int32_t num_slots, int32_t num_
                              const float *state_update, int32_t capacity, const int32_t *accept_len,
                              int32_t *status, gdn_stream_t stream);
 
+/*
+ * gdn_forward for callers that cannot allocate device memory.  The paper has
+ * no counterpart to this entry point.
+ *
+ * Some hosts own all device memory through their own allocator and give an
+ * operator only its declared inputs and outputs (an inference runtime's
+ * custom-operator interface, a serving loop with a fixed memory plan), and
+ * some paths cannot afford a cudaMalloc, which may synchronise the device.
+ * This call behaves exactly like gdn_forward but ignores args->workspace: the
+ * chunked kernel's workspace comes from a fixed 16 KiB array compiled into
+ * the library, which every GPU that loads the library keeps until exit.
+ *
+ *  - Batches of more than GDN_NO_ALLOC_MAX_SEQS sequences that need a
+ *    workspace are rejected with GDN_ERR_WORKSPACE before anything runs.
+ *  - The first call on each device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - All calls share the array (each call rewrites what it uses), so calls
+ *    that overlap on the GPU, e.g. on two streams, race and must not be made.
+ *  - No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+#define GDN_NO_ALLOC_MAX_SEQS 4094
+gdn_status gdn_forward_no_alloc(const gdn_forward_args *args, gdn_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char *gdn_status_string(gdn_status status);
 
