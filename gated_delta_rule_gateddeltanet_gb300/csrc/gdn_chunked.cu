@@ -61,22 +61,20 @@ constexpr int OFF_KQ = 0;                  // [128][128]: rows 0-63 K, 64-127 Q 
 constexpr int OFF_GQ = OFF_KQ + 32768;     // [64][128]: gamma Q                        16 KiB
 constexpr int OFF_KT = OFF_GQ + 16384;     // [128][64]: K^T (dk rows, token columns)  16 KiB
 constexpr int OFF_S16 = OFF_KT + 16384;    // [128][128]: S0 in fp16                    32 KiB
-constexpr int OFF_A32 = OFF_S16;           //   reused once MMA2 is done: A in fp32 [64][65]
+constexpr int OFF_A32 = OFF_S16 + 32768;   //   (R^T/U^T tiles, idle until R^T is built): A in fp32 [64][65]
 constexpr int OFF_RT = OFF_S16 + 32768;    // [128][64]: R^T, then U^T                  16 KiB
 constexpr int OFF_UD = OFF_RT + 16384;     // [128][64]: U^T diag(exp(Gamma_last - Gamma)) 16 KiB
 constexpr int OFF_T = OFF_UD + 16384;      // [64][64]: T                               8 KiB
 constexpr int OFF_PD = OFF_T + 8192;       // [64][64]: P o D                           8 KiB
 constexpr int OFF_V = OFF_PD + 8192;       // [64][128] fp32 v                          32 KiB
-constexpr int OFF_T32 = OFF_V;             //   reused once R^T is built: T in fp32 [64][68]
-constexpr int OFF_M = OFF_V + 64 * 68 * 4; //   and the block-combination scratch [32][36]
+constexpr int OFF_T32 = OFF_V + 32768;     //   (staging, idle from A3 to the next prefetch): T in fp32 [64][68]
+constexpr int OFF_M = OFF_T32 + 64 * 68 * 4; //   and the block-combination scratch [32][36]
 constexpr int OFF_STG = OFF_V + 32768;     // fp16 I/O: raw q, k, v rows of the next chunk  48 KiB
 constexpr int STG_BYTES = 3 * CH * DH * 2;
-// fp16 I/O stages the next chunk through shared memory; fp32 I/O loads directly.
-template <typename TIO>
-constexpr int smem_alloc() { return OFF_STG + (sizeof(TIO) == 2 ? STG_BYTES : 0) + 1024; }  // + alignment slack
-static_assert(OFF_STG + STG_BYTES + 1024 + 2048 <= 227 * 1024, "shared memory budget (dynamic + static)");
-static_assert(64 * 65 * 4 <= 32768, "fp32 A staging fits the fp16 state tile");
-static_assert(OFF_M + 32 * 36 * 4 <= OFF_V + 32768, "fp32 T staging fits the v tile");
+constexpr int SMEM_ALLOC = OFF_STG + STG_BYTES + 1024;  // + slack for the 1024-byte alignment
+static_assert(SMEM_ALLOC + 2048 <= 227 * 1024, "shared memory budget (dynamic + static)");
+static_assert(64 * 65 * 4 <= 32768, "fp32 A staging fits the R^T and U^T tiles");
+static_assert(OFF_M + 32 * 36 * 4 <= OFF_STG + STG_BYTES, "fp32 T staging fits the staging area");
 
 // Byte offset of element (row, k) in a K-major, 128-byte swizzled fp16 tile with R rows.
 __device__ __forceinline__ uint32_t sw(int row, int k, int R) {
@@ -438,11 +436,11 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
 #pragma unroll
                 for (int u = 0; u < TPW; ++u) {
                     const int s = warp + 8 * u;
-                    const float nq = fmaxf(sqrtf(sq[u]), EPS), nk = fmaxf(sqrtf(sk[u]), EPS);
+                    const float iq = 1.f / fmaxf(sqrtf(sq[u]), EPS), ik = 1.f / fmaxf(sqrtf(sk[u]), EPS);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        qv[u][e] = qv[u][e] / nq;
-                        kv[u][e] = kv[u][e] / nk;
+                        qv[u][e] *= iq;
+                        kv[u][e] *= ik;
                     }
                     st_h4(sm + OFF_KQ, sw(s, c, 128), kv[u][0], kv[u][1], kv[u][2], kv[u][3]);
                     st_h4(sm + OFF_KQ, sw(64 + s, c, 128), qv[u][0], qv[u][1], qv[u][2], qv[u][3]);
@@ -498,27 +496,27 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                 if (state_live) ptx::tmem_st_wait();
             }
             mma_ready();
-            // ---- C: MMA1 and MMA2
+            // ---- C: MMA1 (committed on its own, so the inverse can start while
+            //      MMA2 still runs) and MMA2
             if (tid == 0) {
                 ptx::tc_fence_after();
                 const uint32_t i64 = ptx::idesc_f16_f32(128, 64);
                 for (int ks = 0; ks < DH / 16; ++ks) {
+                    const uint64_t dKQ = ptx::sdesc_k_sw128(a_KQ + (ks >> 2) * 16384 + (ks & 3) * 32);
+                    ptx::mma_f16(tm + TM_D1, dKQ, dKQ, i64, ks > 0);
+                }
+                ptx::mma_commit(&sh.bar);
+                for (int ks = 0; ks < DH / 16; ++ks) {
                     const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
                     const uint64_t dKQ = ptx::sdesc_k_sw128(a_KQ + ko);
-                    ptx::mma_f16(tm + TM_D1, dKQ, dKQ, i64, ks > 0);
                     ptx::mma_f16(tm + TM_X, ptx::sdesc_k_sw128(a_S16 + ko), dKQ, i64, ks > 0);
                     ptx::mma_f16(tm + TM_O, ptx::sdesc_k_sw128(a_S16 + ko),
                                  ptx::sdesc_k_sw128(a_GQ + (ks >> 2) * 8192 + (ks & 3) * 32), i64, ks > 0);
                 }
                 ptx::mma_commit(&sh.bar);
             }
-            // the staging area is consumed: fetch the next chunk while this one computes
-            if (STAGED && t0 + CH < eos) {
-                prefetch(t0 + CH);
-                load_pending = true;
-            }
             if (!mma_wait()) { failed = true; break; }
-            // ---- D1: A (fp32 staging) and P o D (fp16 tile) from G and P; R^T from X^T
+            // ---- D1: A (fp32 staging) and P o D (fp16 tile) from G and P
             {
                 float v[32];
                 ptx::tmem_ld32(tm + lane_sel + TM_D1 + half * 32, v);
@@ -543,17 +541,6 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                         st_h4(sm + OFF_PD, sw(r, half * 32 + j, 64), w[0], w[1], w[2], w[3]);
                     }
                 }
-                ptx::tmem_ld32(tm + lane_sel + TM_X + half * 32, v);
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    float w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s = half * 32 + j + e;
-                        w[e] = sh.beta[s] * (V_s[s * DH + row] - sh.gam[s] * v[j + e]);
-                    }
-                    st_h4(sm + OFF_RT, sw(row, half * 32 + j, 128), w[0], w[1], w[2], w[3]);
-                }
             }
             __syncthreads();
             // ---- D2: T = (I + A)^-1 on the CUDA cores, then its fp16 tile
@@ -567,6 +554,27 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                     w[u] = T32[r * TS + s];
                 }
                 st_h4(sm + OFF_T, sw(r, s0, 64), w[0], w[1], w[2], w[3]);
+            }
+            if (!mma_wait()) { failed = true; break; }  // MMA2 (long done by now)
+            // the staging area is free again: fetch the next chunk while this one finishes
+            if (STAGED && t0 + CH < eos) {
+                prefetch(t0 + CH);
+                load_pending = true;
+            }
+            // ---- D3: R^T = (V - diag(gamma) K S0^T)^T diag(beta) from X^T
+            {
+                float v[32];
+                ptx::tmem_ld32(tm + lane_sel + TM_X + half * 32, v);
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    float w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = half * 32 + j + e;
+                        w[e] = sh.beta[s] * (V_s[s * DH + row] - sh.gam[s] * v[j + e]);
+                    }
+                    st_h4(sm + OFF_RT, sw(row, half * 32 + j, 128), w[0], w[1], w[2], w[3]);
+                }
             }
             mma_ready();
             // ---- E: MMA3  U^T = R^T T^T
@@ -662,6 +670,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
     if (failed && tid == 0) {
         flag_error(p.status, GDN_DEVERR_TIMEOUT);
         ptx::mbar_wait_bounded(&sh.bar, phase ^ 1u, WAIT_LIMIT);  // let in-flight MMAs drain
+        ptx::mbar_wait_bounded(&sh.bar, phase, WAIT_LIMIT);
         if (load_pending) ptx::mbar_wait_bounded(&sh.lbar, lphase, WAIT_LIMIT);  // and staged copies
     }
     ptx::tc_fence_before();
@@ -732,7 +741,7 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStre
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto kern = chunked_kernel<TIO>;
-    constexpr int smem = smem_alloc<TIO>();
+    constexpr int smem = SMEM_ALLOC;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long long chains = (long long)p.B * p.Hv;
