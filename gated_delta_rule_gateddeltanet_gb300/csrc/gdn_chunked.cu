@@ -198,6 +198,7 @@ __device__ void tri_inverse(const float *A, float *T32, float *M, int tid) {
 struct Shared {
     float Gam[CH], gam[CH], beta[CH], gate[CH];
     uint64_t bar;   // MMA completion
+    uint64_t bar1;  // MMA1 completion (its own barrier: two commits on one barrier before a wait would alias phases)
     uint64_t lbar;  // staged rows of the next chunk
     uint32_t tmem;
     int item;
@@ -228,6 +229,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
     }
     if (tid == 0) {
         ptx::mbar_init(&sh.bar, 1);
+        ptx::mbar_init(&sh.bar1, 1);
         ptx::mbar_init(&sh.lbar, 1);
         ptx::fence_mbar_init();
     }
@@ -235,7 +237,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tm = sh.tmem;
-    uint32_t phase = 0, lphase = 0;
+    uint32_t phase = 0, phase1 = 0, lphase = 0;
     bool failed = false, load_pending = false;
     constexpr bool STAGED = sizeof(TIO) == 2;
     uint8_t *stg = sm + OFF_STG;
@@ -505,7 +507,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                     const uint64_t dKQ = ptx::sdesc_k_sw128(a_KQ + (ks >> 2) * 16384 + (ks & 3) * 32);
                     ptx::mma_f16(tm + TM_D1, dKQ, dKQ, i64, ks > 0);
                 }
-                ptx::mma_commit(&sh.bar);
+                ptx::mma_commit(&sh.bar1);
                 for (int ks = 0; ks < DH / 16; ++ks) {
                     const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
                     const uint64_t dKQ = ptx::sdesc_k_sw128(a_KQ + ko);
@@ -515,7 +517,12 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                 }
                 ptx::mma_commit(&sh.bar);
             }
-            if (!mma_wait()) { failed = true; break; }
+            {
+                const bool ok = ptx::mbar_wait_bounded(&sh.bar1, phase1, WAIT_LIMIT);
+                phase1 ^= 1u;
+                ptx::tc_fence_after();
+                if (!__syncthreads_and(ok)) { failed = true; break; }
+            }
             // ---- D1: A (fp32 staging) and P o D (fp16 tile) from G and P
             {
                 float v[32];
@@ -671,6 +678,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
         flag_error(p.status, GDN_DEVERR_TIMEOUT);
         ptx::mbar_wait_bounded(&sh.bar, phase ^ 1u, WAIT_LIMIT);  // let in-flight MMAs drain
         ptx::mbar_wait_bounded(&sh.bar, phase, WAIT_LIMIT);
+        ptx::mbar_wait_bounded(&sh.bar1, phase1 ^ 1u, WAIT_LIMIT);
         if (load_pending) ptx::mbar_wait_bounded(&sh.lbar, lphase, WAIT_LIMIT);  // and staged copies
     }
     ptx::tc_fence_before();
