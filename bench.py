@@ -365,9 +365,34 @@ def run_prefill(dev, stream):
         times.append(e0.elapsed_time(e1))
     ms = statistics.median(times)
     T = inp.T
+    lengths = [int(x) for x in np.diff(inp.cu_seqlens)]
+    _, tc_peak, kind = measured_peaks()
+    flops = prefill_algorithmic_flops(T)
+    chunk_heads = sum((L + 63) // 64 for L in lengths) * 48
+    executed = chunk_heads * PREFILL_MMA_FLOPS_PER_CHUNK_HEAD
+    tflops = flops / (ms / 1e3) / 1e12
     return {"workload": "varlen prefill: 8 sequences, lengths U[256,4096] (seeded), Hk=16, Hv=48, d=128, fp16, "
-                        "zero initial state", "tokens": int(T), "lengths": [int(x) for x in np.diff(inp.cu_seqlens)],
-            "plan": plan, "ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "l2": "flushed (256 MiB write)"}
+                        "zero initial state", "tokens": int(T), "lengths": lengths,
+            "plan": plan, "ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "l2": "flushed (256 MiB write)",
+            "roofline": {"bound": "tensor", "kernel": "chunked_kernel<__half>", "achieved": round(tflops, 2),
+                         "peak": tc_peak, "peak_kind": f"{kind} dense bf16 burst (fp16 runs at the bf16 rate)",
+                         "unit": "TFLOP/s", "frac": round(tflops / tc_peak, 4), "algorithmic_flops": flops,
+                         "executed_mma_flops": executed,
+                         "executed_tflops": round(executed / (ms / 1e3) / 1e12, 2)}}
+
+
+# Algorithmic FLOPs of the chunked evaluation per token and value head (chunk
+# C = 64, d = 128, r = 3 value heads per key head): the state-passing products
+# 6 d^2, the intra-chunk products C (2d/r + d + 2d) (K K^T and Q K^T shared by
+# the r value heads of a key head), and the triangular inverse C^2 / 3.
+PREFILL_FLOPS_PER_TOKEN_HEAD = 6 * 128 * 128 + 64 * (2 * 128 / 3 + 128 + 2 * 128) + 64 * 64 / 3
+# tcgen05 FLOPs the kernel issues per (64-token chunk, value head): MMA1 128x64x128,
+# MMA2 128x128x128, MMA3 and MMA4 128x64x64, MMA5 128x128x64.
+PREFILL_MMA_FLOPS_PER_CHUNK_HEAD = 2 * (128 * 64 * 128 + 128 * 128 * 128 + 2 * 128 * 64 * 64 + 128 * 128 * 64)
+
+
+def prefill_algorithmic_flops(tokens, heads=48):
+    return int(tokens * heads * PREFILL_FLOPS_PER_TOKEN_HEAD)
 
 
 def run_spec(dev, stream, lib, sh):
