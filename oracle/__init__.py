@@ -65,7 +65,7 @@ def _load():
             lib.gdn_oracle_replay.restype = i32
             lib.gdn_oracle_replay.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P, P, i32, P]
             lib.conv_oracle_forward.restype = i32
-            lib.conv_oracle_forward.argtypes = [i32] * 5 + [P] * 8 + [i32]
+            lib.conv_oracle_forward.argtypes = [i32] * 5 + [P] * 8 + [i32, P]
             lib.gdn_oracle_threads.restype = i32
             _lib = lib
     return _lib
@@ -156,14 +156,17 @@ def gdn_replay(banks, src_slots, dst_slots, capsules, accept_len, *, num_k_heads
     return banks
 
 
-def conv_forward(x, w, cu_seqlens, conv_state, *, bias=None, state_slots=None, capacity=0):
+def conv_forward(x, w, cu_seqlens, conv_state, *, bias=None, state_slots=None, capacity=0, capture_count=None):
     """FP64 packed depthwise causal conv + SiLU with carried state.
 
-    x: [T, C]; w: [C, K]; conv_state: [slots, C, K-1] (oldest first).
-    Returns ``(out [T,C], new_conv_state, values [B,cap,C] or None)``.
+    x: [T, C]; w: [C, K]; conv_state: [slots, C, K-1] (oldest first);
+    capture_count: optional [B], each in [0, capacity].
+    Returns ``(out [T,C], new_conv_state, values [B,cap,C] or None)``; capture
+    rows that no token fills are NaN.
     """
     x, w, bias = _f64(x), _f64(w), _f64(bias)
     cu, slots = _i32(cu_seqlens), _i32(state_slots)
+    cc = _i32(capture_count)
     T, C = x.shape
     K = w.shape[1]
     state = _f64(conv_state).copy()
@@ -171,7 +174,7 @@ def conv_forward(x, w, cu_seqlens, conv_state, *, bias=None, state_slots=None, c
     out = np.zeros((T, C))
     values = np.full((B, capacity, C), np.nan) if capacity > 0 else None
     rc = _load().conv_oracle_forward(B, T, C, K, state.shape[0], _ptr(x), _ptr(w), _ptr(bias), _ptr(cu),
-                                     _ptr(slots), _ptr(state), _ptr(out), _ptr(values), int(capacity))
+                                     _ptr(slots), _ptr(state), _ptr(out), _ptr(values), int(capacity), _ptr(cc))
     if rc != 0:
         raise OracleError(f"conv_oracle_forward failed with code {rc}")
     return out, state, values

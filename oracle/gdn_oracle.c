@@ -235,18 +235,21 @@ int gdn_oracle_replay(double *banks, int num_slots, int R, int Hk, int Hv, int d
  *   inputs of the extended history.
  *   out [T, C]:  y[t, c] = silu(bias[c] + sum_{j<K} w[c, j] * x_ext[t - (K-1) + j, c])
  *   where x_ext is the history (state) followed by the sequence's tokens.
- *   values [B, cap, C] or NULL: the first min(len_b, cap) appended inputs of
- *   sequence b (the compact capture), or NULL.
- * Returns 0, 1 for a bad packing, 2 for a bad slot.
+ *   values [B, cap, C] or NULL: the first n_b appended inputs of sequence b
+ *   (the compact capture), n_b = min(len_b, cap, capture_count[b]) -- the
+ *   per-request capture_count being optional (NULL: no third bound).
+ * Returns 0, 1 for a bad packing, 2 for a bad slot, 5 for a capture count
+ * outside [0, cap].
  */
 int conv_oracle_forward(int B, int T, int C, int K, int num_slots, const double *x,
                         const double *w, const double *bias, const int32_t *cu,
                         const int32_t *slots, double *conv_state, double *out,
-                        double *values, int cap) {
+                        double *values, int cap, const int32_t *capture_count) {
     if (oracle_check_cu(cu, B, T)) return 1;
     for (int s = 0; s < B; ++s) {
         int slot = slots ? slots[s] : s;
         if (slot < 0 || slot >= num_slots) return 2;
+        if (capture_count && (capture_count[s] < 0 || capture_count[s] > cap)) return 5;
     }
     const int Km1 = K - 1;
 #pragma omp parallel for schedule(static)
@@ -265,7 +268,8 @@ int conv_oracle_forward(int B, int T, int C, int K, int num_slots, const double 
                 for (int j = 0; j + 1 < Km1; ++j) hist[j] = hist[j + 1];
                 if (Km1 > 0) hist[Km1 - 1] = xt;
                 const int tl = t - cu[s];
-                if (values && tl < cap) values[((long)s * cap + tl) * C + c] = xt;
+                const int ncap = capture_count ? capture_count[s] : cap;
+                if (values && tl < cap && tl < ncap) values[((long)s * cap + tl) * C + c] = xt;
             }
             for (int j = 0; j < Km1; ++j) st[j] = hist[j];
         }

@@ -372,3 +372,24 @@ def test_conv_sequential_prefix_equivalence_and_replay():
         _, st_n, _ = oracle.conv_forward(x[:n], w, np.array([0, n]), st0)
         rep = oracle.conv_replay(pool, [0], [1], vals, [n])
         assert np.array_equal(rep[1], st_n[0])
+
+
+def test_conv_capture_count_bounds_the_capture():
+    """The optional per-request capture count limits the compact capture to
+    the first capture_count[b] appended inputs; counts above the capacity are
+    rejected."""
+    rng = np.random.default_rng(12)
+    lengths, C, K, cap = [5, 2, 6], 3, 4, 4
+    T = sum(lengths)
+    x = rng.standard_normal((T, C))
+    w = rng.standard_normal((C, K))
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    st = rng.standard_normal((3, C, K - 1))
+    _, _, full = oracle.conv_forward(x, w, cu, st, capacity=cap)
+    _, _, part = oracle.conv_forward(x, w, cu, st, capacity=cap, capture_count=[2, 4, 0])
+    for s, n in enumerate([2, 4, 0]):
+        m = min(n, lengths[s])
+        assert np.array_equal(part[s, :m], full[s, :m])
+        assert np.all(np.isnan(part[s, m:]))
+    with pytest.raises(oracle.OracleError):
+        oracle.conv_forward(x, w, cu, st, capacity=cap, capture_count=[5, 0, 0])
