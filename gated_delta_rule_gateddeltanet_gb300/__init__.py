@@ -20,12 +20,15 @@ import torch
 
 from .build import LIB as LIB_PATH
 
-__all__ = ["gdn_forward", "gdn_forward_no_alloc", "gdn_replay_prefix", "GdnError", "load_library", "capsule_width",
+__all__ = ["gdn_forward", "gdn_forward_no_alloc", "gdn_replay_prefix", "varlen_causal_conv_with_state",
+           "causal_conv_replay_prefix", "GdnError", "load_library", "capsule_width",
            "STATUS", "DEVERR", "PLAN"]
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_DTYPE", 3: "GDN_ERR_SHAPE", 4: "GDN_ERR_ALIGN",
           5: "GDN_ERR_WORKSPACE", 6: "GDN_ERR_CUDA", 7: "GDN_ERR_UNSUPPORTED", 8: "GDN_ERR_ARG"}
-DEVERR = {"cu_seqlens": 0x1, "state_slot": 0x2, "accept_len": 0x4, "replay_slot": 0x8, "timeout": 0x10}
+DEVERR = {"cu_seqlens": 0x1, "state_slot": 0x2, "accept_len": 0x4, "replay_slot": 0x8, "timeout": 0x10,
+          "capture_count": 0x20}
+ACTIVATION = {"none": 0, "silu": 1}
 PLAN = {"auto": 0, "recurrent": 1, "chunked": 2}
 DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 GATE_MODE = {"raw": 0, "precomputed": 1}
@@ -55,6 +58,19 @@ class ForwardArgs(ctypes.Structure):
     ]
 
 
+class ConvArgs(ctypes.Structure):
+    """Mirror of ``gdn_conv_args`` (include/gdn.h)."""
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32), ("channels", ctypes.c_int32),
+        ("kernel_size", ctypes.c_int32), ("num_state_slots", ctypes.c_int32), ("io_dtype", ctypes.c_int32),
+        ("activation", ctypes.c_int32), ("state_update_capacity", ctypes.c_int32), ("x_stride", ctypes.c_int64),
+        ("x", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+        ("cu_seqlens", ctypes.c_void_p), ("state_slots", ctypes.c_void_p), ("capture_count", ctypes.c_void_p),
+        ("initial_state", ctypes.c_void_p), ("final_state", ctypes.c_void_p), ("output", ctypes.c_void_p),
+        ("state_update", ctypes.c_void_p), ("status", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -76,6 +92,10 @@ def load_library(path: str | None = None):
     lib.gdn_replay_prefix.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P, P, i32, P, P, P]
     lib.gdn_forward_no_alloc.restype = i32
     lib.gdn_forward_no_alloc.argtypes = [ctypes.POINTER(ForwardArgs), P]
+    lib.varlen_causal_conv_with_state.restype = i32
+    lib.varlen_causal_conv_with_state.argtypes = [ctypes.POINTER(ConvArgs), P]
+    lib.causal_conv_replay_prefix.restype = i32
+    lib.causal_conv_replay_prefix.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, i32, P, P, P]
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_status_string.argtypes = [i32]
     if path is None:
@@ -266,3 +286,83 @@ def gdn_replay_prefix(state_banks, src_slots, dst_slots, state_update, accept_le
     if rc != 0:
         raise GdnError(rc, "gdn_replay_prefix")
     return state_banks
+
+
+def build_conv_args(x, weight, cu_seqlens, *, bias=None, initial_state=None, final_state=None, state_slots=None,
+                    capture_count=None, capacity=0, activation="silu", output=None, state_update=None,
+                    status=None, num_state_slots=None):
+    """Fill a ConvArgs struct from tensors; returns (args, outputs, keepalive)."""
+    dev = x.device
+    T, C = x.shape
+    K = weight.shape[1]
+    B = cu_seqlens.shape[0] - 1
+    if x.dtype not in DTYPE:
+        raise TypeError(f"unsupported dtype {x.dtype}")
+    if x.stride(1) != 1:
+        raise ValueError("x: channels must be contiguous")
+    _check(weight, "weight", dtype=torch.float32, device=dev)
+    _check(bias, "bias", dtype=torch.float32, device=dev)
+    for name, t in (("cu_seqlens", cu_seqlens), ("state_slots", state_slots), ("capture_count", capture_count),
+                    ("status", status)):
+        _check(t, name, dtype=torch.int32, device=dev)
+    if num_state_slots is None:
+        src = initial_state if initial_state is not None else final_state
+        num_state_slots = src.shape[0] if src is not None else B
+    if final_state is None:
+        final_state = (initial_state.clone() if initial_state is not None else
+                       torch.zeros((num_state_slots, C, K - 1), dtype=x.dtype, device=dev))
+    for name, t in (("initial_state", initial_state), ("final_state", final_state)):
+        _check(t, name, dtype=x.dtype, device=dev)
+    if output is None:
+        output = torch.empty((T, C), dtype=x.dtype, device=dev)
+    if capacity > 0 and state_update is None:
+        state_update = torch.zeros((B, capacity, C), dtype=x.dtype, device=dev)
+    _check(output, "output", dtype=x.dtype, device=dev)
+    _check(state_update, "state_update", dtype=x.dtype, device=dev)
+    a = ConvArgs()
+    a.num_seqs, a.total_tokens, a.channels, a.kernel_size = B, T, C, K
+    a.num_state_slots, a.io_dtype = int(num_state_slots), DTYPE[x.dtype]
+    a.activation, a.state_update_capacity = ACTIVATION[activation], int(capacity)
+    a.x_stride = x.stride(0) if T > 1 else C
+    a.x, a.weight, a.bias = _ptr(x), _ptr(weight), _ptr(bias)
+    a.cu_seqlens, a.state_slots, a.capture_count = _ptr(cu_seqlens), _ptr(state_slots), _ptr(capture_count)
+    a.initial_state, a.final_state, a.output = _ptr(initial_state), _ptr(final_state), _ptr(output)
+    a.state_update = _ptr(state_update) if capacity > 0 else None
+    a.status = _ptr(status)
+    keep = (x, weight, bias, cu_seqlens, state_slots, capture_count, initial_state, status)
+    return a, (output, final_state, state_update), keep
+
+
+def varlen_causal_conv_with_state(x, weight, cu_seqlens, **kw):
+    """Packed depthwise causal conv (+ SiLU) with carried state (C ABI
+    ``varlen_causal_conv_with_state``).  x: [T, C] fp16/fp32; weight: [C, K]
+    fp32; optional bias [C]; initial_state / final_state [slots, C, K-1] in
+    x's dtype (may be the same tensor); capture_count [B] int32.  Returns
+    ``(output, final_state, state_update)``."""
+    lib = load_library()
+    args, outs, keep = build_conv_args(x, weight, cu_seqlens, **kw)
+    rc = lib.varlen_causal_conv_with_state(ctypes.byref(args), _stream_handle(x.device))
+    if rc != 0:
+        raise GdnError(rc, "varlen_causal_conv_with_state")
+    return outs
+
+
+def causal_conv_replay_prefix(conv_states, src_slots, dst_slots, state_update, accept_len, *, status=None):
+    """Replay accepted captured conv inputs into the destination states, in
+    place (C ABI ``causal_conv_replay_prefix``).  conv_states: [slots, C, K-1];
+    state_update: [R, capacity, C]; src/dst/accept_len: [R] int32."""
+    lib = load_library()
+    S, C, Km1 = conv_states.shape
+    dev = conv_states.device
+    _check(conv_states, "conv_states", device=dev)
+    _check(state_update, "state_update", dtype=conv_states.dtype, device=dev)
+    for name, t in (("src_slots", src_slots), ("dst_slots", dst_slots), ("accept_len", accept_len),
+                    ("status", status)):
+        _check(t, name, dtype=torch.int32, device=dev)
+    cap = state_update.shape[1] if state_update is not None else 0
+    rc = lib.causal_conv_replay_prefix(_ptr(conv_states), S, src_slots.shape[0], C, Km1 + 1, DTYPE[conv_states.dtype],
+                                       _ptr(src_slots), _ptr(dst_slots), _ptr(state_update), cap, _ptr(accept_len),
+                                       _ptr(status), _stream_handle(dev))
+    if rc != 0:
+        raise GdnError(rc, "causal_conv_replay_prefix")
+    return conv_states

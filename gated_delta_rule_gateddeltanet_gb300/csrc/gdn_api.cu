@@ -192,4 +192,83 @@ gdn_status gdn_replay_prefix(float *state_banks, int32_t num_slots, int32_t num_
     return GDN_OK;
 }
 
+gdn_status varlen_causal_conv_with_state(const gdn_conv_args *a, gdn_stream_t stream) {
+    if (!a) return GDN_ERR_NULL;
+    if (a->io_dtype != GDN_F32 && a->io_dtype != GDN_F16) return GDN_ERR_DTYPE;
+    if (a->activation != GDN_ACT_NONE && a->activation != GDN_ACT_SILU) return GDN_ERR_ARG;
+    const int vec = a->io_dtype == GDN_F16 ? 8 : 4;
+    const size_t esz = a->io_dtype == GDN_F16 ? 2 : 4;
+    if (a->num_seqs < 0 || a->num_seqs > 65535 || a->total_tokens < 0 || a->channels <= 0 ||
+        a->channels % vec != 0 || a->kernel_size < 2 || a->kernel_size > 4 || a->state_update_capacity < 0)
+        return GDN_ERR_SHAPE;
+    if (a->x_stride != 0 && a->x_stride < a->channels) return GDN_ERR_SHAPE;
+    if (a->num_seqs == 0) return GDN_OK;
+    if (a->num_state_slots < 1 || (!a->state_slots && a->num_state_slots < a->num_seqs)) return GDN_ERR_SHAPE;
+    if (!a->cu_seqlens || !a->weight || !a->final_state) return GDN_ERR_NULL;
+    if (a->total_tokens > 0 && (!a->x || !a->output)) return GDN_ERR_NULL;
+    if (a->state_update_capacity > 0 && !a->state_update) return GDN_ERR_NULL;
+    const int64_t xs = a->x_stride ? a->x_stride : a->channels;
+    if (!aligned16(a->x) || !aligned16(a->output) || (a->state_update_capacity > 0 && !aligned16(a->state_update)) ||
+        (xs * (int64_t)esz) % 16 != 0)
+        return GDN_ERR_ALIGN;
+    gdn::ConvParams p{};
+    p.B = a->num_seqs;
+    p.T = a->total_tokens;
+    p.C = a->channels;
+    p.K = a->kernel_size;
+    p.num_slots = a->num_state_slots;
+    p.io_f16 = a->io_dtype == GDN_F16;
+    p.silu = a->activation == GDN_ACT_SILU;
+    p.cap = a->state_update_capacity;
+    p.x_stride = xs;
+    p.x = a->x;
+    p.w = a->weight;
+    p.bias = a->bias;
+    p.cu = a->cu_seqlens;
+    p.slots = a->state_slots;
+    p.capture_count = a->capture_count;
+    p.state_in = a->initial_state;
+    p.state_out = a->final_state;
+    p.out = a->output;
+    p.values = p.cap > 0 ? a->state_update : nullptr;
+    p.status = a->status;
+    // enough token blocks to give every SM a few CTAs, at most 64 tokens each
+    const long long cblocks = (a->channels / vec + 255) / 256;
+    long long tpc = (long long)a->total_tokens * cblocks / 608;
+    p.tokens_per_cta = (int)(tpc < 1 ? 1 : (tpc > 64 ? 64 : tpc));
+    if (gdn::launch_conv(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+gdn_status causal_conv_replay_prefix(void *conv_states, int32_t num_slots, int32_t num_requests, int32_t channels,
+                                     int32_t kernel_size, int32_t io_dtype, const int32_t *src_slots,
+                                     const int32_t *dst_slots, const void *state_update, int32_t capacity,
+                                     const int32_t *accept_len, int32_t *status, gdn_stream_t stream) {
+    if (io_dtype != GDN_F32 && io_dtype != GDN_F16) return GDN_ERR_DTYPE;
+    const int vec = io_dtype == GDN_F16 ? 8 : 4;
+    if (num_requests < 0 || num_requests > 65535 || capacity < 0 || channels <= 0 || channels % vec != 0 ||
+        kernel_size < 2 || kernel_size > 4)
+        return GDN_ERR_SHAPE;
+    if (num_requests == 0) return GDN_OK;
+    if (num_slots < 1) return GDN_ERR_SHAPE;
+    if (!conv_states || !src_slots || !dst_slots || !accept_len) return GDN_ERR_NULL;
+    if (capacity > 0 && !state_update) return GDN_ERR_NULL;
+    if (capacity > 0 && !aligned16(state_update)) return GDN_ERR_ALIGN;
+    gdn::ConvReplayParams p{};
+    p.R = num_requests;
+    p.C = channels;
+    p.K = kernel_size;
+    p.num_slots = num_slots;
+    p.cap = capacity;
+    p.io_f16 = io_dtype == GDN_F16;
+    p.states = conv_states;
+    p.values = state_update;
+    p.src = src_slots;
+    p.dst = dst_slots;
+    p.n = accept_len;
+    p.status = status;
+    if (gdn::launch_conv_replay(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
 }  // extern "C"

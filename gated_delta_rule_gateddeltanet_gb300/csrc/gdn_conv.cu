@@ -1,0 +1,306 @@
+// Packed depthwise causal convolution with carried state (and SiLU), its
+// compact value capture, and replay of an accepted prefix of captured values.
+//
+// Source: "[CUDA] Add compact GatedDeltaNet operator", embedded commit "Add
+// compact VarlenCausalConv state updates" (Description, Motivation): packed
+// token-major inputs [num_tokens, channels], a per-request state of the
+// kernel_size - 1 preceding inputs per channel, three outputs [output,
+// final_state, state_update] where state_update holds only the appended
+// values [batch, state_update_capacity, channels], bounded by an optional
+// per-request capture_count; "Add GatedDeltaNet evaluation export for Qwen
+// hybrid models" (Copilot overview): fused depthwise conv1d + SiLU + carried
+// state.
+//
+//   y[t, c] = silu(bias[c] + sum_{j<K} w[c, j] x_ext[t - (K-1) + j, c])
+// where x_ext is the sequence's state (oldest first) followed by its tokens.
+//
+// The path is HBM-bound (K multiply-adds per element moved), so the kernels
+// are laid out for bandwidth: a thread owns 16 bytes of channels (8 fp16 or 4
+// fp32) and a CTA a block of consecutive packed tokens, so every load and
+// store of x, y and the capture is a coalesced 16-byte vector.  Token blocks
+// are independent: the K-1 inputs before a block come from x itself or, at a
+// sequence start, from the state.  The state is therefore only read by the
+// conv kernel; a second small kernel rolls each sequence's state forward
+// afterwards (same thread reads then writes), so updating the state in place
+// is race-free.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int NT = 256;
+
+template <typename T>
+struct Vec;  // 16 bytes of channels
+template <>
+struct Vec<__half> {
+    static constexpr int N = 8;
+};
+template <>
+struct Vec<float> {
+    static constexpr int N = 4;
+};
+
+template <typename T>
+__device__ __forceinline__ void load_vec(const T *p, float (&v)[Vec<T>::N]) {
+    const uint4 raw = *reinterpret_cast<const uint4 *>(p);
+    const T *e = reinterpret_cast<const T *>(&raw);
+#pragma unroll
+    for (int i = 0; i < Vec<T>::N; ++i) v[i] = to_f32(e[i]);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_vec(T *p, const float (&v)[Vec<T>::N]) {
+    uint4 raw;
+    T *e = reinterpret_cast<T *>(&raw);
+#pragma unroll
+    for (int i = 0; i < Vec<T>::N; ++i) e[i] = from_f32<T>(v[i]);
+    *reinterpret_cast<uint4 *>(p) = raw;
+}
+
+__device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
+
+// Sequence holding packed token t: the largest b with cu[b] <= t.
+__device__ __forceinline__ int seq_of(const int32_t *cu, int B, int t) {
+    int lo = 0, hi = B;  // cu[lo] <= t < cu[hi] for a valid packing
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cu[mid] <= t) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+template <typename T, int K>
+__global__ void __launch_bounds__(NT) conv_kernel(const ConvParams p) {
+    constexpr int V = Vec<T>::N;
+    const int cgroups = p.C / V;
+    const int cg = blockIdx.y * NT + threadIdx.x;  // channel group of this thread
+    const int t_begin = blockIdx.x * p.tokens_per_cta;
+    const int t_end = min(t_begin + p.tokens_per_cta, p.T);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && (p.cu[0] != 0 || p.cu[p.B] != p.T))
+        flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
+    if (cg >= cgroups || t_begin >= t_end) return;
+    const int c0 = cg * V;
+    const T *x = static_cast<const T *>(p.x);
+    T *y = static_cast<T *>(p.out);
+    T *vals = static_cast<T *>(p.values);
+    const T *st_in = static_cast<const T *>(p.state_in);
+
+    float w[V][K], bias[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+#pragma unroll
+        for (int j = 0; j < K; ++j) w[i][j] = p.w[(long long)(c0 + i) * K + j];
+        bias[i] = p.bias ? p.bias[c0 + i] : 0.f;
+    }
+
+    int b = seq_of(p.cu, p.B, t_begin);
+    int bos = 0, eos = 0, slot = 0, ncap = 0;
+    bool ok = false;
+    float win[K - 1][V];  // inputs at t-(K-1) .. t-1 (oldest first)
+    auto enter = [&](int t) {  // (re)build the window for token t of sequence b
+        bos = p.cu[b];
+        eos = p.cu[b + 1];
+        slot = p.slots ? p.slots[b] : b;
+        ok = bos >= 0 && eos >= bos && eos <= p.T && slot >= 0 && slot < p.num_slots;
+        ncap = p.cap;
+        if (p.capture_count) {
+            const int cc = p.capture_count[b];
+            if (cc < 0 || cc > p.cap) {
+                if (threadIdx.x == 0 && t == bos) flag_error(p.status, GDN_DEVERR_CAPTURE_COUNT);
+                ncap = 0;
+            } else {
+                ncap = cc;
+            }
+        }
+        if (!ok) {
+            if (threadIdx.x == 0 && t == bos) {
+                if (slot < 0 || slot >= p.num_slots) flag_error(p.status, GDN_DEVERR_STATE_SLOT);
+                else flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
+            }
+            return;
+        }
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) {
+            const int pos = t - (K - 1) + j;  // packed position of window entry j
+            float v[V];
+            if (pos >= bos) {
+                load_vec<T>(x + (long long)pos * p.x_stride + c0, v);
+            } else if (st_in) {
+                const int sj = (K - 1) - (bos - pos);  // state index, oldest first
+                const T *sp = st_in + ((long long)slot * p.C + c0) * (K - 1) + sj;
+#pragma unroll
+                for (int i = 0; i < V; ++i) v[i] = to_f32(sp[i * (K - 1)]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < V; ++i) v[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < V; ++i) win[j][i] = v[i];
+        }
+    };
+    while (b < p.B && p.cu[b + 1] <= t_begin) ++b;  // skip empty sequences
+    if (b >= p.B) return;
+    enter(t_begin);
+    for (int t = t_begin; t < t_end; ++t) {
+        while (t >= eos && b + 1 < p.B) {  // next sequence starts here
+            ++b;
+            enter(t);
+        }
+        if (!ok || t >= eos) continue;
+        float xt[V];
+        load_vec<T>(x + (long long)t * p.x_stride + c0, xt);
+        float yv[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            float acc = bias[i];
+#pragma unroll
+            for (int j = 0; j < K - 1; ++j) acc = fmaf(w[i][j], win[j][i], acc);
+            acc = fmaf(w[i][K - 1], xt[i], acc);
+            yv[i] = p.silu ? silu(acc) : acc;
+        }
+        store_vec<T>(y + (long long)t * p.C + c0, yv);
+        const int tl = t - bos;
+        if (vals && tl < ncap) store_vec<T>(vals + ((long long)b * p.cap + tl) * p.C + c0, xt);
+#pragma unroll
+        for (int j = 0; j + 1 < K - 1; ++j)
+#pragma unroll
+            for (int i = 0; i < V; ++i) win[j][i] = win[j + 1][i];
+#pragma unroll
+        for (int i = 0; i < V; ++i) win[K - 2][i] = xt[i];
+    }
+}
+
+// new state = the last K-1 entries of (old state, the sequence's tokens)
+template <typename T, int K>
+__global__ void __launch_bounds__(NT) conv_state_kernel(const ConvParams p) {
+    constexpr int V = Vec<T>::N;
+    const int cg = blockIdx.x * NT + threadIdx.x;
+    const int b = blockIdx.y;
+    if (cg >= p.C / V) return;
+    const int bos = p.cu[b], eos = p.cu[b + 1];
+    const int slot = p.slots ? p.slots[b] : b;
+    if (bos < 0 || eos < bos || eos > p.T || slot < 0 || slot >= p.num_slots) return;  // flagged by conv_kernel
+    const int c0 = cg * V;
+    const T *x = static_cast<const T *>(p.x);
+    const T *st_in = static_cast<const T *>(p.state_in);
+    T *st_out = static_cast<T *>(p.state_out);
+    const int len = eos - bos;
+    T nw[V][K - 1];
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j) {
+        const int from_end = (K - 1) - j;  // entry j of the new state is the from_end-th last input
+        if (from_end <= len) {
+            const T *xp = x + (long long)(eos - from_end) * p.x_stride + c0;
+            const uint4 raw = *reinterpret_cast<const uint4 *>(xp);
+            const T *e = reinterpret_cast<const T *>(&raw);
+#pragma unroll
+            for (int i = 0; i < V; ++i) nw[i][j] = e[i];
+        } else {
+            const int sj = j + len;  // shifted left by len within the old state
+#pragma unroll
+            for (int i = 0; i < V; ++i)
+                nw[i][j] = st_in ? st_in[((long long)slot * p.C + c0 + i) * (K - 1) + sj] : from_f32<T>(0.f);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) st_out[((long long)slot * p.C + c0 + i) * (K - 1) + j] = nw[i][j];
+}
+
+// Replay: state[dst] = the last K-1 entries of (state[src], values[j, 0..n))
+template <typename T, int K>
+__global__ void __launch_bounds__(NT) conv_replay_kernel(const ConvReplayParams p) {
+    constexpr int V = Vec<T>::N;
+    const int cg = blockIdx.x * NT + threadIdx.x;
+    const int j = blockIdx.y;
+    const int src = p.src[j], dst = p.dst[j], n = p.n[j];
+    const bool leader = blockIdx.x == 0 && threadIdx.x == 0;
+    if (src < 0 || src >= p.num_slots || dst < 0 || dst >= p.num_slots) {
+        if (leader) flag_error(p.status, GDN_DEVERR_REPLAY_SLOT);
+        return;
+    }
+    if (n < 0 || n > p.cap) {
+        if (leader) flag_error(p.status, GDN_DEVERR_ACCEPT_LEN);
+        return;
+    }
+    if (cg >= p.C / V || (src == dst && n == 0)) return;
+    const int c0 = cg * V;
+    T *states = static_cast<T *>(p.states);
+    const T *vals = static_cast<const T *>(p.values);
+    T nw[V][K - 1];
+#pragma unroll
+    for (int e = 0; e < K - 1; ++e) {
+        const int from_end = (K - 1) - e;
+        if (from_end <= n) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(vals + ((long long)j * p.cap + n - from_end) * p.C + c0);
+            const T *el = reinterpret_cast<const T *>(&raw);
+#pragma unroll
+            for (int i = 0; i < V; ++i) nw[i][e] = el[i];
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) nw[i][e] = states[((long long)src * p.C + c0 + i) * (K - 1) + e + n];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+#pragma unroll
+        for (int e = 0; e < K - 1; ++e) states[((long long)dst * p.C + c0 + i) * (K - 1) + e] = nw[i][e];
+}
+
+template <typename T, int K>
+cudaError_t launch_conv_k(const ConvParams &p, cudaStream_t stream) {
+    constexpr int V = Vec<T>::N;
+    const int cgroups = p.C / V;
+    const int cblocks = (cgroups + NT - 1) / NT;
+    if (p.T > 0) {
+        dim3 grid((unsigned)((p.T + p.tokens_per_cta - 1) / p.tokens_per_cta), (unsigned)cblocks);
+        conv_kernel<T, K><<<grid, NT, 0, stream>>>(p);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    dim3 g2((unsigned)cblocks, (unsigned)p.B);
+    conv_state_kernel<T, K><<<g2, NT, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T, int K>
+cudaError_t launch_replay_k(const ConvReplayParams &p, cudaStream_t stream) {
+    constexpr int V = Vec<T>::N;
+    dim3 grid((unsigned)((p.C / V + NT - 1) / NT), (unsigned)p.R);
+    conv_replay_kernel<T, K><<<grid, NT, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_conv_t(const ConvParams &p, cudaStream_t s) {
+    switch (p.K) {
+        case 2: return launch_conv_k<T, 2>(p, s);
+        case 3: return launch_conv_k<T, 3>(p, s);
+        default: return launch_conv_k<T, 4>(p, s);
+    }
+}
+
+template <typename T>
+cudaError_t launch_replay_t(const ConvReplayParams &p, cudaStream_t s) {
+    switch (p.K) {
+        case 2: return launch_replay_k<T, 2>(p, s);
+        case 3: return launch_replay_k<T, 3>(p, s);
+        default: return launch_replay_k<T, 4>(p, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_conv(const ConvParams &p, cudaStream_t stream) {
+    if (p.B == 0) return cudaSuccess;
+    return p.io_f16 ? launch_conv_t<__half>(p, stream) : launch_conv_t<float>(p, stream);
+}
+
+cudaError_t launch_conv_replay(const ConvReplayParams &p, cudaStream_t stream) {
+    if (p.R == 0) return cudaSuccess;
+    return p.io_f16 ? launch_replay_t<__half>(p, stream) : launch_replay_t<float>(p, stream);
+}
+
+}  // namespace gdn

@@ -39,6 +39,29 @@ struct ReplayParams {
     int32_t *status;
 };
 
+// Packed causal convolution (see gdn_conv.cu).
+struct ConvParams {
+    int B, T, C, K, num_slots, io_f16, silu, cap, tokens_per_cta;
+    long long x_stride;
+    const void *x;
+    const float *w, *bias;
+    const int32_t *cu, *slots, *capture_count;
+    const void *state_in;
+    void *state_out, *out, *values;
+    int32_t *status;
+};
+
+struct ConvReplayParams {
+    int R, C, K, num_slots, cap, io_f16;
+    void *states;
+    const void *values;
+    const int32_t *src, *dst, *n;
+    int32_t *status;
+};
+
+cudaError_t launch_conv(const ConvParams &p, cudaStream_t stream);
+cudaError_t launch_conv_replay(const ConvReplayParams &p, cudaStream_t stream);
+
 cudaError_t launch_recurrent(const ForwardParams &p, cudaStream_t stream);
 cudaError_t launch_replay(const ReplayParams &p, cudaStream_t stream);
 

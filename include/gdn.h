@@ -70,6 +70,7 @@ enum {
 #define GDN_DEVERR_ACCEPT_LEN 0x4  /* accept_len[j] outside [0, capacity] */
 #define GDN_DEVERR_REPLAY_SLOT 0x8 /* a replay source or destination slot out of range */
 #define GDN_DEVERR_TIMEOUT 0x10    /* a bounded wait inside a kernel gave up (the unit is not written) */
+#define GDN_DEVERR_CAPTURE_COUNT 0x20 /* conv: capture_count[b] outside [0, capacity] (nothing captured) */
 
 /*
  * Arguments of gdn_forward.
@@ -220,6 +221,91 @@ gdn_status gdn_replay_prefix(float *state_banks, int32_t num_slots, int32_t num_
  */
 #define GDN_NO_ALLOC_MAX_SEQS 4094
 gdn_status gdn_forward_no_alloc(const gdn_forward_args *args, gdn_stream_t stream);
+
+/* Activation applied after the causal convolution. */
+enum { GDN_ACT_NONE = 0, GDN_ACT_SILU = 1 };
+
+/*
+ * Arguments of varlen_causal_conv_with_state.
+ *
+ * Source: "[CUDA] Add compact GatedDeltaNet operator", embedded commit "Add
+ * compact VarlenCausalConv state updates" (Description): packed token-major
+ * input [num_tokens, channels], a per-request state of the kernel_size - 1
+ * preceding inputs of every channel, three outputs [output, final_state,
+ * state_update] where state_update holds only the appended input values,
+ * [batch, state_update_capacity, channels], bounded by an optional
+ * per-request capture_count; "Add GatedDeltaNet evaluation export for Qwen
+ * hybrid models" (Copilot overview): fused depthwise conv1d + SiLU + carried
+ * state.
+ *
+ * For token t of sequence b and channel c, with x_ext the sequence's state
+ * (oldest first) followed by its tokens:
+ *   y[t, c] = act(bias[c] + sum_{j<K} weight[c, j] * x_ext[t - (K-1) + j, c])
+ *
+ * Layouts (T = total_tokens, B = num_seqs, C = channels, K = kernel_size):
+ *   x             device [T, C] io_dtype; token stride x_stride elements (0 = C)
+ *   weight        device [C, K] FP32;  bias device [C] FP32 or NULL
+ *   cu_seqlens    device [B+1] int32;  state_slots device [B] int32 or NULL
+ *   capture_count device [B] int32 in [0, capacity], or NULL (capture up to
+ *                 capacity tokens of every sequence)
+ *   initial_state device [num_state_slots, C, K-1] io_dtype (oldest input
+ *                 first), or NULL for zeros
+ *   final_state   device, same shape; may equal initial_state (in place):
+ *                 becomes the last K-1 inputs of (state, tokens)
+ *   output        device [T, C] io_dtype
+ *   state_update  device [B, capacity, C] io_dtype, or NULL when capacity = 0:
+ *                 row (b, i) = input of token i of sequence b, for
+ *                 i < min(len_b, capacity, capture_count[b]); other rows untouched
+ * C must be a multiple of 8 (fp16) or 4 (fp32); x, output and state_update
+ * 16-byte aligned; K in {2, 3, 4}.  Sequences must use distinct slots.
+ */
+typedef struct gdn_conv_args {
+    int32_t num_seqs;
+    int32_t total_tokens;
+    int32_t channels;
+    int32_t kernel_size;
+    int32_t num_state_slots;
+    int32_t io_dtype;              /* GDN_F32 or GDN_F16 */
+    int32_t activation;            /* GDN_ACT_* */
+    int32_t state_update_capacity; /* 0 = no capture */
+    int64_t x_stride;
+    const void *x;
+    const float *weight;
+    const float *bias;
+    const int32_t *cu_seqlens;
+    const int32_t *state_slots;
+    const int32_t *capture_count;
+    const void *initial_state;
+    void *final_state;
+    void *output;
+    void *state_update;
+    int32_t *status;
+} gdn_conv_args;
+
+/*
+ * Runs the packed causal convolution (see gdn_conv_args); asynchronous on
+ * `stream`.  Device-side data errors set GDN_DEVERR_CU_SEQLENS,
+ * GDN_DEVERR_STATE_SLOT or GDN_DEVERR_CAPTURE_COUNT and skip the sequence.
+ */
+gdn_status varlen_causal_conv_with_state(const gdn_conv_args *args, gdn_stream_t stream);
+
+/*
+ * Replays an accepted prefix of captured conv inputs into an inactive state
+ * bank: for request j, conv_states[dst_slots[j]] = the last K-1 entries of
+ * (conv_states[src_slots[j]], state_update[j, 0 .. accept_len[j])).
+ * Source: "Replay compact fixed state for hybrid decoding" (Summary, Key
+ * changes): compact convolution values replayed into inactive banks.
+ *   conv_states  device [num_slots, C, K-1] io_dtype
+ *   state_update device [num_requests, capacity, C] io_dtype (the capture of
+ *                varlen_causal_conv_with_state)
+ *   src_slots, dst_slots, accept_len  device [num_requests] int32
+ * accept_len[j] = 0 copies the source state.  A destination may equal its own
+ * source but must not be another request's source or destination.
+ */
+gdn_status causal_conv_replay_prefix(void *conv_states, int32_t num_slots, int32_t num_requests, int32_t channels,
+                                     int32_t kernel_size, int32_t io_dtype, const int32_t *src_slots,
+                                     const int32_t *dst_slots, const void *state_update, int32_t capacity,
+                                     const int32_t *accept_len, int32_t *status, gdn_stream_t stream);
 
 /* A static, human-readable name for a status code. */
 const char *gdn_status_string(gdn_status status);

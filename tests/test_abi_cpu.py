@@ -157,3 +157,63 @@ def test_forced_chunked_plan_needs_d128_and_workspace(lib):
     assert lib.gdn_forward(ctypes.byref(_args(max_seqlen=-1)), None) == 3
     # forced chunked plan without workspace
     assert lib.gdn_forward(ctypes.byref(_args(plan=2)), None) == 5
+
+
+def _conv_args(**kw):
+    import gated_delta_rule_gateddeltanet_gb300 as g
+    a = g.ConvArgs()
+    a.num_seqs, a.total_tokens, a.channels, a.kernel_size = 2, 8, 10240, 4
+    a.num_state_slots, a.io_dtype, a.activation = 2, 1, 1
+    fake = ctypes.c_void_p(0x1000)
+    for f in ("x", "weight", "cu_seqlens", "final_state", "output"):
+        setattr(a, f, fake)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(io_dtype=2), 2),                 # BF16 rejected
+    (dict(channels=10), 3),                # not a multiple of 8 fp16 channels
+    (dict(kernel_size=5), 3),
+    (dict(kernel_size=1), 3),
+    (dict(state_update_capacity=-1), 3),
+    (dict(x_stride=100), 3),
+    (dict(num_state_slots=1), 3),
+    (dict(activation=3), 8),
+    (dict(weight=None), 1),
+    (dict(cu_seqlens=None), 1),
+    (dict(state_update_capacity=2), 1),    # capture requested without a buffer
+    (dict(x=ctypes.c_void_p(0x1008)), 4),
+    (dict(x_stride=10244), 4),             # 10244 fp16 = 20488 bytes, not a multiple of 16
+])
+def test_conv_rejects_bad_arguments_before_launch(lib, kw, code):
+    a = _conv_args(**kw)
+    assert lib.varlen_causal_conv_with_state(ctypes.byref(a), None) == code
+
+
+def test_conv_args_layout_matches_c(tmp_path):
+    import gated_delta_rule_gateddeltanet_gb300 as g
+    fields = [f for f, _ in g.ConvArgs._fields_]
+    src = tmp_path / "layout.c"
+    body = "\n".join(f'printf("{f} %zu\\n", offsetof(gdn_conv_args, {f}));' for f in fields)
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gdn.h"\nint main(void){\n'
+                   + body + '\nprintf("sizeof %zu\\n", sizeof(gdn_conv_args));\nreturn 0;}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    for f in fields:
+        assert int(got[f]) == getattr(g.ConvArgs, f).offset, f
+    assert int(got["sizeof"]) == ctypes.sizeof(g.ConvArgs)
+
+
+def test_conv_replay_rejects_bad_arguments(lib):
+    f = lib.causal_conv_replay_prefix
+    fake = ctypes.c_void_p(0x1000)
+    assert f(fake, 4, 2, 10240, 4, 2, fake, fake, fake, 4, fake, None, None) == 2
+    assert f(fake, 4, 2, 10, 4, 1, fake, fake, fake, 4, fake, None, None) == 3
+    assert f(fake, 4, 2, 10240, 7, 1, fake, fake, fake, 4, fake, None, None) == 3
+    assert f(None, 4, 2, 10240, 4, 1, fake, fake, fake, 4, fake, None, None) == 1
+    assert f(fake, 4, 2, 10240, 4, 1, fake, fake, None, 4, fake, None, None) == 1
+    assert f(fake, 4, 0, 10240, 4, 1, None, None, None, 0, None, None, None) == 0

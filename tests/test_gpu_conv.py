@@ -1,0 +1,152 @@
+"""GPU parity of the packed causal convolution, its compact capture and its
+replay against the FP64 oracle, through the C ABI.
+
+Tolerance (max-relative per tensor): FP32 I/O 1e-5; FP16 outputs 2e-3 (one
+FP16 rounding).  The state and the captured values are copies of inputs, so
+they must match bit for bit; so must a replay of captured values.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import max_rel
+from gpu_common import to_dev, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(seed, lengths, C, K, io, slots=None, num_slots=None, state=True):
+    rng = np.random.default_rng(seed)
+    T = int(sum(lengths))
+    x = rng.standard_normal((T, C)).astype(io)
+    w = (rng.standard_normal((C, K)) / 2).astype(np.float32)
+    bias = (rng.standard_normal(C) / 4).astype(np.float32)
+    S = num_slots or len(lengths)
+    st = rng.standard_normal((S, C, K - 1)).astype(io) if state else None
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    return x, w, bias, st, cu
+
+
+def _gpu(x, w, bias, st, cu, *, cap=0, capture_count=None, slots=None, in_place=True, activation="silu",
+         num_slots=None, status=None):
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    init = to_dev(st)
+    S = st.shape[0] if st is not None else (num_slots or len(cu) - 1)
+    C, K = w.shape
+    if in_place and init is not None:
+        final = init
+    else:
+        final = torch.full((S, C, K - 1), float("nan"), dtype=torch.float16 if x.dtype == np.float16 else
+                           torch.float32, device=dev())
+        if init is not None:
+            final.copy_(init)
+    out, final, vals = gdn.varlen_causal_conv_with_state(
+        to_dev(x), to_dev(w), to_dev(cu), bias=to_dev(bias), initial_state=init, final_state=final,
+        state_slots=to_dev(slots), capture_count=to_dev(capture_count), capacity=cap, activation=activation,
+        status=status, num_state_slots=S)
+    torch.cuda.synchronize()
+    return (out.double().cpu().numpy(), final.double().cpu().numpy(),
+            None if vals is None else vals.double().cpu().numpy())
+
+
+def _oracle(x, w, bias, st, cu, *, cap=0, capture_count=None, slots=None, num_slots=None):
+    S = st.shape[0] if st is not None else (num_slots or len(cu) - 1)
+    C, K = w.shape
+    st0 = st if st is not None else np.zeros((S, C, K - 1))
+    return oracle.conv_forward(x, w, cu, st0, bias=bias, state_slots=slots, capacity=cap,
+                               capture_count=capture_count)
+
+
+@pytest.mark.parametrize("io", [np.float16, np.float32])
+@pytest.mark.parametrize("K", [4, 3, 2])
+def test_conv_ragged_many_token_blocks(io, K):
+    lengths = [300, 5, 1, 0, 70, 2, 1700]  # long sequences span many token blocks
+    x, w, bias, st, cu = _inputs(40 + K, lengths, 512, K, io)
+    cap = 6
+    cc = np.array([6, 3, 0, 2, 6, 1, 4], np.int32)
+    got = _gpu(x, w, bias, st, cu, cap=cap, capture_count=cc)
+    want = _oracle(x, w, bias, st, cu, cap=cap, capture_count=cc)
+    tol = 2e-3 if io == np.float16 else 1e-5
+    assert max_rel(got[0], want[0]) <= tol
+    assert np.array_equal(got[1], want[1])  # the state is a copy of inputs
+    for s, L in enumerate(lengths):
+        n = min(L, cap, cc[s])
+        assert np.array_equal(got[2][s, :n], want[2][s, :n])
+        assert np.all(got[2][s, n:] == 0)  # rows past the capture stay untouched (zero-initialised)
+
+
+def test_conv_out_of_place_zero_state_and_slots():
+    lengths = [64, 3, 129]
+    x, w, bias, _, cu = _inputs(50, lengths, 256, 4, np.float32, state=False)
+    got = _gpu(x, w, bias, None, cu, in_place=False, num_slots=3)
+    want = _oracle(x, w, bias, None, cu, num_slots=3)
+    assert max_rel(got[0], want[0]) <= 1e-5
+    assert np.array_equal(got[1], want[1])
+    x, w, bias, st, cu = _inputs(51, lengths, 256, 4, np.float16, num_slots=6)
+    slots = np.array([5, 0, 3], np.int32)
+    got = _gpu(x, w, bias, st, cu, slots=slots, in_place=False)
+    want = _oracle(x, w, bias, st, cu, slots=slots)
+    assert max_rel(got[0], want[0]) <= 2e-3
+    assert np.array_equal(got[1], want[1])  # written slots and untouched ones
+
+
+def test_conv_qwen_geometry_decode_and_prefill():
+    """The conv in front of the GatedDeltaNet of the Qwen3.5/3.8 linear-attention
+    layers: channels = 2*16*128 + 48*128 = 10240, kernel 4, fp16: a 64 x 1-token
+    decode step and an 8-sequence varlen prefill."""
+    from gated_delta_rule_gateddeltanet_gb300 import workloads as wl
+    C = 10240
+    x, w, bias, st, cu = _inputs(52, [1] * 64, C, 4, np.float16)
+    got = _gpu(x, w, bias, st, cu, cap=1)
+    want = _oracle(x, w, bias, st, cu, cap=1)
+    assert max_rel(got[0], want[0]) <= 2e-3 and np.array_equal(got[1], want[1])
+    assert np.array_equal(got[2], want[2])
+    lengths = wl.varlen_prefill_lengths()
+    x, w, bias, st, cu = _inputs(53, lengths, C, 4, np.float16)
+    got = _gpu(x, w, bias, st, cu)
+    want = _oracle(x, w, bias, st, cu)
+    assert max_rel(got[0], want[0]) <= 2e-3 and np.array_equal(got[1], want[1])
+
+
+def test_conv_pack_equals_one_by_one_bitwise():
+    lengths = [17, 512, 1, 93]
+    x, w, bias, st, cu = _inputs(54, lengths, 1024, 4, np.float16)
+    got = _gpu(x, w, bias, st, cu, cap=4, in_place=False)
+    for s, L in enumerate(lengths):
+        t0, t1 = cu[s], cu[s + 1]
+        one = _gpu(x[t0:t1], w, bias, st[s:s + 1], np.array([0, L], np.int32), cap=4, in_place=False)
+        assert np.array_equal(got[0][t0:t1], one[0])
+        assert np.array_equal(got[1][s], one[1][0])
+        assert np.array_equal(got[2][s], one[2][0])
+
+
+def test_conv_replay_every_prefix():
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    L, C, K = 6, 256, 4
+    x, w, bias, st, cu = _inputs(55, [L], C, K, np.float16)
+    _, _, vals = _gpu(x, w, bias, st, cu, cap=L, in_place=False)
+    R = L + 1
+    states = torch.zeros((2 * R, C, K - 1), dtype=torch.float16, device=dev())
+    states[:R] = to_dev(st)
+    vals_dev = to_dev(vals.astype(np.float16)).expand(R, L, C).contiguous()
+    gdn.causal_conv_replay_prefix(states, to_dev(np.arange(R, dtype=np.int32)),
+                                  to_dev(np.arange(R, 2 * R, dtype=np.int32)), vals_dev,
+                                  to_dev(np.arange(R, dtype=np.int32)))
+    torch.cuda.synchronize()
+    got = states.double().cpu().numpy()
+    for n in range(R):
+        _, st_n, _ = oracle.conv_forward(x[:n], w, np.array([0, n]), st, bias=bias)
+        assert np.array_equal(got[R + n], st_n[0])
+        assert np.array_equal(got[n], st[0].astype(np.float64))  # sources untouched
+
+
+def test_conv_status_flags():
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    x, w, bias, st, cu = _inputs(56, [4, 3], 64, 4, np.float32)
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    _gpu(x, w, bias, st, cu, cap=2, capture_count=np.array([3, 1], np.int32), status=status)
+    assert status.item() & gdn.DEVERR["capture_count"]
+    status.zero_()
+    _gpu(x, w, bias, st, cu, slots=np.array([0, 7], np.int32), status=status)
+    assert status.item() & gdn.DEVERR["state_slot"]
