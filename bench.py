@@ -260,6 +260,7 @@ def run_gdn(a, dist: Dist):
     if not a.no_extra and dist.rank == 0:
         extra["prefill"] = run_prefill(dev, stream)
         extra["spec_verify_replay"] = run_spec(dev, stream, lib, sh)
+        extra["causal_conv"] = run_conv(dev, stream)
 
     cpu = None
     if not a.no_cpu and dist.rank == 0 and dist.world == 1:
@@ -461,6 +462,49 @@ def run_spec(dev, stream, lib, sh):
             "replay_frac_hbm": round(rep_bytes / (res["replay"] / 1e3) / 1e9 / hbm_peak, 4),
             "verify_gbs": round(ver_bytes / (res["verify"] / 1e3) / 1e9, 1),
             "l2": f"{NBUF} rotating state pools of 96 MiB"}
+
+
+def run_conv(dev, stream):
+    """The packed causal conv in front of the GatedDeltaNet (channels 2*16*128
+    + 48*128 = 10240, kernel 4, fp16, SiLU, state updated in place) on the
+    decode step (64 x 1 token, capture of 1 token) and on the varlen prefill."""
+    import torch
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    from gated_delta_rule_gateddeltanet_gb300 import workloads as wl
+    C, K = 10240, 4
+    hbm, _, kind = measured_peaks()
+    res = {}
+    for name, lengths, cap in (("decode", [1] * 64, 1), ("prefill", list(wl.varlen_prefill_lengths()), 0)):
+        rng = np.random.default_rng(77)
+        T, B = int(sum(lengths)), len(lengths)
+        x = torch.from_numpy(rng.standard_normal((T, C), dtype=np.float32).astype(np.float16)).to(dev)
+        w = torch.from_numpy(rng.standard_normal((C, K), dtype=np.float32)).to(dev)
+        bias = torch.zeros(C, dtype=torch.float32, device=dev)
+        cu = torch.from_numpy(wl.cu_from_lengths(lengths)).to(dev)
+        states = [torch.zeros((B, C, K - 1), dtype=torch.float16, device=dev) for _ in range(NBUF)]
+        out = torch.empty((T, C), dtype=torch.float16, device=dev)
+        caps = torch.zeros((B, max(cap, 1), C), dtype=torch.float16, device=dev)
+        run = lambda i: gdn.varlen_causal_conv_with_state(x, w, cu, bias=bias, initial_state=states[i % NBUF],
+                                                          final_state=states[i % NBUF], output=out,
+                                                          state_update=caps if cap else None, capacity=cap)
+        for i in range(5):
+            run(i)
+        torch.cuda.synchronize()
+        n = 200 if name == "decode" else 20
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            run(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / n * 1e3
+        nbytes = T * C * 2 * 2 + B * C * (K - 1) * 2 * 2 + T * min(cap, 1) * C * 2 + C * (K + 1) * 4
+        res[name] = {"tokens": T, "us": round(us, 2), "tokens_per_s": round(T / (us / 1e6), 1),
+                     "gbs": round(nbytes / (us / 1e6) / 1e9, 1), "frac_hbm": round(nbytes / (us / 1e6) / 1e9 / hbm, 4),
+                     "algorithmic_bytes": nbytes}
+    res["workload"] = ("causal conv: channels 10240, kernel 4, fp16, SiLU, in-place state; decode 64 x 1 token "
+                       "(2 launches incl. state update, Python binding), prefill 8 x U[256,4096] tokens")
+    return res
 
 
 # ---------------------------------------------------------------- CPU oracle (baseline and reference arm)
