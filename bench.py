@@ -484,9 +484,15 @@ def run_conv(dev, stream):
         states = [torch.zeros((B, C, K - 1), dtype=torch.float16, device=dev) for _ in range(NBUF)]
         out = torch.empty((T, C), dtype=torch.float16, device=dev)
         caps = torch.zeros((B, max(cap, 1), C), dtype=torch.float16, device=dev)
-        run = lambda i: gdn.varlen_causal_conv_with_state(x, w, cu, bias=bias, initial_state=states[i % NBUF],
-                                                          final_state=states[i % NBUF], output=out,
-                                                          state_update=caps if cap else None, capacity=cap)
+        lib = gdn.load_library()
+        sh = ctypes.c_void_p(stream.cuda_stream)
+        args = [gdn.build_conv_args(x, w, cu, bias=bias, initial_state=states[i], final_state=states[i], output=out,
+                                    state_update=caps if cap else None, capacity=cap)[0] for i in range(NBUF)]
+
+        def run(i):
+            rc = lib.varlen_causal_conv_with_state(ctypes.byref(args[i % NBUF]), sh)
+            if rc:
+                raise gdn.GdnError(rc, "varlen_causal_conv_with_state")
         for i in range(5):
             run(i)
         torch.cuda.synchronize()
@@ -503,7 +509,7 @@ def run_conv(dev, stream):
                      "gbs": round(nbytes / (us / 1e6) / 1e9, 1), "frac_hbm": round(nbytes / (us / 1e6) / 1e9 / hbm, 4),
                      "algorithmic_bytes": nbytes}
     res["workload"] = ("causal conv: channels 10240, kernel 4, fp16, SiLU, in-place state; decode 64 x 1 token "
-                       "(2 launches incl. state update, Python binding), prefill 8 x U[256,4096] tokens")
+                       "(2 launches incl. state update, C ABI with prebuilt arguments), prefill 8 x U[256,4096] tokens")
     return res
 
 

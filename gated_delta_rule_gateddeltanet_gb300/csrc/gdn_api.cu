@@ -233,7 +233,7 @@ gdn_status varlen_causal_conv_with_state(const gdn_conv_args *a, gdn_stream_t st
     p.values = p.cap > 0 ? a->state_update : nullptr;
     p.status = a->status;
     // enough token blocks to give every SM a few CTAs, at most 64 tokens each
-    const long long cblocks = (a->channels / vec + 255) / 256;
+    const long long cblocks = (a->channels / 4 + 255) / 256;  // the kernel's threads own 4 channels
     long long tpc = (long long)a->total_tokens * cblocks / 608;
     p.tokens_per_cta = (int)(tpc < 1 ? 1 : (tpc > 64 ? 64 : tpc));
     if (gdn::launch_conv(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;

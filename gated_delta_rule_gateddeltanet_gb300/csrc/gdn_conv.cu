@@ -15,14 +15,19 @@
 // where x_ext is the sequence's state (oldest first) followed by its tokens.
 //
 // The path is HBM-bound (K multiply-adds per element moved), so the kernels
-// are laid out for bandwidth: a thread owns 16 bytes of channels (8 fp16 or 4
-// fp32) and a CTA a block of consecutive packed tokens, so every load and
-// store of x, y and the capture is a coalesced 16-byte vector.  Token blocks
+// are laid out for bandwidth: a thread owns 4 channels (an 8- or 16-byte
+// vector) and a CTA a block of consecutive packed tokens, so every load and
+// store of x, y and the capture is coalesced across the warp.  Each thread
+// issues the loads of GROUP tokens before computing any of them, so several
+// loads per thread are in flight (registers stay low enough for 8 CTAs per
+// SM).  Token blocks
 // are independent: the K-1 inputs before a block come from x itself or, at a
 // sequence start, from the state.  The state is therefore only read by the
 // conv kernel; a second small kernel rolls each sequence's state forward
 // afterwards (same thread reads then writes), so updating the state in place
 // is race-free.
+#include <type_traits>
+
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -30,32 +35,39 @@ namespace {
 
 constexpr int NT = 256;
 
+constexpr int GROUP = 4;  // tokens whose loads are issued together
+
+// A thread's 4 channels: one 8-byte (fp16) or 16-byte (fp32) vector.
 template <typename T>
-struct Vec;  // 16 bytes of channels
-template <>
-struct Vec<__half> {
-    static constexpr int N = 8;
-};
-template <>
-struct Vec<float> {
+struct Vec {
     static constexpr int N = 4;
+    using Raw = typename std::conditional<sizeof(T) == 2, uint2, uint4>::type;
 };
 
 template <typename T>
-__device__ __forceinline__ void load_vec(const T *p, float (&v)[Vec<T>::N]) {
-    const uint4 raw = *reinterpret_cast<const uint4 *>(p);
-    const T *e = reinterpret_cast<const T *>(&raw);
-#pragma unroll
-    for (int i = 0; i < Vec<T>::N; ++i) v[i] = to_f32(e[i]);
+__device__ __forceinline__ typename Vec<T>::Raw load_raw(const T *p) {
+    return __ldg(reinterpret_cast<const typename Vec<T>::Raw *>(p));  // read-only path: x is never written here
 }
 
 template <typename T>
-__device__ __forceinline__ void store_vec(T *p, const float (&v)[Vec<T>::N]) {
-    uint4 raw;
+__device__ __forceinline__ void unpack(const typename Vec<T>::Raw &raw, float (&v)[4]) {
+    const T *e = reinterpret_cast<const T *>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = to_f32(e[i]);
+}
+
+template <typename T>
+__device__ __forceinline__ void load_vec(const T *p, float (&v)[4]) {
+    unpack<T>(load_raw<T>(p), v);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_vec(T *p, const float (&v)[4]) {
+    typename Vec<T>::Raw raw;
     T *e = reinterpret_cast<T *>(&raw);
 #pragma unroll
-    for (int i = 0; i < Vec<T>::N; ++i) e[i] = from_f32<T>(v[i]);
-    *reinterpret_cast<uint4 *>(p) = raw;
+    for (int i = 0; i < 4; ++i) e[i] = from_f32<T>(v[i]);
+    *reinterpret_cast<typename Vec<T>::Raw *>(p) = raw;
 }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
@@ -71,7 +83,7 @@ __device__ __forceinline__ int seq_of(const int32_t *cu, int B, int t) {
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(NT) conv_kernel(const ConvParams p) {
+__global__ void __launch_bounds__(NT, 4) conv_kernel(const ConvParams p) {
     constexpr int V = Vec<T>::N;
     const int cgroups = p.C / V;
     const int cg = blockIdx.y * NT + threadIdx.x;  // channel group of this thread
@@ -142,32 +154,41 @@ __global__ void __launch_bounds__(NT) conv_kernel(const ConvParams p) {
     while (b < p.B && p.cu[b + 1] <= t_begin) ++b;  // skip empty sequences
     if (b >= p.B) return;
     enter(t_begin);
-    for (int t = t_begin; t < t_end; ++t) {
-        while (t >= eos && b + 1 < p.B) {  // next sequence starts here
-            ++b;
-            enter(t);
+    for (int tg = t_begin; tg < t_end; tg += GROUP) {
+        typename Vec<T>::Raw raw[GROUP];
+#pragma unroll
+        for (int g = 0; g < GROUP; ++g)
+            if (tg + g < t_end) raw[g] = load_raw<T>(x + (long long)(tg + g) * p.x_stride + c0);
+#pragma unroll
+        for (int g = 0; g < GROUP; ++g) {
+            const int t = tg + g;
+            if (t >= t_end) break;
+            while (t >= eos && b + 1 < p.B) {  // next sequence starts here
+                ++b;
+                enter(t);
+            }
+            if (!ok || t >= eos) continue;
+            float xt[V];
+            unpack<T>(raw[g], xt);
+            float yv[V];
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                float acc = bias[i];
+#pragma unroll
+                for (int j = 0; j < K - 1; ++j) acc = fmaf(w[i][j], win[j][i], acc);
+                acc = fmaf(w[i][K - 1], xt[i], acc);
+                yv[i] = p.silu ? silu(acc) : acc;
+            }
+            store_vec<T>(y + (long long)t * p.C + c0, yv);
+            const int tl = t - bos;
+            if (vals && tl < ncap) store_vec<T>(vals + ((long long)b * p.cap + tl) * p.C + c0, xt);
+#pragma unroll
+            for (int j = 0; j + 1 < K - 1; ++j)
+#pragma unroll
+                for (int i = 0; i < V; ++i) win[j][i] = win[j + 1][i];
+#pragma unroll
+            for (int i = 0; i < V; ++i) win[K - 2][i] = xt[i];
         }
-        if (!ok || t >= eos) continue;
-        float xt[V];
-        load_vec<T>(x + (long long)t * p.x_stride + c0, xt);
-        float yv[V];
-#pragma unroll
-        for (int i = 0; i < V; ++i) {
-            float acc = bias[i];
-#pragma unroll
-            for (int j = 0; j < K - 1; ++j) acc = fmaf(w[i][j], win[j][i], acc);
-            acc = fmaf(w[i][K - 1], xt[i], acc);
-            yv[i] = p.silu ? silu(acc) : acc;
-        }
-        store_vec<T>(y + (long long)t * p.C + c0, yv);
-        const int tl = t - bos;
-        if (vals && tl < ncap) store_vec<T>(vals + ((long long)b * p.cap + tl) * p.C + c0, xt);
-#pragma unroll
-        for (int j = 0; j + 1 < K - 1; ++j)
-#pragma unroll
-            for (int i = 0; i < V; ++i) win[j][i] = win[j + 1][i];
-#pragma unroll
-        for (int i = 0; i < V; ++i) win[K - 2][i] = xt[i];
     }
 }
 
@@ -192,7 +213,7 @@ __global__ void __launch_bounds__(NT) conv_state_kernel(const ConvParams p) {
         const int from_end = (K - 1) - j;  // entry j of the new state is the from_end-th last input
         if (from_end <= len) {
             const T *xp = x + (long long)(eos - from_end) * p.x_stride + c0;
-            const uint4 raw = *reinterpret_cast<const uint4 *>(xp);
+            const typename Vec<T>::Raw raw = load_raw<T>(xp);
             const T *e = reinterpret_cast<const T *>(&raw);
 #pragma unroll
             for (int i = 0; i < V; ++i) nw[i][j] = e[i];
@@ -234,7 +255,7 @@ __global__ void __launch_bounds__(NT) conv_replay_kernel(const ConvReplayParams 
     for (int e = 0; e < K - 1; ++e) {
         const int from_end = (K - 1) - e;
         if (from_end <= n) {
-            const uint4 raw = *reinterpret_cast<const uint4 *>(vals + ((long long)j * p.cap + n - from_end) * p.C + c0);
+            const typename Vec<T>::Raw raw = load_raw<T>(vals + ((long long)j * p.cap + n - from_end) * p.C + c0);
             const T *el = reinterpret_cast<const T *>(&raw);
 #pragma unroll
             for (int i = 0; i < V; ++i) nw[i][e] = el[i];
