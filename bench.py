@@ -487,7 +487,8 @@ def run_conv(dev, stream):
         lib = gdn.load_library()
         sh = ctypes.c_void_p(stream.cuda_stream)
         args = [gdn.build_conv_args(x, w, cu, bias=bias, initial_state=states[i], final_state=states[i], output=out,
-                                    state_update=caps if cap else None, capacity=cap)[0] for i in range(NBUF)]
+                                    state_update=caps if cap else None, capacity=cap,
+                                    max_seqlen=max(lengths))[0] for i in range(NBUF)]
 
         def run(i):
             rc = lib.varlen_causal_conv_with_state(ctypes.byref(args[i % NBUF]), sh)
@@ -509,7 +510,8 @@ def run_conv(dev, stream):
                      "gbs": round(nbytes / (us / 1e6) / 1e9, 1), "frac_hbm": round(nbytes / (us / 1e6) / 1e9 / hbm, 4),
                      "algorithmic_bytes": nbytes}
     res["workload"] = ("causal conv: channels 10240, kernel 4, fp16, SiLU, in-place state; decode 64 x 1 token "
-                       "(2 launches incl. state update, C ABI with prebuilt arguments), prefill 8 x U[256,4096] tokens")
+                       "(max_seqlen hint 1: one launch), prefill 8 x U[256,4096] tokens (conv + state roll: 2 launches); C ABI with "
+                       "prebuilt arguments")
     return res
 
 

@@ -63,7 +63,8 @@ class ConvArgs(ctypes.Structure):
     _fields_ = [
         ("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32), ("channels", ctypes.c_int32),
         ("kernel_size", ctypes.c_int32), ("num_state_slots", ctypes.c_int32), ("io_dtype", ctypes.c_int32),
-        ("activation", ctypes.c_int32), ("state_update_capacity", ctypes.c_int32), ("x_stride", ctypes.c_int64),
+        ("activation", ctypes.c_int32), ("state_update_capacity", ctypes.c_int32), ("max_seqlen", ctypes.c_int32),
+        ("x_stride", ctypes.c_int64),
         ("x", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("bias", ctypes.c_void_p),
         ("cu_seqlens", ctypes.c_void_p), ("state_slots", ctypes.c_void_p), ("capture_count", ctypes.c_void_p),
         ("initial_state", ctypes.c_void_p), ("final_state", ctypes.c_void_p), ("output", ctypes.c_void_p),
@@ -290,7 +291,7 @@ def gdn_replay_prefix(state_banks, src_slots, dst_slots, state_update, accept_le
 
 def build_conv_args(x, weight, cu_seqlens, *, bias=None, initial_state=None, final_state=None, state_slots=None,
                     capture_count=None, capacity=0, activation="silu", output=None, state_update=None,
-                    status=None, num_state_slots=None):
+                    status=None, num_state_slots=None, max_seqlen=0):
     """Fill a ConvArgs struct from tensors; returns (args, outputs, keepalive)."""
     dev = x.device
     T, C = x.shape
@@ -323,6 +324,7 @@ def build_conv_args(x, weight, cu_seqlens, *, bias=None, initial_state=None, fin
     a.num_seqs, a.total_tokens, a.channels, a.kernel_size = B, T, C, K
     a.num_state_slots, a.io_dtype = int(num_state_slots), DTYPE[x.dtype]
     a.activation, a.state_update_capacity = ACTIVATION[activation], int(capacity)
+    a.max_seqlen = int(max_seqlen or 0)
     a.x_stride = x.stride(0) if T > 1 else C
     a.x, a.weight, a.bias = _ptr(x), _ptr(weight), _ptr(bias)
     a.cu_seqlens, a.state_slots, a.capture_count = _ptr(cu_seqlens), _ptr(state_slots), _ptr(capture_count)

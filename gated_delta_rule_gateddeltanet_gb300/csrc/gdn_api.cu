@@ -201,7 +201,7 @@ gdn_status varlen_causal_conv_with_state(const gdn_conv_args *a, gdn_stream_t st
     if (a->num_seqs < 0 || a->num_seqs > 65535 || a->total_tokens < 0 || a->channels <= 0 ||
         a->channels % vec != 0 || a->kernel_size < 2 || a->kernel_size > 4 || a->state_update_capacity < 0)
         return GDN_ERR_SHAPE;
-    if (a->x_stride != 0 && a->x_stride < a->channels) return GDN_ERR_SHAPE;
+    if ((a->x_stride != 0 && a->x_stride < a->channels) || a->max_seqlen < 0) return GDN_ERR_SHAPE;
     if (a->num_seqs == 0) return GDN_OK;
     if (a->num_state_slots < 1 || (!a->state_slots && a->num_state_slots < a->num_seqs)) return GDN_ERR_SHAPE;
     if (!a->cu_seqlens || !a->weight || !a->final_state) return GDN_ERR_NULL;
@@ -236,6 +236,9 @@ gdn_status varlen_causal_conv_with_state(const gdn_conv_args *a, gdn_stream_t st
     const long long cblocks = (a->channels / 4 + 255) / 256;  // the kernel's threads own 4 channels
     long long tpc = (long long)a->total_tokens * cblocks / 608;
     p.tokens_per_cta = (int)(tpc < 1 ? 1 : (tpc > 64 ? 64 : tpc));
+    // Sequences of at most one token always lie inside one token block, where the
+    // conv kernel writes their state itself; empty ones keep an in-place state.
+    p.skip_state_kernel = a->max_seqlen == 1 && a->initial_state == a->final_state;
     if (gdn::launch_conv(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
     return GDN_OK;
 }

@@ -72,6 +72,8 @@ __device__ __forceinline__ void store_vec(T *p, const float (&v)[4]) {
 
 __device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
 
+constexpr int CU_SMEM = 4096;  // cu_seqlens entries staged in shared memory for the search
+
 // Sequence holding packed token t: the largest b with cu[b] <= t.
 __device__ __forceinline__ int seq_of(const int32_t *cu, int B, int t) {
     int lo = 0, hi = B;  // cu[lo] <= t < cu[hi] for a valid packing
@@ -91,12 +93,18 @@ __global__ void __launch_bounds__(NT, 4) conv_kernel(const ConvParams p) {
     const int t_end = min(t_begin + p.tokens_per_cta, p.T);
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && (p.cu[0] != 0 || p.cu[p.B] != p.T))
         flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
+    __shared__ int32_t cu_s[CU_SMEM];
+    const bool cu_staged = p.B + 1 <= CU_SMEM;
+    if (cu_staged)
+        for (int i = threadIdx.x; i <= p.B; i += NT) cu_s[i] = p.cu[i];
+    __syncthreads();
     if (cg >= cgroups || t_begin >= t_end) return;
     const int c0 = cg * V;
     const T *x = static_cast<const T *>(p.x);
     T *y = static_cast<T *>(p.out);
     T *vals = static_cast<T *>(p.values);
     const T *st_in = static_cast<const T *>(p.state_in);
+    T *st_out = static_cast<T *>(p.state_out);
 
     float w[V][K], bias[V];
 #pragma unroll
@@ -106,7 +114,7 @@ __global__ void __launch_bounds__(NT, 4) conv_kernel(const ConvParams p) {
         bias[i] = p.bias ? p.bias[c0 + i] : 0.f;
     }
 
-    int b = seq_of(p.cu, p.B, t_begin);
+    int b = seq_of(cu_staged ? cu_s : p.cu, p.B, t_begin);
     int bos = 0, eos = 0, slot = 0, ncap = 0;
     bool ok = false;
     float win[K - 1][V];  // inputs at t-(K-1) .. t-1 (oldest first)
@@ -188,6 +196,15 @@ __global__ void __launch_bounds__(NT, 4) conv_kernel(const ConvParams p) {
                 for (int i = 0; i < V; ++i) win[j][i] = win[j + 1][i];
 #pragma unroll
             for (int i = 0; i < V; ++i) win[K - 2][i] = xt[i];
+            // A sequence that lies wholly inside this token block is read and
+            // written by this thread only: its new state is the window now.
+            if (t == eos - 1 && bos >= t_begin) {
+                T *sp = st_out + ((long long)slot * p.C + c0) * (K - 1);
+#pragma unroll
+                for (int i = 0; i < V; ++i)
+#pragma unroll
+                    for (int j = 0; j < K - 1; ++j) sp[i * (K - 1) + j] = from_f32<T>(win[j][i]);
+            }
         }
     }
 }
@@ -202,6 +219,7 @@ __global__ void __launch_bounds__(NT) conv_state_kernel(const ConvParams p) {
     const int bos = p.cu[b], eos = p.cu[b + 1];
     const int slot = p.slots ? p.slots[b] : b;
     if (bos < 0 || eos < bos || eos > p.T || slot < 0 || slot >= p.num_slots) return;  // flagged by conv_kernel
+    if (eos > bos && bos / p.tokens_per_cta == (eos - 1) / p.tokens_per_cta) return;  // written by conv_kernel
     const int c0 = cg * V;
     const T *x = static_cast<const T *>(p.x);
     const T *st_in = static_cast<const T *>(p.state_in);
@@ -281,6 +299,7 @@ cudaError_t launch_conv_k(const ConvParams &p, cudaStream_t stream) {
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    if (p.skip_state_kernel) return cudaSuccess;  // every sequence is whole inside one token block, state in place
     dim3 g2((unsigned)cblocks, (unsigned)p.B);
     conv_state_kernel<T, K><<<g2, NT, 0, stream>>>(p);
     return cudaGetLastError();

@@ -42,6 +42,7 @@ struct ReplayParams {
 // Packed causal convolution (see gdn_conv.cu).
 struct ConvParams {
     int B, T, C, K, num_slots, io_f16, silu, cap, tokens_per_cta;
+    int skip_state_kernel;  // 1: no sequence straddles token blocks and the state is updated in place
     long long x_stride;
     const void *x;
     const float *w, *bias;

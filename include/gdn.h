@@ -268,6 +268,10 @@ typedef struct gdn_conv_args {
     int32_t io_dtype;              /* GDN_F32 or GDN_F16 */
     int32_t activation;            /* GDN_ACT_* */
     int32_t state_update_capacity; /* 0 = no capture */
+    int32_t max_seqlen;            /* upper bound on the longest sequence, 0 = unknown.  A
+                                      performance hint: a bound of 1 (decode) with an
+                                      in-place state skips the state-rolling launch.
+                                      Results do not depend on it. */
     int64_t x_stride;
     const void *x;
     const float *weight;

@@ -29,7 +29,7 @@ def _inputs(seed, lengths, C, K, io, slots=None, num_slots=None, state=True):
 
 
 def _gpu(x, w, bias, st, cu, *, cap=0, capture_count=None, slots=None, in_place=True, activation="silu",
-         num_slots=None, status=None):
+         num_slots=None, status=None, max_seqlen=0):
     import gated_delta_rule_gateddeltanet_gb300 as gdn
     init = to_dev(st)
     S = st.shape[0] if st is not None else (num_slots or len(cu) - 1)
@@ -44,7 +44,7 @@ def _gpu(x, w, bias, st, cu, *, cap=0, capture_count=None, slots=None, in_place=
     out, final, vals = gdn.varlen_causal_conv_with_state(
         to_dev(x), to_dev(w), to_dev(cu), bias=to_dev(bias), initial_state=init, final_state=final,
         state_slots=to_dev(slots), capture_count=to_dev(capture_count), capacity=cap, activation=activation,
-        status=status, num_state_slots=S)
+        status=status, num_state_slots=S, max_seqlen=max_seqlen)
     torch.cuda.synchronize()
     return (out.double().cpu().numpy(), final.double().cpu().numpy(),
             None if vals is None else vals.double().cpu().numpy())
@@ -98,10 +98,11 @@ def test_conv_qwen_geometry_decode_and_prefill():
     from gated_delta_rule_gateddeltanet_gb300 import workloads as wl
     C = 10240
     x, w, bias, st, cu = _inputs(52, [1] * 64, C, 4, np.float16)
-    got = _gpu(x, w, bias, st, cu, cap=1)
     want = _oracle(x, w, bias, st, cu, cap=1)
-    assert max_rel(got[0], want[0]) <= 2e-3 and np.array_equal(got[1], want[1])
-    assert np.array_equal(got[2], want[2])
+    for hint in (0, 1):  # a max_seqlen hint of 1 skips the state-rolling launch
+        got = _gpu(x, w, bias, st, cu, cap=1, max_seqlen=hint)
+        assert max_rel(got[0], want[0]) <= 2e-3 and np.array_equal(got[1], want[1])
+        assert np.array_equal(got[2], want[2])
     lengths = wl.varlen_prefill_lengths()
     x, w, bias, st, cu = _inputs(53, lengths, C, 4, np.float16)
     got = _gpu(x, w, bias, st, cu)
