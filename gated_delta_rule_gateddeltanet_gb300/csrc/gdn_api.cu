@@ -209,6 +209,7 @@ gdn_status varlen_causal_conv_with_state(const gdn_conv_args *a, gdn_stream_t st
     if (a->state_update_capacity > 0 && !a->state_update) return GDN_ERR_NULL;
     const int64_t xs = a->x_stride ? a->x_stride : a->channels;
     if (!aligned16(a->x) || !aligned16(a->output) || (a->state_update_capacity > 0 && !aligned16(a->state_update)) ||
+        !aligned16(a->final_state) || (a->initial_state && !aligned16(a->initial_state)) ||
         (xs * (int64_t)esz) % 16 != 0)
         return GDN_ERR_ALIGN;
     gdn::ConvParams p{};
@@ -232,9 +233,11 @@ gdn_status varlen_causal_conv_with_state(const gdn_conv_args *a, gdn_stream_t st
     p.out = a->output;
     p.values = p.cap > 0 ? a->state_update : nullptr;
     p.status = a->status;
-    // enough token blocks to give every SM a few CTAs, at most 64 tokens each
+    // as many tokens per CTA as keep the grid within about one wave of 4 CTAs
+    // per SM (at most 64): small batches are latency-bound, so a second
+    // partial wave costs a full CTA latency
     const long long cblocks = (a->channels / 4 + 255) / 256;  // the kernel's threads own 4 channels
-    long long tpc = (long long)a->total_tokens * cblocks / 608;
+    long long tpc = ((long long)a->total_tokens * cblocks + 607) / 608;
     p.tokens_per_cta = (int)(tpc < 1 ? 1 : (tpc > 64 ? 64 : tpc));
     // Sequences of at most one token always lie inside one token block, where the
     // conv kernel writes their state itself; empty ones keep an in-place state.

@@ -72,6 +72,27 @@ __device__ __forceinline__ void store_vec(T *p, const float (&v)[4]) {
 
 __device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
 
+// A thread's block of the state: 4 channels x (K-1) entries, contiguous, moved
+// as 8-byte (fp16) or 16-byte (fp32) words.
+template <typename T, int K>
+struct StateBlock {
+    using Word = typename Vec<T>::Raw;
+    static constexpr int WORDS = (K - 1) * 4 * (int)sizeof(T) / (int)sizeof(Word);
+    union {
+        Word w[WORDS];
+        T e[(K - 1) * 4];
+    };
+    __device__ __forceinline__ void load(const T *p) {
+#pragma unroll
+        for (int i = 0; i < WORDS; ++i) w[i] = reinterpret_cast<const Word *>(p)[i];
+    }
+    __device__ __forceinline__ void store(T *p) const {
+#pragma unroll
+        for (int i = 0; i < WORDS; ++i) reinterpret_cast<Word *>(p)[i] = w[i];
+    }
+    __device__ __forceinline__ T &at(int channel, int j) { return e[channel * (K - 1) + j]; }
+};
+
 constexpr int CU_SMEM = 4096;  // cu_seqlens entries staged in shared memory for the search
 
 // Sequence holding packed token t: the largest b with cu[b] <= t.
@@ -85,7 +106,7 @@ __device__ __forceinline__ int seq_of(const int32_t *cu, int B, int t) {
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(NT, 4) conv_kernel(const ConvParams p) {
+__global__ void __launch_bounds__(NT, sizeof(T) == 2 ? 4 : 3) conv_kernel(const ConvParams p) {
     constexpr int V = Vec<T>::N;
     const int cgroups = p.C / V;
     const int cg = blockIdx.y * NT + threadIdx.x;  // channel group of this thread
@@ -93,6 +114,15 @@ __global__ void __launch_bounds__(NT, 4) conv_kernel(const ConvParams p) {
     const int t_end = min(t_begin + p.tokens_per_cta, p.T);
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && (p.cu[0] != 0 || p.cu[p.B] != p.T))
         flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
+    // the first tokens' loads go out before anything else, so they overlap the search
+    const T *xg0 = static_cast<const T *>(p.x);
+    const int c0_early = (blockIdx.y * NT + threadIdx.x) * Vec<T>::N;
+    typename Vec<T>::Raw raw[GROUP];
+    if (c0_early < p.C) {
+#pragma unroll
+        for (int g = 0; g < GROUP; ++g)
+            if (t_begin + g < t_end) raw[g] = load_raw<T>(xg0 + (long long)(t_begin + g) * p.x_stride + c0_early);
+    }
     __shared__ int32_t cu_s[CU_SMEM];
     const bool cu_staged = p.B + 1 <= CU_SMEM;
     if (cu_staged)
@@ -118,9 +148,10 @@ __global__ void __launch_bounds__(NT, 4) conv_kernel(const ConvParams p) {
     int bos = 0, eos = 0, slot = 0, ncap = 0;
     bool ok = false;
     float win[K - 1][V];  // inputs at t-(K-1) .. t-1 (oldest first)
+    const int32_t *cu = cu_staged ? cu_s : p.cu;
     auto enter = [&](int t) {  // (re)build the window for token t of sequence b
-        bos = p.cu[b];
-        eos = p.cu[b + 1];
+        bos = cu[b];
+        eos = cu[b + 1];
         slot = p.slots ? p.slots[b] : b;
         ok = bos >= 0 && eos >= bos && eos <= p.T && slot >= 0 && slot < p.num_slots;
         ncap = p.cap;
@@ -140,17 +171,25 @@ __global__ void __launch_bounds__(NT, 4) conv_kernel(const ConvParams p) {
             }
             return;
         }
+        StateBlock<T, K> sb;
+        const bool need_state = t - (K - 1) < bos && st_in;
+        if (need_state) sb.load(st_in + ((long long)slot * p.C + c0) * (K - 1));
 #pragma unroll
         for (int j = 0; j < K - 1; ++j) {
             const int pos = t - (K - 1) + j;  // packed position of window entry j
             float v[V];
             if (pos >= bos) {
                 load_vec<T>(x + (long long)pos * p.x_stride + c0, v);
-            } else if (st_in) {
+            } else if (need_state) {
                 const int sj = (K - 1) - (bos - pos);  // state index, oldest first
-                const T *sp = st_in + ((long long)slot * p.C + c0) * (K - 1) + sj;
 #pragma unroll
-                for (int i = 0; i < V; ++i) v[i] = to_f32(sp[i * (K - 1)]);
+                for (int i = 0; i < V; ++i) {  // select with constant indices: keeps sb in registers
+                    float e = 0.f;
+#pragma unroll
+                    for (int q = 0; q < K - 1; ++q)
+                        if (q == sj) e = to_f32(sb.at(i, q));
+                    v[i] = e;
+                }
             } else {
 #pragma unroll
                 for (int i = 0; i < V; ++i) v[i] = 0.f;
@@ -159,14 +198,15 @@ __global__ void __launch_bounds__(NT, 4) conv_kernel(const ConvParams p) {
             for (int i = 0; i < V; ++i) win[j][i] = v[i];
         }
     };
-    while (b < p.B && p.cu[b + 1] <= t_begin) ++b;  // skip empty sequences
+    while (b < p.B && cu[b + 1] <= t_begin) ++b;  // skip empty sequences
     if (b >= p.B) return;
     enter(t_begin);
     for (int tg = t_begin; tg < t_end; tg += GROUP) {
-        typename Vec<T>::Raw raw[GROUP];
+        if (tg != t_begin) {
 #pragma unroll
-        for (int g = 0; g < GROUP; ++g)
-            if (tg + g < t_end) raw[g] = load_raw<T>(x + (long long)(tg + g) * p.x_stride + c0);
+            for (int g = 0; g < GROUP; ++g)
+                if (tg + g < t_end) raw[g] = load_raw<T>(x + (long long)(tg + g) * p.x_stride + c0);
+        }
 #pragma unroll
         for (int g = 0; g < GROUP; ++g) {
             const int t = tg + g;
@@ -199,11 +239,12 @@ __global__ void __launch_bounds__(NT, 4) conv_kernel(const ConvParams p) {
             // A sequence that lies wholly inside this token block is read and
             // written by this thread only: its new state is the window now.
             if (t == eos - 1 && bos >= t_begin) {
-                T *sp = st_out + ((long long)slot * p.C + c0) * (K - 1);
+                StateBlock<T, K> sb;
 #pragma unroll
                 for (int i = 0; i < V; ++i)
 #pragma unroll
-                    for (int j = 0; j < K - 1; ++j) sp[i * (K - 1) + j] = from_f32<T>(win[j][i]);
+                    for (int j = 0; j < K - 1; ++j) sb.at(i, j) = from_f32<T>(win[j][i]);
+                sb.store(st_out + ((long long)slot * p.C + c0) * (K - 1));
             }
         }
     }
