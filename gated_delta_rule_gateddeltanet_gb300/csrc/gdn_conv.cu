@@ -35,7 +35,9 @@ namespace {
 
 constexpr int NT = 256;
 
-constexpr int GROUP = 4;  // tokens whose loads are issued together
+// tokens whose loads are issued together: 64 bytes in flight per thread
+template <typename T>
+constexpr int group_of() { return sizeof(T) == 2 ? 8 : 4; }
 
 // A thread's 4 channels: one 8-byte (fp16) or 16-byte (fp32) vector.
 template <typename T>
@@ -108,6 +110,7 @@ __device__ __forceinline__ int seq_of(const int32_t *cu, int B, int t) {
 template <typename T, int K>
 __global__ void __launch_bounds__(NT, sizeof(T) == 2 ? 4 : 3) conv_kernel(const ConvParams p) {
     constexpr int V = Vec<T>::N;
+    constexpr int GROUP = group_of<T>();
     const int cgroups = p.C / V;
     const int cg = blockIdx.y * NT + threadIdx.x;  // channel group of this thread
     const int t_begin = blockIdx.x * p.tokens_per_cta;
