@@ -40,7 +40,7 @@
 namespace gdn {
 namespace {
 
-constexpr int NT = 256;
+constexpr int NT = 512;  // 16 warps: four per tensor-memory lane quarter
 constexpr int CH = 64;   // chunk length
 constexpr int DH = 128;  // dk = dv on this path
 constexpr float EPS = 1e-6f;
@@ -131,66 +131,55 @@ __device__ void tri_inverse(const float *A, float *T32, float *M, int tid) {
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            float acc = 0.f;
+            float acc0 = 0.f, acc1 = 0.f;  // two partial sums shorten the dependency chain
 #pragma unroll
-            for (int s = 0; s < r; ++s) acc = fmaf(A[(o + r) * AS + o + s], x[s], acc);
-            x[r] = (r < c) ? 0.f : (r == c ? 1.f : -acc);
+            for (int s = 0; s < r; s += 2) {
+                acc0 = fmaf(A[(o + r) * AS + o + s], x[s], acc0);
+                if (s + 1 < r) acc1 = fmaf(A[(o + r) * AS + o + s + 1], x[s + 1], acc1);
+            }
+            x[r] = (r < c) ? 0.f : (r == c ? 1.f : -(acc0 + acc1));
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) T32[(o + r) * TS + o + c] = x[r];
     }
     __syncthreads();
-    // level 1: the two 32 x 32 diagonal blocks (offset o = 0, 32), two outputs per thread
+    // level 1: the two 32 x 32 diagonal blocks (o = 0, 32), one output per thread
     {
-        const int pr = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2, o = 32 * pr;
-        float* Mp = M + pr * 16 * MS;
-        float a0 = 0.f, a1 = 0.f;
+        const int pr = tid >> 8, r = (tid >> 4) & 15, c = tid & 15, o = 32 * pr;
+        float *Mp = M + pr * 16 * MS;
+        float a0 = 0.f;
 #pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            const float a = A[(o + 16 + r) * AS + o + s];
-            a0 = fmaf(a, T32[(o + s) * TS + o + c0], a0);
-            a1 = fmaf(a, T32[(o + s) * TS + o + c0 + 1], a1);
-        }
-        Mp[r * MS + c0] = a0;
-        Mp[r * MS + c0 + 1] = a1;
+        for (int s = 0; s < 16; ++s) a0 = fmaf(A[(o + 16 + r) * AS + o + s], T32[(o + s) * TS + o + c], a0);
+        Mp[r * MS + c] = a0;
         __syncthreads();
-        float b0 = 0.f, b1 = 0.f;
+        float b0 = 0.f;
 #pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            const float t = T32[(o + 16 + r) * TS + o + 16 + s];
-            b0 = fmaf(t, Mp[s * MS + c0], b0);
-            b1 = fmaf(t, Mp[s * MS + c0 + 1], b1);
-        }
-        T32[(o + 16 + r) * TS + o + c0] = -b0;
-        T32[(o + 16 + r) * TS + o + c0 + 1] = -b1;
+        for (int s = 0; s < 16; ++s) b0 = fmaf(T32[(o + 16 + r) * TS + o + 16 + s], Mp[s * MS + c], b0);
+        T32[(o + 16 + r) * TS + o + c] = -b0;
         __syncthreads();
     }
-    // level 2: the lower-left 32 x 32 block, four consecutive outputs per thread
+    // level 2: the lower-left 32 x 32 block, two consecutive outputs per thread
     {
-        const int r = tid >> 3, c0 = (tid & 7) * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int r = tid >> 4, c0 = (tid & 15) * 2;
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int s = 0; s < 32; ++s) {
             const float a = A[(32 + r) * AS + s];
-            const float4 t = *reinterpret_cast<const float4 *>(T32 + s * TS + c0);
+            const float2 t = *reinterpret_cast<const float2 *>(T32 + s * TS + c0);
             acc.x = fmaf(a, t.x, acc.x);
             acc.y = fmaf(a, t.y, acc.y);
-            acc.z = fmaf(a, t.z, acc.z);
-            acc.w = fmaf(a, t.w, acc.w);
         }
-        *reinterpret_cast<float4 *>(M + r * MS + c0) = acc;
+        *reinterpret_cast<float2 *>(M + r * MS + c0) = acc;
         __syncthreads();
-        float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+        float2 out = make_float2(0.f, 0.f);
 #pragma unroll
         for (int s = 0; s < 32; ++s) {
             const float t = T32[(32 + r) * TS + 32 + s];
-            const float4 m = *reinterpret_cast<const float4 *>(M + s * MS + c0);
+            const float2 m = *reinterpret_cast<const float2 *>(M + s * MS + c0);
             out.x = fmaf(t, m.x, out.x);
             out.y = fmaf(t, m.y, out.y);
-            out.z = fmaf(t, m.z, out.z);
-            out.w = fmaf(t, m.w, out.w);
         }
-        *reinterpret_cast<float4 *>(T32 + (32 + r) * TS + c0) = make_float4(-out.x, -out.y, -out.z, -out.w);
+        *reinterpret_cast<float2 *>(T32 + (32 + r) * TS + c0) = make_float2(-out.x, -out.y);
         __syncthreads();
     }
 }
@@ -210,9 +199,13 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ Shared sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
-    const int row = quarter * 32 + lane;  // the tensor-memory lane this thread reads
+    // Tensor memory: a warp reaches only the 32 lanes of its quarter (warp % 4);
+    // the four warps of a quarter split the columns.
+    const int quarter = warp & 3, cq = warp >> 2;
+    const int row = quarter * 32 + lane;  // the tensor-memory lane (matrix row) of this thread
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
+    const int c16 = cq * 16;  // this thread's 16 columns of a 64-column region
+    const int c32 = cq * 32;  // this thread's 32 columns of a 128-column region
 
     float *V_s = reinterpret_cast<float *>(sm + OFF_V);
     float *A32 = reinterpret_cast<float *>(sm + OFF_A32);
@@ -314,24 +307,22 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
 
         // ---- chain start: the initial state into tensor memory
         if (has_init) {
-            const float *src = p.init + head_off + (size_t)row * DH + half * 64;
+            const float *src = p.init + head_off + (size_t)row * DH + c32;
+            float v[32];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 x = *reinterpret_cast<const float4 *>(src + c * 32 + j);
-                    v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
-                }
-                ptx::tmem_st32(tm + lane_sel + TM_S + half * 64 + c * 32, v);
+            for (int j = 0; j < 32; j += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(src + j);
+                v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
             }
+            ptx::tmem_st32(tm + lane_sel + TM_S + c32, v);
             ptx::tmem_st_wait();
         }
         bool state_live = has_init;  // does TM_S hold the state (else it is zero)?
 
         for (int t0 = bos; t0 < eos && !failed; t0 += CH) {
             const int n = min(CH, eos - t0);
-            // ---- A1: gates and the within-chunk cumulative log decay (warp 0)
+            // ---- A1: gates and the within-chunk cumulative log decay (warp 0;
+            //      the other warps start on A2/A3, which do not need them)
             if (warp == 0) {
                 float lg[2], bt[2], gt[2];
 #pragma unroll
@@ -395,15 +386,14 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                 }
                 *reinterpret_cast<float4 *>(V_s + s * DH + c4) = make_float4(v[0], v[1], v[2], v[3]);
             }
-            __syncthreads();
-            // ---- A3: normalised k and q into the operand tiles; each warp handles
-            //      its 8 tokens together so their loads and reductions overlap
+            // ---- A3: normalised k and q into the [K;Q] tile; each warp handles
+            //      its 4 tokens together so their loads and reductions overlap
             {
                 constexpr int TPW = CH / (NT / 32);  // tokens per warp
                 float qv[TPW][4], kv[TPW][4], sq[TPW], sk[TPW];
 #pragma unroll
                 for (int u = 0; u < TPW; ++u) {
-                    const int s = warp + 8 * u;
+                    const int s = warp + (NT / 32) * u;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) qv[u][e] = kv[u][e] = 0.f;
                     if (s < n) {
@@ -437,7 +427,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                 const int c = lane * 4;
 #pragma unroll
                 for (int u = 0; u < TPW; ++u) {
-                    const int s = warp + 8 * u;
+                    const int s = warp + (NT / 32) * u;
                     const float iq = 1.f / fmaxf(sqrtf(sq[u]), EPS), ik = 1.f / fmaxf(sqrtf(sk[u]), EPS);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -446,8 +436,6 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                     }
                     st_h4(sm + OFF_KQ, sw(s, c, 128), kv[u][0], kv[u][1], kv[u][2], kv[u][3]);
                     st_h4(sm + OFF_KQ, sw(64 + s, c, 128), qv[u][0], qv[u][1], qv[u][2], qv[u][3]);
-                    const float gm = sh.gam[s];
-                    st_h4(sm + OFF_GQ, sw(s, c, 64), gm * qv[u][0], gm * qv[u][1], gm * qv[u][2], gm * qv[u][3]);
                     const int tl = t0 + s - bos;
                     if (p.caps && h % p.r == 0 && s < n && tl < p.cap) {
                         float *dst = p.caps + ((long long)b * p.cap + tl) * p.W + p.Hv + (long long)kh * DH + c;
@@ -457,12 +445,12 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                 }
             }
             __syncthreads();
-            // ---- A4: K^T tile from the K rows (thread: one dk row, 32 tokens)
+            // ---- A4: K^T (thread: one dk row, 16 tokens) and gamma Q (from the fp16 Q rows)
             {
-                const int j = tid >> 1, sg = (tid & 1) * 32;
+                const int j = tid >> 2, sg = (tid & 3) * 16;
                 const uint8_t *kq = sm + OFF_KQ;
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
+                for (int m = 0; m < 2; ++m) {
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -473,29 +461,41 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                     }
                     *reinterpret_cast<uint4 *>(sm + OFF_KT + sw(j, sg + 8 * m, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
+#pragma unroll
+                for (int it = 0; it < 2; ++it) {
+                    const int e = tid + NT * it;       // 64 rows x 16 pieces of 8 elements
+                    const int s = e >> 4, k8 = (e & 15) * 8;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(kq + sw(64 + s, k8, 128));
+                    const float gm = sh.gam[s];
+                    const __half2 *hq = reinterpret_cast<const __half2 *>(&raw);
+                    uint4 o;
+                    __half2 *ho = reinterpret_cast<__half2 *>(&o);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 f = __half22float2(hq[q]);
+                        ho[q] = __floats2half2_rn(gm * f.x, gm * f.y);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + OFF_GQ + sw(s, k8, 64)) = o;
+                }
             }
             // ---- B: S0 -> fp16 operand tile; the tensor-memory state becomes gamma_last S0
             {
                 const float gl = sh.gam[n - 1];
+                float v[32];
+                if (state_live) {
+                    ptx::tmem_ld32(tm + lane_sel + TM_S + c32, v);
+                } else {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int col = half * 64 + c * 32;
-                    float v[32];
-                    if (state_live) {
-                        ptx::tmem_ld32(tm + lane_sel + TM_S + col, v);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = 0.f;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4) st_h4(sm + OFF_S16, sw(row, col + j, 128), v[j], v[j + 1], v[j + 2], v[j + 3]);
-                    if (state_live) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] *= gl;
-                        ptx::tmem_st32(tm + lane_sel + TM_S + col, v);
-                    }
+                    for (int j = 0; j < 32; ++j) v[j] = 0.f;
                 }
-                if (state_live) ptx::tmem_st_wait();
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) st_h4(sm + OFF_S16, sw(row, c32 + j, 128), v[j], v[j + 1], v[j + 2], v[j + 3]);
+                if (state_live) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] *= gl;
+                    ptx::tmem_st32(tm + lane_sel + TM_S + c32, v);
+                    ptx::tmem_st_wait();
+                }
             }
             mma_ready();
             // ---- C: MMA1 (committed on its own, so the inverse can start while
@@ -525,42 +525,39 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
             }
             // ---- D1: A (fp32 staging) and P o D (fp16 tile) from G and P
             {
-                float v[32];
-                ptx::tmem_ld32(tm + lane_sel + TM_D1 + half * 32, v);
+                float v[16];
+                ptx::tmem_ld16(tm + lane_sel + TM_D1 + c16, v);
                 const int r = row & 63;
                 const float Gr = sh.Gam[r];
                 if (quarter < 2) {
                     const float br = sh.beta[r];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int s = half * 32 + j;
+                    for (int j = 0; j < 16; ++j) {
+                        const int s = c16 + j;
                         A32[r * AS + s] = (s < r) ? br * __expf(Gr - sh.Gam[s]) * v[j] : 0.f;
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
+                    for (int j = 0; j < 16; j += 4) {
                         float w[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int s = half * 32 + j + e;
+                            const int s = c16 + j + e;
                             w[e] = (s <= r) ? v[j + e] * __expf(Gr - sh.Gam[s]) : 0.f;
                         }
-                        st_h4(sm + OFF_PD, sw(r, half * 32 + j, 64), w[0], w[1], w[2], w[3]);
+                        st_h4(sm + OFF_PD, sw(r, c16 + j, 64), w[0], w[1], w[2], w[3]);
                     }
                 }
             }
             __syncthreads();
             // ---- D2: T = (I + A)^-1 on the CUDA cores, then its fp16 tile
             tri_inverse(A32, T32, Mws, tid);
-            for (int e = tid; e < CH * CH / 4; e += NT) {
-                const int r = e >> 4, s0 = (e & 15) * 4;
-                float w[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int s = s0 + u;
-                    w[u] = T32[r * TS + s];
-                }
-                st_h4(sm + OFF_T, sw(r, s0, 64), w[0], w[1], w[2], w[3]);
+            for (int it = 0; it < 2; ++it) {
+                const int e = tid + NT * it;
+                const int r = e >> 4, s0 = (e & 15) * 4;
+                const float4 w = *reinterpret_cast<const float4 *>(T32 + r * TS + s0);
+                st_h4(sm + OFF_T, sw(r, s0, 64), w.x, w.y, w.z, w.w);
             }
             if (!mma_wait()) { failed = true; break; }  // MMA2 (long done by now)
             // the staging area is free again: fetch the next chunk while this one finishes
@@ -570,17 +567,17 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
             }
             // ---- D3: R^T = (V - diag(gamma) K S0^T)^T diag(beta) from X^T
             {
-                float v[32];
-                ptx::tmem_ld32(tm + lane_sel + TM_X + half * 32, v);
+                float v[16];
+                ptx::tmem_ld16(tm + lane_sel + TM_X + c16, v);
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
+                for (int j = 0; j < 16; j += 4) {
                     float w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int s = half * 32 + j + e;
+                        const int s = c16 + j + e;
                         w[e] = sh.beta[s] * (V_s[s * DH + row] - sh.gam[s] * v[j + e]);
                     }
-                    st_h4(sm + OFF_RT, sw(row, half * 32 + j, 128), w[0], w[1], w[2], w[3]);
+                    st_h4(sm + OFF_RT, sw(row, c16 + j, 128), w[0], w[1], w[2], w[3]);
                 }
             }
             mma_ready();
@@ -596,21 +593,21 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
             if (!mma_wait()) { failed = true; break; }
             // ---- F: U^T -> fp16 operands (plain and decayed to the chunk end); capsule deltas
             {
-                float v[32];
-                ptx::tmem_ld32(tm + lane_sel + TM_D3 + half * 32, v);
+                float v[16];
+                ptx::tmem_ld16(tm + lane_sel + TM_D3 + c16, v);
                 const float Gl = sh.Gam[n - 1];
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
+                for (int j = 0; j < 16; j += 4) {
                     float w[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) w[e] = __expf(Gl - sh.Gam[half * 32 + j + e]) * v[j + e];
-                    st_h4(sm + OFF_RT, sw(row, half * 32 + j, 128), v[j], v[j + 1], v[j + 2], v[j + 3]);
-                    st_h4(sm + OFF_UD, sw(row, half * 32 + j, 128), w[0], w[1], w[2], w[3]);
+                    for (int e = 0; e < 4; ++e) w[e] = __expf(Gl - sh.Gam[c16 + j + e]) * v[j + e];
+                    st_h4(sm + OFF_RT, sw(row, c16 + j, 128), v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    st_h4(sm + OFF_UD, sw(row, c16 + j, 128), w[0], w[1], w[2], w[3]);
                 }
                 if (p.caps) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int s = half * 32 + j, tl = t0 + s - bos;
+                    for (int j = 0; j < 16; ++j) {
+                        const int s = c16 + j, tl = t0 + s - bos;
                         if (s < n && tl < p.cap)
                             p.caps[((long long)b * p.cap + tl) * p.W + ubase + (long long)h * DH + row] = v[j];
                     }
@@ -634,11 +631,11 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
             // ---- H: outputs, staged through shared memory (the v tile is free) and
             //      written as contiguous 16-byte pieces of each token's dv row
             {
-                float v[32];
-                ptx::tmem_ld32(tm + lane_sel + TM_O + half * 32, v);
+                float v[16];
+                ptx::tmem_ld16(tm + lane_sel + TM_O + c16, v);
                 TIO *ost = reinterpret_cast<TIO *>(sm + OFF_V);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) ost[(half * 32 + j) * DH + row] = from_f32<TIO>(p.scale * v[j]);
+                for (int j = 0; j < 16; ++j) ost[(c16 + j) * DH + row] = from_f32<TIO>(p.scale * v[j]);
                 __syncthreads();
                 constexpr int VEC = 16 / sizeof(TIO);  // elements per 16-byte piece
                 for (int e = tid; e < n * (DH / VEC); e += NT) {
@@ -654,20 +651,17 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
         if (failed) break;
         // ---- chain end: the final state
         {
-            float *dst = p.final_state + head_off + (size_t)row * DH + half * 64;
+            float *dst = p.final_state + head_off + (size_t)row * DH + c32;
+            float v[32];
+            if (state_live) {
+                ptx::tmem_ld32(tm + lane_sel + TM_S + c32, v);
+            } else {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float v[32];
-                if (state_live) {
-                    ptx::tmem_ld32(tm + lane_sel + TM_S + half * 64 + c * 32, v);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = 0.f;
-                }
-#pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4 *>(dst + c * 32 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
             }
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
         ptx::tc_fence_before();
         __syncthreads();
