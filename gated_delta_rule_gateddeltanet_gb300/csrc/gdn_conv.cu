@@ -37,7 +37,7 @@ constexpr int NT = 256;
 
 // tokens whose loads are issued together
 template <typename T>
-constexpr int group_of() { return 4; }
+__host__ __device__ constexpr int group_of() { return 4; }
 
 // A thread's 4 channels: one 8-byte (fp16) or 16-byte (fp32) vector.
 template <typename T>
