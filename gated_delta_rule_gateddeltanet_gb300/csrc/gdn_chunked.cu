@@ -20,8 +20,11 @@
 // Every product is an M = 128 tcgen05.mma (kind::f16, fp16 operands, fp32
 // accumulators in tensor memory) with both operands K-major in the 128-byte
 // swizzled layout, the value dimension (dv = 128) as M:
-//   MMA1  [K;Q] K^T            -> G = K K^T, P = Q K^T      (128 x 64, K = dk)
+//   MMA1  [Q;K] K^T            -> P = Q K^T, G = K K^T      (128 x 64, K = dk)
 //   MMA2  S0 [K ; gamma Q]^T   -> X^T = S0 K^T, S0 (gamma Q)^T (128 x 128, K = dk)
+// Q, K and gamma Q are the three 64-row bands of one 192-row tile, so MMA1
+// reads rows 0-127 and MMA2 rows 64-191 (one N = 128 MMA instead of two
+// N = 64 ones that would each re-read S0).
 //   MMA3  R^T T^T              -> U^T                        (128 x 64, K = n)
 //   MMA4  U^T (P o D)^T        accumulated onto S0 (gamma Q)^T -> O^T
 //   MMA5  (U^T diag) K         accumulated onto gamma_last S0 -> S1 (128 x 128, K = n)
@@ -50,16 +53,17 @@ constexpr int TMEM_COLS = 512;
 
 // Tensor-memory columns (128 lanes each).
 constexpr uint32_t TM_S = 0;     // FP32 state S (dv lanes x dk columns)
-constexpr uint32_t TM_D1 = 128;  // G (lanes 0-63) and P (lanes 64-127), 64 columns
+constexpr uint32_t TM_D1 = 128;  // P (lanes 0-63) and G (lanes 64-127), 64 columns
 constexpr uint32_t TM_D3 = 192;  // U^T, 64 columns
 constexpr uint32_t TM_X = 256;   // X^T = S0 K^T, 64 columns
 constexpr uint32_t TM_O = 320;   // S0 (gamma Q)^T + U^T (P o D)^T, 64 columns
 
 // Shared-memory layout (bytes from a 1024-byte aligned base).  fp16 tiles are
 // K-major with the 128-byte swizzle.
-constexpr int OFF_KQ = 0;                  // [128][128]: rows 0-63 K, 64-127 Q        32 KiB
-constexpr int OFF_GQ = OFF_KQ + 32768;     // [64][128]: gamma Q                        16 KiB
-constexpr int OFF_KT = OFF_GQ + 16384;     // [128][64]: K^T (dk rows, token columns)  16 KiB
+constexpr int OFF_QKG = 0;                 // [192][128]: rows 0-63 Q, 64-127 K, 128-191 gamma Q  48 KiB
+constexpr int QKG_ROWS = 192;
+constexpr int QKG_KB = QKG_ROWS * 128;     // bytes between its two 64-element K blocks
+constexpr int OFF_KT = OFF_QKG + 49152;    // [128][64]: K^T (dk rows, token columns)  16 KiB
 constexpr int OFF_S16 = OFF_KT + 16384;    // [128][128]: S0 in fp16                    32 KiB
 constexpr int OFF_A32 = OFF_S16 + 32768;   //   (R^T/U^T tiles, idle until R^T is built): A in fp32 [64][65]
 constexpr int OFF_RT = OFF_S16 + 32768;    // [128][64]: R^T, then U^T                  16 KiB
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
     float *A32 = reinterpret_cast<float *>(sm + OFF_A32);
     float *T32 = reinterpret_cast<float *>(sm + OFF_T32);
     float *Mws = reinterpret_cast<float *>(sm + OFF_M);
-    const uint32_t a_KQ = ptx::smem_u32(sm + OFF_KQ), a_GQ = ptx::smem_u32(sm + OFF_GQ);
+    const uint32_t a_QKG = ptx::smem_u32(sm + OFF_QKG);
     const uint32_t a_KT = ptx::smem_u32(sm + OFF_KT), a_S16 = ptx::smem_u32(sm + OFF_S16);
     const uint32_t a_RT = ptx::smem_u32(sm + OFF_RT), a_UD = ptx::smem_u32(sm + OFF_UD);
     const uint32_t a_T = ptx::smem_u32(sm + OFF_T), a_PD = ptx::smem_u32(sm + OFF_PD);
@@ -386,7 +390,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                 }
                 *reinterpret_cast<float4 *>(V_s + s * DH + c4) = make_float4(v[0], v[1], v[2], v[3]);
             }
-            // ---- A3: normalised k and q into the [K;Q] tile; each warp handles
+            // ---- A3: normalised q and k into the [Q;K;gamma Q] tile; each warp handles
             //      its 4 tokens together so their loads and reductions overlap
             {
                 constexpr int TPW = CH / (NT / 32);  // tokens per warp
@@ -434,8 +438,8 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                         qv[u][e] *= iq;
                         kv[u][e] *= ik;
                     }
-                    st_h4(sm + OFF_KQ, sw(s, c, 128), kv[u][0], kv[u][1], kv[u][2], kv[u][3]);
-                    st_h4(sm + OFF_KQ, sw(64 + s, c, 128), qv[u][0], qv[u][1], qv[u][2], qv[u][3]);
+                    st_h4(sm + OFF_QKG, sw(s, c, QKG_ROWS), qv[u][0], qv[u][1], qv[u][2], qv[u][3]);
+                    st_h4(sm + OFF_QKG, sw(64 + s, c, QKG_ROWS), kv[u][0], kv[u][1], kv[u][2], kv[u][3]);
                     const int tl = t0 + s - bos;
                     if (p.caps && h % p.r == 0 && s < n && tl < p.cap) {
                         float *dst = p.caps + ((long long)b * p.cap + tl) * p.W + p.Hv + (long long)kh * DH + c;
@@ -448,15 +452,15 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
             // ---- A4: K^T (thread: one dk row, 16 tokens) and gamma Q (from the fp16 Q rows)
             {
                 const int j = tid >> 2, sg = (tid & 3) * 16;
-                const uint8_t *kq = sm + OFF_KQ;
+                const uint8_t *kq = sm + OFF_QKG;
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int s = sg + 8 * m + 2 * e;
-                        const unsigned short lo = *reinterpret_cast<const unsigned short *>(kq + sw(s, j, 128));
-                        const unsigned short hi = *reinterpret_cast<const unsigned short *>(kq + sw(s + 1, j, 128));
+                        const unsigned short lo = *reinterpret_cast<const unsigned short *>(kq + sw(64 + s, j, QKG_ROWS));
+                        const unsigned short hi = *reinterpret_cast<const unsigned short *>(kq + sw(65 + s, j, QKG_ROWS));
                         w[e] = (uint32_t)lo | ((uint32_t)hi << 16);
                     }
                     *reinterpret_cast<uint4 *>(sm + OFF_KT + sw(j, sg + 8 * m, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -465,7 +469,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                 for (int it = 0; it < 2; ++it) {
                     const int e = tid + NT * it;       // 64 rows x 16 pieces of 8 elements
                     const int s = e >> 4, k8 = (e & 15) * 8;
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(kq + sw(64 + s, k8, 128));
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(kq + sw(s, k8, QKG_ROWS));
                     const float gm = sh.gam[s];
                     const __half2 *hq = reinterpret_cast<const __half2 *>(&raw);
                     uint4 o;
@@ -475,7 +479,7 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                         const float2 f = __half22float2(hq[q]);
                         ho[q] = __floats2half2_rn(gm * f.x, gm * f.y);
                     }
-                    *reinterpret_cast<uint4 *>(sm + OFF_GQ + sw(s, k8, 64)) = o;
+                    *reinterpret_cast<uint4 *>(sm + OFF_QKG + sw(128 + s, k8, QKG_ROWS)) = o;
                 }
             }
             // ---- B: S0 -> fp16 operand tile; the tensor-memory state becomes gamma_last S0
@@ -503,17 +507,17 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
             if (tid == 0) {
                 ptx::tc_fence_after();
                 const uint32_t i64 = ptx::idesc_f16_f32(128, 64);
+                const uint32_t i128 = ptx::idesc_f16_f32(128, 128);
                 for (int ks = 0; ks < DH / 16; ++ks) {
-                    const uint64_t dKQ = ptx::sdesc_k_sw128(a_KQ + (ks >> 2) * 16384 + (ks & 3) * 32);
-                    ptx::mma_f16(tm + TM_D1, dKQ, dKQ, i64, ks > 0);
+                    const uint32_t ko = (ks >> 2) * QKG_KB + (ks & 3) * 32;
+                    ptx::mma_f16(tm + TM_D1, ptx::sdesc_k_sw128(a_QKG + ko),
+                                 ptx::sdesc_k_sw128(a_QKG + 64 * 128 + ko), i64, ks > 0);
                 }
                 ptx::mma_commit(&sh.bar1);
                 for (int ks = 0; ks < DH / 16; ++ks) {
-                    const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    const uint64_t dKQ = ptx::sdesc_k_sw128(a_KQ + ko);
-                    ptx::mma_f16(tm + TM_X, ptx::sdesc_k_sw128(a_S16 + ko), dKQ, i64, ks > 0);
-                    ptx::mma_f16(tm + TM_O, ptx::sdesc_k_sw128(a_S16 + ko),
-                                 ptx::sdesc_k_sw128(a_GQ + (ks >> 2) * 8192 + (ks & 3) * 32), i64, ks > 0);
+                    const uint32_t ko = (ks >> 2) * QKG_KB + (ks & 3) * 32;
+                    ptx::mma_f16(tm + TM_X, ptx::sdesc_k_sw128(a_S16 + (ks >> 2) * 16384 + (ks & 3) * 32),
+                                 ptx::sdesc_k_sw128(a_QKG + 64 * 128 + ko), i128, ks > 0);  // X and S0 (gamma Q)^T
                 }
                 ptx::mma_commit(&sh.bar);
             }
@@ -529,14 +533,14 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                 ptx::tmem_ld16(tm + lane_sel + TM_D1 + c16, v);
                 const int r = row & 63;
                 const float Gr = sh.Gam[r];
-                if (quarter < 2) {
+                if (quarter >= 2) {  // lanes 64-127: G
                     const float br = sh.beta[r];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int s = c16 + j;
                         A32[r * AS + s] = (s < r) ? br * __expf(Gr - sh.Gam[s]) * v[j] : 0.f;
                     }
-                } else {
+                } else {  // lanes 0-63: P
 #pragma unroll
                     for (int j = 0; j < 16; j += 4) {
                         float w[4];
@@ -559,7 +563,8 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
                 const float4 w = *reinterpret_cast<const float4 *>(T32 + r * TS + s0);
                 st_h4(sm + OFF_T, sw(r, s0, 64), w.x, w.y, w.z, w.w);
             }
-            if (!mma_wait()) { failed = true; break; }  // MMA2 (long done by now)
+            // ---- D2w: wait for MMA2
+            if (!mma_wait()) { failed = true; break; }
             // the staging area is free again: fetch the next chunk while this one finishes
             if (STAGED && t0 + CH < eos) {
                 prefetch(t0 + CH);
