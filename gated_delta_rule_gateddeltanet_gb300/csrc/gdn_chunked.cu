@@ -33,10 +33,18 @@
 // inverse runs on the CUDA cores in FP32 (16 x 16 diagonal blocks by forward
 // substitution, then two levels of block combination).
 //
+// Staging: with fp16 I/O the q, k and v rows of the next chunk arrive by three
+// 2-D TMA copies (tensor maps over the packed [T, heads * 128] arrays, one
+// 64-token x 128-element box each) while the current chunk computes.
+//
 // Scheduling: a persistent grid of one CTA per SM (the shared-memory
 // footprint forces one) pulls (sequence, value head) chains from a list that a
 // one-CTA planning kernel sorts longest-first, through an atomic counter in
 // the caller's workspace.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <mutex>
+
 #include "gdn_internal.cuh"
 #include "ptx.cuh"
 
@@ -123,11 +131,52 @@ __device__ __forceinline__ void ld4<__half>(const __half *p, float (&v)[4]) {
 // are dense, fully unrolled and register-tiled so their shared-memory loads
 // pipeline.
 constexpr int AS = 65, TS = 68, MS = 36;
+
+// Dense 4 x 4 register tile of C = X Y (X: rows of X_, stride xs; Y: 16-byte
+// aligned rows of Y_, stride ys), K-deep, fully unrolled: each loaded value
+// feeds four FMAs, which keeps the block products off the shared-memory
+// bandwidth limit.
+template <int K>
+__device__ __forceinline__ void tile4x4(const float *X_, int xs, const float *Y_, int ys, float (&c)[4][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) c[i][j] = 0.f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const float4 y = *reinterpret_cast<const float4 *>(Y_ + k * ys);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float x = X_[i * xs + k];
+            c[i][0] = fmaf(x, y.x, c[i][0]);
+            c[i][1] = fmaf(x, y.y, c[i][1]);
+            c[i][2] = fmaf(x, y.z, c[i][2]);
+            c[i][3] = fmaf(x, y.w, c[i][3]);
+        }
+    }
+}
+
+__device__ __forceinline__ void store4x4(float *C_, int cs, const float (&c)[4][4], float sign) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4 *>(C_ + i * cs) =
+            make_float4(sign * c[i][0], sign * c[i][1], sign * c[i][2], sign * c[i][3]);
+}
+
+// Unit lower-triangular inverse T = (I + A)^-1 of a 64 x 64 strictly lower A
+// (fp32, row stride AS, shared) into T32 (row stride TS).  The four 16 x 16
+// diagonal blocks come from forward substitution; the off-diagonal blocks from
+// the block identity [[L11, 0], [L21, L22]]^-1 = [[T11, 0], [-T22 L21 T11, T22]],
+// first for the two 32 x 32 diagonal blocks, then for the whole matrix.  Only
+// the strictly lower half and the two upper 16 x 16 blocks inside the 32 x 32
+// diagonal blocks are written (the latter as zeros: they are read as part of
+// T11 and T22); the upper-right 32 x 32 quadrant is never read.
 __device__ void tri_inverse(const float *A, float *T32, float *M, int tid) {
-    // entries outside the diagonal 16 x 16 blocks start at zero
-    for (int e = tid; e < 64 * 64; e += NT) {
-        const int r = e >> 6, c = e & 63;
-        if ((r >> 4) != (c >> 4)) T32[r * TS + c] = 0.f;
+    // zeros above the diagonal blocks inside the two 32 x 32 diagonal blocks
+    {
+        const int e = tid;  // 512 threads, 2 blocks x 256 entries
+        const int pr = e >> 8, r = (e >> 4) & 15, c = e & 15, o = 32 * pr;
+        T32[(o + r) * TS + o + 16 + c] = 0.f;
     }
     // level 0: the diagonal 16 x 16 blocks, one column per thread
     if (tid < 64) {
@@ -147,45 +196,38 @@ __device__ void tri_inverse(const float *A, float *T32, float *M, int tid) {
         for (int r = 0; r < 16; ++r) T32[(o + r) * TS + o + c] = x[r];
     }
     __syncthreads();
-    // level 1: the two 32 x 32 diagonal blocks (o = 0, 32), one output per thread
-    {
-        const int pr = tid >> 8, r = (tid >> 4) & 15, c = tid & 15, o = 32 * pr;
+    // level 1: for both 32 x 32 diagonal blocks (o = 0, 32), M = A21 T11 then
+    // T21 = -T22 M, 16 x 16 each: one warp per block, a 4 x 4 tile per lane
+    if (tid < 64) {
+        const int pr = tid >> 5, l = tid & 31, r0 = (l >> 2) * 4, c0 = (l & 3) * 4, o = 32 * pr;
+        float c[4][4];
         float *Mp = M + pr * 16 * MS;
-        float a0 = 0.f;
-#pragma unroll
-        for (int s = 0; s < 16; ++s) a0 = fmaf(A[(o + 16 + r) * AS + o + s], T32[(o + s) * TS + o + c], a0);
-        Mp[r * MS + c] = a0;
-        __syncthreads();
-        float b0 = 0.f;
-#pragma unroll
-        for (int s = 0; s < 16; ++s) b0 = fmaf(T32[(o + 16 + r) * TS + o + 16 + s], Mp[s * MS + c], b0);
-        T32[(o + 16 + r) * TS + o + c] = -b0;
-        __syncthreads();
-    }
-    // level 2: the lower-left 32 x 32 block, two consecutive outputs per thread
-    {
-        const int r = tid >> 4, c0 = (tid & 15) * 2;
-        float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int s = 0; s < 32; ++s) {
-            const float a = A[(32 + r) * AS + s];
-            const float2 t = *reinterpret_cast<const float2 *>(T32 + s * TS + c0);
-            acc.x = fmaf(a, t.x, acc.x);
-            acc.y = fmaf(a, t.y, acc.y);
+        if (r0 < 16) {
+            tile4x4<16>(A + (o + 16 + r0) * AS + o, AS, T32 + o * TS + o + c0, TS, c);
+            store4x4(Mp + r0 * MS + c0, MS, c, 1.f);
         }
-        *reinterpret_cast<float2 *>(M + r * MS + c0) = acc;
-        __syncthreads();
-        float2 out = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int s = 0; s < 32; ++s) {
-            const float t = T32[(32 + r) * TS + 32 + s];
-            const float2 m = *reinterpret_cast<const float2 *>(M + s * MS + c0);
-            out.x = fmaf(t, m.x, out.x);
-            out.y = fmaf(t, m.y, out.y);
+        __syncwarp();
+        if (r0 < 16) {
+            tile4x4<16>(T32 + (o + 16 + r0) * TS + o + 16, TS, Mp + c0, MS, c);
+            store4x4(T32 + (o + 16 + r0) * TS + o + c0, TS, c, -1.f);
         }
-        *reinterpret_cast<float2 *>(T32 + (32 + r) * TS + c0) = make_float2(-out.x, -out.y);
-        __syncthreads();
     }
+    __syncthreads();
+    // level 2: the lower-left 32 x 32 block, a 4 x 4 tile per thread (64 threads)
+    if (tid < 64) {
+        const int r0 = (tid >> 3) * 4, c0 = (tid & 7) * 4;
+        float c[4][4];
+        tile4x4<32>(A + (32 + r0) * AS, AS, T32 + c0, TS, c);
+        store4x4(M + r0 * MS + c0, MS, c, 1.f);
+    }
+    __syncthreads();
+    if (tid < 64) {
+        const int r0 = (tid >> 3) * 4, c0 = (tid & 7) * 4;
+        float c[4][4];
+        tile4x4<32>(T32 + (32 + r0) * TS + 32, TS, M + c0, MS, c);
+        store4x4(T32 + (32 + r0) * TS + c0, TS, c, -1.f);
+    }
+    __syncthreads();
 }
 
 struct Shared {
@@ -198,7 +240,9 @@ struct Shared {
 };
 
 template <typename TIO>
-__global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, int32_t *ws) {
+__global__ void __launch_bounds__(NT, 1)
+    chunked_kernel(const ForwardParams p, int32_t *ws, const __grid_constant__ CUtensorMap map_q,
+                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ Shared sh;
@@ -275,20 +319,15 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
         const size_t head_off = ((size_t)slot * p.Hv + h) * (size_t)DH * DH;
         const bool has_init = p.init != nullptr;
 
-        // Bulk copies of the q, k, v rows of the chunk starting at token tc into
-        // the staging area (row s of tensor j at stg + j*16 KiB + s*256 B).
+        // TMA copies of the q, k, v rows of the chunk starting at token tc into
+        // the staging area (row s of tensor j at stg + j*16 KiB + s*256 B); rows
+        // past the sequence are loaded (or zero-filled past T) and ignored.
         auto prefetch = [&](int tc) {
-            const int nn = min(CH, eos - tc);
-            if (tid == 0) ptx::mbar_arrive_expect_tx(&sh.lbar, (uint32_t)(3 * nn * DH * 2));
-            if (tid < 3 * CH) {
-                const int j = tid / CH, s = tid % CH;
-                if (s < nn) {
-                    const long long t = tc + s;
-                    const TIO *src = j == 0 ? qg + t * p.q_stride + (long long)kh * DH
-                                   : j == 1 ? kg + t * p.k_stride + (long long)kh * DH
-                                            : vg + t * p.v_stride + (long long)h * DH;
-                    ptx::bulk_g2s(stg + j * (CH * DH * 2) + s * (DH * 2), src, DH * 2, &sh.lbar);
-                }
+            if (tid == 0) {
+                ptx::mbar_arrive_expect_tx(&sh.lbar, (uint32_t)(3 * CH * DH * 2));
+                ptx::tma_load_2d(stg, &map_q, kh * DH, tc, &sh.lbar);
+                ptx::tma_load_2d(stg + CH * DH * 2, &map_k, kh * DH, tc, &sh.lbar);
+                ptx::tma_load_2d(stg + 2 * CH * DH * 2, &map_v, h * DH, tc, &sh.lbar);
             }
         };
         // raw gate inputs of the chunk starting at tc, two tokens per lane of warp 0
@@ -560,7 +599,8 @@ __global__ void __launch_bounds__(NT, 1) chunked_kernel(const ForwardParams p, i
             for (int it = 0; it < 2; ++it) {
                 const int e = tid + NT * it;
                 const int r = e >> 4, s0 = (e & 15) * 4;
-                const float4 w = *reinterpret_cast<const float4 *>(T32 + r * TS + s0);
+                const float4 w = (r < 32 && s0 >= 32) ? make_float4(0.f, 0.f, 0.f, 0.f)  // upper-right quadrant
+                                                      : *reinterpret_cast<const float4 *>(T32 + r * TS + s0);
                 st_h4(sm + OFF_T, sw(r, s0, 64), w.x, w.y, w.z, w.w);
             }
             // ---- D2w: wait for MMA2
@@ -742,8 +782,44 @@ int num_sms() {
     return cached;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Tensor map over a packed fp16 [T, row_elems] array with `stride` elements
+// between tokens; boxes of 64 tokens x 128 elements, zero fill out of range.
+bool encode_rows(CUtensorMap *map, const void *base, long long row_elems, long long stride, int T) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)(T > 0 ? T : 1)};
+    const cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
+    const cuuint32_t box[2] = {DH, CH};
+    const cuuint32_t estride[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename TIO>
 cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStream_t stream) {
+    CUtensorMap mq{}, mk{}, mv{};
+    if (sizeof(TIO) == 2) {
+        if (!encode_rows(&mq, p.q, (long long)p.Hk * DH, p.q_stride, p.T) ||
+            !encode_rows(&mk, p.k, (long long)p.Hk * DH, p.k_stride, p.T) ||
+            !encode_rows(&mv, p.v, (long long)p.Hv * DH, p.v_stride, p.T))
+            return cudaErrorInvalidValue;
+    }
     plan_kernel<<<1, 1024, 0, stream>>>(p.cu, p.B, p.T, min_len, ws);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -753,7 +829,7 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStre
     if (e != cudaSuccess) return e;
     const long long chains = (long long)p.B * p.Hv;
     const int grid = (int)(chains < num_sms() ? chains : num_sms());
-    kern<<<grid, NT, smem, stream>>>(p, ws);
+    kern<<<grid, NT, smem, stream>>>(p, ws, mq, mk, mv);
     return cudaGetLastError();
 }
 

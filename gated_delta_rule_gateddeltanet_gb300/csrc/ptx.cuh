@@ -68,6 +68,18 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
         : "memory");
 }
 
+// Global -> shared copy of one 2-D box described by a tensor map (a
+// __grid_constant__ kernel parameter), at element coordinates (x, y);
+// completion signalled on `bar` as transaction bytes.  Out-of-range elements
+// are filled with zeros and still counted.
+__device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tensor_map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(tensor_map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Shared -> global, tracked by the issuing thread's bulk async-groups.
 __device__ __forceinline__ void bulk_s2g(void *dst_gmem, const void *src_smem, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst_gmem),
