@@ -132,35 +132,61 @@ __device__ __forceinline__ void ld4<__half>(const __half *p, float (&v)[4]) {
 // pipeline.
 constexpr int AS = 65, TS = 68, MS = 36;
 
-// Dense 4 x 4 register tile of C = X Y (X: rows of X_, stride xs; Y: 16-byte
-// aligned rows of Y_, stride ys), K-deep, fully unrolled: each loaded value
-// feeds four FMAs, which keeps the block products off the shared-memory
-// bandwidth limit.
-template <int K>
-__device__ __forceinline__ void tile4x4(const float *X_, int xs, const float *Y_, int ys, float (&c)[4][4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) c[i][j] = 0.f;
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-        const float4 y = *reinterpret_cast<const float4 *>(Y_ + k * ys);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float x = X_[i * xs + k];
-            c[i][0] = fmaf(x, y.x, c[i][0]);
-            c[i][1] = fmaf(x, y.y, c[i][1]);
-            c[i][2] = fmaf(x, y.z, c[i][2]);
-            c[i][3] = fmaf(x, y.w, c[i][3]);
-        }
-    }
+// ---- FP32-accurate small products on the warp-level tensor cores
+//
+// The block products of the triangular inverse are 16 x 16 and 32 x 32: too
+// small for tcgen05 (M >= 64) and, on the CUDA cores, bound by shared-memory
+// traffic.  They run as mma.sync m16n8k8 TF32 products with each operand split
+// into a TF32 high part and a TF32 remainder (x = hi + lo), accumulating
+// hi*hi + hi*lo + lo*hi in FP32: the dropped lo*lo term is ~2^-22 relative, so
+// the result is as accurate as an FP32 product.
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
 }
 
-__device__ __forceinline__ void store4x4(float *C_, int cs, const float (&c)[4][4], float sign) {
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    hi = to_tf32(x);
+    lo = to_tf32(x - __uint_as_float(hi));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// One warp: the 16 x 8 tile C = X Y with X [16][K] (row stride xs) and
+// Y [K][8] (row stride ys), both fp32 in shared memory; C written with the
+// given sign to C_ (row stride cs).  m16n8k8 fragment layout: lane = 4 g + t;
+// A holds (g, t), (g+8, t), (g, t+4), (g+8, t+4); B holds (t, g), (t+4, g);
+// C holds (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1).
+template <int K>
+__device__ __forceinline__ void warp_tile_16x8(const float *X_, int xs, const float *Y_, int ys, float *C_, int cs,
+                                               float sign, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<float4 *>(C_ + i * cs) =
-            make_float4(sign * c[i][0], sign * c[i][1], sign * c[i][2], sign * c[i][3]);
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        split_tf32(X_[g * xs + k0 + t], ah[0], al[0]);
+        split_tf32(X_[(g + 8) * xs + k0 + t], ah[1], al[1]);
+        split_tf32(X_[g * xs + k0 + t + 4], ah[2], al[2]);
+        split_tf32(X_[(g + 8) * xs + k0 + t + 4], ah[3], al[3]);
+        split_tf32(Y_[(k0 + t) * ys + g], bh[0], bl[0]);
+        split_tf32(Y_[(k0 + t + 4) * ys + g], bh[1], bl[1]);
+        mma_tf32(d, al, bh);
+        mma_tf32(d, ah, bl);
+        mma_tf32(d, ah, bh);
+    }
+    C_[g * cs + 2 * t] = sign * d[0];
+    C_[g * cs + 2 * t + 1] = sign * d[1];
+    C_[(g + 8) * cs + 2 * t] = sign * d[2];
+    C_[(g + 8) * cs + 2 * t + 1] = sign * d[3];
 }
 
 // Unit lower-triangular inverse T = (I + A)^-1 of a 64 x 64 strictly lower A
@@ -172,6 +198,7 @@ __device__ __forceinline__ void store4x4(float *C_, int cs, const float (&c)[4][
 // diagonal blocks are written (the latter as zeros: they are read as part of
 // T11 and T22); the upper-right 32 x 32 quadrant is never read.
 __device__ void tri_inverse(const float *A, float *T32, float *M, int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
     // zeros above the diagonal blocks inside the two 32 x 32 diagonal blocks
     {
         const int e = tid;  // 512 threads, 2 blocks x 256 entries
@@ -196,36 +223,30 @@ __device__ void tri_inverse(const float *A, float *T32, float *M, int tid) {
         for (int r = 0; r < 16; ++r) T32[(o + r) * TS + o + c] = x[r];
     }
     __syncthreads();
-    // level 1: for both 32 x 32 diagonal blocks (o = 0, 32), M = A21 T11 then
-    // T21 = -T22 M, 16 x 16 each: one warp per block, a 4 x 4 tile per lane
-    if (tid < 64) {
-        const int pr = tid >> 5, l = tid & 31, r0 = (l >> 2) * 4, c0 = (l & 3) * 4, o = 32 * pr;
-        float c[4][4];
+    // level 1, for both 32 x 32 diagonal blocks (o = 0, 32): M = A21 T11 then
+    // T21 = -T22 M (16 x 16 each), one 16 x 8 tile per warp (warps 0-3)
+    if (warp < 4) {
+        const int pr = warp >> 1, n0 = (warp & 1) * 8, o = 32 * pr;
         float *Mp = M + pr * 16 * MS;
-        if (r0 < 16) {
-            tile4x4<16>(A + (o + 16 + r0) * AS + o, AS, T32 + o * TS + o + c0, TS, c);
-            store4x4(Mp + r0 * MS + c0, MS, c, 1.f);
-        }
-        __syncwarp();
-        if (r0 < 16) {
-            tile4x4<16>(T32 + (o + 16 + r0) * TS + o + 16, TS, Mp + c0, MS, c);
-            store4x4(T32 + (o + 16 + r0) * TS + o + c0, TS, c, -1.f);
-        }
+        warp_tile_16x8<16>(A + (o + 16) * AS + o, AS, T32 + o * TS + o + n0, TS, Mp + n0, MS, 1.f, lane);
     }
     __syncthreads();
-    // level 2: the lower-left 32 x 32 block, a 4 x 4 tile per thread (64 threads)
-    if (tid < 64) {
-        const int r0 = (tid >> 3) * 4, c0 = (tid & 7) * 4;
-        float c[4][4];
-        tile4x4<32>(A + (32 + r0) * AS, AS, T32 + c0, TS, c);
-        store4x4(M + r0 * MS + c0, MS, c, 1.f);
+    if (warp < 4) {
+        const int pr = warp >> 1, n0 = (warp & 1) * 8, o = 32 * pr;
+        const float *Mp = M + pr * 16 * MS;
+        warp_tile_16x8<16>(T32 + (o + 16) * TS + o + 16, TS, Mp + n0, MS, T32 + (o + 16) * TS + o + n0, TS, -1.f,
+                           lane);
     }
     __syncthreads();
-    if (tid < 64) {
-        const int r0 = (tid >> 3) * 4, c0 = (tid & 7) * 4;
-        float c[4][4];
-        tile4x4<32>(T32 + (32 + r0) * TS + 32, TS, M + c0, MS, c);
-        store4x4(T32 + (32 + r0) * TS + c0, TS, c, -1.f);
+    // level 2: the lower-left 32 x 32 block, one 16 x 8 tile per warp (warps 0-7)
+    if (warp < 8) {
+        const int m0 = (warp >> 2) * 16, n0 = (warp & 3) * 8;
+        warp_tile_16x8<32>(A + (32 + m0) * AS, AS, T32 + n0, TS, M + m0 * MS + n0, MS, 1.f, lane);
+    }
+    __syncthreads();
+    if (warp < 8) {
+        const int m0 = (warp >> 2) * 16, n0 = (warp & 3) * 8;
+        warp_tile_16x8<32>(T32 + (32 + m0) * TS + 32, TS, M + n0, MS, T32 + (32 + m0) * TS + n0, TS, -1.f, lane);
     }
     __syncthreads();
 }
