@@ -367,7 +367,59 @@ __global__ void __launch_bounds__(NT, 1)
             prefetch(bos);
             load_pending = true;
         }
-        if (warp == 0 && bos < eos) prefetch_gates(bos);
+        // Gates of the chunk starting at tc (warp 0, two tokens per lane) from
+        // the prefetched raw inputs ga/gb, then the raw inputs of the chunk after
+        // it: effective decay, beta, and the within-chunk cumulative log decay.
+        auto chunk_gates = [&](int tc) {
+            const int nn = min(CH, eos - tc);
+            float lg[2], bt[2], gt[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int s = lane + 32 * u;
+                lg[u] = 0.f; bt[u] = 0.f; gt[u] = 1.f;
+                if (s < nn) {
+                    const float av = ga[u], bv = gb[u];
+                    if (p.gate_raw) {
+                        const float l = -expf(p.A_log[h]) * softplus_f(av + p.dt_bias[h]);
+                        gt[u] = expf(l);
+                        lg[u] = fmaxf(l, LOG_DECAY_FLOOR);
+                        bt[u] = 1.f / (1.f + expf(-bv));
+                    } else {
+                        gt[u] = av;
+                        lg[u] = av > 0.f ? fmaxf(logf(av), LOG_DECAY_FLOOR) : LOG_DECAY_FLOOR;
+                        bt[u] = bv;
+                    }
+                }
+            }
+            if (tc + CH < eos) prefetch_gates(tc + CH);  // in flight until this is called again
+            float c0 = lg[0], c1 = lg[1];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y0 = __shfl_up_sync(0xffffffffu, c0, o);
+                const float y1 = __shfl_up_sync(0xffffffffu, c1, o);
+                if (lane >= o) { c0 += y0; c1 += y1; }
+            }
+            c1 += __shfl_sync(0xffffffffu, c0, 31);
+            sh.Gam[lane] = c0;
+            sh.Gam[lane + 32] = c1;
+            sh.gam[lane] = expf(c0);
+            sh.gam[lane + 32] = expf(c1);
+            sh.beta[lane] = bt[0];
+            sh.beta[lane + 32] = bt[1];
+            sh.gate[lane] = gt[0];
+            sh.gate[lane + 32] = gt[1];
+            if (p.caps) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int s = lane + 32 * u, tl = tc + s - bos;
+                    if (s < nn && tl < p.cap) p.caps[((long long)b * p.cap + tl) * p.W + h] = gt[u];
+                }
+            }
+        };
+        if (warp == 0 && bos < eos) {
+            prefetch_gates(bos);
+            chunk_gates(bos);  // the first chunk's; later chunks' are computed during the previous chunk
+        }
 
         // ---- chain start: the initial state into tensor memory
         if (has_init) {
@@ -385,53 +437,8 @@ __global__ void __launch_bounds__(NT, 1)
 
         for (int t0 = bos; t0 < eos && !failed; t0 += CH) {
             const int n = min(CH, eos - t0);
-            // ---- A1: gates and the within-chunk cumulative log decay (warp 0;
-            //      the other warps start on A2/A3, which do not need them)
-            if (warp == 0) {
-                float lg[2], bt[2], gt[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int s = lane + 32 * u;
-                    lg[u] = 0.f; bt[u] = 0.f; gt[u] = 1.f;
-                    if (s < n) {
-                        const float av = ga[u], bv = gb[u];
-                        if (p.gate_raw) {
-                            const float l = -expf(p.A_log[h]) * softplus_f(av + p.dt_bias[h]);
-                            gt[u] = expf(l);
-                            lg[u] = fmaxf(l, LOG_DECAY_FLOOR);
-                            bt[u] = 1.f / (1.f + expf(-bv));
-                        } else {
-                            gt[u] = av;
-                            lg[u] = av > 0.f ? fmaxf(logf(av), LOG_DECAY_FLOOR) : LOG_DECAY_FLOOR;
-                            bt[u] = bv;
-                        }
-                    }
-                }
-                if (t0 + CH < eos) prefetch_gates(t0 + CH);  // in flight for the rest of the chunk
-                float c0 = lg[0], c1 = lg[1];
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float y0 = __shfl_up_sync(0xffffffffu, c0, o);
-                    const float y1 = __shfl_up_sync(0xffffffffu, c1, o);
-                    if (lane >= o) { c0 += y0; c1 += y1; }
-                }
-                c1 += __shfl_sync(0xffffffffu, c0, 31);
-                sh.Gam[lane] = c0;
-                sh.Gam[lane + 32] = c1;
-                sh.gam[lane] = expf(c0);
-                sh.gam[lane + 32] = expf(c1);
-                sh.beta[lane] = bt[0];
-                sh.beta[lane + 32] = bt[1];
-                sh.gate[lane] = gt[0];
-                sh.gate[lane + 32] = gt[1];
-                if (p.caps) {
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int s = lane + 32 * u, tl = t0 + s - bos;
-                        if (s < n && tl < p.cap) p.caps[((long long)b * p.cap + tl) * p.W + h] = gt[u];
-                    }
-                }
-            }
+            // ---- A1: (the gates of this chunk were computed by warp 0 during the
+            //      previous chunk's last MMA wait, or at the chain start)
             if (STAGED) {
                 const bool ok = ptx::mbar_wait_bounded(&sh.lbar, lphase, WAIT_LIMIT);
                 lphase ^= 1u;
@@ -692,6 +699,8 @@ __global__ void __launch_bounds__(NT, 1)
                 }
                 ptx::mma_commit(&sh.bar);
             }
+            // the next chunk's gates while MMA4/5 run (nothing reads them after F)
+            if (warp == 0 && t0 + CH < eos) chunk_gates(t0 + CH);
             if (!mma_wait()) { failed = true; break; }
             state_live = true;
             // ---- H: outputs, staged through shared memory (the v tile is free) and
