@@ -370,6 +370,9 @@ __global__ void __launch_bounds__(NT, 1)
         // Gates of the chunk starting at tc (warp 0, two tokens per lane) from
         // the prefetched raw inputs ga/gb, then the raw inputs of the chunk after
         // it: effective decay, beta, and the within-chunk cumulative log decay.
+        // per-head gate parameters, loaded once per chain
+        const float expA = (warp == 0 && p.gate_raw) ? expf(p.A_log[h]) : 0.f;
+        const float dtb = (warp == 0 && p.gate_raw) ? p.dt_bias[h] : 0.f;
         auto chunk_gates = [&](int tc) {
             const int nn = min(CH, eos - tc);
             float lg[2], bt[2], gt[2];
@@ -380,7 +383,7 @@ __global__ void __launch_bounds__(NT, 1)
                 if (s < nn) {
                     const float av = ga[u], bv = gb[u];
                     if (p.gate_raw) {
-                        const float l = -expf(p.A_log[h]) * softplus_f(av + p.dt_bias[h]);
+                        const float l = -expA * softplus_f(av + dtb);
                         gt[u] = expf(l);
                         lg[u] = fmaxf(l, LOG_DECAY_FLOOR);
                         bt[u] = 1.f / (1.f + expf(-bv));
