@@ -379,7 +379,10 @@ def run_prefill(dev, stream):
                          "peak": tc_peak, "peak_kind": f"{kind} dense bf16 burst (fp16 runs at the bf16 rate)",
                          "unit": "TFLOP/s", "frac": round(tflops / tc_peak, 4), "algorithmic_flops": flops,
                          "executed_mma_flops": executed,
-                         "executed_tflops": round(executed / (ms / 1e3) / 1e12, 2)}}
+                         "executed_tflops": round(executed / (ms / 1e3) / 1e12, 2),
+                         "traffic": recorded_traffic(os.path.join(ROOT, "gated_delta_rule_gateddeltanet_gb300", "csrc",
+                                                                  "gdn_chunked.cu"),
+                                                     "varlen_prefill.chunked_kernel.ncu.md")}}
 
 
 # Algorithmic FLOPs of the chunked evaluation per token and value head (chunk
