@@ -261,6 +261,7 @@ def run_gdn(a, dist: Dist):
         extra["prefill"] = run_prefill(dev, stream)
         extra["spec_verify_replay"] = run_spec(dev, stream, lib, sh)
         extra["causal_conv"] = run_conv(dev, stream)
+        extra["serving_mix"] = run_serving_mix(dev, stream, lib, sh)
 
     cpu = None
     if not a.no_cpu and dist.rank == 0 and dist.world == 1:
@@ -523,6 +524,71 @@ def run_conv(dev, stream):
                        "(max_seqlen hint 1: one launch), prefill 8 x U[256,4096] tokens (conv + state roll: 2 launches); C ABI with "
                        "prebuilt arguments, launches captured in a CUDA graph and replayed")
     return res
+
+
+def run_serving_mix(dev, stream, lib, sh):
+    """32 x 2048-token packed prefill (zero initial state) followed by 256
+    single-token decode steps on the resulting FP32 states, updated in place.
+    Every decode step has fresh seeded inputs, copied to the device before the
+    timed region; the launches go through the C ABI with prebuilt arguments."""
+    import torch
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    from gated_delta_rule_gateddeltanet_gb300 import workloads as wl
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    pre = wl.serving_mix_prefill()
+    B, L = pre.B, 2048
+    state = torch.zeros((B, 48, 128, 128), dtype=torch.float32, device=dev)
+    pout = torch.empty((pre.T, 48, 128), dtype=torch.float16, device=dev)
+    ws = torch.empty(4096, dtype=torch.uint8, device=dev)  # the chain list: (B + 2) int32
+    keep = []
+    pargs, _, k0 = gdn.build_forward_args(t(pre.q), t(pre.k), t(pre.v), t(pre.a), t(pre.b), t(pre.cu_seqlens),
+                                          A_log=t(pre.A_log), dt_bias=t(pre.dt_bias), final_state=state,
+                                          output=pout, max_seqlen=L, workspace=ws)
+    keep.append(k0)
+    steps = 256
+    dargs = []
+    dout = torch.empty((B, 48, 128), dtype=torch.float16, device=dev)
+    for s in range(steps):
+        d = wl.serving_mix_decode(s, pre)
+        args, _, kk = gdn.build_forward_args(t(d.q), t(d.k), t(d.v), t(d.a), t(d.b), t(d.cu_seqlens),
+                                             A_log=t(d.A_log), dt_bias=t(d.dt_bias), initial_state=state,
+                                             final_state=state, output=dout, max_seqlen=1)
+        dargs.append(args)
+        keep.append(kk)
+
+    def call(args):
+        rc = lib.gdn_forward(ctypes.byref(args), sh)
+        if rc:
+            raise gdn.GdnError(rc, "gdn_forward")
+
+    def once():
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        state.zero_()
+        ev[0].record(stream)
+        call(pargs)
+        ev[1].record(stream)
+        for a in dargs:
+            call(a)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])
+
+    once()  # warm-up
+    runs = [once() for _ in range(3)]
+    p_ms = statistics.median(r[0] for r in runs)
+    d_ms = statistics.median(r[1] for r in runs)
+    hbm, tc, kind = measured_peaks()
+    dec_bytes = decode_bytes_per_launch(B, 16, 48, 128, 128)
+    return {"workload": "serving mix: 32 x 2048-token packed prefill (fp16, Hk=16, Hv=48, d=128, zero initial "
+                        "state) then 256 single-token decode steps on the resulting fp32 states, fresh seeded "
+                        "inputs per step, state updated in place",
+            "prefill_ms": round(p_ms, 3), "prefill_tokens_per_s": round(pre.T / (p_ms / 1e3), 1),
+            "prefill_tflops": round(prefill_algorithmic_flops(pre.T) / (p_ms / 1e3) / 1e12, 2),
+            "decode_ms_total": round(d_ms, 3), "decode_us_per_step": round(d_ms / steps * 1e3, 2),
+            "decode_tokens_per_s": round(B * steps / (d_ms / 1e3), 1),
+            "decode_frac_hbm": round(dec_bytes / (d_ms / steps / 1e3) / 1e9 / hbm, 4),
+            "tokens_per_s": round((pre.T + B * steps) / ((p_ms + d_ms) / 1e3), 1),
+            "launches": 2 + steps}
 
 
 # ---------------------------------------------------------------- CPU oracle (baseline and reference arm)
