@@ -350,22 +350,29 @@ def run_prefill(dev, stream):
     flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MiB
     plan = "auto"
     maxlen = int(np.diff(inp.cu_seqlens).max())
-    ws = torch.empty(4096, dtype=torch.uint8, device=dev)
-    run = lambda: gdn.gdn_forward(q, k, v, aa, bb, cu, A_log=A_log, dt_bias=dt_bias, final_state=final, output=out,
-                                  plan=plan, max_seqlen=maxlen, workspace=ws)
-    for _ in range(2):
-        run()
-    iters = 5
-    times = []
-    for _ in range(iters):
-        _flush_l2(flush)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        run()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1))
-    ms = statistics.median(times)
+    args, _, _ = gdn.build_forward_args(q, k, v, aa, bb, cu, A_log=A_log, dt_bias=dt_bias, final_state=final,
+                                        output=out, plan=plan, max_seqlen=maxlen)
+    ws_two_phase = torch.empty(gdn.workspace_size(args), dtype=torch.uint8, device=dev)
+    ws_single = torch.empty(4096, dtype=torch.uint8, device=dev)  # the chain list only: single-kernel evaluation
+
+    def timed(ws):
+        run = lambda: gdn.gdn_forward(q, k, v, aa, bb, cu, A_log=A_log, dt_bias=dt_bias, final_state=final,
+                                      output=out, plan=plan, max_seqlen=maxlen, workspace=ws)
+        for _ in range(2):
+            run()
+        times = []
+        for _ in range(5):
+            _flush_l2(flush)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    ms = timed(ws_two_phase)
+    ms_single = timed(ws_single)
     T = inp.T
     lengths = [int(x) for x in np.diff(inp.cu_seqlens)]
     _, tc_peak, kind = measured_peaks()
@@ -376,14 +383,17 @@ def run_prefill(dev, stream):
     return {"workload": "varlen prefill: 8 sequences, lengths U[256,4096] (seeded), Hk=16, Hv=48, d=128, fp16, "
                         "zero initial state", "tokens": int(T), "lengths": lengths,
             "plan": plan, "ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "l2": "flushed (256 MiB write)",
-            "roofline": {"bound": "tensor", "kernel": "chunked_kernel<__half>", "achieved": round(tflops, 2),
+            "workspace_bytes": int(ws_two_phase.numel()),
+            "single_kernel_ms": round(ms_single, 4),
+            "roofline": {"bound": "tensor", "kernel": "wy_prep_kernel + wy_scan_kernel (two-phase chunked)",
+                         "achieved": round(tflops, 2),
                          "peak": tc_peak, "peak_kind": f"{kind} dense bf16 burst (fp16 runs at the bf16 rate)",
                          "unit": "TFLOP/s", "frac": round(tflops / tc_peak, 4), "algorithmic_flops": flops,
                          "executed_mma_flops": executed,
                          "executed_tflops": round(executed / (ms / 1e3) / 1e12, 2),
                          "traffic": recorded_traffic(os.path.join(ROOT, "gated_delta_rule_gateddeltanet_gb300", "csrc",
-                                                                  "gdn_chunked.cu"),
-                                                     "varlen_prefill.chunked_kernel.ncu.md")}}
+                                                                  "gdn_chunked_wy.cu"),
+                                                     "varlen_prefill.wy_kernels.ncu.md")}}
 
 
 # Algorithmic FLOPs of the chunked evaluation per token and value head (chunk
@@ -391,9 +401,11 @@ def run_prefill(dev, stream):
 # 6 d^2, the intra-chunk products C (2d/r + d + 2d) (K K^T and Q K^T shared by
 # the r value heads of a key head), and the triangular inverse C^2 / 3.
 PREFILL_FLOPS_PER_TOKEN_HEAD = 6 * 128 * 128 + 64 * (2 * 128 / 3 + 128 + 2 * 128) + 64 * 64 / 3
-# tcgen05 FLOPs the kernel issues per (64-token chunk, value head): MMA1 128x64x128,
-# MMA2 128x128x128, MMA3 and MMA4 128x64x64, MMA5 128x128x64.
-PREFILL_MMA_FLOPS_PER_CHUNK_HEAD = 2 * (128 * 64 * 128 + 128 * 128 * 128 + 2 * 128 * 64 * 64 + 128 * 128 * 64)
+# tcgen05 FLOPs the two-phase path issues per (64-token chunk, value head): in
+# the scan kernel MMA2 128x128x128, MMA3 and MMA4 128x64x64, MMA5 128x128x64;
+# in the prep kernel [Q;K]K^T 128x64x128 once per key head (r = 3 value heads).
+PREFILL_MMA_FLOPS_PER_CHUNK_HEAD = (2 * (128 * 128 * 128 + 2 * 128 * 64 * 64 + 128 * 128 * 64)
+                                    + 2 * 128 * 64 * 128 // 3)
 
 
 def prefill_algorithmic_flops(tokens, heads=48):
@@ -539,12 +551,13 @@ def run_serving_mix(dev, stream, lib, sh):
     B, L = pre.B, 2048
     state = torch.zeros((B, 48, 128, 128), dtype=torch.float32, device=dev)
     pout = torch.empty((pre.T, 48, 128), dtype=torch.float16, device=dev)
-    ws = torch.empty(4096, dtype=torch.uint8, device=dev)  # the chain list: (B + 2) int32
     keep = []
     pargs, _, k0 = gdn.build_forward_args(t(pre.q), t(pre.k), t(pre.v), t(pre.a), t(pre.b), t(pre.cu_seqlens),
                                           A_log=t(pre.A_log), dt_bias=t(pre.dt_bias), final_state=state,
-                                          output=pout, max_seqlen=L, workspace=ws)
-    keep.append(k0)
+                                          output=pout, max_seqlen=L)
+    ws = torch.empty(gdn.workspace_size(pargs), dtype=torch.uint8, device=dev)
+    pargs.workspace, pargs.workspace_bytes = ctypes.c_void_p(ws.data_ptr()), ws.numel()
+    keep += [k0, ws]
     steps = 256
     dargs = []
     dout = torch.empty((B, 48, 128), dtype=torch.float16, device=dev)

@@ -1,0 +1,108 @@
+// Tile helpers shared by the tensor-core chunked kernels: the byte layout of
+// K-major fp16 operand tiles in the 128-byte swizzled canonical form that
+// tcgen05 shared-memory descriptors describe, vector conversions into such
+// tiles, and FP32-accurate warp-level products for the small blocks of the
+// triangular inverse.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace gdn {
+namespace ct {
+
+// Byte offset of element (row, k) in a K-major, 128-byte swizzled fp16 tile with R rows.
+__device__ __forceinline__ uint32_t sw(int row, int k, int R) {
+    const int kb = k >> 6, kk = k & 63;
+    return (uint32_t)(kb * R * 128 + row * 128 + ((((kk >> 3) ^ (row & 7)) & 7) << 4) + (kk & 7) * 2);
+}
+
+__device__ __forceinline__ void st_h(uint8_t *base, uint32_t off, float x) {
+    *reinterpret_cast<__half *>(base + off) = __float2half_rn(x);
+}
+
+// Four consecutive elements (k % 4 == 0) of one row: one 8-byte store.
+__device__ __forceinline__ void st_h4(uint8_t *base, uint32_t off, float a, float b, float c, float d) {
+    __half2 lo = __floats2half2_rn(a, b), hi = __floats2half2_rn(c, d);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t *>(&lo);
+    v.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(base + off) = v;
+}
+
+template <typename T>
+__device__ __forceinline__ void ld4(const T *p, float (&v)[4]);
+template <>
+__device__ __forceinline__ void ld4<float>(const float *p, float (&v)[4]) {
+    const float4 x = *reinterpret_cast<const float4 *>(p);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+template <>
+__device__ __forceinline__ void ld4<__half>(const __half *p, float (&v)[4]) {
+    const uint2 x = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&x.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&x.y));
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+
+
+// ---- FP32-accurate small products on the warp-level tensor cores
+//
+// The block products of the triangular inverse are 16 x 16 and 32 x 32: too
+// small for tcgen05 (M >= 64) and, on the CUDA cores, bound by shared-memory
+// traffic.  They run as mma.sync m16n8k8 TF32 products with each operand split
+// into a TF32 high part and a TF32 remainder (x = hi + lo), accumulating
+// hi*hi + hi*lo + lo*hi in FP32: the dropped lo*lo term is ~2^-22 relative, so
+// the result is as accurate as an FP32 product.
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    hi = to_tf32(x);
+    lo = to_tf32(x - __uint_as_float(hi));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// One warp: the 16 x 8 tile C = X Y with X [16][K] (row stride xs) and
+// Y [K][8] (row stride ys), both fp32 in shared memory; C written with the
+// given sign to C_ (row stride cs).  m16n8k8 fragment layout: lane = 4 g + t;
+// A holds (g, t), (g+8, t), (g, t+4), (g+8, t+4); B holds (t, g), (t+4, g);
+// C holds (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1).
+template <int K>
+__device__ __forceinline__ void warp_tile_16x8(const float *X_, int xs, const float *Y_, int ys, float *C_, int cs,
+                                               float sign, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        split_tf32(X_[g * xs + k0 + t], ah[0], al[0]);
+        split_tf32(X_[(g + 8) * xs + k0 + t], ah[1], al[1]);
+        split_tf32(X_[g * xs + k0 + t + 4], ah[2], al[2]);
+        split_tf32(X_[(g + 8) * xs + k0 + t + 4], ah[3], al[3]);
+        split_tf32(Y_[(k0 + t) * ys + g], bh[0], bl[0]);
+        split_tf32(Y_[(k0 + t + 4) * ys + g], bh[1], bl[1]);
+        mma_tf32(d, al, bh);
+        mma_tf32(d, ah, bl);
+        mma_tf32(d, ah, bh);
+    }
+    C_[g * cs + 2 * t] = sign * d[0];
+    C_[g * cs + 2 * t + 1] = sign * d[1];
+    C_[(g + 8) * cs + 2 * t] = sign * d[2];
+    C_[(g + 8) * cs + 2 * t + 1] = sign * d[3];
+}
+
+
+}  // namespace ct
+}  // namespace gdn

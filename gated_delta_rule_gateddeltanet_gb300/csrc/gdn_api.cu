@@ -111,6 +111,18 @@ gdn_status resolve_forward(const gdn_forward_args *a, gdn::ForwardParams *out) {
 
 }  // namespace
 
+namespace gdn {
+// Workspace of the single-kernel chunked evaluation (the chain list only), or
+// 0 when these arguments never reach a chunked kernel.
+gdn_status single_kernel_workspace_size(const gdn_forward_args *args, size_t *bytes) {
+    if (!bytes) return GDN_ERR_NULL;
+    const gdn_status st = check_sizes(args);
+    if (st != GDN_OK) return st;
+    *bytes = wants_chunked(args) ? chunked_workspace_bytes(args->num_seqs) : 0;
+    return GDN_OK;
+}
+}  // namespace gdn
+
 extern "C" {
 
 const char *gdn_status_string(gdn_status status) {
@@ -132,7 +144,9 @@ gdn_status gdn_forward_workspace_size(const gdn_forward_args *args, size_t *byte
     if (!bytes) return GDN_ERR_NULL;
     const gdn_status st = check_sizes(args);
     if (st != GDN_OK) return st;
-    *bytes = wants_chunked(args) ? gdn::chunked_workspace_bytes(args->num_seqs) : 0;
+    *bytes = wants_chunked(args) ? gdn::chunked_wy_workspace_bytes(args->num_seqs, args->total_tokens,
+                                                                   args->num_k_heads, args->num_v_heads)
+                                 : 0;
     return GDN_OK;
 }
 
@@ -147,11 +161,17 @@ gdn_status gdn_forward(const gdn_forward_args *a, gdn_stream_t stream) {
         chunked = false;  // the automatic plan keeps every sequence on the recurrent kernel
     }
     if (chunked) {
-        if (!a->workspace || a->workspace_bytes < gdn::chunked_workspace_bytes(a->num_seqs) ||
-            (reinterpret_cast<uintptr_t>(a->workspace) & 15u))
-            return GDN_ERR_WORKSPACE;
+        // A workspace of gdn_forward_workspace_size bytes runs the two-phase
+        // chunked evaluation; one that only holds the chain list runs the
+        // single-kernel one (same results up to rounding, slower).
+        if (!a->workspace || (reinterpret_cast<uintptr_t>(a->workspace) & 15u)) return GDN_ERR_WORKSPACE;
+        const bool two_phase = a->workspace_bytes >= gdn::chunked_wy_workspace_bytes(a->num_seqs, a->total_tokens,
+                                                                                   a->num_k_heads, a->num_v_heads);
+        if (!two_phase && a->workspace_bytes < gdn::chunked_workspace_bytes(a->num_seqs)) return GDN_ERR_WORKSPACE;
         const int min_len = a->plan == GDN_PLAN_CHUNKED ? -1 : gdn::RECURRENT_MAX_LEN;
-        if (gdn::launch_chunked(p, min_len, a->workspace, s) != cudaSuccess) return GDN_ERR_CUDA;
+        const cudaError_t e = two_phase ? gdn::launch_chunked_wy(p, min_len, a->workspace, s)
+                                        : gdn::launch_chunked(p, min_len, a->workspace, s);
+        if (e != cudaSuccess) return GDN_ERR_CUDA;
         if (a->plan == GDN_PLAN_CHUNKED) return GDN_OK;
         p.max_len = gdn::RECURRENT_MAX_LEN;
     }

@@ -45,11 +45,14 @@
 #include <cudaTypedefs.h>
 #include <mutex>
 
+#include "chunk_tiles.cuh"
 #include "gdn_internal.cuh"
 #include "ptx.cuh"
 
 namespace gdn {
 namespace {
+
+using namespace ct;
 
 constexpr int NT = 512;  // 16 warps: four per tensor-memory lane quarter
 constexpr int CH = 64;   // chunk length
@@ -88,106 +91,8 @@ static_assert(SMEM_ALLOC + 2048 <= 227 * 1024, "shared memory budget (dynamic + 
 static_assert(64 * 65 * 4 <= 32768, "fp32 A staging fits the R^T and U^T tiles");
 static_assert(OFF_M + 32 * 36 * 4 <= OFF_STG + STG_BYTES, "fp32 T staging fits the staging area");
 
-// Byte offset of element (row, k) in a K-major, 128-byte swizzled fp16 tile with R rows.
-__device__ __forceinline__ uint32_t sw(int row, int k, int R) {
-    const int kb = k >> 6, kk = k & 63;
-    return (uint32_t)(kb * R * 128 + row * 128 + ((((kk >> 3) ^ (row & 7)) & 7) << 4) + (kk & 7) * 2);
-}
-
-__device__ __forceinline__ void st_h(uint8_t *base, uint32_t off, float x) {
-    *reinterpret_cast<__half *>(base + off) = __float2half_rn(x);
-}
-
-// Four consecutive elements (k % 4 == 0) of one row: one 8-byte store.
-__device__ __forceinline__ void st_h4(uint8_t *base, uint32_t off, float a, float b, float c, float d) {
-    __half2 lo = __floats2half2_rn(a, b), hi = __floats2half2_rn(c, d);
-    uint2 v;
-    v.x = *reinterpret_cast<uint32_t *>(&lo);
-    v.y = *reinterpret_cast<uint32_t *>(&hi);
-    *reinterpret_cast<uint2 *>(base + off) = v;
-}
-
-template <typename T>
-__device__ __forceinline__ void ld4(const T *p, float (&v)[4]);
-template <>
-__device__ __forceinline__ void ld4<float>(const float *p, float (&v)[4]) {
-    const float4 x = *reinterpret_cast<const float4 *>(p);
-    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-}
-template <>
-__device__ __forceinline__ void ld4<__half>(const __half *p, float (&v)[4]) {
-    const uint2 x = *reinterpret_cast<const uint2 *>(p);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&x.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&x.y));
-    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
-}
-
-// Unit lower-triangular inverse T = (I + A)^-1 of a 64 x 64 strictly lower A
-// (fp32, row stride AS, shared), written in full (ones on the diagonal, zeros
-// above) into T32 (row stride TS).  The four 16 x 16 diagonal blocks come from
-// forward substitution; the off-diagonal blocks from the block identity
-// [[L11, 0], [L21, L22]]^-1 = [[T11, 0], [-T22 L21 T11, T22]], first for the
-// two 32 x 32 diagonal blocks, then for the whole matrix.  The block products
-// are dense, fully unrolled and register-tiled so their shared-memory loads
-// pipeline.
+// Row strides (floats) of the fp32 A and T staging and of the block-product scratch.
 constexpr int AS = 65, TS = 68, MS = 36;
-
-// ---- FP32-accurate small products on the warp-level tensor cores
-//
-// The block products of the triangular inverse are 16 x 16 and 32 x 32: too
-// small for tcgen05 (M >= 64) and, on the CUDA cores, bound by shared-memory
-// traffic.  They run as mma.sync m16n8k8 TF32 products with each operand split
-// into a TF32 high part and a TF32 remainder (x = hi + lo), accumulating
-// hi*hi + hi*lo + lo*hi in FP32: the dropped lo*lo term is ~2^-22 relative, so
-// the result is as accurate as an FP32 product.
-
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    hi = to_tf32(x);
-    lo = to_tf32(x - __uint_as_float(hi));
-}
-
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// One warp: the 16 x 8 tile C = X Y with X [16][K] (row stride xs) and
-// Y [K][8] (row stride ys), both fp32 in shared memory; C written with the
-// given sign to C_ (row stride cs).  m16n8k8 fragment layout: lane = 4 g + t;
-// A holds (g, t), (g+8, t), (g, t+4), (g+8, t+4); B holds (t, g), (t+4, g);
-// C holds (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1).
-template <int K>
-__device__ __forceinline__ void warp_tile_16x8(const float *X_, int xs, const float *Y_, int ys, float *C_, int cs,
-                                               float sign, int lane) {
-    const int g = lane >> 2, t = lane & 3;
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        uint32_t ah[4], al[4], bh[2], bl[2];
-        split_tf32(X_[g * xs + k0 + t], ah[0], al[0]);
-        split_tf32(X_[(g + 8) * xs + k0 + t], ah[1], al[1]);
-        split_tf32(X_[g * xs + k0 + t + 4], ah[2], al[2]);
-        split_tf32(X_[(g + 8) * xs + k0 + t + 4], ah[3], al[3]);
-        split_tf32(Y_[(k0 + t) * ys + g], bh[0], bl[0]);
-        split_tf32(Y_[(k0 + t + 4) * ys + g], bh[1], bl[1]);
-        mma_tf32(d, al, bh);
-        mma_tf32(d, ah, bl);
-        mma_tf32(d, ah, bh);
-    }
-    C_[g * cs + 2 * t] = sign * d[0];
-    C_[g * cs + 2 * t + 1] = sign * d[1];
-    C_[(g + 8) * cs + 2 * t] = sign * d[2];
-    C_[(g + 8) * cs + 2 * t + 1] = sign * d[3];
-}
 
 // Unit lower-triangular inverse T = (I + A)^-1 of a 64 x 64 strictly lower A
 // (fp32, row stride AS, shared) into T32 (row stride TS).  The four 16 x 16
@@ -815,42 +720,13 @@ int num_sms() {
     return cached;
 }
 
-// cuTensorMapEncodeTiled from the driver, looked up once.
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// Tensor map over a packed fp16 [T, row_elems] array with `stride` elements
-// between tokens; boxes of 64 tokens x 128 elements, zero fill out of range.
-bool encode_rows(CUtensorMap *map, const void *base, long long row_elems, long long stride, int T) {
-    auto encode = tensor_map_encoder();
-    if (!encode) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)(T > 0 ? T : 1)};
-    const cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
-    const cuuint32_t box[2] = {DH, CH};
-    const cuuint32_t estride[2] = {1, 1};
-    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estride,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <typename TIO>
 cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStream_t stream) {
     CUtensorMap mq{}, mk{}, mv{};
     if (sizeof(TIO) == 2) {
-        if (!encode_rows(&mq, p.q, (long long)p.Hk * DH, p.q_stride, p.T) ||
-            !encode_rows(&mk, p.k, (long long)p.Hk * DH, p.k_stride, p.T) ||
-            !encode_rows(&mv, p.v, (long long)p.Hv * DH, p.v_stride, p.T))
+        if (!encode_rows_f16(&mq, p.q, (long long)p.Hk * DH, p.q_stride, p.T, DH, CH) ||
+            !encode_rows_f16(&mk, p.k, (long long)p.Hk * DH, p.k_stride, p.T, DH, CH) ||
+            !encode_rows_f16(&mv, p.v, (long long)p.Hv * DH, p.v_stride, p.T, DH, CH))
             return cudaErrorInvalidValue;
     }
     plan_kernel<<<1, 1024, 0, stream>>>(p.cu, p.B, p.T, min_len, ws);
@@ -867,6 +743,34 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStre
 }
 
 }  // namespace
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool encode_rows_f16(CUtensorMap *map, const void *base, long long row_elems, long long stride, int T, int box_x,
+                     int box_y) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)(T > 0 ? T : 1)};
+    const cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)box_x, (cuuint32_t)box_y};
+    const cuuint32_t estride[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 size_t chunked_workspace_bytes(int B) { return ((size_t)(B + 2) * sizeof(int32_t) + 255) & ~size_t(255); }
 

@@ -1,0 +1,845 @@
+// Two-phase chunked (WY / UT-transform) gated delta rule on the tcgen05 tensor
+// cores: a parallel phase over every (64-token chunk, key head) and a
+// sequential state-passing phase over every (sequence, value head) chain.
+//
+// Operator: "[CUDA] Add compact GatedDeltaNet operator" (Description) -- the
+// tensor-core chunked prefill path of the GatedDeltaNet operator; same results
+// as the token-by-token recurrence, evaluated 64 tokens at a time.
+//
+// Algebra, per (sequence, value head) chain and chunk of n <= 64 tokens, with
+// S0 the dv x dk state entering the chunk, Gamma_r the within-chunk cumulative
+// log decay and gamma_r = exp(Gamma_r):
+//   A[r,s] = beta_r exp(Gamma_r - Gamma_s) (k_r . k_s)  (s < r);   T = (I + A)^-1
+//   PD[r,s] = exp(Gamma_r - Gamma_s) (q_r . k_s)        (s <= r)
+//   X = S0 K^T,  O' = S0 Q^T                            (dv x n)
+//   R^T[i,s] = beta_s (v_s[i] - gamma_s X[i,s]);   U^T = R^T T^T   (the capsule deltas)
+//   o_r = scale (gamma_r O'[:,r] + (U^T PD^T)[:,r])
+//   S1 = gamma_last S0 + (U^T diag(exp(Gamma_last - Gamma))) K
+// This follows from S_r = gamma_r S0 + sum_{s<=r} (gamma_r/gamma_s) u_s k_s^T
+// and u_r = beta_r (v_r - g_r S_{r-1} k_r).  Only differences Gamma_r - Gamma_s
+// with r >= s are exponentiated.
+//
+// Everything in the first two lines depends on the chunk's own inputs only,
+// not on the state, so it leaves the sequential critical path:
+//
+//  wy_prep_kernel (one CTA per (chunk, key head), four CTAs per SM): L2-normal-
+//    ises q and k, forms the [Q;K] and K^T fp16 operand tiles, runs
+//    [Q;K] K^T on the tensor cores (P = QK^T and G = KK^T, shared by the key
+//    head's value heads), and for each of its value heads computes the gates,
+//    A, P o D and the FP32 triangular inverse T.  It writes byte images of the
+//    operand tiles, already in the swizzled shared-memory layout the MMAs
+//    read, to the caller's workspace (one 48 KiB record per (chunk, key head),
+//    one 16.75 KiB record per (chunk, value head)), plus the capsule's k and g.
+//
+//  wy_scan_kernel (persistent, one CTA per SM, chains longest-first): keeps the
+//    FP32 state in tensor memory and, per chunk, loads the two records with
+//    bulk copies (and v with a 2-D TMA copy) one chunk ahead, then runs three
+//    dependent tensor-core steps:
+//      MMA2  S0 [Q;K]^T     -> O', X                (128 x 128, K = dk)
+//      MMA3  R^T T^T        -> U^T                  (128 x 64,  K = n)
+//      MMA4  U^T PD^T       -> Y                    (128 x 64,  K = n)
+//      MMA5  (U^T diag) K   accumulated onto gamma_last S0   (128 x 128, K = n)
+//    with the CUDA-core work between them (fp16 state copy, R^T, U^T and its
+//    decayed copy, capsule deltas, outputs) done by all 16 warps.
+//
+// Every MMA is kind::f16 (fp16 operands, FP32 accumulation in tensor memory)
+// with both operands K-major in the 128-byte swizzled layout and the value
+// dimension dv = 128 as M.  Numerics are those of the single-kernel chunked
+// evaluation (same fp16 operand roundings), except that gamma scales the
+// FP32 MMA result O' instead of an fp16 copy of Q.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "chunk_tiles.cuh"
+#include "gdn_internal.cuh"
+#include "ptx.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace ct;
+
+constexpr int CH = 64;   // chunk length
+constexpr int DH = 128;  // dk = dv on this path
+constexpr float EPS = 1e-6f;
+constexpr float LOG_DECAY_FLOOR = -200.f;  // exp(-200) is 0 in fp32; keeps Gamma well-conditioned
+constexpr long long WAIT_LIMIT = 4000000000LL;
+
+// Workspace records (byte images of shared-memory operand tiles).
+constexpr int KREC_BYTES = 49152;  // [Q;K] tile (2 K-blocks x 128 rows x 128 B) + K^T tile (128 rows x 128 B)
+constexpr int KREC_KT = 32768;
+constexpr int VREC_T = 0;          // T, [64][64] fp16
+constexpr int VREC_PD = 8192;      // P o D, [64][64] fp16
+constexpr int VREC_GATES = 16384;  // Gamma[64], beta[64], gamma[64] fp32
+constexpr int VREC_BYTES = 16384 + 3 * CH * 4;
+static_assert(VREC_BYTES % 128 == 0, "records stay 128-byte aligned");
+
+size_t header_bytes(int B) { return ((size_t)(3 + 2 * (size_t)B) * 4 + 1023) & ~size_t(1023); }
+long long max_chunks(int B, int T) { return (long long)T / CH + B; }
+
+// ---------------------------------------------------------------- plan
+
+// Workspace header: ws[0] = work counter, ws[1] = number of sequences on this
+// path, ws[2 .. 2+B) = those sequences longest-first (counting sort on the
+// number of chunks), ws[2+B .. 3+2B) = chunk_base: the index of each
+// sequence's first chunk in the record arrays (sequences not on this path
+// own no chunks); chunk_base[B] = total chunks.  Chunk counts above 1022 share
+// the first bin (they are all scheduled first).  Sequences with a bad packing
+// are left out (the recurrent kernel reports them).
+constexpr int PLAN_BINS = 1024;
+constexpr int PLAN_NT = 1024;
+__global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int B, int T, int min_len, int32_t *ws) {
+    __shared__ int hist[PLAN_BINS];
+    __shared__ int warp_sum[PLAN_NT / 32];
+    __shared__ int total;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // chunks of sequence b on this path (an empty sequence has none but is still
+    // listed: its final state is its initial state), or -1 when it is not
+    auto chunks_of = [&](int b) -> int {
+        const int lo = cu[b], hi = cu[b + 1];
+        if (lo < 0 || hi < lo || hi > T || hi - lo <= min_len) return -1;
+        return (hi - lo + CH - 1) / CH;
+    };
+    for (int i = tid; i < PLAN_BINS; i += PLAN_NT) hist[i] = 0;
+    __syncthreads();
+    for (int b = tid; b < B; b += PLAN_NT) {
+        const int c = chunks_of(b);
+        if (c >= 0) atomicAdd(&hist[PLAN_BINS - 1 - min(c, PLAN_BINS - 1)], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int i = 0; i < PLAN_BINS; ++i) {
+            const int c = hist[i];
+            hist[i] = run;
+            run += c;
+        }
+        total = run;
+    }
+    __syncthreads();
+    for (int b = tid; b < B; b += PLAN_NT) {
+        const int c = chunks_of(b);
+        if (c >= 0) ws[2 + atomicAdd(&hist[PLAN_BINS - 1 - min(c, PLAN_BINS - 1)], 1)] = b;
+    }
+    // chunk_base: exclusive prefix sum of the chunk counts in sequence order;
+    // thread t owns the contiguous sequences [t * per, (t + 1) * per)
+    int32_t *cbase = ws + 2 + B;
+    const int per = (B + PLAN_NT - 1) / PLAN_NT;
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) local += max(chunks_of(b), 0);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_sum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    int run = incl - local + (warp > 0 ? warp_sum[warp - 1] : 0);
+    for (int b = b0; b < b1; ++b) {
+        cbase[b] = run;
+        run += max(chunks_of(b), 0);
+    }
+    if (tid == PLAN_NT - 1) cbase[B] = warp_sum[31];
+    if (tid == 0) {
+        ws[0] = 0;
+        ws[1] = total;
+    }
+}
+
+// ---------------------------------------------------------------- triangular inverse
+
+// In-place unit lower-triangular inverse: AT holds a 64 x 64 strictly lower A
+// (fp32, row stride AS, zeros on and above the diagonal) and receives
+// T = (I + A)^-1 in full.  The four 16 x 16 diagonal blocks come from forward
+// substitution (one column per thread); the off-diagonal blocks from the block
+// identity [[L11, 0], [L21, L22]]^-1 = [[T11, 0], [-T22 L21 T11, T22]], first
+// inside the two 32 x 32 diagonal blocks, then for the lower-left quadrant.
+// Each block of A is read (into the product M = L21 T11) before the block of
+// T that replaces it is written.  256 threads; ends with a barrier.
+constexpr int AS = 65, MS = 36;
+__device__ void tri_inverse_inplace(float *AT, float *M, int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
+    float x[16];
+    const int blk = tid >> 4, c = tid & 15, o = blk * 16;
+    if (tid < 64) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc0 = 0.f, acc1 = 0.f;  // two partial sums shorten the dependency chain
+#pragma unroll
+            for (int s = 0; s < r; s += 2) {
+                acc0 = fmaf(AT[(o + r) * AS + o + s], x[s], acc0);
+                if (s + 1 < r) acc1 = fmaf(AT[(o + r) * AS + o + s + 1], x[s + 1], acc1);
+            }
+            x[r] = (r < c) ? 0.f : (r == c ? 1.f : -(acc0 + acc1));
+        }
+    }
+    __syncthreads();  // every diagonal block of A is read before T overwrites it
+    if (tid < 64) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) AT[(o + r) * AS + o + c] = x[r];
+    }
+    __syncthreads();
+    // inside the 32 x 32 diagonal blocks (o = 0, 32): M = A21 T11, T21 = -T22 M
+    if (warp < 4) {
+        const int pr = warp >> 1, n0 = (warp & 1) * 8, ob = 32 * pr;
+        warp_tile_16x8<16>(AT + (ob + 16) * AS + ob, AS, AT + ob * AS + ob + n0, AS, M + pr * 16 * MS + n0, MS, 1.f,
+                           lane);
+    }
+    __syncthreads();
+    if (warp < 4) {
+        const int pr = warp >> 1, n0 = (warp & 1) * 8, ob = 32 * pr;
+        warp_tile_16x8<16>(AT + (ob + 16) * AS + ob + 16, AS, M + pr * 16 * MS + n0, MS,
+                           AT + (ob + 16) * AS + ob + n0, AS, -1.f, lane);
+    }
+    __syncthreads();
+    // the lower-left 32 x 32 quadrant: M = A21 T11, T21 = -T22 M (one 16 x 8 tile per warp)
+    {
+        const int m0 = (warp >> 2) * 16, n0 = (warp & 3) * 8;
+        warp_tile_16x8<32>(AT + (32 + m0) * AS, AS, AT + n0, AS, M + m0 * MS + n0, MS, 1.f, lane);
+    }
+    __syncthreads();
+    {
+        const int m0 = (warp >> 2) * 16, n0 = (warp & 3) * 8;
+        warp_tile_16x8<32>(AT + (32 + m0) * AS + 32, AS, M + n0, MS, AT + (32 + m0) * AS + n0, AS, -1.f, lane);
+    }
+    __syncthreads();
+}
+
+// Gates of the 64 tokens [t0, t0 + 64) of value head h (one warp, two tokens
+// per lane): effective decay g, beta, and the within-chunk cumulative log
+// decay Gamma (log decays floored at LOG_DECAY_FLOOR).  Tokens at or past
+// `n` get g = 1, beta = 0 (no effect).  Writes Gamma, beta and exp(Gamma) to
+// G[0..64), G[64..128), G[128..192) and returns each lane's two decays.
+__device__ __forceinline__ void chunk_gates(const ForwardParams &p, int t0, int n, int h, float *G, float (&gt)[2],
+                                            int lane) {
+    float lg[2], bt[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int s = lane + 32 * u;
+        lg[u] = 0.f;
+        bt[u] = 0.f;
+        gt[u] = 1.f;
+        if (s < n) {
+            const long long t = (long long)t0 + s;
+            const float av = p.a[t * p.Hv + h], bv = p.b[t * p.Hv + h];
+            if (p.gate_raw) {
+                const float l = -expf(p.A_log[h]) * softplus_f(av + p.dt_bias[h]);
+                gt[u] = expf(l);
+                lg[u] = fmaxf(l, LOG_DECAY_FLOOR);
+                bt[u] = 1.f / (1.f + expf(-bv));
+            } else {
+                gt[u] = av;
+                lg[u] = av > 0.f ? fmaxf(logf(av), LOG_DECAY_FLOOR) : LOG_DECAY_FLOOR;
+                bt[u] = bv;
+            }
+        }
+    }
+    float c0 = lg[0], c1 = lg[1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y0 = __shfl_up_sync(0xffffffffu, c0, o);
+        const float y1 = __shfl_up_sync(0xffffffffu, c1, o);
+        if (lane >= o) {
+            c0 += y0;
+            c1 += y1;
+        }
+    }
+    c1 += __shfl_sync(0xffffffffu, c0, 31);
+    G[lane] = c0;
+    G[lane + 32] = c1;
+    G[CH + lane] = bt[0];
+    G[CH + lane + 32] = bt[1];
+    G[2 * CH + lane] = expf(c0);
+    G[2 * CH + lane + 32] = expf(c1);
+}
+
+// ---------------------------------------------------------------- phase 1: per (chunk, key head)
+
+constexpr int PT = 256;  // threads of the prep kernel
+// Shared memory of the prep kernel (offsets from a 1024-byte aligned base).
+// The first 48 KiB hold the key-head record image ([Q;K] tile, then K^T
+// tile); once its bulk store has read it, the same bytes hold A / T (fp32),
+// the block-product scratch and the value-head record image.
+constexpr int P_AT = 0;                    // [64][AS] fp32
+constexpr int P_M = 64 * AS * 4;           // [32][MS] fp32
+constexpr int P_VREC = 21504;              // value-head record image (1024-byte aligned)
+constexpr int PREP_SMEM = KREC_BYTES + 1024;
+static_assert(P_M + 32 * MS * 4 <= P_VREC && P_VREC + VREC_BYTES <= KREC_BYTES, "prep shared-memory layout");
+
+template <typename TIO>
+__global__ void __launch_bounds__(PT, 4)
+    wy_prep_kernel(const ForwardParams p, const int32_t *ws, uint8_t *krec, uint8_t *vrec) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const int g = blockIdx.x / p.Hk, kh = blockIdx.x % p.Hk;
+    const int32_t *cbase = ws + 2 + p.B;
+    if (g >= cbase[p.B]) return;  // past the last chunk (the grid is sized by an upper bound)
+    int lo = 0, hi = p.B;         // the sequence b with cbase[b] <= g < cbase[b + 1]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cbase[mid] <= g) lo = mid;
+        else hi = mid;
+    }
+    const int b = lo;
+    const int bos = p.cu[b], eos = p.cu[b + 1];
+    const int t0 = bos + CH * (g - cbase[b]);
+    const int n = min(CH, eos - t0);
+
+    if (warp == 0) {
+        ptx::tmem_alloc(&tmem_base, 64);
+        ptx::tmem_relinquish();
+    }
+    if (tid == 0) {
+        ptx::mbar_init(&bar, 1);
+        ptx::fence_mbar_init();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tm = tmem_base;
+
+    // ---- normalised q (rows 0-63) and k (rows 64-127) of the [Q;K] tile; rows
+    //      past the sequence are zero.  Warp w handles tokens w, w + 8, ...; four
+    //      tokens at a time so their loads and reductions overlap.
+    const TIO *qg = static_cast<const TIO *>(p.q);
+    const TIO *kg = static_cast<const TIO *>(p.k);
+#pragma unroll 1
+    for (int round = 0; round < 2; ++round) {
+        float qv[4][4], kv[4][4], sq[4], sk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int s = warp + 8 * (u + 4 * round);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) qv[u][e] = kv[u][e] = 0.f;
+            if (s < n) {
+                const long long t = (long long)t0 + s;
+                ld4<TIO>(qg + t * p.q_stride + (long long)kh * DH + lane * 4, qv[u]);
+                ld4<TIO>(kg + t * p.k_stride + (long long)kh * DH + lane * 4, kv[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            sq[u] = sk[u] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sq[u] = fmaf(qv[u][e], qv[u][e], sq[u]);
+                sk[u] = fmaf(kv[u][e], kv[u][e], sk[u]);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], off);
+                sk[u] += __shfl_xor_sync(0xffffffffu, sk[u], off);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int s = warp + 8 * (u + 4 * round);
+            const float iq = 1.f / fmaxf(sqrtf(sq[u]), EPS), ik = 1.f / fmaxf(sqrtf(sk[u]), EPS);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                qv[u][e] *= iq;
+                kv[u][e] *= ik;
+            }
+            const int c = lane * 4;
+            st_h4(sm, sw(s, c, 128), qv[u][0], qv[u][1], qv[u][2], qv[u][3]);
+            st_h4(sm, sw(64 + s, c, 128), kv[u][0], kv[u][1], kv[u][2], kv[u][3]);
+            const int tl = t0 + s - bos;
+            if (p.caps && s < n && tl < p.cap) {
+                float *dst = p.caps + ((long long)b * p.cap + tl) * p.W + p.Hv + (long long)kh * DH + c;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dst[e] = kv[u][e];  // rows need not be 16-byte aligned
+            }
+        }
+    }
+    __syncthreads();
+    // ---- K^T tile (row j = feature, 64 token columns) from the K rows: thread
+    //      (j, half) gathers 32 tokens as four 8-element pieces
+    {
+        const int j = tid >> 1, sg = (tid & 1) * 32;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int s = sg + 8 * m + 2 * e;
+                const unsigned short a0 = *reinterpret_cast<const unsigned short *>(sm + sw(64 + s, j, 128));
+                const unsigned short a1 = *reinterpret_cast<const unsigned short *>(sm + sw(65 + s, j, 128));
+                w[e] = (uint32_t)a0 | ((uint32_t)a1 << 16);
+            }
+            *reinterpret_cast<uint4 *>(sm + KREC_KT + sw(j, sg + 8 * m, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    // ---- [Q;K] K^T on the tensor cores (P in lanes 0-63, G in lanes 64-127),
+    //      and the key-head record to the workspace
+    if (tid == 0) {
+        ptx::tc_fence_after();
+        const uint32_t a_qk = ptx::smem_u32(sm);
+        const uint32_t i64 = ptx::idesc_f16_f32(128, 64);
+        for (int ks = 0; ks < DH / 16; ++ks) {
+            const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
+            ptx::mma_f16(tm, ptx::sdesc_k_sw128(a_qk + ko), ptx::sdesc_k_sw128(a_qk + 64 * 128 + ko), i64, ks > 0);
+        }
+        ptx::mma_commit(&bar);
+        ptx::bulk_s2g(krec + ((size_t)g * p.Hk + kh) * KREC_BYTES, sm, KREC_BYTES);
+        ptx::bulk_commit();
+    }
+    bool ok = ptx::mbar_wait_bounded(&bar, 0, WAIT_LIMIT);
+    ptx::tc_fence_after();
+    if (tid == 0) ptx::bulk_wait_read_all();  // the tile bytes may be reused from here on
+    ok = __syncthreads_and(ok);
+
+    // ---- per value head of this key head: gates, A and P o D, T, record
+    float *AT = reinterpret_cast<float *>(sm + P_AT);
+    float *Mw = reinterpret_cast<float *>(sm + P_M);
+    uint8_t *vimg = sm + P_VREC;
+    float *G = reinterpret_cast<float *>(vimg + VREC_GATES);  // Gamma | beta | gamma
+    const int quarter = warp & 3, c32 = (warp >> 2) * 32;
+    const int row = quarter * 32 + lane;  // tensor-memory lane of this thread
+    const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
+#pragma unroll 1
+    for (int i = 0; ok && i < p.r; ++i) {
+        const int h = kh * p.r + i;
+        if (warp == 0) {
+            float gt[2];
+            chunk_gates(p, t0, n, h, G, gt, lane);
+            if (p.caps) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int s = lane + 32 * u, tl = t0 + s - bos;
+                    if (s < n && tl < p.cap) p.caps[((long long)b * p.cap + tl) * p.W + h] = gt[u];
+                }
+            }
+        }
+        __syncthreads();
+        {
+            float v[32];
+            ptx::tmem_ld32(tm + lane_sel + c32, v);
+            const int r = row & 63;
+            const float Gr = G[r];
+            if (quarter >= 2) {  // lanes 64-127: G = K K^T -> A (strictly lower)
+                const float br = G[CH + r];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int s = c32 + j;
+                    AT[r * AS + s] = (s < r) ? br * __expf(Gr - G[s]) * v[j] : 0.f;
+                }
+            } else {  // lanes 0-63: P = Q K^T -> P o D (lower, diagonal included)
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    float w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = c32 + j + e;
+                        w[e] = (s <= r) ? v[j + e] * __expf(Gr - G[s]) : 0.f;
+                    }
+                    st_h4(vimg + VREC_PD, sw(r, c32 + j, 64), w[0], w[1], w[2], w[3]);
+                }
+            }
+        }
+        __syncthreads();
+        tri_inverse_inplace(AT, Mw, tid);
+        {  // T -> fp16 tile: thread (r, 16-column group)
+            const int r = tid >> 2, s0 = (tid & 3) * 16;
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+                st_h4(vimg + VREC_T, sw(r, s0 + j, 64), AT[r * AS + s0 + j], AT[r * AS + s0 + j + 1],
+                      AT[r * AS + s0 + j + 2], AT[r * AS + s0 + j + 3]);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            ptx::bulk_s2g(vrec + ((size_t)g * p.Hv + h) * VREC_BYTES, vimg, VREC_BYTES);
+            ptx::bulk_commit();
+            ptx::bulk_wait_read_all();
+        }
+        __syncthreads();
+    }
+    if (!ok && tid == 0) {
+        flag_error(p.status, GDN_DEVERR_TIMEOUT);
+        ptx::mbar_wait_bounded(&bar, 0, WAIT_LIMIT);  // let the MMA drain before tensor memory is freed
+    }
+    if (tid == 0) ptx::bulk_wait_all();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tm, 64);
+    }
+}
+
+// ---------------------------------------------------------------- phase 2: per (sequence, value head) chain
+
+constexpr int NT = 512;  // 16 warps: four per tensor-memory lane quarter
+constexpr int TMEM_COLS = 512;
+// Tensor-memory columns (128 lanes each).
+constexpr uint32_t TM_S = 0;    // FP32 state S (dv lanes x dk columns)
+constexpr uint32_t TM_O = 128;  // O' = S0 Q^T (64 columns), then X = S0 K^T at TM_X
+constexpr uint32_t TM_X = 192;
+constexpr uint32_t TM_U = 256;  // U^T
+constexpr uint32_t TM_Y = 320;  // U^T (P o D)^T
+
+// Shared memory (offsets from a 1024-byte aligned base): two stages holding
+// one chunk's inputs each, then the fp16 state copy and the R^T / U^T tile.
+constexpr int S_KREC = 0;                   // key-head record: [Q;K] tile, K^T tile at S_KREC + KREC_KT
+constexpr int S_VREC = KREC_BYTES;          // value-head record: T, P o D, gates
+constexpr int S_V = 66560;                  // fp16 v rows of the chunk [64][128]; then U^T diag(...) tile
+constexpr int STAGE_BYTES = S_V + 16384;    // 81 KiB
+constexpr int OFF_S16 = 2 * STAGE_BYTES;    // [128][128] fp16 S0 (two K-blocks)
+constexpr int OFF_RT = OFF_S16 + 32768;     // [128][64] fp16 R^T, then U^T
+constexpr int SCAN_SMEM = OFF_RT + 16384 + 1024;  // + slack for the 1024-byte alignment
+static_assert(S_VREC + VREC_BYTES <= S_V && S_V % 1024 == 0, "stage layout");
+static_assert(SCAN_SMEM + 1024 <= 227 * 1024, "shared memory budget (dynamic + static)");
+
+template <typename TIO>
+__global__ void __launch_bounds__(NT, 1)
+    wy_scan_kernel(const ForwardParams p, int32_t *ws, const uint8_t *krec, const uint8_t *vrec,
+                   const __grid_constant__ CUtensorMap map_v) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t bar;      // MMA completion
+    __shared__ __align__(8) uint64_t lbar[2];  // stage loads
+    __shared__ uint32_t tmem_base;
+    __shared__ int item_s;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // Tensor memory: a warp reaches only the 32 lanes of its quarter (warp % 4);
+    // the four warps of a quarter split the columns.
+    const int quarter = warp & 3, cq = warp >> 2;
+    const int row = quarter * 32 + lane;  // the tensor-memory lane (state / output row) of this thread
+    const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
+    const int c16 = cq * 16, c32 = cq * 32;
+
+    if (warp == 0) {
+        ptx::tmem_alloc(&tmem_base, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if (tid == 0) {
+        ptx::mbar_init(&bar, 1);
+        ptx::mbar_init(&lbar[0], 1);
+        ptx::mbar_init(&lbar[1], 1);
+        ptx::fence_mbar_init();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tm = tmem_base;
+    uint32_t phase = 0, lph[2] = {0u, 0u};
+    bool pending[2] = {false, false};
+    bool failed = false;
+    constexpr bool STAGED = sizeof(TIO) == 2;
+    const uint32_t a_S16 = ptx::smem_u32(sm + OFF_S16), a_RT = ptx::smem_u32(sm + OFF_RT);
+
+    auto mma_wait = [&]() -> bool {
+        const bool ok = ptx::mbar_wait_bounded(&bar, phase, WAIT_LIMIT);
+        phase ^= 1u;
+        ptx::tc_fence_after();
+        return __syncthreads_and(ok);
+    };
+    auto mma_ready = [&]() {  // this thread's smem / tmem writes become visible to the next MMA
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+    };
+    auto stage_wait = [&](int st) -> bool {
+        const bool ok = ptx::mbar_wait_bounded(&lbar[st], lph[st], WAIT_LIMIT);
+        lph[st] ^= 1u;
+        pending[st] = false;
+        return __syncthreads_and(ok);
+    };
+
+    const int n_items = ws[1] * p.Hv;
+    const int32_t *cbase = ws + 2 + p.B;
+    const TIO *vg = static_cast<const TIO *>(p.v);
+    TIO *og = static_cast<TIO *>(p.out);
+    const long long ubase = (long long)p.Hv + (long long)p.Hk * DH;
+
+    while (!failed) {
+        if (tid == 0) item_s = atomicAdd(&ws[0], 1);
+        __syncthreads();
+        const int item = item_s;
+        __syncthreads();
+        if (item >= n_items) break;
+        const int b = ws[2 + item / p.Hv], h = item % p.Hv, kh = h / p.r;
+        const int bos = p.cu[b], eos = p.cu[b + 1];
+        const int nc = (eos - bos + CH - 1) / CH;
+        const long long gbase = cbase[b];
+        const int slot = p.slots ? p.slots[b] : b;
+        if (slot < 0 || slot >= p.num_slots) {
+            if (tid == 0 && h == 0) flag_error(p.status, GDN_DEVERR_STATE_SLOT);
+            continue;
+        }
+        const size_t head_off = ((size_t)slot * p.Hv + h) * (size_t)DH * DH;
+
+        // chunk c's records (and fp16 v rows) into stage st
+        auto stage_load = [&](int c, int st) {
+            if (tid == 0) {
+                uint8_t *stage = sm + st * STAGE_BYTES;
+                ptx::mbar_arrive_expect_tx(&lbar[st], (uint32_t)(KREC_BYTES + VREC_BYTES + (STAGED ? CH * DH * 2 : 0)));
+                ptx::bulk_g2s(stage + S_KREC, krec + ((gbase + c) * p.Hk + kh) * KREC_BYTES, KREC_BYTES, &lbar[st]);
+                ptx::bulk_g2s(stage + S_VREC, vrec + ((gbase + c) * p.Hv + h) * VREC_BYTES, VREC_BYTES, &lbar[st]);
+                if (STAGED) ptx::tma_load_2d(stage + S_V, &map_v, h * DH, bos + CH * c, &lbar[st]);
+            }
+            pending[st] = true;
+        };
+        // S0 -> fp16 operand tile; the tensor-memory state becomes gamma_last S0
+        bool state_live = p.init != nullptr;
+        auto build_s16 = [&](const float *G, int n) {
+            const float gl = G[2 * CH + n - 1];
+            float v[32];
+            if (state_live) {
+                ptx::tmem_ld32(tm + lane_sel + TM_S + c32, v);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                st_h4(sm + OFF_S16, sw(row, c32 + j, 128), v[j], v[j + 1], v[j + 2], v[j + 3]);
+            if (state_live) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= gl;
+                ptx::tmem_st32(tm + lane_sel + TM_S + c32, v);
+                ptx::tmem_st_wait();
+            }
+        };
+
+        // ---- chain start: the initial state into tensor memory, chunk 0's inputs
+        if (state_live) {
+            const float *src = p.init + head_off + (size_t)row * DH + c32;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(src + j);
+                v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
+            }
+            ptx::tmem_st32(tm + lane_sel + TM_S + c32, v);
+            ptx::tmem_st_wait();
+        }
+        if (nc > 0) {
+            stage_load(0, 0);
+            if (!stage_wait(0)) { failed = true; break; }
+            build_s16(reinterpret_cast<const float *>(sm + S_VREC + VREC_GATES), min(CH, eos - bos));
+        }
+        mma_ready();
+
+        for (int c = 0; c < nc && !failed; ++c) {
+            const int st = c & 1;
+            uint8_t *stage = sm + st * STAGE_BYTES;
+            const float *G = reinterpret_cast<const float *>(stage + S_VREC + VREC_GATES);
+            const float *Gam = G, *bet = G + CH, *gmm = G + 2 * CH;
+            const int t0 = bos + CH * c, n = min(CH, eos - t0);
+            const uint32_t a_st = ptx::smem_u32(stage);
+            // the other stage was last read by chunk c - 1, which is complete
+            if (c + 1 < nc) stage_load(c + 1, st ^ 1);
+            // ---- MMA2: [O' | X] = S0 [Q;K]^T
+            if (tid == 0) {
+                ptx::tc_fence_after();
+                const uint32_t i128 = ptx::idesc_f16_f32(128, 128);
+                for (int ks = 0; ks < DH / 16; ++ks) {
+                    const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    ptx::mma_f16(tm + TM_O, ptx::sdesc_k_sw128(a_S16 + ko), ptx::sdesc_k_sw128(a_st + S_KREC + ko),
+                                 i128, ks > 0);
+                }
+                ptx::mma_commit(&bar);
+            }
+            if (!mma_wait()) { failed = true; break; }
+            // ---- R^T = (V - diag(gamma) K S0^T)^T diag(beta) from X
+            {
+                float x[16];
+                ptx::tmem_ld16(tm + lane_sel + TM_X + c16, x);
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) {
+                    float w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = c16 + j + e;
+                        float vv;
+                        if (STAGED)
+                            vv = to_f32(reinterpret_cast<const TIO *>(stage + S_V)[s * DH + row]);
+                        else
+                            vv = s < n ? to_f32(vg[(long long)(t0 + s) * p.v_stride + (long long)h * DH + row]) : 0.f;
+                        w[e] = bet[s] * (vv - gmm[s] * x[j + e]);
+                    }
+                    st_h4(sm + OFF_RT, sw(row, c16 + j, 128), w[0], w[1], w[2], w[3]);
+                }
+            }
+            mma_ready();
+            // ---- MMA3: U^T = R^T T^T
+            if (tid == 0) {
+                ptx::tc_fence_after();
+                const uint32_t i64 = ptx::idesc_f16_f32(128, 64);
+                for (int ks = 0; ks < CH / 16; ++ks)
+                    ptx::mma_f16(tm + TM_U, ptx::sdesc_k_sw128(a_RT + ks * 32),
+                                 ptx::sdesc_k_sw128(a_st + S_VREC + VREC_T + ks * 32), i64, ks > 0);
+                ptx::mma_commit(&bar);
+            }
+            if (!mma_wait()) { failed = true; break; }
+            // ---- U^T -> fp16 operands (plain, and decayed to the chunk end in the
+            //      v tile, which is free now); capsule deltas
+            {
+                float u[16];
+                ptx::tmem_ld16(tm + lane_sel + TM_U + c16, u);
+                const float Gl = Gam[n - 1];
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) {
+                    float w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) w[e] = __expf(Gl - Gam[c16 + j + e]) * u[j + e];
+                    st_h4(sm + OFF_RT, sw(row, c16 + j, 128), u[j], u[j + 1], u[j + 2], u[j + 3]);
+                    st_h4(stage + S_V, sw(row, c16 + j, 128), w[0], w[1], w[2], w[3]);
+                }
+                if (p.caps) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int s = c16 + j, tl = t0 + s - bos;
+                        if (s < n && tl < p.cap)
+                            p.caps[((long long)b * p.cap + tl) * p.W + ubase + (long long)h * DH + row] = u[j];
+                    }
+                }
+            }
+            mma_ready();
+            // ---- MMA4 (Y = U^T (P o D)^T) and MMA5 (state)
+            if (tid == 0) {
+                ptx::tc_fence_after();
+                const uint32_t i64 = ptx::idesc_f16_f32(128, 64), i128 = ptx::idesc_f16_f32(128, 128);
+                const uint32_t a_ud = a_st + S_V, a_pd = a_st + S_VREC + VREC_PD, a_kt = a_st + S_KREC + KREC_KT;
+                for (int ks = 0; ks < CH / 16; ++ks) {
+                    ptx::mma_f16(tm + TM_Y, ptx::sdesc_k_sw128(a_RT + ks * 32), ptx::sdesc_k_sw128(a_pd + ks * 32),
+                                 i64, ks > 0);
+                    ptx::mma_f16(tm + TM_S, ptx::sdesc_k_sw128(a_ud + ks * 32), ptx::sdesc_k_sw128(a_kt + ks * 32),
+                                 i128, (state_live || ks > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(&bar);
+            }
+            if (!mma_wait()) { failed = true; break; }
+            state_live = true;
+            if (c + 1 < nc && !stage_wait(st ^ 1)) { failed = true; break; }
+            // ---- outputs o = scale (gamma O' + Y), and the next chunk's fp16 state copy
+            {
+                float o1[16], y[16];
+                ptx::tmem_ld16(tm + lane_sel + TM_O + c16, o1);
+                ptx::tmem_ld16(tm + lane_sel + TM_Y + c16, y);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int s = c16 + j;
+                    if (s < n)
+                        og[((long long)(t0 + s) * p.Hv + h) * DH + row] = from_f32<TIO>(p.scale * fmaf(gmm[s], o1[j], y[j]));
+                }
+            }
+            if (c + 1 < nc)
+                build_s16(reinterpret_cast<const float *>(sm + (st ^ 1) * STAGE_BYTES + S_VREC + VREC_GATES),
+                          min(CH, eos - t0 - CH));
+            mma_ready();
+        }
+        if (failed) break;
+        // ---- chain end: the final state
+        {
+            ptx::tc_fence_after();
+            float *dst = p.final_state + head_off + (size_t)row * DH + c32;
+            float v[32];
+            if (state_live) {
+                ptx::tmem_ld32(tm + lane_sel + TM_S + c32, v);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+        ptx::tc_fence_after();
+    }
+
+    if (failed && tid == 0) {
+        flag_error(p.status, GDN_DEVERR_TIMEOUT);
+        ptx::mbar_wait_bounded(&bar, phase ^ 1u, WAIT_LIMIT);  // let in-flight MMAs drain
+        ptx::mbar_wait_bounded(&bar, phase, WAIT_LIMIT);
+        for (int st = 0; st < 2; ++st)  // and staged copies
+            if (pending[st]) ptx::mbar_wait_bounded(&lbar[st], lph[st], WAIT_LIMIT);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tm, TMEM_COLS);
+    }
+}
+
+int num_sms() {
+    static int cached = 0;
+    if (cached == 0) {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            cached = n;
+        else
+            cached = 148;
+    }
+    return cached;
+}
+
+template <typename TIO>
+cudaError_t launch_io(const ForwardParams &p, int min_len, uint8_t *ws, cudaStream_t stream) {
+    CUtensorMap mv{};
+    if (sizeof(TIO) == 2 && !encode_rows_f16(&mv, p.v, (long long)p.Hv * DH, p.v_stride, p.T, DH, CH))
+        return cudaErrorInvalidValue;
+    int32_t *hdr = reinterpret_cast<int32_t *>(ws);
+    const long long maxch = max_chunks(p.B, p.T);
+    uint8_t *krec = ws + header_bytes(p.B);
+    uint8_t *vrec = krec + (size_t)maxch * p.Hk * KREC_BYTES;
+    wy_plan_kernel<<<1, PLAN_NT, 0, stream>>>(p.cu, p.B, p.T, min_len, hdr);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long prep_ctas = maxch * p.Hk;
+    if (prep_ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    auto prep = wy_prep_kernel<TIO>;
+    e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
+    if (e != cudaSuccess) return e;
+    if (prep_ctas > 0) prep<<<(unsigned)prep_ctas, PT, PREP_SMEM, stream>>>(p, hdr, krec, vrec);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    auto scan = wy_scan_kernel<TIO>;
+    e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, SCAN_SMEM);
+    if (e != cudaSuccess) return e;
+    const long long chains = (long long)p.B * p.Hv;
+    const int grid = (int)(chains < num_sms() ? chains : num_sms());
+    scan<<<grid, NT, SCAN_SMEM, stream>>>(p, hdr, krec, vrec, mv);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t chunked_wy_workspace_bytes(int B, int T, int Hk, int Hv) {
+    const long long maxch = max_chunks(B, T);
+    return header_bytes(B) + (size_t)maxch * ((size_t)Hk * KREC_BYTES + (size_t)Hv * VREC_BYTES);
+}
+
+cudaError_t launch_chunked_wy(const ForwardParams &p, int min_len, void *workspace, cudaStream_t stream) {
+    if (p.B == 0) return cudaSuccess;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    return p.io_f16 ? launch_io<__half>(p, min_len, ws, stream) : launch_io<float>(p, min_len, ws, stream);
+}
+
+}  // namespace gdn

@@ -1,6 +1,7 @@
 // Internal launch interface of libgdn.so (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -72,6 +73,21 @@ cudaError_t launch_replay(const ReplayParams &p, cudaStream_t stream);
 bool chunked_supported(int dk, int dv);
 size_t chunked_workspace_bytes(int B);
 cudaError_t launch_chunked(const ForwardParams &p, int min_len, void *workspace, cudaStream_t stream);
+
+// Two-phase chunked path (a parallel per-chunk kernel, then the sequential
+// state-passing kernel): faster, and needs chunked_wy_workspace_bytes of
+// workspace for the per-chunk records (about 1.6 MB per 64 tokens at
+// Hk = 16, Hv = 48, d = 128).
+size_t chunked_wy_workspace_bytes(int B, int T, int Hk, int Hv);
+// Workspace of the single-kernel chunked evaluation for these arguments (0 if
+// no chunked kernel can run); argument errors as gdn_forward_workspace_size.
+gdn_status single_kernel_workspace_size(const gdn_forward_args *args, size_t *bytes);
+cudaError_t launch_chunked_wy(const ForwardParams &p, int min_len, void *workspace, cudaStream_t stream);
+
+// Tensor map over a packed fp16 [T, row_elems] array with `stride` elements
+// between tokens, boxes of box_y tokens x box_x elements, zero fill past T.
+bool encode_rows_f16(CUtensorMap *map, const void *base, long long row_elems, long long stride, int T, int box_x,
+                     int box_y);
 
 // Sequences up to this many tokens stay on the recurrent kernel under the
 // automatic plan; longer ones go to the chunked kernel.

@@ -8,7 +8,9 @@
 // kernel's workspace; others run on latency-critical paths where a
 // cudaMalloc, which may synchronise the device, is not acceptable.  This entry
 // point takes the workspace from a fixed array compiled into the library
-// instead of from the caller.
+// instead of from the caller.  That array holds the chain list of the
+// single-kernel chunked evaluation (the two-phase one needs per-chunk records
+// that grow with the batch), so long sequences run on that kernel here.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds it (16 KiB) until the process exits.  In host code its name is
@@ -53,7 +55,7 @@ gdn_status scratch_address(void **out) {
 extern "C" gdn_status gdn_forward_no_alloc(const gdn_forward_args *args, gdn_stream_t stream) {
     if (!args) return GDN_ERR_NULL;
     size_t need = 0;
-    gdn_status st = gdn_forward_workspace_size(args, &need);
+    gdn_status st = gdn::single_kernel_workspace_size(args, &need);
     if (st != GDN_OK) return st;
     if (need > sizeof(g_no_alloc_scratch)) return GDN_ERR_WORKSPACE;  // more than GDN_NO_ALLOC_MAX_SEQS sequences
     gdn_forward_args a = *args;

@@ -154,11 +154,20 @@ typedef struct gdn_forward_args {
 
 /*
  * Bytes of device workspace gdn_forward needs for these arguments (sizes,
- * plan and max_seqlen only are read).  Non-zero exactly when the chunked
- * kernel may run; it then holds the chunked kernel's longest-first list of
- * sequences and its work counter ((B + 2) int32, rounded up to 256 bytes).
- * The workspace must be 16-byte aligned and not shared by calls that overlap
- * on the GPU.  Returns GDN_OK and writes *bytes, or an argument error.
+ * plan and max_seqlen only are read).  Non-zero exactly when a chunked
+ * (tensor-core) kernel may run.  The size is that of the two-phase chunked
+ * evaluation: a header (work counter, the longest-first list of sequences,
+ * each sequence's first chunk) plus one record per (64-token chunk, key head)
+ * of 48 KiB and one per (chunk, value head) of 17,152 bytes, for at most
+ * T/64 + B chunks -- about 1.6 MB per 64 tokens at Hk = 16, Hv = 48.
+ *
+ * gdn_forward also accepts a smaller workspace of at least (B + 2) int32
+ * (rounded up to 256 bytes): it then runs the single-kernel chunked
+ * evaluation, which keeps only the sequence list and work counter there.
+ * Both give the same results up to floating-point rounding; the two-phase one
+ * is faster.  The workspace must be 16-byte aligned and not shared by calls
+ * that overlap on the GPU.  Returns GDN_OK and writes *bytes, or an argument
+ * error.
  */
 gdn_status gdn_forward_workspace_size(const gdn_forward_args *args, size_t *bytes);
 
@@ -207,9 +216,10 @@ gdn_status gdn_replay_prefix(float *state_banks, int32_t num_slots, int32_t num_
  * operator only its declared inputs and outputs (an inference runtime's
  * custom-operator interface, a serving loop with a fixed memory plan), and
  * some paths cannot afford a cudaMalloc, which may synchronise the device.
- * This call behaves exactly like gdn_forward but ignores args->workspace: the
- * chunked kernel's workspace comes from a fixed 16 KiB array compiled into
- * the library, which every GPU that loads the library keeps until exit.
+ * This call behaves like gdn_forward but ignores args->workspace: long
+ * sequences run on the single-kernel chunked evaluation, whose workspace (the
+ * sequence list and work counter) comes from a fixed 16 KiB array compiled
+ * into the library, which every GPU that loads the library keeps until exit.
  *
  *  - Batches of more than GDN_NO_ALLOC_MAX_SEQS sequences that need a
  *    workspace are rejected with GDN_ERR_WORKSPACE before anything runs.

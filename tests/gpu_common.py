@@ -19,9 +19,18 @@ def to_dev(x, dtype=None):
     return t.to(dev())
 
 
+def single_kernel_workspace(inp):
+    """A workspace that holds only the chain list ((B + 2) int32): gdn_forward
+    then runs the single-kernel chunked evaluation instead of the two-phase one."""
+    n = ((inp.B + 2) * 4 + 255) // 256 * 256
+    return torch.zeros(n, dtype=torch.uint8, device=dev())
+
+
 def run_gpu(inp, *, plan="auto", capacity=None, gate_mode="raw", a=None, b=None, in_place=True,
-            status=None, final_state=None, max_seqlen=0):
-    """Runs gdn_forward on ``inp`` (a workloads.GdnInputs); returns numpy arrays."""
+            status=None, final_state=None, max_seqlen=0, workspace=None):
+    """Runs gdn_forward on ``inp`` (a workloads.GdnInputs); returns numpy arrays.
+    ``workspace=None`` lets the binding allocate what gdn_forward_workspace_size
+    asks for (the two-phase chunked evaluation)."""
     import gated_delta_rule_gateddeltanet_gb300 as gdn
     cap = inp.capacity if capacity is None else capacity
     Hk, Hv, dk, dv = inp.dims
@@ -39,7 +48,7 @@ def run_gpu(inp, *, plan="auto", capacity=None, gate_mode="raw", a=None, b=None,
         to_dev(inp.b if b is None else b), to_dev(inp.cu_seqlens), A_log=to_dev(inp.A_log),
         dt_bias=to_dev(inp.dt_bias), gate_mode=gate_mode, initial_state=init, final_state=final_state,
         state_slots=to_dev(inp.state_slots), capacity=cap, plan=plan, status=status,
-        num_state_slots=final_state.shape[0], max_seqlen=max_seqlen)
+        num_state_slots=final_state.shape[0], max_seqlen=max_seqlen, workspace=workspace)
     torch.cuda.synchronize()
     return (out.double().cpu().numpy(), final.double().cpu().numpy(),
             None if caps is None else caps.double().cpu().numpy())

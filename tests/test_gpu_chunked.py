@@ -1,5 +1,10 @@
 """GPU parity of the tcgen05 chunked-prefill path against the FP64 oracle.
 
+Both chunked evaluations are covered: the two-phase one (a parallel per-chunk
+kernel, then the state-passing kernel), which gdn_forward runs with the
+workspace gdn_forward_workspace_size asks for, and the single-kernel one,
+which it runs when the workspace only holds the chain list.
+
 Tolerance: 2e-3 max-relative (max |gpu - oracle| / max |oracle| per tensor) on
 outputs, final states and capsule deltas -- the tensor cores take fp16
 operands (normalised q and k, the fp16 copy of the state, the delta terms and
@@ -15,7 +20,7 @@ import torch
 
 import oracle
 from helpers import max_rel
-from gpu_common import run_gpu, run_oracle, to_dev, dev, capsule_parts
+from gpu_common import run_gpu, run_oracle, to_dev, dev, capsule_parts, single_kernel_workspace
 
 from gated_delta_rule_gateddeltanet_gb300 import workloads as wl
 
@@ -45,17 +50,33 @@ def _check(inp, gpu, ref, cap=None):
 
 
 LENGTHS = [0, 1, 63, 64, 65, 130, 200, 7]
+PATHS = ["two_phase", "single_kernel"]
 
 
+def _ws(path, inp):
+    return single_kernel_workspace(inp) if path == "single_kernel" else None
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("io", [np.float16, np.float32])
-def test_forced_chunked_ragged_with_state_and_capsules(io):
+def test_forced_chunked_ragged_with_state_and_capsules(io, path):
     inp = wl.make_inputs(201, LENGTHS, Hk=2, Hv=6, dk=128, dv=128, io_dtype=io, state_std=0.02, capacity=70)
-    _check(inp, run_gpu(inp, plan="chunked", in_place=False), run_oracle(inp))
+    _check(inp, run_gpu(inp, plan="chunked", in_place=False, workspace=_ws(path, inp)), run_oracle(inp))
 
 
-def test_forced_chunked_zero_initial_state():
+@pytest.mark.parametrize("path", PATHS)
+def test_forced_chunked_zero_initial_state(path):
     inp = wl.make_inputs(202, [129, 3, 64], Hk=1, Hv=3, dk=128, dv=128, io_dtype=np.float16)
-    _check(inp, run_gpu(inp, plan="chunked", in_place=False), run_oracle(inp))
+    _check(inp, run_gpu(inp, plan="chunked", in_place=False, workspace=_ws(path, inp)), run_oracle(inp))
+
+
+def test_two_phase_gqa_ratios_and_many_chunks():
+    """Key heads shared by 1, 2 and 4 value heads; a 20-chunk sequence next to
+    sequences that end one token into a chunk and one token short of it."""
+    for Hk, Hv, seed in ((3, 3, 211), (2, 4, 212), (1, 4, 213)):
+        inp = wl.make_inputs(seed, [1280, 129, 127, 40], Hk=Hk, Hv=Hv, dk=128, dv=128, io_dtype=np.float16,
+                             state_std=0.02, capacity=130)
+        _check(inp, run_gpu(inp, in_place=True), run_oracle(inp))
 
 
 def test_auto_plan_mixes_both_kernels():
@@ -65,7 +86,8 @@ def test_auto_plan_mixes_both_kernels():
     _check(inp, run_gpu(inp, in_place=True), run_oracle(inp))
 
 
-def test_chunked_precomputed_gate_extremes():
+@pytest.mark.parametrize("path", PATHS)
+def test_chunked_precomputed_gate_extremes(path):
     """Decays of exactly 0 and 1 and beta of 0 and 1 inside chunks."""
     inp = wl.make_inputs(204, [150, 70], Hk=1, Hv=2, dk=128, dv=128, io_dtype=np.float32, state_std=0.02)
     rng = np.random.default_rng(5)
@@ -76,38 +98,41 @@ def test_chunked_precomputed_gate_extremes():
     g[60, 1] = 0.0
     beta[20:30, :] = 0.0
     beta[31, :] = 1.0
-    _check(inp, run_gpu(inp, plan="chunked", gate_mode="precomputed", a=g, b=beta, in_place=False),
+    _check(inp, run_gpu(inp, plan="chunked", gate_mode="precomputed", a=g, b=beta, in_place=False,
+                        workspace=_ws(path, inp)),
            run_oracle(inp, gate_mode="precomputed", a=g, b=beta))
 
 
-def test_chunked_pack_equals_one_by_one_bitwise():
+@pytest.mark.parametrize("path", PATHS)
+def test_chunked_pack_equals_one_by_one_bitwise(path):
     lengths = [40, 100, 70, 33]
     inp = wl.make_inputs(205, lengths, Hk=2, Hv=6, dk=128, dv=128, io_dtype=np.float16, state_std=0.02,
                          capacity=8)
-    out, final, caps = run_gpu(inp, in_place=False)
+    out, final, caps = run_gpu(inp, in_place=False, workspace=_ws(path, inp))
     cu = inp.cu_seqlens
     for s, L in enumerate(lengths):
         t0, t1 = cu[s], cu[s + 1]
         one = wl.GdnInputs(inp.q[t0:t1], inp.k[t0:t1], inp.v[t0:t1], inp.a[t0:t1], inp.b[t0:t1], inp.A_log,
                            inp.dt_bias, np.array([0, L], np.int32), inp.initial_state[s:s + 1], None, 8)
-        o1, f1, c1 = run_gpu(one, in_place=False)
+        o1, f1, c1 = run_gpu(one, in_place=False, workspace=_ws(path, one))
         assert np.array_equal(out[t0:t1], o1)
         assert np.array_equal(final[s], f1[0])
         assert np.array_equal(caps[s], c1[0])
 
 
-def test_chunked_slots_and_status():
+@pytest.mark.parametrize("path", PATHS)
+def test_chunked_slots_and_status(path):
     import gated_delta_rule_gateddeltanet_gb300 as gdn
     inp = wl.make_inputs(206, [80, 90, 40], Hk=1, Hv=2, dk=128, dv=128, io_dtype=np.float16, state_std=0.02,
                          num_slots=6, state_slots=[4, 1, 2])
-    out, final, _ = run_gpu(inp, plan="chunked", in_place=False)
+    out, final, _ = run_gpu(inp, plan="chunked", in_place=False, workspace=_ws(path, inp))
     _check(inp, (out, final, None), run_oracle(inp))
     for untouched in (0, 3, 5):
         assert np.array_equal(final[untouched], inp.initial_state[untouched].astype(np.float64))
     status = torch.zeros(1, dtype=torch.int32, device=dev())
     bad = wl.GdnInputs(inp.q, inp.k, inp.v, inp.a, inp.b, inp.A_log, inp.dt_bias, inp.cu_seqlens,
                        inp.initial_state, np.array([4, 9, 2], np.int32))
-    _, final2, _ = run_gpu(bad, plan="chunked", in_place=False, status=status)
+    _, final2, _ = run_gpu(bad, plan="chunked", in_place=False, status=status, workspace=_ws(path, bad))
     assert status.item() & gdn.DEVERR["state_slot"]
     assert np.array_equal(final2[4], final[4]) and np.array_equal(final2[2], final[2])
 
