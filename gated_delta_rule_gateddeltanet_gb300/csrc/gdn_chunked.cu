@@ -724,9 +724,9 @@ template <typename TIO>
 cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStream_t stream) {
     CUtensorMap mq{}, mk{}, mv{};
     if (sizeof(TIO) == 2) {
-        if (!encode_rows_f16(&mq, p.q, (long long)p.Hk * DH, p.q_stride, p.T, DH, CH) ||
-            !encode_rows_f16(&mk, p.k, (long long)p.Hk * DH, p.k_stride, p.T, DH, CH) ||
-            !encode_rows_f16(&mv, p.v, (long long)p.Hv * DH, p.v_stride, p.T, DH, CH))
+        if (!encode_rows_f16(&mq, p.q, (long long)p.Hk * DH, p.q_stride, p.T, DH, CH, false) ||
+            !encode_rows_f16(&mk, p.k, (long long)p.Hk * DH, p.k_stride, p.T, DH, CH, false) ||
+            !encode_rows_f16(&mv, p.v, (long long)p.Hv * DH, p.v_stride, p.T, DH, CH, false))
             return cudaErrorInvalidValue;
     }
     plan_kernel<<<1, 1024, 0, stream>>>(p.cu, p.B, p.T, min_len, ws);
@@ -760,7 +760,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 bool encode_rows_f16(CUtensorMap *map, const void *base, long long row_elems, long long stride, int T, int box_x,
-                     int box_y) {
+                     int box_y, bool swizzle128) {
     auto encode = tensor_map_encoder();
     if (!encode) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)(T > 0 ? T : 1)};
@@ -768,7 +768,8 @@ bool encode_rows_f16(CUtensorMap *map, const void *base, long long row_elems, lo
     const cuuint32_t box[2] = {(cuuint32_t)box_x, (cuuint32_t)box_y};
     const cuuint32_t estride[2] = {1, 1};
     return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estride,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

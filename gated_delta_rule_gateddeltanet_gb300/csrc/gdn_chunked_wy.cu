@@ -29,7 +29,7 @@
 //    A, P o D and the FP32 triangular inverse T.  It writes byte images of the
 //    operand tiles, already in the swizzled shared-memory layout the MMAs
 //    read, to the caller's workspace (one 48 KiB record per (chunk, key head),
-//    one 16.75 KiB record per (chunk, value head)), plus the capsule's k and g.
+//    one 17 KiB record per (chunk, value head)), plus the capsule's k and g.
 //
 //  wy_scan_kernel (persistent, one CTA per SM, chains longest-first): keeps the
 //    FP32 state in tensor memory and, per chunk, loads the two records with
@@ -70,8 +70,9 @@ constexpr int KREC_BYTES = 49152;  // [Q;K] tile (2 K-blocks x 128 rows x 128 B)
 constexpr int KREC_KT = 32768;
 constexpr int VREC_T = 0;          // T, [64][64] fp16
 constexpr int VREC_PD = 8192;      // P o D, [64][64] fp16
-constexpr int VREC_GATES = 16384;  // Gamma[64], beta[64], gamma[64] fp32
-constexpr int VREC_BYTES = 16384 + 3 * CH * 4;
+constexpr int VREC_F = 16384;      // per-token factors (fp32, 64 each): beta, beta*gamma, gamma, exp(Gamma_last - Gamma)
+constexpr int F_BETA = 0, F_BG = CH, F_GAMMA = 2 * CH, F_DECAY = 3 * CH;
+constexpr int VREC_BYTES = VREC_F + 4 * CH * 4;
 static_assert(VREC_BYTES % 128 == 0, "records stay 128-byte aligned");
 
 size_t header_bytes(int B) { return ((size_t)(3 + 2 * (size_t)B) * 4 + 1023) & ~size_t(1023); }
@@ -218,13 +219,16 @@ __device__ void tri_inverse_inplace(float *AT, float *M, int tid) {
 }
 
 // Gates of the 64 tokens [t0, t0 + 64) of value head h (one warp, two tokens
-// per lane): effective decay g, beta, and the within-chunk cumulative log
-// decay Gamma (log decays floored at LOG_DECAY_FLOOR).  Tokens at or past
-// `n` get g = 1, beta = 0 (no effect).  Writes Gamma, beta and exp(Gamma) to
-// G[0..64), G[64..128), G[128..192) and returns each lane's two decays.
-__device__ __forceinline__ void chunk_gates(const ForwardParams &p, int t0, int n, int h, float *G, float (&gt)[2],
-                                            int lane) {
-    float lg[2], bt[2];
+// per lane).  Raw mode: g = exp(-exp(A_log) softplus(a + dt_bias)),
+// beta = sigmoid(b); precomputed mode: g = a, beta = b.  Log decays are
+// floored at LOG_DECAY_FLOOR; tokens at or past `n` get g = 1, beta = 0 (no
+// effect).  Writes the within-chunk cumulative log decay Gamma and beta to
+// shared memory, the scan kernel's per-token factors (beta, beta gamma,
+// gamma = exp(Gamma), exp(Gamma_last - Gamma)) to the record at `fdst`, and
+// the capsule decays.
+__device__ __forceinline__ void chunk_gates(const ForwardParams &p, int t0, int n, int h, int b, int bos,
+                                            float *Gam, float *Beta, float *fdst, int lane) {
+    float lg[2], bt[2], gt[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const int s = lane + 32 * u;
@@ -246,46 +250,74 @@ __device__ __forceinline__ void chunk_gates(const ForwardParams &p, int t0, int 
             }
         }
     }
-    float c0 = lg[0], c1 = lg[1];
+    float c[2] = {lg[0], lg[1]};
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const float y0 = __shfl_up_sync(0xffffffffu, c0, o);
-        const float y1 = __shfl_up_sync(0xffffffffu, c1, o);
+        const float y0 = __shfl_up_sync(0xffffffffu, c[0], o);
+        const float y1 = __shfl_up_sync(0xffffffffu, c[1], o);
         if (lane >= o) {
-            c0 += y0;
-            c1 += y1;
+            c[0] += y0;
+            c[1] += y1;
         }
     }
-    c1 += __shfl_sync(0xffffffffu, c0, 31);
-    G[lane] = c0;
-    G[lane + 32] = c1;
-    G[CH + lane] = bt[0];
-    G[CH + lane + 32] = bt[1];
-    G[2 * CH + lane] = expf(c0);
-    G[2 * CH + lane + 32] = expf(c1);
+    c[1] += __shfl_sync(0xffffffffu, c[0], 31);
+    const float l0 = __shfl_sync(0xffffffffu, c[0], (n - 1) & 31);
+    const float l1 = __shfl_sync(0xffffffffu, c[1], (n - 1) & 31);
+    const float Gl = n - 1 < 32 ? l0 : l1;  // Gamma of the chunk's last token
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int s = lane + 32 * u;
+        const float gm = expf(c[u]);
+        Gam[s] = c[u];
+        Beta[s] = bt[u];
+        fdst[F_BETA + s] = bt[u];
+        fdst[F_BG + s] = bt[u] * gm;
+        fdst[F_GAMMA + s] = gm;
+        fdst[F_DECAY + s] = expf(Gl - c[u]);
+        const int tl = t0 + s - bos;
+        if (p.caps && s < n && tl < p.cap) p.caps[((long long)b * p.cap + tl) * p.W + h] = gt[u];
+    }
+}
+
+// Eight consecutive elements (k % 8 == 0) of one row of a swizzled fp16 tile: one 16-byte store.
+__device__ __forceinline__ void st_h8(uint8_t *base, uint32_t off, const float *x) {
+    uint4 v;
+    __half2 h0 = __floats2half2_rn(x[0], x[1]), h1 = __floats2half2_rn(x[2], x[3]);
+    __half2 h2 = __floats2half2_rn(x[4], x[5]), h3 = __floats2half2_rn(x[6], x[7]);
+    v.x = *reinterpret_cast<uint32_t *>(&h0);
+    v.y = *reinterpret_cast<uint32_t *>(&h1);
+    v.z = *reinterpret_cast<uint32_t *>(&h2);
+    v.w = *reinterpret_cast<uint32_t *>(&h3);
+    *reinterpret_cast<uint4 *>(base + off) = v;
 }
 
 // ---------------------------------------------------------------- phase 1: per (chunk, key head)
 
 constexpr int PT = 256;  // threads of the prep kernel
+constexpr int GH = 8;    // value heads whose gates are computed together (one warp each)
 // Shared memory of the prep kernel (offsets from a 1024-byte aligned base).
 // The first 48 KiB hold the key-head record image ([Q;K] tile, then K^T
-// tile); once its bulk store has read it, the same bytes hold A / T (fp32),
-// the block-product scratch and the value-head record image.
+// tile); with fp16 I/O the raw q and k rows land there by 2-D TMA copies in
+// the swizzled layout and are normalised in place.  Once the record's bulk
+// store has read it, the same bytes hold A / T (fp32), the block-product
+// scratch and the T and P o D tiles of one value head.
 constexpr int P_AT = 0;                    // [64][AS] fp32
 constexpr int P_M = 64 * AS * 4;           // [32][MS] fp32
-constexpr int P_VREC = 21504;              // value-head record image (1024-byte aligned)
+constexpr int P_TPD = 21504;               // T and P o D tiles (1024-byte aligned), 16 KiB
 constexpr int PREP_SMEM = KREC_BYTES + 1024;
-static_assert(P_M + 32 * MS * 4 <= P_VREC && P_VREC + VREC_BYTES <= KREC_BYTES, "prep shared-memory layout");
+static_assert(P_M + 32 * MS * 4 <= P_TPD && P_TPD + VREC_F <= KREC_BYTES, "prep shared-memory layout");
 
 template <typename TIO>
 __global__ void __launch_bounds__(PT, 4)
-    wy_prep_kernel(const ForwardParams p, const int32_t *ws, uint8_t *krec, uint8_t *vrec) {
+    wy_prep_kernel(const ForwardParams p, const int32_t *ws, uint8_t *krec, uint8_t *vrec,
+                   const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t bar;
+    __shared__ __align__(8) uint64_t bar, lbar;
     __shared__ uint32_t tmem_base;
+    __shared__ float Gam_s[GH][CH], Beta_s[GH][CH];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr bool STAGED = sizeof(TIO) == 2;
 
     const int g = blockIdx.x / p.Hk, kh = blockIdx.x % p.Hk;
     const int32_t *cbase = ws + 2 + p.B;
@@ -301,26 +333,51 @@ __global__ void __launch_bounds__(PT, 4)
     const int t0 = bos + CH * (g - cbase[b]);
     const int n = min(CH, eos - t0);
 
+    // fp16: the chunk's q rows (tile rows 0-63) and k rows (64-127), both
+    // 64-element halves of each, by swizzled 2-D TMA copies; rows past the
+    // sequence arrive too and are zeroed when normalising
+    if (tid == 0) {
+        ptx::mbar_init(&bar, 1);
+        ptx::mbar_init(&lbar, 1);
+        ptx::fence_mbar_init();
+        if (STAGED) {
+            ptx::mbar_arrive_expect_tx(&lbar, 2 * CH * DH * 2);
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                ptx::tma_load_2d(sm + kb * 16384, &map_q, kh * DH + kb * 64, t0, &lbar);
+                ptx::tma_load_2d(sm + kb * 16384 + CH * 128, &map_k, kh * DH + kb * 64, t0, &lbar);
+            }
+        }
+    }
+    __syncwarp();
     if (warp == 0) {
         ptx::tmem_alloc(&tmem_base, 64);
         ptx::tmem_relinquish();
     }
-    if (tid == 0) {
-        ptx::mbar_init(&bar, 1);
-        ptx::fence_mbar_init();
-    }
+    // gates of the first GH value heads while the rows are in flight
+    auto gates_group = [&](int i0) {
+        const int wi = warp, i = i0 + wi;
+        if (wi < GH && i < p.r) {
+            const int h = kh * p.r + i;
+            chunk_gates(p, t0, n, h, b, bos, Gam_s[wi], Beta_s[wi],
+                        reinterpret_cast<float *>(vrec + ((size_t)g * p.Hv + h) * VREC_BYTES + VREC_F), lane);
+        }
+    };
+    gates_group(0);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tm = tmem_base;
+    bool ok = true;
+    if (STAGED) ok = ptx::mbar_wait_bounded(&lbar, 0, WAIT_LIMIT);
+    ok = __syncthreads_and(ok);
 
-    // ---- normalised q (rows 0-63) and k (rows 64-127) of the [Q;K] tile; rows
-    //      past the sequence are zero.  Warp w handles tokens w, w + 8, ...; four
-    //      tokens at a time so their loads and reductions overlap.
+    // ---- L2-normalised q and k rows of the [Q;K] tile (zero past the
+    //      sequence); warp w handles tokens w, w + 8, ...
     const TIO *qg = static_cast<const TIO *>(p.q);
     const TIO *kg = static_cast<const TIO *>(p.k);
 #pragma unroll 1
-    for (int round = 0; round < 2; ++round) {
+    for (int round = 0; ok && round < 2; ++round) {
         float qv[4][4], kv[4][4], sq[4], sk[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -328,9 +385,14 @@ __global__ void __launch_bounds__(PT, 4)
 #pragma unroll
             for (int e = 0; e < 4; ++e) qv[u][e] = kv[u][e] = 0.f;
             if (s < n) {
-                const long long t = (long long)t0 + s;
-                ld4<TIO>(qg + t * p.q_stride + (long long)kh * DH + lane * 4, qv[u]);
-                ld4<TIO>(kg + t * p.k_stride + (long long)kh * DH + lane * 4, kv[u]);
+                if (STAGED) {
+                    ld4<__half>(reinterpret_cast<const __half *>(sm + sw(s, lane * 4, 128)), qv[u]);
+                    ld4<__half>(reinterpret_cast<const __half *>(sm + sw(64 + s, lane * 4, 128)), kv[u]);
+                } else {
+                    const long long t = (long long)t0 + s;
+                    ld4<TIO>(qg + t * p.q_stride + (long long)kh * DH + lane * 4, qv[u]);
+                    ld4<TIO>(kg + t * p.k_stride + (long long)kh * DH + lane * 4, kv[u]);
+                }
             }
         }
 #pragma unroll
@@ -373,7 +435,7 @@ __global__ void __launch_bounds__(PT, 4)
     __syncthreads();
     // ---- K^T tile (row j = feature, 64 token columns) from the K rows: thread
     //      (j, half) gathers 32 tokens as four 8-element pieces
-    {
+    if (ok) {
         const int j = tid >> 1, sg = (tid & 1) * 32;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -393,7 +455,7 @@ __global__ void __launch_bounds__(PT, 4)
     __syncthreads();
     // ---- [Q;K] K^T on the tensor cores (P in lanes 0-63, G in lanes 64-127),
     //      and the key-head record to the workspace
-    if (tid == 0) {
+    if (ok && tid == 0) {
         ptx::tc_fence_after();
         const uint32_t a_qk = ptx::smem_u32(sm);
         const uint32_t i64 = ptx::idesc_f16_f32(128, 64);
@@ -405,56 +467,49 @@ __global__ void __launch_bounds__(PT, 4)
         ptx::bulk_s2g(krec + ((size_t)g * p.Hk + kh) * KREC_BYTES, sm, KREC_BYTES);
         ptx::bulk_commit();
     }
-    bool ok = ptx::mbar_wait_bounded(&bar, 0, WAIT_LIMIT);
+    const bool mma_issued = ok;
+    if (ok) ok = ptx::mbar_wait_bounded(&bar, 0, WAIT_LIMIT);
     ptx::tc_fence_after();
     if (tid == 0) ptx::bulk_wait_read_all();  // the tile bytes may be reused from here on
     ok = __syncthreads_and(ok);
 
-    // ---- per value head of this key head: gates, A and P o D, T, record
+    // ---- per value head of this key head: A and P o D, T, record
     float *AT = reinterpret_cast<float *>(sm + P_AT);
     float *Mw = reinterpret_cast<float *>(sm + P_M);
-    uint8_t *vimg = sm + P_VREC;
-    float *G = reinterpret_cast<float *>(vimg + VREC_GATES);  // Gamma | beta | gamma
+    uint8_t *tpd = sm + P_TPD;
     const int quarter = warp & 3, c32 = (warp >> 2) * 32;
     const int row = quarter * 32 + lane;  // tensor-memory lane of this thread
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
 #pragma unroll 1
     for (int i = 0; ok && i < p.r; ++i) {
-        const int h = kh * p.r + i;
-        if (warp == 0) {
-            float gt[2];
-            chunk_gates(p, t0, n, h, G, gt, lane);
-            if (p.caps) {
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int s = lane + 32 * u, tl = t0 + s - bos;
-                    if (s < n && tl < p.cap) p.caps[((long long)b * p.cap + tl) * p.W + h] = gt[u];
-                }
-            }
+        const int h = kh * p.r + i, wi = i % GH;
+        if (i > 0 && wi == 0) {  // the next group of heads' gates
+            gates_group(i);
+            __syncthreads();
         }
-        __syncthreads();
         {
             float v[32];
             ptx::tmem_ld32(tm + lane_sel + c32, v);
             const int r = row & 63;
-            const float Gr = G[r];
+            const float *Gm = Gam_s[wi];
+            const float Gr = Gm[r];
             if (quarter >= 2) {  // lanes 64-127: G = K K^T -> A (strictly lower)
-                const float br = G[CH + r];
+                const float br = Beta_s[wi][r];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int s = c32 + j;
-                    AT[r * AS + s] = (s < r) ? br * __expf(Gr - G[s]) * v[j] : 0.f;
+                    AT[r * AS + s] = (s < r) ? br * __expf(Gr - Gm[s]) * v[j] : 0.f;
                 }
             } else {  // lanes 0-63: P = Q K^T -> P o D (lower, diagonal included)
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    float w[4];
+                for (int j = 0; j < 32; j += 8) {
+                    float w[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
+                    for (int e = 0; e < 8; ++e) {
                         const int s = c32 + j + e;
-                        w[e] = (s <= r) ? v[j + e] * __expf(Gr - G[s]) : 0.f;
+                        w[e] = (s <= r) ? v[j + e] * __expf(Gr - Gm[s]) : 0.f;
                     }
-                    st_h4(vimg + VREC_PD, sw(r, c32 + j, 64), w[0], w[1], w[2], w[3]);
+                    st_h8(tpd + VREC_PD, sw(r, c32 + j, 64), w);
                 }
             }
         }
@@ -463,14 +518,17 @@ __global__ void __launch_bounds__(PT, 4)
         {  // T -> fp16 tile: thread (r, 16-column group)
             const int r = tid >> 2, s0 = (tid & 3) * 16;
 #pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                st_h4(vimg + VREC_T, sw(r, s0 + j, 64), AT[r * AS + s0 + j], AT[r * AS + s0 + j + 1],
-                      AT[r * AS + s0 + j + 2], AT[r * AS + s0 + j + 3]);
+            for (int j = 0; j < 16; j += 8) {
+                float w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[e] = AT[r * AS + s0 + j + e];
+                st_h8(tpd + VREC_T, sw(r, s0 + j, 64), w);
+            }
         }
         ptx::fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
-            ptx::bulk_s2g(vrec + ((size_t)g * p.Hv + h) * VREC_BYTES, vimg, VREC_BYTES);
+            ptx::bulk_s2g(vrec + ((size_t)g * p.Hv + h) * VREC_BYTES, tpd, VREC_F);
             ptx::bulk_commit();
             ptx::bulk_wait_read_all();
         }
@@ -478,7 +536,8 @@ __global__ void __launch_bounds__(PT, 4)
     }
     if (!ok && tid == 0) {
         flag_error(p.status, GDN_DEVERR_TIMEOUT);
-        ptx::mbar_wait_bounded(&bar, 0, WAIT_LIMIT);  // let the MMA drain before tensor memory is freed
+        if (mma_issued) ptx::mbar_wait_bounded(&bar, 0, WAIT_LIMIT);  // let the MMA drain before tensor memory is freed
+        if (STAGED) ptx::mbar_wait_bounded(&lbar, 0, WAIT_LIMIT);      // and the row copies
     }
     if (tid == 0) ptx::bulk_wait_all();
     ptx::tc_fence_before();
@@ -493,23 +552,23 @@ __global__ void __launch_bounds__(PT, 4)
 
 constexpr int NT = 512;  // 16 warps: four per tensor-memory lane quarter
 constexpr int TMEM_COLS = 512;
-// Tensor-memory columns (128 lanes each).
-constexpr uint32_t TM_S = 0;    // FP32 state S (dv lanes x dk columns)
-constexpr uint32_t TM_O = 128;  // O' = S0 Q^T (64 columns), then X = S0 K^T at TM_X
-constexpr uint32_t TM_X = 192;
-constexpr uint32_t TM_U = 256;  // U^T
-constexpr uint32_t TM_Y = 320;  // U^T (P o D)^T
+// Tensor-memory columns (128 lanes each).  MMA2's result is double-buffered
+// so that chunk c - 1's outputs are read while chunk c's MMA2 runs.
+constexpr uint32_t TM_S = 0;     // FP32 state S (dv lanes x dk columns)
+constexpr uint32_t TM_OX = 128;  // two buffers of 128 columns: O' = S0 Q^T (64), then X = S0 K^T (64)
+constexpr uint32_t TM_U = 384;   // U^T
+constexpr uint32_t TM_Y = 448;   // U^T (P o D)^T
 
 // Shared memory (offsets from a 1024-byte aligned base): two stages holding
 // one chunk's inputs each, then the fp16 state copy and the R^T / U^T tile.
 constexpr int S_KREC = 0;                   // key-head record: [Q;K] tile, K^T tile at S_KREC + KREC_KT
-constexpr int S_VREC = KREC_BYTES;          // value-head record: T, P o D, gates
-constexpr int S_V = 66560;                  // fp16 v rows of the chunk [64][128]; then U^T diag(...) tile
-constexpr int STAGE_BYTES = S_V + 16384;    // 81 KiB
+constexpr int S_VREC = KREC_BYTES;          // value-head record: T, P o D, per-token factors
+constexpr int S_V = S_VREC + VREC_BYTES;    // fp16 v rows of the chunk [64][128]; then U^T diag(decay) tile
+constexpr int STAGE_BYTES = S_V + 16384;
 constexpr int OFF_S16 = 2 * STAGE_BYTES;    // [128][128] fp16 S0 (two K-blocks)
 constexpr int OFF_RT = OFF_S16 + 32768;     // [128][64] fp16 R^T, then U^T
 constexpr int SCAN_SMEM = OFF_RT + 16384 + 1024;  // + slack for the 1024-byte alignment
-static_assert(S_VREC + VREC_BYTES <= S_V && S_V % 1024 == 0, "stage layout");
+static_assert(S_V % 1024 == 0 && STAGE_BYTES % 1024 == 0, "stage layout");
 static_assert(SCAN_SMEM + 1024 <= 227 * 1024, "shared memory budget (dynamic + static)");
 
 template <typename TIO>
@@ -522,6 +581,7 @@ __global__ void __launch_bounds__(NT, 1)
     __shared__ __align__(8) uint64_t lbar[2];  // stage loads
     __shared__ uint32_t tmem_base;
     __shared__ int item_s;
+    __shared__ float gam_prev[CH];             // gamma of the chunk whose outputs are pending
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Tensor memory: a warp reaches only the 32 lanes of its quarter (warp % 4);
     // the four warps of a quarter split the columns.
@@ -591,9 +651,9 @@ __global__ void __launch_bounds__(NT, 1)
         }
         const size_t head_off = ((size_t)slot * p.Hv + h) * (size_t)DH * DH;
 
-        // chunk c's records (and fp16 v rows) into stage st
+        // chunk c's records (and fp16 v rows) into stage st (issued by warp 1)
         auto stage_load = [&](int c, int st) {
-            if (tid == 0) {
+            if (tid == 32) {
                 uint8_t *stage = sm + st * STAGE_BYTES;
                 ptx::mbar_arrive_expect_tx(&lbar[st], (uint32_t)(KREC_BYTES + VREC_BYTES + (STAGED ? CH * DH * 2 : 0)));
                 ptx::bulk_g2s(stage + S_KREC, krec + ((gbase + c) * p.Hk + kh) * KREC_BYTES, KREC_BYTES, &lbar[st]);
@@ -604,8 +664,8 @@ __global__ void __launch_bounds__(NT, 1)
         };
         // S0 -> fp16 operand tile; the tensor-memory state becomes gamma_last S0
         bool state_live = p.init != nullptr;
-        auto build_s16 = [&](const float *G, int n) {
-            const float gl = G[2 * CH + n - 1];
+        auto build_s16 = [&](const float *F, int n) {
+            const float gl = F[F_GAMMA + n - 1];
             float v[32];
             if (state_live) {
                 ptx::tmem_ld32(tm + lane_sel + TM_S + c32, v);
@@ -614,13 +674,25 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int j = 0; j < 32; ++j) v[j] = 0.f;
             }
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                st_h4(sm + OFF_S16, sw(row, c32 + j, 128), v[j], v[j + 1], v[j + 2], v[j + 3]);
+            for (int j = 0; j < 32; j += 8) st_h8(sm + OFF_S16, sw(row, c32 + j, 128), v + j);
             if (state_live) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] *= gl;
                 ptx::tmem_st32(tm + lane_sel + TM_S + c32, v);
                 ptx::tmem_st_wait();
+            }
+        };
+        // outputs of the chunk starting at tp (n tokens): o = scale (gamma O' + Y)
+        auto write_outputs = [&](int tp, int n, uint32_t ox) {
+            float o1[16], y[16];
+            ptx::tmem_ld16(tm + lane_sel + ox + c16, o1);
+            ptx::tmem_ld16(tm + lane_sel + TM_Y + c16, y);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int s = c16 + j;
+                if (s < n)
+                    og[((long long)(tp + s) * p.Hv + h) * DH + row] =
+                        from_f32<TIO>(p.scale * fmaf(gam_prev[s], o1[j], y[j]));
             }
         };
 
@@ -639,50 +711,54 @@ __global__ void __launch_bounds__(NT, 1)
         if (nc > 0) {
             stage_load(0, 0);
             if (!stage_wait(0)) { failed = true; break; }
-            build_s16(reinterpret_cast<const float *>(sm + S_VREC + VREC_GATES), min(CH, eos - bos));
+            build_s16(reinterpret_cast<const float *>(sm + S_VREC + VREC_F), min(CH, eos - bos));
         }
         mma_ready();
 
         for (int c = 0; c < nc && !failed; ++c) {
             const int st = c & 1;
             uint8_t *stage = sm + st * STAGE_BYTES;
-            const float *G = reinterpret_cast<const float *>(stage + S_VREC + VREC_GATES);
-            const float *Gam = G, *bet = G + CH, *gmm = G + 2 * CH;
+            const float *F = reinterpret_cast<const float *>(stage + S_VREC + VREC_F);
             const int t0 = bos + CH * c, n = min(CH, eos - t0);
             const uint32_t a_st = ptx::smem_u32(stage);
-            // the other stage was last read by chunk c - 1, which is complete
-            if (c + 1 < nc) stage_load(c + 1, st ^ 1);
+            const uint32_t ox = TM_OX + 128u * (uint32_t)st;
             // ---- MMA2: [O' | X] = S0 [Q;K]^T
             if (tid == 0) {
                 ptx::tc_fence_after();
                 const uint32_t i128 = ptx::idesc_f16_f32(128, 128);
                 for (int ks = 0; ks < DH / 16; ++ks) {
                     const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    ptx::mma_f16(tm + TM_O, ptx::sdesc_k_sw128(a_S16 + ko), ptx::sdesc_k_sw128(a_st + S_KREC + ko),
+                    ptx::mma_f16(tm + ox, ptx::sdesc_k_sw128(a_S16 + ko), ptx::sdesc_k_sw128(a_st + S_KREC + ko),
                                  i128, ks > 0);
                 }
                 ptx::mma_commit(&bar);
             }
+            // the other stage was last read by chunk c - 1, which is complete
+            // (its gamma was copied to gam_prev)
+            if (c + 1 < nc) stage_load(c + 1, st ^ 1);
+            // ---- while MMA2 runs: the outputs of chunk c - 1
+            if (c > 0) write_outputs(t0 - CH, CH, TM_OX + 128u * (uint32_t)(st ^ 1));
             if (!mma_wait()) { failed = true; break; }
-            // ---- R^T = (V - diag(gamma) K S0^T)^T diag(beta) from X
+            // ---- R^T = diag(beta) V - diag(beta gamma) X^T, transposed; this chunk's gamma for its outputs
             {
                 float x[16];
-                ptx::tmem_ld16(tm + lane_sel + TM_X + c16, x);
+                ptx::tmem_ld16(tm + lane_sel + ox + 64 + c16, x);
 #pragma unroll
-                for (int j = 0; j < 16; j += 4) {
-                    float w[4];
+                for (int j = 0; j < 16; j += 8) {
+                    float w[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
+                    for (int e = 0; e < 8; ++e) {
                         const int s = c16 + j + e;
                         float vv;
                         if (STAGED)
                             vv = to_f32(reinterpret_cast<const TIO *>(stage + S_V)[s * DH + row]);
                         else
                             vv = s < n ? to_f32(vg[(long long)(t0 + s) * p.v_stride + (long long)h * DH + row]) : 0.f;
-                        w[e] = bet[s] * (vv - gmm[s] * x[j + e]);
+                        w[e] = fmaf(F[F_BETA + s], vv, -F[F_BG + s] * x[j + e]);
                     }
-                    st_h4(sm + OFF_RT, sw(row, c16 + j, 128), w[0], w[1], w[2], w[3]);
+                    st_h8(sm + OFF_RT, sw(row, c16 + j, 128), w);
                 }
+                if (tid < CH) gam_prev[tid] = F[F_GAMMA + tid];
             }
             mma_ready();
             // ---- MMA3: U^T = R^T T^T
@@ -696,27 +772,16 @@ __global__ void __launch_bounds__(NT, 1)
             }
             if (!mma_wait()) { failed = true; break; }
             // ---- U^T -> fp16 operands (plain, and decayed to the chunk end in the
-            //      v tile, which is free now); capsule deltas
-            {
-                float u[16];
-                ptx::tmem_ld16(tm + lane_sel + TM_U + c16, u);
-                const float Gl = Gam[n - 1];
+            //      v tile, which is free now)
+            float u[16];
+            ptx::tmem_ld16(tm + lane_sel + TM_U + c16, u);
 #pragma unroll
-                for (int j = 0; j < 16; j += 4) {
-                    float w[4];
+            for (int j = 0; j < 16; j += 8) {
+                float w[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) w[e] = __expf(Gl - Gam[c16 + j + e]) * u[j + e];
-                    st_h4(sm + OFF_RT, sw(row, c16 + j, 128), u[j], u[j + 1], u[j + 2], u[j + 3]);
-                    st_h4(stage + S_V, sw(row, c16 + j, 128), w[0], w[1], w[2], w[3]);
-                }
-                if (p.caps) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int s = c16 + j, tl = t0 + s - bos;
-                        if (s < n && tl < p.cap)
-                            p.caps[((long long)b * p.cap + tl) * p.W + ubase + (long long)h * DH + row] = u[j];
-                    }
-                }
+                for (int e = 0; e < 8; ++e) w[e] = F[F_DECAY + c16 + j + e] * u[j + e];
+                st_h8(sm + OFF_RT, sw(row, c16 + j, 128), u + j);
+                st_h8(stage + S_V, sw(row, c16 + j, 128), w);
             }
             mma_ready();
             // ---- MMA4 (Y = U^T (P o D)^T) and MMA5 (state)
@@ -732,24 +797,25 @@ __global__ void __launch_bounds__(NT, 1)
                 }
                 ptx::mma_commit(&bar);
             }
-            if (!mma_wait()) { failed = true; break; }
-            state_live = true;
-            if (c + 1 < nc && !stage_wait(st ^ 1)) { failed = true; break; }
-            // ---- outputs o = scale (gamma O' + Y), and the next chunk's fp16 state copy
-            {
-                float o1[16], y[16];
-                ptx::tmem_ld16(tm + lane_sel + TM_O + c16, o1);
-                ptx::tmem_ld16(tm + lane_sel + TM_Y + c16, y);
+            // the capsule deltas while MMA4/5 run
+            if (p.caps) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int s = c16 + j;
-                    if (s < n)
-                        og[((long long)(t0 + s) * p.Hv + h) * DH + row] = from_f32<TIO>(p.scale * fmaf(gmm[s], o1[j], y[j]));
+                    const int s = c16 + j, tl = t0 + s - bos;
+                    if (s < n && tl < p.cap)
+                        p.caps[((long long)b * p.cap + tl) * p.W + ubase + (long long)h * DH + row] = u[j];
                 }
             }
-            if (c + 1 < nc)
-                build_s16(reinterpret_cast<const float *>(sm + (st ^ 1) * STAGE_BYTES + S_VREC + VREC_GATES),
+            if (!mma_wait()) { failed = true; break; }
+            state_live = true;
+            // ---- the next chunk's fp16 state copy (its inputs first)
+            if (c + 1 < nc) {
+                if (!stage_wait(st ^ 1)) { failed = true; break; }
+                build_s16(reinterpret_cast<const float *>(sm + (st ^ 1) * STAGE_BYTES + S_VREC + VREC_F),
                           min(CH, eos - t0 - CH));
+            } else {
+                write_outputs(t0, n, ox);  // the last chunk's outputs: no MMA left to overlap
+            }
             mma_ready();
         }
         if (failed) break;
@@ -777,7 +843,9 @@ __global__ void __launch_bounds__(NT, 1)
         flag_error(p.status, GDN_DEVERR_TIMEOUT);
         ptx::mbar_wait_bounded(&bar, phase ^ 1u, WAIT_LIMIT);  // let in-flight MMAs drain
         ptx::mbar_wait_bounded(&bar, phase, WAIT_LIMIT);
-        for (int st = 0; st < 2; ++st)  // and staged copies
+    }
+    if (failed && tid == 32) {  // and the staged copies this warp issued
+        for (int st = 0; st < 2; ++st)
             if (pending[st]) ptx::mbar_wait_bounded(&lbar[st], lph[st], WAIT_LIMIT);
     }
     ptx::tc_fence_before();
@@ -802,9 +870,15 @@ int num_sms() {
 
 template <typename TIO>
 cudaError_t launch_io(const ForwardParams &p, int min_len, uint8_t *ws, cudaStream_t stream) {
-    CUtensorMap mv{};
-    if (sizeof(TIO) == 2 && !encode_rows_f16(&mv, p.v, (long long)p.Hv * DH, p.v_stride, p.T, DH, CH))
-        return cudaErrorInvalidValue;
+    CUtensorMap mq{}, mk{}, mv{};
+    if (sizeof(TIO) == 2) {
+        // q, k: 64-token x 64-feature boxes in the 128-byte swizzle of the MMA operand tiles;
+        // v: 64-token x 128-feature rows as they are
+        if (!encode_rows_f16(&mq, p.q, (long long)p.Hk * DH, p.q_stride, p.T, 64, CH, true) ||
+            !encode_rows_f16(&mk, p.k, (long long)p.Hk * DH, p.k_stride, p.T, 64, CH, true) ||
+            !encode_rows_f16(&mv, p.v, (long long)p.Hv * DH, p.v_stride, p.T, DH, CH, false))
+            return cudaErrorInvalidValue;
+    }
     int32_t *hdr = reinterpret_cast<int32_t *>(ws);
     const long long maxch = max_chunks(p.B, p.T);
     uint8_t *krec = ws + header_bytes(p.B);
@@ -817,7 +891,7 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, uint8_t *ws, cudaStre
     auto prep = wy_prep_kernel<TIO>;
     e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
     if (e != cudaSuccess) return e;
-    if (prep_ctas > 0) prep<<<(unsigned)prep_ctas, PT, PREP_SMEM, stream>>>(p, hdr, krec, vrec);
+    if (prep_ctas > 0) prep<<<(unsigned)prep_ctas, PT, PREP_SMEM, stream>>>(p, hdr, krec, vrec, mq, mk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto scan = wy_scan_kernel<TIO>;

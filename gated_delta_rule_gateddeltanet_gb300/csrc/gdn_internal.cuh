@@ -85,9 +85,11 @@ gdn_status single_kernel_workspace_size(const gdn_forward_args *args, size_t *by
 cudaError_t launch_chunked_wy(const ForwardParams &p, int min_len, void *workspace, cudaStream_t stream);
 
 // Tensor map over a packed fp16 [T, row_elems] array with `stride` elements
-// between tokens, boxes of box_y tokens x box_x elements, zero fill past T.
+// between tokens, boxes of box_y tokens x box_x elements, zero fill past T;
+// with swizzle128 (box_x = 64) each box lands in shared memory in the
+// 128-byte swizzled layout of a K-major MMA operand tile.
 bool encode_rows_f16(CUtensorMap *map, const void *base, long long row_elems, long long stride, int T, int box_x,
-                     int box_y);
+                     int box_y, bool swizzle128);
 
 // Sequences up to this many tokens stay on the recurrent kernel under the
 // automatic plan; longer ones go to the chunked kernel.
