@@ -279,6 +279,15 @@ __device__ __forceinline__ void chunk_gates(const ForwardParams &p, int t0, int 
     }
 }
 
+// Sixteen consecutive floats from 16-byte aligned shared memory (four 16-byte loads).
+__device__ __forceinline__ void ld_f16x(const float *src, float (&x)[16]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 v = reinterpret_cast<const float4 *>(src)[q];
+        x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+    }
+}
+
 // Eight consecutive elements (k % 8 == 0) of one row of a swizzled fp16 tile: one 16-byte store.
 __device__ __forceinline__ void st_h8(uint8_t *base, uint32_t off, const float *x) {
     uint4 v;
@@ -372,82 +381,112 @@ __global__ void __launch_bounds__(PT, 4)
     if (STAGED) ok = ptx::mbar_wait_bounded(&lbar, 0, WAIT_LIMIT);
     ok = __syncthreads_and(ok);
 
-    // ---- L2-normalised q and k rows of the [Q;K] tile (zero past the
-    //      sequence); warp w handles tokens w, w + 8, ...
-    const TIO *qg = static_cast<const TIO *>(p.q);
-    const TIO *kg = static_cast<const TIO *>(p.k);
+    // ---- L2-normalised q and k rows of the [Q;K] tile (zero past the sequence)
+    if (STAGED) {
+        // in place: four lanes per token (32 features each, as four 16-byte
+        // pieces of the swizzled row), warp w handles tokens 8w .. 8w+7
+        const int s = warp * 8 + (lane >> 2), qp = lane & 3;
+        const int tl = t0 + s - bos;
 #pragma unroll 1
-    for (int round = 0; ok && round < 2; ++round) {
-        float qv[4][4], kv[4][4], sq[4], sk[4];
+        for (int which = 0; ok && which < 2; ++which) {  // q rows, then k rows
+            const int rrow = which * 64 + s;
+            float x[32];
+            float ss = 0.f;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int s = warp + 8 * (u + 4 * round);
+            for (int m = 0; m < 4; ++m) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(sm + sw(rrow, 32 * qp + 8 * m, 128));
+                const __half2 *hv = reinterpret_cast<const __half2 *>(&raw);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) qv[u][e] = kv[u][e] = 0.f;
-            if (s < n) {
-                if (STAGED) {
-                    ld4<__half>(reinterpret_cast<const __half *>(sm + sw(s, lane * 4, 128)), qv[u]);
-                    ld4<__half>(reinterpret_cast<const __half *>(sm + sw(64 + s, lane * 4, 128)), kv[u]);
-                } else {
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(hv[e]);
+                    x[8 * m + 2 * e] = f.x;
+                    x[8 * m + 2 * e + 1] = f.y;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ss = fmaf(x[e], x[e], ss);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            const float inv = 1.f / fmaxf(sqrtf(ss), EPS);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = s < n ? x[e] * inv : 0.f;  // rows past the sequence become zero
+#pragma unroll
+            for (int m = 0; m < 4; ++m) st_h8(sm, sw(rrow, 32 * qp + 8 * m, 128), x + 8 * m);
+            if (which == 1 && p.caps && s < n && tl < p.cap) {
+                float *dst = p.caps + ((long long)b * p.cap + tl) * p.W + p.Hv + (long long)kh * DH + 32 * qp;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) dst[e] = x[e];  // rows need not be 16-byte aligned
+            }
+        }
+    } else {
+        // from global memory: warp w handles tokens w, w + 8, ..., four at a time
+        const TIO *qg = static_cast<const TIO *>(p.q);
+        const TIO *kg = static_cast<const TIO *>(p.k);
+#pragma unroll 1
+        for (int round = 0; ok && round < 2; ++round) {
+            float qv[4][4], kv[4][4], sq[4], sk[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int s = warp + 8 * (u + 4 * round);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) qv[u][e] = kv[u][e] = 0.f;
+                if (s < n) {
                     const long long t = (long long)t0 + s;
                     ld4<TIO>(qg + t * p.q_stride + (long long)kh * DH + lane * 4, qv[u]);
                     ld4<TIO>(kg + t * p.k_stride + (long long)kh * DH + lane * 4, kv[u]);
                 }
             }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            sq[u] = sk[u] = 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                sq[u] = fmaf(qv[u][e], qv[u][e], sq[u]);
-                sk[u] = fmaf(kv[u][e], kv[u][e], sk[u]);
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], off);
-                sk[u] += __shfl_xor_sync(0xffffffffu, sk[u], off);
+                sq[u] = sk[u] = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    sq[u] = fmaf(qv[u][e], qv[u][e], sq[u]);
+                    sk[u] = fmaf(kv[u][e], kv[u][e], sk[u]);
+                }
             }
-        }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int s = warp + 8 * (u + 4 * round);
-            const float iq = 1.f / fmaxf(sqrtf(sq[u]), EPS), ik = 1.f / fmaxf(sqrtf(sk[u]), EPS);
+            for (int off = 16; off > 0; off >>= 1) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                qv[u][e] *= iq;
-                kv[u][e] *= ik;
+                for (int u = 0; u < 4; ++u) {
+                    sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], off);
+                    sk[u] += __shfl_xor_sync(0xffffffffu, sk[u], off);
+                }
             }
-            const int c = lane * 4;
-            st_h4(sm, sw(s, c, 128), qv[u][0], qv[u][1], qv[u][2], qv[u][3]);
-            st_h4(sm, sw(64 + s, c, 128), kv[u][0], kv[u][1], kv[u][2], kv[u][3]);
-            const int tl = t0 + s - bos;
-            if (p.caps && s < n && tl < p.cap) {
-                float *dst = p.caps + ((long long)b * p.cap + tl) * p.W + p.Hv + (long long)kh * DH + c;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) dst[e] = kv[u][e];  // rows need not be 16-byte aligned
+            for (int u = 0; u < 4; ++u) {
+                const int s = warp + 8 * (u + 4 * round);
+                const float iq = 1.f / fmaxf(sqrtf(sq[u]), EPS), ik = 1.f / fmaxf(sqrtf(sk[u]), EPS);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    qv[u][e] *= iq;
+                    kv[u][e] *= ik;
+                }
+                const int c = lane * 4;
+                st_h4(sm, sw(s, c, 128), qv[u][0], qv[u][1], qv[u][2], qv[u][3]);
+                st_h4(sm, sw(64 + s, c, 128), kv[u][0], kv[u][1], kv[u][2], kv[u][3]);
+                const int tl = t0 + s - bos;
+                if (p.caps && s < n && tl < p.cap) {
+                    float *dst = p.caps + ((long long)b * p.cap + tl) * p.W + p.Hv + (long long)kh * DH + c;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dst[e] = kv[u][e];  // rows need not be 16-byte aligned
+                }
             }
         }
     }
     __syncthreads();
-    // ---- K^T tile (row j = feature, 64 token columns) from the K rows: thread
-    //      (j, half) gathers 32 tokens as four 8-element pieces
+    // ---- K^T tile (row j = feature, 64 token columns) from the K rows: 128
+    //      8 x 8 blocks moved by transposing matrix loads and matrix stores, four
+    //      blocks per instruction, four instructions per warp
     if (ok) {
-        const int j = tid >> 1, sg = (tid & 1) * 32;
+        const int m = lane >> 3, rr = lane & 7;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int s = sg + 8 * m + 2 * e;
-                const unsigned short a0 = *reinterpret_cast<const unsigned short *>(sm + sw(64 + s, j, 128));
-                const unsigned short a1 = *reinterpret_cast<const unsigned short *>(sm + sw(65 + s, j, 128));
-                w[e] = (uint32_t)a0 | ((uint32_t)a1 << 16);
-            }
-            *reinterpret_cast<uint4 *>(sm + KREC_KT + sw(j, sg + 8 * m, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int it = 0; it < 4; ++it) {
+            const int tile = (warp * 4 + it) * 4 + m;  // 0..127: 8 token blocks x 16 feature blocks
+            const int s0 = (tile & 7) * 8, j0 = (tile >> 3) * 8;
+            uint32_t r[4];
+            ptx::ldmatrix_x4_trans(r, ptx::smem_u32(sm + sw(64 + s0 + rr, j0, 128)));
+            ptx::stmatrix_x4(ptx::smem_u32(sm + KREC_KT + sw(j0 + rr, s0, 128)), r);
         }
     }
     ptx::fence_proxy_async_smem();
@@ -487,7 +526,17 @@ __global__ void __launch_bounds__(PT, 4)
             gates_group(i);
             __syncthreads();
         }
-        {
+        if ((quarter & 1) == 0 && c32 == 32) {  // rows 0-31, columns 32-63: above the diagonal, all zero
+            const int r = row & 63;
+            if (quarter >= 2) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) AT[r * AS + c32 + j] = 0.f;
+            } else {
+                const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) st_h8(tpd + VREC_PD, sw(r, c32 + j, 64), z);
+            }
+        } else {
             float v[32];
             ptx::tmem_ld32(tm + lane_sel + c32, v);
             const int r = row & 63;
@@ -581,7 +630,7 @@ __global__ void __launch_bounds__(NT, 1)
     __shared__ __align__(8) uint64_t lbar[2];  // stage loads
     __shared__ uint32_t tmem_base;
     __shared__ int item_s;
-    __shared__ float gam_prev[CH];             // gamma of the chunk whose outputs are pending
+    __shared__ __align__(16) float gam_prev[CH];  // gamma of the chunk whose outputs are pending
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Tensor memory: a warp reaches only the 32 lanes of its quarter (warp % 4);
     // the four warps of a quarter split the columns.
@@ -608,7 +657,12 @@ __global__ void __launch_bounds__(NT, 1)
     bool pending[2] = {false, false};
     bool failed = false;
     constexpr bool STAGED = sizeof(TIO) == 2;
-    const uint32_t a_S16 = ptx::smem_u32(sm + OFF_S16), a_RT = ptx::smem_u32(sm + OFF_RT);
+    // Shared-memory descriptors: a step of 16 elements along K adds 32 bytes,
+    // i.e. 2 to the descriptor's address field (addresses stay below 256 KiB,
+    // so the 14-bit field never carries).
+    const uint64_t d_S16 = ptx::sdesc_k_sw128(ptx::smem_u32(sm + OFF_S16));
+    const uint64_t d_RT = ptx::sdesc_k_sw128(ptx::smem_u32(sm + OFF_RT));
+    constexpr uint32_t I64 = ptx::idesc_f16_f32(128, 64), I128 = ptx::idesc_f16_f32(128, 128);
 
     auto mma_wait = [&]() -> bool {
         const bool ok = ptx::mbar_wait_bounded(&bar, phase, WAIT_LIMIT);
@@ -651,9 +705,9 @@ __global__ void __launch_bounds__(NT, 1)
         }
         const size_t head_off = ((size_t)slot * p.Hv + h) * (size_t)DH * DH;
 
-        // chunk c's records (and fp16 v rows) into stage st (issued by warp 1)
+        // chunk c's records (and fp16 v rows) into stage st
         auto stage_load = [&](int c, int st) {
-            if (tid == 32) {
+            if (tid == 0) {
                 uint8_t *stage = sm + st * STAGE_BYTES;
                 ptx::mbar_arrive_expect_tx(&lbar[st], (uint32_t)(KREC_BYTES + VREC_BYTES + (STAGED ? CH * DH * 2 : 0)));
                 ptx::bulk_g2s(stage + S_KREC, krec + ((gbase + c) * p.Hk + kh) * KREC_BYTES, KREC_BYTES, &lbar[st]);
@@ -684,15 +738,15 @@ __global__ void __launch_bounds__(NT, 1)
         };
         // outputs of the chunk starting at tp (n tokens): o = scale (gamma O' + Y)
         auto write_outputs = [&](int tp, int n, uint32_t ox) {
-            float o1[16], y[16];
+            float o1[16], y[16], gm[16];
             ptx::tmem_ld16(tm + lane_sel + ox + c16, o1);
             ptx::tmem_ld16(tm + lane_sel + TM_Y + c16, y);
+            ld_f16x(gam_prev + c16, gm);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int s = c16 + j;
                 if (s < n)
-                    og[((long long)(tp + s) * p.Hv + h) * DH + row] =
-                        from_f32<TIO>(p.scale * fmaf(gam_prev[s], o1[j], y[j]));
+                    og[((long long)(tp + s) * p.Hv + h) * DH + row] = from_f32<TIO>(p.scale * fmaf(gm[j], o1[j], y[j]));
             }
         };
 
@@ -710,6 +764,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
         if (nc > 0) {
             stage_load(0, 0);
+            if (nc > 1) stage_load(1, 1);
             if (!stage_wait(0)) { failed = true; break; }
             build_s16(reinterpret_cast<const float *>(sm + S_VREC + VREC_F), min(CH, eos - bos));
         }
@@ -725,17 +780,13 @@ __global__ void __launch_bounds__(NT, 1)
             // ---- MMA2: [O' | X] = S0 [Q;K]^T
             if (tid == 0) {
                 ptx::tc_fence_after();
-                const uint32_t i128 = ptx::idesc_f16_f32(128, 128);
+                const uint64_t bd = ptx::sdesc_k_sw128(a_st + S_KREC);
                 for (int ks = 0; ks < DH / 16; ++ks) {
-                    const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    ptx::mma_f16(tm + ox, ptx::sdesc_k_sw128(a_S16 + ko), ptx::sdesc_k_sw128(a_st + S_KREC + ko),
-                                 i128, ks > 0);
+                    const uint32_t ko = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                    ptx::mma_f16(tm + ox, d_S16 + ko, bd + ko, I128, ks > 0);
                 }
                 ptx::mma_commit(&bar);
             }
-            // the other stage was last read by chunk c - 1, which is complete
-            // (its gamma was copied to gam_prev)
-            if (c + 1 < nc) stage_load(c + 1, st ^ 1);
             // ---- while MMA2 runs: the outputs of chunk c - 1
             if (c > 0) write_outputs(t0 - CH, CH, TM_OX + 128u * (uint32_t)(st ^ 1));
             if (!mma_wait()) { failed = true; break; }
@@ -743,6 +794,9 @@ __global__ void __launch_bounds__(NT, 1)
             {
                 float x[16];
                 ptx::tmem_ld16(tm + lane_sel + ox + 64 + c16, x);
+                float be[16], bg[16];
+                ld_f16x(F + F_BETA + c16, be);
+                ld_f16x(F + F_BG + c16, bg);
 #pragma unroll
                 for (int j = 0; j < 16; j += 8) {
                     float w[8];
@@ -754,7 +808,7 @@ __global__ void __launch_bounds__(NT, 1)
                             vv = to_f32(reinterpret_cast<const TIO *>(stage + S_V)[s * DH + row]);
                         else
                             vv = s < n ? to_f32(vg[(long long)(t0 + s) * p.v_stride + (long long)h * DH + row]) : 0.f;
-                        w[e] = fmaf(F[F_BETA + s], vv, -F[F_BG + s] * x[j + e]);
+                        w[e] = fmaf(be[j + e], vv, -bg[j + e] * x[j + e]);
                     }
                     st_h8(sm + OFF_RT, sw(row, c16 + j, 128), w);
                 }
@@ -764,22 +818,21 @@ __global__ void __launch_bounds__(NT, 1)
             // ---- MMA3: U^T = R^T T^T
             if (tid == 0) {
                 ptx::tc_fence_after();
-                const uint32_t i64 = ptx::idesc_f16_f32(128, 64);
-                for (int ks = 0; ks < CH / 16; ++ks)
-                    ptx::mma_f16(tm + TM_U, ptx::sdesc_k_sw128(a_RT + ks * 32),
-                                 ptx::sdesc_k_sw128(a_st + S_VREC + VREC_T + ks * 32), i64, ks > 0);
+                const uint64_t bd = ptx::sdesc_k_sw128(a_st + S_VREC + VREC_T);
+                for (int ks = 0; ks < CH / 16; ++ks) ptx::mma_f16(tm + TM_U, d_RT + 2 * ks, bd + 2 * ks, I64, ks > 0);
                 ptx::mma_commit(&bar);
             }
             if (!mma_wait()) { failed = true; break; }
             // ---- U^T -> fp16 operands (plain, and decayed to the chunk end in the
             //      v tile, which is free now)
-            float u[16];
+            float u[16], dc[16];
             ptx::tmem_ld16(tm + lane_sel + TM_U + c16, u);
+            ld_f16x(F + F_DECAY + c16, dc);
 #pragma unroll
             for (int j = 0; j < 16; j += 8) {
                 float w[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) w[e] = F[F_DECAY + c16 + j + e] * u[j + e];
+                for (int e = 0; e < 8; ++e) w[e] = dc[j + e] * u[j + e];
                 st_h8(sm + OFF_RT, sw(row, c16 + j, 128), u + j);
                 st_h8(stage + S_V, sw(row, c16 + j, 128), w);
             }
@@ -787,13 +840,11 @@ __global__ void __launch_bounds__(NT, 1)
             // ---- MMA4 (Y = U^T (P o D)^T) and MMA5 (state)
             if (tid == 0) {
                 ptx::tc_fence_after();
-                const uint32_t i64 = ptx::idesc_f16_f32(128, 64), i128 = ptx::idesc_f16_f32(128, 128);
-                const uint32_t a_ud = a_st + S_V, a_pd = a_st + S_VREC + VREC_PD, a_kt = a_st + S_KREC + KREC_KT;
+                const uint64_t ud = ptx::sdesc_k_sw128(a_st + S_V), pd = ptx::sdesc_k_sw128(a_st + S_VREC + VREC_PD);
+                const uint64_t kt = ptx::sdesc_k_sw128(a_st + S_KREC + KREC_KT);
                 for (int ks = 0; ks < CH / 16; ++ks) {
-                    ptx::mma_f16(tm + TM_Y, ptx::sdesc_k_sw128(a_RT + ks * 32), ptx::sdesc_k_sw128(a_pd + ks * 32),
-                                 i64, ks > 0);
-                    ptx::mma_f16(tm + TM_S, ptx::sdesc_k_sw128(a_ud + ks * 32), ptx::sdesc_k_sw128(a_kt + ks * 32),
-                                 i128, (state_live || ks > 0) ? 1u : 0u);
+                    ptx::mma_f16(tm + TM_Y, d_RT + 2 * ks, pd + 2 * ks, I64, ks > 0);
+                    ptx::mma_f16(tm + TM_S, ud + 2 * ks, kt + 2 * ks, I128, (state_live || ks > 0) ? 1u : 0u);
                 }
                 ptx::mma_commit(&bar);
             }
@@ -808,6 +859,8 @@ __global__ void __launch_bounds__(NT, 1)
             }
             if (!mma_wait()) { failed = true; break; }
             state_live = true;
+            // this stage is free now (its gamma was copied to gam_prev): chunk c + 2 goes there
+            if (c + 2 < nc) stage_load(c + 2, st);
             // ---- the next chunk's fp16 state copy (its inputs first)
             if (c + 1 < nc) {
                 if (!stage_wait(st ^ 1)) { failed = true; break; }
@@ -843,9 +896,7 @@ __global__ void __launch_bounds__(NT, 1)
         flag_error(p.status, GDN_DEVERR_TIMEOUT);
         ptx::mbar_wait_bounded(&bar, phase ^ 1u, WAIT_LIMIT);  // let in-flight MMAs drain
         ptx::mbar_wait_bounded(&bar, phase, WAIT_LIMIT);
-    }
-    if (failed && tid == 32) {  // and the staged copies this warp issued
-        for (int st = 0; st < 2; ++st)
+        for (int st = 0; st < 2; ++st)  // and the staged copies
             if (pending[st]) ptx::mbar_wait_bounded(&lbar[st], lph[st], WAIT_LIMIT);
     }
     ptx::tc_fence_before();

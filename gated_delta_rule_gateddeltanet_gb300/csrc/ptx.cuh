@@ -110,6 +110,28 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 
+// ---------------------------------------------------------------- 8 x 8 b16 matrix moves (warp-wide)
+
+// Four 8 x 8 b16 matrices from shared memory, transposed: lanes 8i .. 8i+7
+// give the addresses of the eight 16-byte rows of matrix i; thread t receives
+// in r[i] the elements (2(t%4), t/4) and (2(t%4)+1, t/4) of matrix i.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t row_addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(row_addr)
+                 : "memory");
+}
+
+// Four 8 x 8 b16 matrices to shared memory: lanes 8i .. 8i+7 give the row
+// addresses of matrix i; thread t holds in r[i] the elements (t/4, 2(t%4)) and
+// (t/4, 2(t%4)+1) of matrix i.  After ldmatrix_x4_trans this stores the
+// transposes.
+__device__ __forceinline__ void stmatrix_x4(uint32_t row_addr, const uint32_t (&r)[4]) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(row_addr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05 (5th-generation tensor cores)
 
 // Tensor-memory allocation: executed by one full warp.  The allocated base
