@@ -169,7 +169,10 @@ __global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int
 // inside the two 32 x 32 diagonal blocks, then for the lower-left quadrant.
 // Each block of A is read (into the product M = L21 T11) before the block of
 // T that replaces it is written.  256 threads; ends with a barrier.
-constexpr int AS = 65, MS = 36;
+// Row strides (floats): AS = 68 makes the warp-level product loads of the A / T
+// blocks conflict-free (rows land 4 banks apart); MS = 40 does the same for the
+// scratch M read as the right-hand factor.
+constexpr int AS = 68, MS = 40;
 __device__ void tri_inverse_inplace(float *AT, float *M, int tid) {
     const int warp = tid >> 5, lane = tid & 31;
     float x[16];
@@ -312,7 +315,7 @@ constexpr int GH = 8;    // value heads whose gates are computed together (one w
 // scratch and the T and P o D tiles of one value head.
 constexpr int P_AT = 0;                    // [64][AS] fp32
 constexpr int P_M = 64 * AS * 4;           // [32][MS] fp32
-constexpr int P_TPD = 21504;               // T and P o D tiles (1024-byte aligned), 16 KiB
+constexpr int P_TPD = 23552;               // T and P o D tiles (1024-byte aligned), 16 KiB
 constexpr int PREP_SMEM = KREC_BYTES + 1024;
 static_assert(P_M + 32 * MS * 4 <= P_TPD && P_TPD + VREC_F <= KREC_BYTES, "prep shared-memory layout");
 
@@ -569,8 +572,10 @@ __global__ void __launch_bounds__(PT, 4)
 #pragma unroll
             for (int j = 0; j < 16; j += 8) {
                 float w[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) w[e] = AT[r * AS + s0 + j + e];
+                const float4 a = *reinterpret_cast<const float4 *>(AT + r * AS + s0 + j);
+                const float4 c = *reinterpret_cast<const float4 *>(AT + r * AS + s0 + j + 4);
+                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+                w[4] = c.x; w[5] = c.y; w[6] = c.z; w[7] = c.w;
                 st_h8(tpd + VREC_T, sw(r, s0 + j, 64), w);
             }
         }
