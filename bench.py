@@ -262,6 +262,7 @@ def run_gdn(a, dist: Dist):
         extra["spec_verify_replay"] = run_spec(dev, stream, lib, sh)
         extra["causal_conv"] = run_conv(dev, stream)
         extra["serving_mix"] = run_serving_mix(dev, stream, lib, sh)
+        extra["state_transpose"] = run_transpose(dev, stream, lib, sh)
 
     cpu = None
     if not a.no_cpu and dist.rank == 0 and dist.world == 1:
@@ -602,6 +603,38 @@ def run_serving_mix(dev, stream, lib, sh):
             "decode_frac_hbm": round(dec_bytes / (d_ms / steps / 1e3) / 1e9 / hbm, 4),
             "tokens_per_s": round((pre.T + B * steps) / ((p_ms + d_ms) / 1e3), 1),
             "launches": 2 + steps}
+
+
+def run_transpose(dev, stream, lib, sh):
+    """K-major <-> V-major conversion of the decode step's state pool
+    (64 x 48 matrices of 128 x 128 FP32 = 192 MiB each way), 4 rotating pairs."""
+    import torch
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    n = 64 * 48
+    pairs = [(torch.randn((n, 128, 128), device=dev), torch.empty((n, 128, 128), device=dev)) for _ in range(NBUF)]
+
+    def call(i):
+        src, dst = pairs[i % NBUF]
+        rc = lib.gdn_state_transpose(ctypes.c_void_p(src.data_ptr()), ctypes.c_void_p(dst.data_ptr()), n, 128, 128,
+                                     sh)
+        if rc:
+            raise gdn.GdnError(rc, "gdn_state_transpose")
+    for i in range(5):
+        call(i)
+    torch.cuda.synchronize()
+    reps = 40
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(reps):
+        call(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / reps * 1e3
+    hbm, _, _ = measured_peaks()
+    nbytes = 2 * n * 128 * 128 * 4
+    return {"workload": "state layout conversion: 3072 matrices of 128 x 128 fp32 (the decode pool), 4 rotating pairs",
+            "us": round(us, 2), "gbs": round(nbytes / (us / 1e6) / 1e9, 1),
+            "frac_hbm": round(nbytes / (us / 1e6) / 1e9 / hbm, 4)}
 
 
 # ---------------------------------------------------------------- CPU oracle (baseline and reference arm)

@@ -20,7 +20,7 @@ import torch
 
 from .build import LIB as LIB_PATH
 
-__all__ = ["gdn_forward", "gdn_forward_no_alloc", "gdn_replay_prefix", "varlen_causal_conv_with_state",
+__all__ = ["gdn_forward", "gdn_forward_dense", "state_transpose", "gdn_forward_no_alloc", "gdn_replay_prefix", "varlen_causal_conv_with_state",
            "causal_conv_replay_prefix", "GdnError", "load_library", "capsule_width",
            "STATUS", "DEVERR", "PLAN"]
 
@@ -97,6 +97,10 @@ def load_library(path: str | None = None):
     lib.varlen_causal_conv_with_state.argtypes = [ctypes.POINTER(ConvArgs), P]
     lib.causal_conv_replay_prefix.restype = i32
     lib.causal_conv_replay_prefix.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, i32, P, P, P]
+    lib.gdn_forward_dense.restype = i32
+    lib.gdn_forward_dense.argtypes = [ctypes.POINTER(ForwardArgs), i32, P]
+    lib.gdn_state_transpose.restype = i32
+    lib.gdn_state_transpose.argtypes = [P, P, ctypes.c_int64, i32, i32, P]
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_status_string.argtypes = [i32]
     if path is None:
@@ -141,12 +145,13 @@ def _token_stride(t, name, inner):
 def build_forward_args(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, gate_mode="raw",
                        initial_state=None, final_state=None, state_slots=None, output=None,
                        state_update=None, capacity=0, scale=0.0, plan="auto", status=None,
-                       num_state_slots=None, workspace=None, max_seqlen=0):
-    """Fill a ForwardArgs struct from tensors; returns (args, outputs, keepalive)."""
+                       num_state_slots=None, workspace=None, max_seqlen=0, num_seqs=None):
+    """Fill a ForwardArgs struct from tensors; returns (args, outputs, keepalive).
+    ``cu_seqlens=None`` (rank-4 calls) takes the batch size from ``num_seqs``."""
     dev = q.device
     T, Hk, dk = q.shape
     Hv, dv = v.shape[1], v.shape[2]
-    B = cu_seqlens.shape[0] - 1
+    B = cu_seqlens.shape[0] - 1 if cu_seqlens is not None else int(num_seqs)
     if q.dtype not in DTYPE:
         raise TypeError(f"unsupported dtype {q.dtype}")
     for name, t in (("k", k), ("v", v)):
@@ -246,6 +251,46 @@ def gdn_forward(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, gate_mod
     if rc != 0:
         raise GdnError(rc, "gdn_forward")
     return outs
+
+
+def gdn_forward_dense(q, k, v, a, b, *, workspace=None, **kw):
+    """Rank-4 inputs (C ABI ``gdn_forward_dense``): q, k [B, S, Hk, dk], v
+    [B, S, Hv, dv], a, b [B, S, Hv], contiguous.  Other keyword arguments as
+    for ``gdn_forward`` (states stay V-major [slots, Hv, dv, dk]; see
+    ``state_transpose`` for the dense export's K-major layout).  Returns
+    ``(output [B, S, Hv, dv], final_state, state_update)``."""
+    lib = load_library()
+    B, S = q.shape[0], q.shape[1]
+    flat = lambda t: None if t is None else t.reshape(B * S, *t.shape[2:])
+    output = kw.pop("output", None)
+    if output is not None:
+        output = output.view(B * S, *output.shape[2:])
+    args, (out, final, caps), keep = build_forward_args(flat(q), flat(k), flat(v), flat(a), flat(b), None,
+                                                        output=output, workspace=workspace, num_seqs=B, **kw)
+    need = workspace_size(args)
+    if need > 0 and workspace is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+        args.workspace, args.workspace_bytes = ctypes.c_void_p(ws.data_ptr()), need
+        keep = keep + (ws,)
+    rc = lib.gdn_forward_dense(ctypes.byref(args), S, _stream_handle(q.device))
+    if rc != 0:
+        raise GdnError(rc, "gdn_forward_dense")
+    return out.view(B, S, *out.shape[1:]), final, caps
+
+
+def state_transpose(src, dst=None):
+    """Transposes the last two dims of an FP32 CUDA tensor (C ABI
+    ``gdn_state_transpose``): K-major [.., dk, dv] <-> V-major [.., dv, dk]."""
+    _check(src, "src", dtype=torch.float32)
+    rows, cols = src.shape[-2], src.shape[-1]
+    if dst is None:
+        dst = torch.empty(*src.shape[:-2], cols, rows, dtype=torch.float32, device=src.device)
+    _check(dst, "dst", dtype=torch.float32, device=src.device)
+    num = src.numel() // max(rows * cols, 1) if rows * cols else 0
+    rc = load_library().gdn_state_transpose(_ptr(src), _ptr(dst), num, rows, cols, _stream_handle(src.device))
+    if rc != 0:
+        raise GdnError(rc, "gdn_state_transpose")
+    return dst
 
 
 def gdn_forward_no_alloc(q, k, v, a, b, cu_seqlens, **kw):

@@ -61,12 +61,14 @@ bool chunked_aligned(const gdn_forward_args *a, const gdn::ForwardParams &p) {
 }
 
 // Checks a forward call completely (sizes, pointers, alignment) and resolves
-// it into kernel parameters.  Returns GDN_OK with *out filled, or the error.
-gdn_status resolve_forward(const gdn_forward_args *a, gdn::ForwardParams *out) {
+// it into kernel parameters.  dense_S >= 0: rank-4 inputs of dense_S tokens
+// per sequence (cu_seqlens unused); -1: packed inputs.  Returns GDN_OK with
+// *out filled, or the error.
+gdn_status resolve_forward(const gdn_forward_args *a, int dense_S, gdn::ForwardParams *out) {
     const gdn_status st = check_sizes(a);
     if (st != GDN_OK) return st;
     if (a->num_seqs == 0) return GDN_OK;
-    if (!a->cu_seqlens || !a->final_state) return GDN_ERR_NULL;
+    if ((dense_S < 0 && !a->cu_seqlens) || !a->final_state) return GDN_ERR_NULL;
     if (a->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->a || !a->b || !a->output)) return GDN_ERR_NULL;
     if (a->gate_mode == GDN_GATES_RAW && (!a->A_log || !a->dt_bias)) return GDN_ERR_NULL;
     if (a->state_update_capacity > 0 && !a->state_update) return GDN_ERR_NULL;
@@ -96,7 +98,8 @@ gdn_status resolve_forward(const gdn_forward_args *a, gdn::ForwardParams *out) {
     p.b = a->b;
     p.A_log = a->A_log;
     p.dt_bias = a->dt_bias;
-    p.cu = a->cu_seqlens;
+    p.cu = dense_S < 0 ? a->cu_seqlens : nullptr;
+    p.dense_S = dense_S < 0 ? 0 : dense_S;
     p.slots = a->state_slots;
     p.init = a->initial_state;
     p.final_state = a->final_state;
@@ -123,36 +126,11 @@ gdn_status single_kernel_workspace_size(const gdn_forward_args *args, size_t *by
 }
 }  // namespace gdn
 
-extern "C" {
+namespace {
 
-const char *gdn_status_string(gdn_status status) {
-    switch (status) {
-        case GDN_OK: return "ok";
-        case GDN_ERR_NULL: return "a required pointer is NULL";
-        case GDN_ERR_DTYPE: return "unsupported I/O dtype (FP16 and FP32 only; BF16 is rejected)";
-        case GDN_ERR_SHAPE: return "inconsistent or unsupported sizes";
-        case GDN_ERR_ALIGN: return "a state pointer is not 16-byte aligned";
-        case GDN_ERR_WORKSPACE: return "workspace missing or too small";
-        case GDN_ERR_CUDA: return "CUDA launch error";
-        case GDN_ERR_UNSUPPORTED: return "the forced plan does not support these sizes";
-        case GDN_ERR_ARG: return "unknown enum value in the arguments";
-    }
-    return "unknown status";
-}
-
-gdn_status gdn_forward_workspace_size(const gdn_forward_args *args, size_t *bytes) {
-    if (!bytes) return GDN_ERR_NULL;
-    const gdn_status st = check_sizes(args);
-    if (st != GDN_OK) return st;
-    *bytes = wants_chunked(args) ? gdn::chunked_wy_workspace_bytes(args->num_seqs, args->total_tokens,
-                                                                   args->num_k_heads, args->num_v_heads)
-                                 : 0;
-    return GDN_OK;
-}
-
-gdn_status gdn_forward(const gdn_forward_args *a, gdn_stream_t stream) {
+gdn_status forward_impl(const gdn_forward_args *a, int dense_S, gdn_stream_t stream) {
     gdn::ForwardParams p{};
-    const gdn_status st = resolve_forward(a, &p);
+    const gdn_status st = resolve_forward(a, dense_S, &p);
     if (st != GDN_OK || a->num_seqs == 0) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     bool chunked = wants_chunked(a);
@@ -176,6 +154,61 @@ gdn_status gdn_forward(const gdn_forward_args *a, gdn_stream_t stream) {
         p.max_len = gdn::RECURRENT_MAX_LEN;
     }
     if (gdn::launch_recurrent(p, s) != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_status_string(gdn_status status) {
+    switch (status) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_NULL: return "a required pointer is NULL";
+        case GDN_ERR_DTYPE: return "unsupported I/O dtype (FP16 and FP32 only; BF16 is rejected)";
+        case GDN_ERR_SHAPE: return "inconsistent or unsupported sizes";
+        case GDN_ERR_ALIGN: return "a state pointer is not 16-byte aligned";
+        case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+        case GDN_ERR_CUDA: return "CUDA launch error";
+        case GDN_ERR_UNSUPPORTED: return "the forced plan does not support these sizes";
+        case GDN_ERR_ARG: return "invalid argument value (unknown enum, cu_seqlens given to the rank-4 call, or overlapping buffers)";
+    }
+    return "unknown status";
+}
+
+gdn_status gdn_forward_workspace_size(const gdn_forward_args *args, size_t *bytes) {
+    if (!bytes) return GDN_ERR_NULL;
+    const gdn_status st = check_sizes(args);
+    if (st != GDN_OK) return st;
+    *bytes = wants_chunked(args) ? gdn::chunked_wy_workspace_bytes(args->num_seqs, args->total_tokens,
+                                                                   args->num_k_heads, args->num_v_heads)
+                                 : 0;
+    return GDN_OK;
+}
+
+gdn_status gdn_forward(const gdn_forward_args *a, gdn_stream_t stream) { return forward_impl(a, -1, stream); }
+
+gdn_status gdn_forward_dense(const gdn_forward_args *args, int32_t seq_len, gdn_stream_t stream) {
+    if (!args) return GDN_ERR_NULL;
+    if (args->cu_seqlens) return GDN_ERR_ARG;  // rank-4 inputs carry their lengths in seq_len
+    if (seq_len < 0 || (int64_t)args->num_seqs * seq_len != (int64_t)args->total_tokens) return GDN_ERR_SHAPE;
+    gdn_forward_args a = *args;
+    // every sequence has seq_len tokens: a tighter bound than the caller's hint
+    if (a.max_seqlen == 0 || a.max_seqlen > seq_len) a.max_seqlen = seq_len;
+    return forward_impl(&a, seq_len, stream);
+}
+
+gdn_status gdn_state_transpose(const float *src, float *dst, int64_t num_matrices, int32_t rows, int32_t cols,
+                               gdn_stream_t stream) {
+    if (num_matrices < 0 || rows < 0 || cols < 0) return GDN_ERR_SHAPE;
+    if (num_matrices == 0 || rows == 0 || cols == 0) return GDN_OK;
+    if (!src || !dst) return GDN_ERR_NULL;
+    const int64_t bytes = num_matrices * (int64_t)rows * cols * 4;
+    const char *s0 = reinterpret_cast<const char *>(src), *d0 = reinterpret_cast<const char *>(dst);
+    if (s0 < d0 + bytes && d0 < s0 + bytes) return GDN_ERR_ARG;  // source and destination overlap
+    if (gdn::launch_transpose(src, dst, num_matrices, rows, cols, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return GDN_ERR_CUDA;
     return GDN_OK;
 }
 

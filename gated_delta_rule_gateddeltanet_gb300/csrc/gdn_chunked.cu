@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
         if (item >= n_items) break;
         const int b = ws[2 + item / p.Hv], h = item % p.Hv, kh = h / p.r;
-        const int bos = p.cu[b], eos = p.cu[b + 1];
+        const int bos = seq_start(p.cu, p.dense_S, b), eos = seq_start(p.cu, p.dense_S, b + 1);
         const int slot = p.slots ? p.slots[b] : b;
         if (slot < 0 || slot >= p.num_slots) {
             if (tid == 0 && h == 0) flag_error(p.status, GDN_DEVERR_STATE_SLOT);
@@ -671,14 +671,15 @@ __global__ void __launch_bounds__(NT, 1)
 // sort on the number of chunks).  Sequences with a bad packing are left out
 // (the recurrent kernel reports them).
 constexpr int PLAN_BINS = 1024;
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *cu, int B, int T, int min_len, int32_t *ws) {
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *cu, int dense_S, int B, int T, int min_len,
+                                                    int32_t *ws) {
     __shared__ int hist[PLAN_BINS];
     __shared__ int total;
     const int tid = threadIdx.x;
     for (int i = tid; i < PLAN_BINS; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     auto key = [&](int b) -> int {
-        const int lo = cu[b], hi = cu[b + 1];
+        const int lo = seq_start(cu, dense_S, b), hi = seq_start(cu, dense_S, b + 1);
         if (lo < 0 || hi < lo || hi > T || hi - lo <= min_len) return -1;
         const int chunks = min((hi - lo + CH - 1) / CH, PLAN_BINS - 1);
         return PLAN_BINS - 1 - chunks;  // descending length
@@ -729,7 +730,7 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStre
             !encode_rows_f16(&mv, p.v, (long long)p.Hv * DH, p.v_stride, p.T, DH, CH, false))
             return cudaErrorInvalidValue;
     }
-    plan_kernel<<<1, 1024, 0, stream>>>(p.cu, p.B, p.T, min_len, ws);
+    plan_kernel<<<1, 1024, 0, stream>>>(p.cu, p.dense_S, p.B, p.T, min_len, ws);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto kern = chunked_kernel<TIO>;

@@ -89,7 +89,8 @@ long long max_chunks(int B, int T) { return (long long)T / CH + B; }
 // are left out (the recurrent kernel reports them).
 constexpr int PLAN_BINS = 1024;
 constexpr int PLAN_NT = 1024;
-__global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int B, int T, int min_len, int32_t *ws) {
+__global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int dense_S, int B, int T, int min_len,
+                                                          int32_t *ws) {
     __shared__ int hist[PLAN_BINS];
     __shared__ int warp_sum[PLAN_NT / 32];
     __shared__ int total;
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int
     // chunks of sequence b on this path (an empty sequence has none but is still
     // listed: its final state is its initial state), or -1 when it is not
     auto chunks_of = [&](int b) -> int {
-        const int lo = cu[b], hi = cu[b + 1];
+        const int lo = seq_start(cu, dense_S, b), hi = seq_start(cu, dense_S, b + 1);
         if (lo < 0 || hi < lo || hi > T || hi - lo <= min_len) return -1;
         return (hi - lo + CH - 1) / CH;
     };
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(PT, 4)
         else hi = mid;
     }
     const int b = lo;
-    const int bos = p.cu[b], eos = p.cu[b + 1];
+    const int bos = seq_start(p.cu, p.dense_S, b), eos = seq_start(p.cu, p.dense_S, b + 1);
     const int t0 = bos + CH * (g - cbase[b]);
     const int n = min(CH, eos - t0);
 
@@ -700,7 +701,7 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
         if (item >= n_items) break;
         const int b = ws[2 + item / p.Hv], h = item % p.Hv, kh = h / p.r;
-        const int bos = p.cu[b], eos = p.cu[b + 1];
+        const int bos = seq_start(p.cu, p.dense_S, b), eos = seq_start(p.cu, p.dense_S, b + 1);
         const int nc = (eos - bos + CH - 1) / CH;
         const long long gbase = cbase[b];
         const int slot = p.slots ? p.slots[b] : b;
@@ -939,7 +940,7 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, uint8_t *ws, cudaStre
     const long long maxch = max_chunks(p.B, p.T);
     uint8_t *krec = ws + header_bytes(p.B);
     uint8_t *vrec = krec + (size_t)maxch * p.Hk * KREC_BYTES;
-    wy_plan_kernel<<<1, PLAN_NT, 0, stream>>>(p.cu, p.B, p.T, min_len, hdr);
+    wy_plan_kernel<<<1, PLAN_NT, 0, stream>>>(p.cu, p.dense_S, p.B, p.T, min_len, hdr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long prep_ctas = maxch * p.Hk;

@@ -29,7 +29,15 @@ struct ForwardParams {
     int32_t *status;
     // Sequences with more tokens than this are left to the chunked kernel.
     int max_len;
+    // Rank-4 [B, S, H, D] inputs: cu is null and sequence b owns tokens
+    // [b S, (b + 1) S) with S = dense_S.  0 for packed inputs.
+    int dense_S;
 };
+
+// First token of sequence b (b may be B: one past the last sequence).
+__host__ __device__ __forceinline__ int seq_start(const int32_t *cu, int dense_S, int b) {
+    return cu ? cu[b] : b * dense_S;
+}
 
 struct ReplayParams {
     int R, Hk, Hv, dk, dv, r, num_slots, cap;
@@ -65,6 +73,8 @@ cudaError_t launch_conv(const ConvParams &p, cudaStream_t stream);
 cudaError_t launch_conv_replay(const ConvReplayParams &p, cudaStream_t stream);
 
 cudaError_t launch_recurrent(const ForwardParams &p, cudaStream_t stream);
+// dst[m] = src[m]^T for `num` row-major rows x cols FP32 matrices.
+cudaError_t launch_transpose(const float *src, float *dst, long long num, int rows, int cols, cudaStream_t stream);
 cudaError_t launch_replay(const ReplayParams &p, cudaStream_t stream);
 
 // Chunked tensor-core path: sequences with more than `min_len` tokens

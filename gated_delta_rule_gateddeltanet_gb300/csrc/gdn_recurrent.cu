@@ -66,8 +66,8 @@ __global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p)
     const int l = lane % LPR, grp = lane / LPR;
     const bool leader = (rb == 0 && h == 0 && tid == 0);
 
-    if (b == 0 && leader && (p.cu[0] != 0 || p.cu[p.B] != p.T)) flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
-    const int bos = p.cu[b], eos = p.cu[b + 1];
+    if (p.cu && b == 0 && leader && (p.cu[0] != 0 || p.cu[p.B] != p.T)) flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
+    const int bos = seq_start(p.cu, p.dense_S, b), eos = seq_start(p.cu, p.dense_S, b + 1);
     if (bos < 0 || eos < bos || eos > p.T) {
         if (leader) flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
         return;

@@ -43,7 +43,8 @@ typedef enum gdn_status {
     GDN_ERR_WORKSPACE = 5,   /* workspace missing or smaller than gdn_forward_workspace_size */
     GDN_ERR_CUDA = 6,        /* the CUDA runtime reported an error at launch */
     GDN_ERR_UNSUPPORTED = 7, /* a forced plan that these sizes do not support */
-    GDN_ERR_ARG = 8          /* an enum field holds an unknown value */
+    GDN_ERR_ARG = 8          /* an enum field holds an unknown value, or another argument value is
+                                invalid for the call (see each entry point) */
 } gdn_status;
 
 /* I/O dtypes of q, k, v and output.  Gates and states are always FP32. */
@@ -177,6 +178,40 @@ gdn_status gdn_forward_workspace_size(const gdn_forward_args *args, size_t *byte
  * Asynchronous on `stream`.
  */
 gdn_status gdn_forward(const gdn_forward_args *args, gdn_stream_t stream);
+
+/*
+ * gdn_forward on rank-4 (dense) inputs.
+ *
+ * Source: "[CUDA] Add compact GatedDeltaNet operator" (Description) supports
+ * ragged and rank-4 inputs; "Add GatedDeltaNet evaluation export for Qwen
+ * hybrid models" (Copilot overview, builder review) describes the dense
+ * layout [B, S, ...] next to the packed token-major one.
+ *
+ * The batch is num_seqs sequences of exactly seq_len tokens each:
+ *   q, k [B, S, Hk, dk], v [B, S, Hv, dv], a, b [B, S, Hv], output
+ *   [B, S, Hv, dv] -- in memory the same as the packed layouts with
+ *   T = B * S tokens, so strides and every other field mean what they mean
+ *   for gdn_forward.  args->cu_seqlens must be NULL (GDN_ERR_ARG otherwise);
+ *   args->total_tokens must equal num_seqs * seq_len (GDN_ERR_SHAPE).
+ * The state is V-major [slots, Hv, dv, dk] as everywhere in this library;
+ * callers that keep the dense export's K-major state [.., dk, dv] convert it
+ * with gdn_state_transpose before and after the call.  Workspace: as
+ * gdn_forward_workspace_size reports for these arguments.  Results are
+ * bitwise those of gdn_forward with cu_seqlens = {0, S, 2S, ..., B S}.
+ */
+gdn_status gdn_forward_dense(const gdn_forward_args *args, int32_t seq_len, gdn_stream_t stream);
+
+/*
+ * dst[m] = src[m]^T for num_matrices row-major rows x cols FP32 matrices
+ * (device pointers, packed one after another).  Converts recurrent states
+ * between the K-major layout of the dense export, [.., dk, dv], and the
+ * V-major layout of the packed operator, [.., dv, dk] ("Add GatedDeltaNet
+ * evaluation export for Qwen hybrid models", builder review): K-major to
+ * V-major is rows = dk, cols = dv; back is rows = dv, cols = dk.  src and dst
+ * must not overlap (GDN_ERR_ARG).  Asynchronous on `stream`.
+ */
+gdn_status gdn_state_transpose(const float *src, float *dst, int64_t num_matrices, int32_t rows, int32_t cols,
+                               gdn_stream_t stream);
 
 /*
  * Replays an accepted prefix of capsules into an inactive state bank.

@@ -227,3 +227,26 @@ def test_conv_replay_rejects_bad_arguments(lib):
     assert f(None, 4, 2, 10240, 4, 1, fake, fake, fake, 4, fake, None, None) == 1
     assert f(fake, 4, 2, 10240, 4, 1, fake, fake, None, 4, fake, None, None) == 1
     assert f(fake, 4, 0, 10240, 4, 1, None, None, None, 0, None, None, None) == 0
+
+
+def test_dense_and_transpose_reject_bad_arguments_before_launch(lib):
+    # rank-4 entry point: cu_seqlens must be absent, and B * S must equal T
+    a = _args(num_seqs=2, total_tokens=8)
+    assert lib.gdn_forward_dense(ctypes.byref(a), 4, None) == 8          # cu_seqlens given
+    a.cu_seqlens = None
+    assert lib.gdn_forward_dense(ctypes.byref(a), 3, None) == 3          # 2 x 3 != 8
+    assert lib.gdn_forward_dense(ctypes.byref(a), -1, None) == 3
+    assert lib.gdn_forward_dense(None, 4, None) == 1
+    a = _args(num_seqs=2, total_tokens=8, io_dtype=2)
+    a.cu_seqlens = None
+    assert lib.gdn_forward_dense(ctypes.byref(a), 4, None) == 2          # BF16 still rejected
+    a = _args(num_seqs=0, total_tokens=0)
+    a.cu_seqlens = None
+    assert lib.gdn_forward_dense(ctypes.byref(a), 5, None) == 0          # empty batch: nothing to do
+    # state transpose
+    P = ctypes.c_void_p
+    assert lib.gdn_state_transpose(P(0x1000), P(0x100000), -1, 128, 128, None) == 3
+    assert lib.gdn_state_transpose(P(0x1000), P(0x100000), 0, 128, 128, None) == 0   # nothing to move
+    assert lib.gdn_state_transpose(None, P(0x100000), 4, 128, 128, None) == 1
+    # 4 matrices of 128 x 128 floats = 256 KiB: destinations inside that range overlap the source
+    assert lib.gdn_state_transpose(P(0x100000), P(0x100000 + 4096), 4, 128, 128, None) == 8
