@@ -263,6 +263,7 @@ def run_gdn(a, dist: Dist):
         extra["causal_conv"] = run_conv(dev, stream)
         extra["serving_mix"] = run_serving_mix(dev, stream, lib, sh)
         extra["state_transpose"] = run_transpose(dev, stream, lib, sh)
+        extra["spec_step_graph"] = run_spec_step(dev, stream)
 
     cpu = None
     if not a.no_cpu and dist.rank == 0 and dist.world == 1:
@@ -635,6 +636,47 @@ def run_transpose(dev, stream, lib, sh):
     return {"workload": "state layout conversion: 3072 matrices of 128 x 128 fp32 (the decode pool), 4 rotating pairs",
             "us": round(us, 2), "gbs": round(nbytes / (us / 1e6) / 1e9, 1),
             "frac_hbm": round(nbytes / (us / 1e6) / 1e9 / hbm, 4)}
+
+
+def run_spec_step(dev, stream):
+    """A whole speculative step of one layer (conv with capture -> gdn_forward
+    with capsules on the fused q|k|v view -> conv replay -> GDN replay),
+    16 requests x 4 drafts at the Qwen geometry, launched eagerly through the
+    C ABI with prebuilt arguments vs replayed from one CUDA graph."""
+    import torch
+    from gated_delta_rule_gateddeltanet_gb300.spec_step import SpeculativeStep
+    from gated_delta_rule_gateddeltanet_gb300 import workloads as wl
+    R, D, Hk, Hv, d = 16, 4, 16, 48, 128
+    C = 2 * Hk * d + Hv * d
+    inp = wl.spec_verify()
+    g = torch.Generator().manual_seed(11)
+    s = SpeculativeStep(torch.randn((C, 4), generator=g).to(dev), torch.zeros(C, device=dev),
+                        torch.randn((2 * R, C, 3), generator=g).to(torch.float16).to(dev),
+                        torch.from_numpy(inp.A_log).to(dev), torch.from_numpy(inp.dt_bias).to(dev),
+                        torch.randn((2 * R, Hv, d, d), generator=g).mul_(0.02).to(dev), num_k_heads=Hk, drafts=D)
+    s.x.copy_(torch.randn((R * D, C), generator=g).to(torch.float16))
+    s.a.copy_(torch.from_numpy(inp.a))
+    s.b.copy_(torch.from_numpy(inp.b))
+    s.accept_len.copy_(torch.from_numpy(inp.extra["accept_len"]))
+    s.capture()
+    res = {}
+    for name, fn in (("eager_us", lambda: s.run_eager(stream)), ("graph_us", s.replay)):
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
+        n = 200
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = round(e0.elapsed_time(e1) / n * 1e3, 2)
+    res["workload"] = ("speculative step of one layer: 16 requests x 4 drafts, conv (10240 channels, capture) + "
+                       "gdn_forward (capsules) + conv replay + GDN replay of U{0..4} accepted tokens; 4 launches "
+                       "eager (prebuilt C-ABI arguments) vs one CUDA-graph replay")
+    res["tokens_per_s_graph"] = round(R * D / (res["graph_us"] / 1e6), 1)
+    return res
 
 
 # ---------------------------------------------------------------- CPU oracle (baseline and reference arm)
