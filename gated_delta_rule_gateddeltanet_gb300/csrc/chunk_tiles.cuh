@@ -1,7 +1,7 @@
 // Tile helpers shared by the tensor-core chunked kernels: the byte layout of
 // K-major fp16 operand tiles in the 128-byte swizzled canonical form that
 // tcgen05 shared-memory descriptors describe, vector conversions into such
-// tiles, and FP32-accurate warp-level products for the small blocks of the
+// tiles, and warp-level TF32 products for the small blocks of the
 // triangular inverse.
 #pragma once
 
@@ -46,24 +46,21 @@ __device__ __forceinline__ void ld4<__half>(const __half *p, float (&v)[4]) {
 }
 
 
-// ---- FP32-accurate small products on the warp-level tensor cores
+// ---- Small products on the warp-level tensor cores
 //
 // The block products of the triangular inverse are 16 x 16 and 32 x 32: too
 // small for tcgen05 (M >= 64) and, on the CUDA cores, bound by shared-memory
-// traffic.  They run as mma.sync m16n8k8 TF32 products with each operand split
-// into a TF32 high part and a TF32 remainder (x = hi + lo), accumulating
-// hi*hi + hi*lo + lo*hi in FP32: the dropped lo*lo term is ~2^-22 relative, so
-// the result is as accurate as an FP32 product.
+// traffic.  They run as mma.sync m16n8k8 TF32 products (10-bit mantissas, FP32
+// accumulation).  The inverse only feeds the tensor cores as an fp16 operand
+// (also a 10-bit mantissa), and at the full varlen prefill (15,991 tokens)
+// TF32 products gave the same end-to-end error against the FP64 oracle as
+// FP32-accurate split products (output 8.10e-4, state 5.77e-4 vs 5.80e-4
+// max-relative): the fp16 operand roundings dominate.
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
     return r;
-}
-
-__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    hi = to_tf32(x);
-    lo = to_tf32(x - __uint_as_float(hi));
 }
 
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
@@ -86,15 +83,13 @@ __device__ __forceinline__ void warp_tile_16x8(const float *X_, int xs, const fl
     float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k0 = 0; k0 < K; k0 += 8) {
-        uint32_t ah[4], al[4], bh[2], bl[2];
-        split_tf32(X_[g * xs + k0 + t], ah[0], al[0]);
-        split_tf32(X_[(g + 8) * xs + k0 + t], ah[1], al[1]);
-        split_tf32(X_[g * xs + k0 + t + 4], ah[2], al[2]);
-        split_tf32(X_[(g + 8) * xs + k0 + t + 4], ah[3], al[3]);
-        split_tf32(Y_[(k0 + t) * ys + g], bh[0], bl[0]);
-        split_tf32(Y_[(k0 + t + 4) * ys + g], bh[1], bl[1]);
-        mma_tf32(d, al, bh);
-        mma_tf32(d, ah, bl);
+        uint32_t ah[4], bh[2];
+        ah[0] = to_tf32(X_[g * xs + k0 + t]);
+        ah[1] = to_tf32(X_[(g + 8) * xs + k0 + t]);
+        ah[2] = to_tf32(X_[g * xs + k0 + t + 4]);
+        ah[3] = to_tf32(X_[(g + 8) * xs + k0 + t + 4]);
+        bh[0] = to_tf32(Y_[(k0 + t) * ys + g]);
+        bh[1] = to_tf32(Y_[(k0 + t + 4) * ys + g]);
         mma_tf32(d, ah, bh);
     }
     C_[g * cs + 2 * t] = sign * d[0];

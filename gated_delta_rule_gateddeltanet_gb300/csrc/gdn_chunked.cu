@@ -30,8 +30,9 @@
 //   MMA5  (U^T diag) K         accumulated onto gamma_last S0 -> S1 (128 x 128, K = n)
 // The FP32 state lives in tensor memory for the whole chain (128 columns);
 // its fp16 copy for MMA2 is rebuilt from it every chunk.  The triangular
-// inverse runs on the CUDA cores in FP32 (16 x 16 diagonal blocks by forward
-// substitution, then two levels of block combination).
+// inverse is stored in FP32: 16 x 16 diagonal blocks by forward substitution
+// on the CUDA cores, then two levels of block combination as warp-level TF32
+// products.
 //
 // Staging: with fp16 I/O the q, k and v rows of the next chunk arrive by three
 // 2-D TMA copies (tensor maps over the packed [T, heads * 128] arrays, one

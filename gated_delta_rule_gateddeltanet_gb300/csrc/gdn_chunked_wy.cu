@@ -26,7 +26,7 @@
 //    ises q and k, forms the [Q;K] and K^T fp16 operand tiles, runs
 //    [Q;K] K^T on the tensor cores (P = QK^T and G = KK^T, shared by the key
 //    head's value heads), and for each of its value heads computes the gates,
-//    A, P o D and the FP32 triangular inverse T.  It writes byte images of the
+//    A, P o D and the triangular inverse T.  It writes byte images of the
 //    operand tiles, already in the swizzled shared-memory layout the MMAs
 //    read, to the caller's workspace (one 48 KiB record per (chunk, key head),
 //    one 17 KiB record per (chunk, value head)), plus the capsule's k and g.
@@ -167,8 +167,8 @@ __global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int
 // T = (I + A)^-1 in full.  The four 16 x 16 diagonal blocks come from forward
 // substitution (one column per thread); the off-diagonal blocks from the block
 // identity [[L11, 0], [L21, L22]]^-1 = [[T11, 0], [-T22 L21 T11, T22]], first
-// inside the two 32 x 32 diagonal blocks, then for the lower-left quadrant.
-// Each block of A is read (into the product M = L21 T11) before the block of
+// inside the two 32 x 32 diagonal blocks, then for the lower-left quadrant
+// (warp-level TF32 products, FP32 storage).  Each block of A is read (into the product M = L21 T11) before the block of
 // T that replaces it is written.  256 threads; ends with a barrier.
 // Row strides (floats): AS = 68 makes the warp-level product loads of the A / T
 // blocks conflict-free (rows land 4 banks apart); MS = 40 does the same for the

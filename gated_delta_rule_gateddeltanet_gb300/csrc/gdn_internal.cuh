@@ -130,17 +130,23 @@ __device__ __forceinline__ float warp_sum(float x) {
 // softplus(x) = log(1 + e^x), evaluated without overflow.
 __device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
 
-// Effective decay and beta of one (token, value head).
-__device__ __forceinline__ void gates(const ForwardParams &p, long long t, int h, float &g, float &beta) {
-    const float av = p.a[t * p.Hv + h];
-    const float bv = p.b[t * p.Hv + h];
-    if (p.gate_raw) {
-        g = expf(-expf(p.A_log[h]) * softplus_f(av + p.dt_bias[h]));
+// Effective decay and beta from one (token, value head)'s gate inputs: raw
+// (a, b, A_log, dt_bias) or precomputed (a = g, b = beta).
+__device__ __forceinline__ void gates_from(int raw, float av, float bv, float A_log, float dt_bias, float &g,
+                                           float &beta) {
+    if (raw) {
+        g = expf(-expf(A_log) * softplus_f(av + dt_bias));
         beta = 1.f / (1.f + expf(-bv));
     } else {
         g = av;
         beta = bv;
     }
+}
+
+// Effective decay and beta of one (token, value head).
+__device__ __forceinline__ void gates(const ForwardParams &p, long long t, int h, float &g, float &beta) {
+    gates_from(p.gate_raw, p.a[t * p.Hv + h], p.b[t * p.Hv + h], p.gate_raw ? p.A_log[h] : 0.f,
+               p.gate_raw ? p.dt_bias[h] : 0.f, g, beta);
 }
 
 }  // namespace gdn

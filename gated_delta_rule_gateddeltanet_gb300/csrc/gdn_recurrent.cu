@@ -108,28 +108,59 @@ __global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p)
 
     for (int t0 = bos; t0 < eos; t0 += TB) {
         const int nt = min(TB, eos - t0);
-        // ---- stage: normalised q and k, k.q and gates; one warp per token
-        if (warp < nt) {
+        // ---- stage: every global load of the round is issued first (v entries of
+        //      the tile's rows, q and k rows, gate inputs), then the normalised q
+        //      and k, k.q and the gates (one warp per token)
+        constexpr int VPT = (TB * ROWS + NT - 1) / NT;
+        float vreg[VPT];
+#pragma unroll
+        for (int m = 0; m < VPT; ++m) {
+            const int i = tid + m * NT, tt = i / ROWS, rr = i % ROWS;
+            vreg[m] = (i < nt * ROWS && rr < rows_here)
+                          ? to_f32(vg[(long long)(t0 + tt) * p.v_stride + (long long)h * p.dv + rb * ROWS + rr])
+                          : 0.f;
+        }
+        const bool stager = warp < nt;
+        float qv[EPL], kv[EPL];
+        float ga = 0.f, gb = 0.f, gA = 0.f, gd = 0.f;
+        if (stager) {
             const long long t = t0 + warp;
             const TIO *qp = qg + t * p.q_stride + (long long)kh * DK + lane * EPL;
             const TIO *kp = kg + t * p.k_stride + (long long)kh * DK + lane * EPL;
-            float qv[EPL], kv[EPL];
-            float sq = 0.f, sk = 0.f;
 #pragma unroll
             for (int e = 0; e < EPL; ++e) {
                 qv[e] = to_f32(qp[e]);
                 kv[e] = to_f32(kp[e]);
+            }
+            if (lane == 0) {
+                ga = p.a[t * p.Hv + h];
+                gb = p.b[t * p.Hv + h];
+                if (p.gate_raw) {
+                    gA = p.A_log[h];
+                    gd = p.dt_bias[h];
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < VPT; ++m) {
+            const int i = tid + m * NT;
+            if (i < nt * ROWS) v_s[i / ROWS][i % ROWS] = vreg[m];
+        }
+        if (stager) {
+            float sq = 0.f, sk = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
                 sq = fmaf(qv[e], qv[e], sq);
                 sk = fmaf(kv[e], kv[e], sk);
             }
             sq = warp_sum(sq);
             sk = warp_sum(sk);
-            const float nq = fmaxf(sqrtf(sq), EPS), nk = fmaxf(sqrtf(sk), EPS);
+            const float iq = 1.f / fmaxf(sqrtf(sq), EPS), ik = 1.f / fmaxf(sqrtf(sk), EPS);
             float kq = 0.f;
 #pragma unroll
             for (int e = 0; e < EPL; ++e) {
-                qv[e] = qv[e] / nq;
-                kv[e] = kv[e] / nk;
+                qv[e] *= iq;
+                kv[e] *= ik;
                 qn_s[warp][lane * EPL + e] = qv[e];
                 kn_s[warp][lane * EPL + e] = kv[e];
                 kq = fmaf(qv[e], kv[e], kq);
@@ -137,17 +168,11 @@ __global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p)
             kq = warp_sum(kq);
             if (lane == 0) {
                 float g, beta;
-                gates(p, t, h, g, beta);
+                gates_from(p.gate_raw, ga, gb, gA, gd, g, beta);
                 g_s[warp] = g;
                 beta_s[warp] = beta;
                 kq_s[warp] = kq;
             }
-        }
-        for (int i = tid; i < nt * ROWS; i += NT) {
-            const int tt = i / ROWS, rr = i % ROWS;
-            v_s[tt][rr] = rr < rows_here
-                              ? to_f32(vg[(long long)(t0 + tt) * p.v_stride + (long long)h * p.dv + rb * ROWS + rr])
-                              : 0.f;
         }
         __syncthreads();
         if (tile_pending) {
