@@ -20,7 +20,7 @@ import torch
 
 from .build import LIB as LIB_PATH
 
-__all__ = ["gdn_forward", "gdn_forward_dense", "state_transpose", "gdn_forward_no_alloc", "gdn_replay_prefix", "varlen_causal_conv_with_state",
+__all__ = ["gdn_forward", "ForwardCall", "gdn_forward_dense", "state_transpose", "gdn_forward_no_alloc", "gdn_replay_prefix", "varlen_causal_conv_with_state",
            "causal_conv_replay_prefix", "GdnError", "load_library", "capsule_width",
            "STATUS", "DEVERR", "PLAN"]
 
@@ -251,6 +251,36 @@ def gdn_forward(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, gate_mod
     if rc != 0:
         raise GdnError(rc, "gdn_forward")
     return outs
+
+
+class ForwardCall:
+    """A gdn_forward call whose arguments are resolved once: the same device
+    buffers (inputs, states, outputs, workspace) serve every launch, and
+    ``launch()`` is a single C-ABI call with no argument marshalling.  Suits a
+    serving loop that refills fixed input buffers every step (e.g. by copies
+    from pinned host memory) and calls the operator on them.  Arguments as for
+    ``gdn_forward``; the tensors must stay alive and in place while the object
+    is used.  ``outputs`` is ``(output, final_state, state_update)``."""
+
+    def __init__(self, q, k, v, a, b, cu_seqlens, **kw):
+        workspace = kw.pop("workspace", None)
+        self.args, self.outputs, keep = build_forward_args(q, k, v, a, b, cu_seqlens, workspace=workspace, **kw)
+        need = workspace_size(self.args)
+        if need > 0 and workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            self.args.workspace, self.args.workspace_bytes = ctypes.c_void_p(workspace.data_ptr()), need
+        self._keep = keep + (workspace,)
+        self._lib = load_library()
+        self._ref = ctypes.byref(self.args)
+        self._device = q.device
+
+    def launch(self, stream=None):
+        """Runs the call on ``stream`` (a torch.cuda.Stream; default: the current stream)."""
+        h = ctypes.c_void_p((stream or torch.cuda.current_stream(self._device)).cuda_stream)
+        rc = self._lib.gdn_forward(self._ref, h)
+        if rc != 0:
+            raise GdnError(rc, "gdn_forward")
+        return self.outputs
 
 
 def gdn_forward_dense(q, k, v, a, b, *, workspace=None, **kw):
