@@ -283,10 +283,11 @@ __device__ __forceinline__ void chunk_gates(const ForwardParams &p, int t0, int 
     }
 }
 
-// Sixteen consecutive floats from 16-byte aligned shared memory (four 16-byte loads).
-__device__ __forceinline__ void ld_f16x(const float *src, float (&x)[16]) {
+// N consecutive floats (N a multiple of 4) from 16-byte aligned shared memory.
+template <int N>
+__device__ __forceinline__ void ld_fn(const float *src, float (&x)[N]) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < N / 4; ++q) {
         const float4 v = reinterpret_cast<const float4 *>(src)[q];
         x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
     }
@@ -605,7 +606,10 @@ __global__ void __launch_bounds__(PT, 4)
 
 // ---------------------------------------------------------------- phase 2: per (sequence, value head) chain
 
-constexpr int NT = 512;  // 16 warps: four per tensor-memory lane quarter
+constexpr int NT = 512;  // 16 warps: four per tensor-memory lane quarter (32 warps measured slower)
+// Columns a thread handles of a 64-column (CW) and of a 128-column (CS) region.
+constexpr int CW = 64 / (NT / 128), CS = 2 * CW;
+static_assert(CW % 8 == 0, "16-byte tile stores need 8-column pieces");
 constexpr int TMEM_COLS = 512;
 // Tensor-memory columns (128 lanes each).  MMA2's result is double-buffered
 // so that chunk c - 1's outputs are read while chunk c's MMA2 runs.
@@ -639,11 +643,11 @@ __global__ void __launch_bounds__(NT, 1)
     __shared__ __align__(16) float gam_prev[CH];  // gamma of the chunk whose outputs are pending
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Tensor memory: a warp reaches only the 32 lanes of its quarter (warp % 4);
-    // the four warps of a quarter split the columns.
+    // the NT / 128 warps of a quarter split the columns.
     const int quarter = warp & 3, cq = warp >> 2;
     const int row = quarter * 32 + lane;  // the tensor-memory lane (state / output row) of this thread
     const uint32_t lane_sel = (uint32_t)(quarter * 32) << 16;
-    const int c16 = cq * 16, c32 = cq * 32;
+    const int c16 = cq * CW, c32 = cq * CS;  // this thread's first column of a 64- / 128-column region
 
     if (warp == 0) {
         ptx::tmem_alloc(&tmem_base, TMEM_COLS);
@@ -726,30 +730,30 @@ __global__ void __launch_bounds__(NT, 1)
         bool state_live = p.init != nullptr;
         auto build_s16 = [&](const float *F, int n) {
             const float gl = F[F_GAMMA + n - 1];
-            float v[32];
+            float v[CS];
             if (state_live) {
-                ptx::tmem_ld32(tm + lane_sel + TM_S + c32, v);
+                ptx::tmem_ld<CS>(tm + lane_sel + TM_S + c32, v);
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                for (int j = 0; j < CS; ++j) v[j] = 0.f;
             }
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) st_h8(sm + OFF_S16, sw(row, c32 + j, 128), v + j);
+            for (int j = 0; j < CS; j += 8) st_h8(sm + OFF_S16, sw(row, c32 + j, 128), v + j);
             if (state_live) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] *= gl;
-                ptx::tmem_st32(tm + lane_sel + TM_S + c32, v);
+                for (int j = 0; j < CS; ++j) v[j] *= gl;
+                ptx::tmem_st<CS>(tm + lane_sel + TM_S + c32, v);
                 ptx::tmem_st_wait();
             }
         };
         // outputs of the chunk starting at tp (n tokens): o = scale (gamma O' + Y)
         auto write_outputs = [&](int tp, int n, uint32_t ox) {
-            float o1[16], y[16], gm[16];
-            ptx::tmem_ld16(tm + lane_sel + ox + c16, o1);
-            ptx::tmem_ld16(tm + lane_sel + TM_Y + c16, y);
-            ld_f16x(gam_prev + c16, gm);
+            float o1[CW], y[CW], gm[CW];
+            ptx::tmem_ld<CW>(tm + lane_sel + ox + c16, o1);
+            ptx::tmem_ld<CW>(tm + lane_sel + TM_Y + c16, y);
+            ld_fn<CW>(gam_prev + c16, gm);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < CW; ++j) {
                 const int s = c16 + j;
                 if (s < n)
                     og[((long long)(tp + s) * p.Hv + h) * DH + row] = from_f32<TIO>(p.scale * fmaf(gm[j], o1[j], y[j]));
@@ -759,13 +763,13 @@ __global__ void __launch_bounds__(NT, 1)
         // ---- chain start: the initial state into tensor memory, chunk 0's inputs
         if (state_live) {
             const float *src = p.init + head_off + (size_t)row * DH + c32;
-            float v[32];
+            float v[CS];
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
+            for (int j = 0; j < CS; j += 4) {
                 const float4 x = *reinterpret_cast<const float4 *>(src + j);
                 v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
             }
-            ptx::tmem_st32(tm + lane_sel + TM_S + c32, v);
+            ptx::tmem_st<CS>(tm + lane_sel + TM_S + c32, v);
             ptx::tmem_st_wait();
         }
         if (nc > 0) {
@@ -798,13 +802,13 @@ __global__ void __launch_bounds__(NT, 1)
             if (!mma_wait()) { failed = true; break; }
             // ---- R^T = diag(beta) V - diag(beta gamma) X^T, transposed; this chunk's gamma for its outputs
             {
-                float x[16];
-                ptx::tmem_ld16(tm + lane_sel + ox + 64 + c16, x);
-                float be[16], bg[16];
-                ld_f16x(F + F_BETA + c16, be);
-                ld_f16x(F + F_BG + c16, bg);
+                float x[CW];
+                ptx::tmem_ld<CW>(tm + lane_sel + ox + 64 + c16, x);
+                float be[CW], bg[CW];
+                ld_fn<CW>(F + F_BETA + c16, be);
+                ld_fn<CW>(F + F_BG + c16, bg);
 #pragma unroll
-                for (int j = 0; j < 16; j += 8) {
+                for (int j = 0; j < CW; j += 8) {
                     float w[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
@@ -831,11 +835,11 @@ __global__ void __launch_bounds__(NT, 1)
             if (!mma_wait()) { failed = true; break; }
             // ---- U^T -> fp16 operands (plain, and decayed to the chunk end in the
             //      v tile, which is free now)
-            float u[16], dc[16];
-            ptx::tmem_ld16(tm + lane_sel + TM_U + c16, u);
-            ld_f16x(F + F_DECAY + c16, dc);
+            float u[CW], dc[CW];
+            ptx::tmem_ld<CW>(tm + lane_sel + TM_U + c16, u);
+            ld_fn<CW>(F + F_DECAY + c16, dc);
 #pragma unroll
-            for (int j = 0; j < 16; j += 8) {
+            for (int j = 0; j < CW; j += 8) {
                 float w[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) w[e] = dc[j + e] * u[j + e];
@@ -857,7 +861,7 @@ __global__ void __launch_bounds__(NT, 1)
             // the capsule deltas while MMA4/5 run
             if (p.caps) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
+                for (int j = 0; j < CW; ++j) {
                     const int s = c16 + j, tl = t0 + s - bos;
                     if (s < n && tl < p.cap)
                         p.caps[((long long)b * p.cap + tl) * p.W + ubase + (long long)h * DH + row] = u[j];
@@ -882,15 +886,15 @@ __global__ void __launch_bounds__(NT, 1)
         {
             ptx::tc_fence_after();
             float *dst = p.final_state + head_off + (size_t)row * DH + c32;
-            float v[32];
+            float v[CS];
             if (state_live) {
-                ptx::tmem_ld32(tm + lane_sel + TM_S + c32, v);
+                ptx::tmem_ld<CS>(tm + lane_sel + TM_S + c32, v);
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                for (int j = 0; j < CS; ++j) v[j] = 0.f;
             }
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
+            for (int j = 0; j < CS; j += 4)
                 *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
         ptx::tc_fence_before();
