@@ -205,3 +205,16 @@ def test_serving_mix_sampled():
     torch.cuda.synchronize()
     assert max_rel(np.array(outs_gpu), np.array(outs_ref)) <= TOL
     assert max_rel(state.double().cpu().numpy()[sample], ref_state) <= TOL
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_chunked_many_sequences(path):
+    """3000 sequences (33 to 200 tokens, one empty) on the chunked path: the
+    planning kernel's longest-first list and per-sequence chunk offsets span
+    many threads and warps of its prefix sum."""
+    rng = np.random.default_rng(214)
+    lengths = rng.integers(33, 201, 3000)
+    lengths[1234] = 0
+    inp = wl.make_inputs(215, lengths, Hk=1, Hv=1, dk=128, dv=128, io_dtype=np.float16, state_std=0.02,
+                         capacity=2)
+    _check(inp, run_gpu(inp, plan="chunked", in_place=False, workspace=_ws(path, inp)), run_oracle(inp))
