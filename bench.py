@@ -510,11 +510,23 @@ def run_spec(dev, stream, lib, sh):
                                                dt_bias=d["dt_bias"], initial_state=pool, final_state=scratch,
                                                state_slots=None, output=d["out"], state_update=caps, capacity=4,
                                                num_state_slots=16, max_seqlen=4)
+        # the same verify writing no final state (its capsules are what the replay needs)
+        args_ns, _, keep_ns = gdn.build_forward_args(d["q"], d["k"], d["v"], d["a"], d["b"], d["cu"],
+                                                     A_log=d["A_log"], dt_bias=d["dt_bias"], initial_state=pool,
+                                                     state_slots=None, output=d["out"], state_update=caps,
+                                                     capacity=4, num_state_slots=16, max_seqlen=4,
+                                                     write_final_state=False)
         d["args"], d["keep"], d["acc"] = args, keep, int(inp.extra["accept_len"].sum())
+        d["args_ns"], d["keep_ns"] = args_ns, keep_ns
         pools.append(d)
 
     def verify(i):
         rc = lib.gdn_forward(ctypes.byref(pools[i % NBUF]["args"]), sh)
+        if rc:
+            raise gdn.GdnError(rc, "gdn_forward")
+
+    def verify_no_state(i):
+        rc = lib.gdn_forward(ctypes.byref(pools[i % NBUF]["args_ns"]), sh)
         if rc:
             raise gdn.GdnError(rc, "gdn_forward")
 
@@ -528,7 +540,7 @@ def run_spec(dev, stream, lib, sh):
             raise gdn.GdnError(rc, "gdn_replay_prefix")
 
     res = {}
-    for name, fn in (("verify", verify), ("replay", replay)):
+    for name, fn in (("verify", verify), ("verify_no_state", verify_no_state), ("replay", replay)):
         for i in range(20):
             fn(i)
         torch.cuda.synchronize()
@@ -548,6 +560,7 @@ def run_spec(dev, stream, lib, sh):
     return {"workload": "spec verify + replay: 16 requests x 4 draft tokens, Hk=16, Hv=48, d=128, fp16, "
                         "capsules for all tokens, replay of U{0..4} accepted into the inactive bank",
             "verify_us": round(res["verify"] * 1e3, 2), "replay_us": round(res["replay"] * 1e3, 2),
+            "verify_no_final_state_us": round(res["verify_no_state"] * 1e3, 2),
             "verify_tokens_per_s": round(64 / (res["verify"] / 1e3), 1),
             "replay_gbs": round(rep_bytes / (res["replay"] / 1e3) / 1e9, 1),
             "replay_frac_hbm": round(rep_bytes / (res["replay"] / 1e3) / 1e9 / hbm_peak, 4),

@@ -145,9 +145,12 @@ def _token_stride(t, name, inner):
 def build_forward_args(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, gate_mode="raw",
                        initial_state=None, final_state=None, state_slots=None, output=None,
                        state_update=None, capacity=0, scale=0.0, plan="auto", status=None,
-                       num_state_slots=None, workspace=None, max_seqlen=0, num_seqs=None):
+                       num_state_slots=None, workspace=None, max_seqlen=0, num_seqs=None,
+                       write_final_state=True):
     """Fill a ForwardArgs struct from tensors; returns (args, outputs, keepalive).
-    ``cu_seqlens=None`` (rank-4 calls) takes the batch size from ``num_seqs``."""
+    ``cu_seqlens=None`` (rank-4 calls) takes the batch size from ``num_seqs``.
+    ``write_final_state=False`` passes no final-state buffer: the kernels then
+    write no state (the returned final_state is None)."""
     dev = q.device
     T, Hk, dk = q.shape
     Hv, dv = v.shape[1], v.shape[2]
@@ -168,7 +171,9 @@ def build_forward_args(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, g
             num_state_slots = final_state.shape[0]
         else:
             num_state_slots = B
-    if final_state is None:
+    if not write_final_state:
+        final_state = None
+    elif final_state is None:
         final_state = (torch.empty if initial_state is not None else torch.zeros)(
             (num_state_slots, Hv, dv, dk), dtype=torch.float32, device=dev)
         if initial_state is not None:
@@ -222,7 +227,7 @@ def workspace_size(args: ForwardArgs) -> int:
 def gdn_forward(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, gate_mode="raw",
                 initial_state=None, final_state=None, state_slots=None, output=None,
                 state_update=None, capacity=0, scale=0.0, plan="auto", status=None,
-                num_state_slots=None, workspace=None, max_seqlen=0):
+                num_state_slots=None, workspace=None, max_seqlen=0, write_final_state=True):
     """Gated delta rule over a packed varlen batch (C ABI ``gdn_forward``).
 
     q, k: [T, Hk, dk] fp16/fp32 CUDA; v: [T, Hv, dv]; a, b: [T, Hv] fp32 (raw
@@ -241,7 +246,7 @@ def gdn_forward(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, gate_mod
                                           final_state=final_state, state_slots=state_slots, output=output,
                                           state_update=state_update, capacity=capacity, scale=scale, plan=plan,
                                           status=status, num_state_slots=num_state_slots, workspace=workspace,
-                                          max_seqlen=max_seqlen)
+                                          max_seqlen=max_seqlen, write_final_state=write_final_state)
     need = workspace_size(args)
     if need > 0 and workspace is None:
         ws = torch.empty(need, dtype=torch.uint8, device=q.device)

@@ -68,11 +68,12 @@ gdn_status resolve_forward(const gdn_forward_args *a, int dense_S, gdn::ForwardP
     const gdn_status st = check_sizes(a);
     if (st != GDN_OK) return st;
     if (a->num_seqs == 0) return GDN_OK;
-    if ((dense_S < 0 && !a->cu_seqlens) || !a->final_state) return GDN_ERR_NULL;
+    if (dense_S < 0 && !a->cu_seqlens) return GDN_ERR_NULL;
     if (a->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->a || !a->b || !a->output)) return GDN_ERR_NULL;
     if (a->gate_mode == GDN_GATES_RAW && (!a->A_log || !a->dt_bias)) return GDN_ERR_NULL;
     if (a->state_update_capacity > 0 && !a->state_update) return GDN_ERR_NULL;
-    if (!aligned16(a->final_state) || (a->initial_state && !aligned16(a->initial_state))) return GDN_ERR_ALIGN;
+    if ((a->final_state && !aligned16(a->final_state)) || (a->initial_state && !aligned16(a->initial_state)))
+        return GDN_ERR_ALIGN;
 
     gdn::ForwardParams p{};
     p.B = a->num_seqs;

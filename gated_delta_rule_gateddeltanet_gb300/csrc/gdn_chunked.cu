@@ -633,8 +633,8 @@ __global__ void __launch_bounds__(NT, 1)
             ptx::tc_fence_after();
         }
         if (failed) break;
-        // ---- chain end: the final state
-        {
+        // ---- chain end: the final state (unless the caller asked for none)
+        if (p.final_state) {
             float *dst = p.final_state + head_off + (size_t)row * DH + c32;
             float v[32];
             if (state_live) {

@@ -882,8 +882,8 @@ __global__ void __launch_bounds__(NT, 1)
             mma_ready();
         }
         if (failed) break;
-        // ---- chain end: the final state
-        {
+        // ---- chain end: the final state (unless the caller asked for none)
+        if (p.final_state) {
             ptx::tc_fence_after();
             float *dst = p.final_state + head_off + (size_t)row * DH + c32;
             float v[CS];

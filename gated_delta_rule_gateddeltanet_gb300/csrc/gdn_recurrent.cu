@@ -278,7 +278,8 @@ __global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p)
             return;
         }
     }
-    // ---- the tile goes back with one bulk store
+    // ---- the tile goes back with one bulk store (unless the caller asked for no final state)
+    if (!p.final_state) return;
     ptx::fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {

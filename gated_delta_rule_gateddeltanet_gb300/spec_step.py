@@ -26,8 +26,9 @@ recorded into a CUDA graph:
 Every per-step quantity is device memory read at replay time (inputs, gate
 inputs, slot lists, accepted lengths), so one graph serves every step: the
 caller writes the step's inputs and accepted lengths, replays, and publishes
-by swapping ``src`` and ``dst`` (``publish()``).  The speculative final states
-of steps 1 and 2 go to scratch pools; the committed bank is never written.
+by swapping ``src`` and ``dst`` (``publish()``).  The speculative final conv
+states go to a scratch pool and the GDN verify writes no final state at all
+(gdn_forward with no final-state buffer); the committed bank is never written.
 """
 from __future__ import annotations
 
@@ -46,7 +47,8 @@ class SpeculativeStep:
     conv_bank: [2R, C, K-1] (io dtype) and gdn_bank: [2R, Hv, d, d] fp32 hold
     the committed and inactive states; ``src``/``dst`` (device int32 [R])
     name each request's committed and inactive slot (initially 0..R-1 and
-    R..2R-1).  Inputs per step: ``x`` [R*D, C], ``a``, ``b`` [R*D, Hv] (raw
+    R..2R-1).  ``keep_verify_state=True`` also writes the verify pass's own
+    final GDN states to ``gdn_scratch``.  Inputs per step: ``x`` [R*D, C], ``a``, ``b`` [R*D, Hv] (raw
     gate inputs) and ``accept_len`` [R] int32 in [0, D], all device tensors
     owned by this object (write into them, then call ``replay()``).
     Outputs: ``out`` [R*D, Hv, d] and the captures ``conv_values``,
@@ -54,7 +56,7 @@ class SpeculativeStep:
     """
 
     def __init__(self, conv_weight, conv_bias, conv_bank, A_log, dt_bias, gdn_bank, *, num_k_heads, drafts,
-                 activation="silu"):
+                 activation="silu", keep_verify_state=False):
         dev = conv_bank.device
         self.dev = dev
         two_r, C, km1 = conv_bank.shape
@@ -79,7 +81,10 @@ class SpeculativeStep:
         self.conv_values = torch.zeros((R, drafts, C), dtype=dt, device=dev)
         self.capsules = torch.zeros((R, drafts, capsule_width(Hk, Hv, d, d)), dtype=torch.float32, device=dev)
         self.conv_scratch = torch.empty_like(conv_bank)
-        self.gdn_scratch = torch.empty_like(gdn_bank)
+        # the verify pass's own final GDN states are not needed (the accepted
+        # prefix is replayed from the committed state), so none are written
+        # unless asked for
+        self.gdn_scratch = torch.empty_like(gdn_bank) if keep_verify_state else None
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
 
         self.conv_args, _, k1 = build_conv_args(
@@ -92,7 +97,8 @@ class SpeculativeStep:
         self.fwd_args, _, k2 = build_forward_args(
             q, k, v, self.a, self.b, self.cu, A_log=A_log, dt_bias=dt_bias, initial_state=gdn_bank,
             final_state=self.gdn_scratch, state_slots=self.src, output=self.out, state_update=self.capsules,
-            capacity=drafts, status=self.status, num_state_slots=two_r, max_seqlen=drafts)
+            capacity=drafts, status=self.status, num_state_slots=two_r, max_seqlen=drafts,
+            write_final_state=keep_verify_state)
         need = workspace_size(self.fwd_args)
         self.workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
         if need:

@@ -101,7 +101,12 @@ enum {
  *   state_slots   device [B] int32, or NULL for slot b = b
  *   initial_state device [num_state_slots, Hv, dv, dk] FP32, or NULL for zeros
  *   final_state   device, same shape; may equal initial_state (in place).
- *                 Only the slots named by the batch are written.
+ *                 Only the slots named by the batch are written.  NULL: the
+ *                 final states are not written at all -- for a speculative
+ *                 verify pass whose accepted prefix is rebuilt later from the
+ *                 committed state and the capsules ("Replay compact fixed
+ *                 state for hybrid decoding", Summary), this saves the write
+ *                 of every touched state.
  *   output        device [T, Hv, dv] io_dtype, contiguous
  *   state_update  device [B, capacity, W] FP32 with W = Hv + Hk*dk + Hv*dv, or
  *                 NULL when capacity = 0.  Row (b, i) describes token i of

@@ -84,8 +84,7 @@ def _args(**kw):
     (dict(gate_mode=5), 8),
     (dict(plan=9), 8),
     (dict(A_log=None), 1),                   # raw gates need A_log and dt_bias
-    (dict(cu_seqlens=None), 1),
-    (dict(final_state=None), 1),
+    (dict(cu_seqlens=None), 1),             # (final_state may be NULL: no state is written)
     (dict(state_update_capacity=4), 1),      # capsules requested without a buffer
     (dict(final_state=ctypes.c_void_p(0x1004)), 4),
 ])

@@ -290,3 +290,22 @@ def test_prepared_forward_call_equals_gdn_forward():
                                     final_state=ref_state, max_seqlen=1)
         torch.cuda.synchronize()
         assert torch.equal(out, o2) and torch.equal(fin, f2)
+
+
+@pytest.mark.parametrize("plan,lengths", [("recurrent", [4] * 16), ("chunked", [100, 70, 3])])
+def test_no_final_state_changes_nothing_else(plan, lengths):
+    """With no final-state buffer the kernels write no state; outputs and
+    capsules are bitwise those of the same call with a final state."""
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    inp = wl.make_inputs(520, lengths, Hk=2, Hv=6, dk=128, dv=128, io_dtype=np.float16, state_std=0.02,
+                         capacity=4)
+    args = lambda: (to_dev(inp.q), to_dev(inp.k), to_dev(inp.v), to_dev(inp.a), to_dev(inp.b), to_dev(inp.cu_seqlens))
+    init = to_dev(inp.initial_state)
+    o1, f1, c1 = gdn.gdn_forward(*args(), A_log=to_dev(inp.A_log), dt_bias=to_dev(inp.dt_bias), initial_state=init,
+                                 final_state=torch.empty_like(init), capacity=4, plan=plan)
+    o2, f2, c2 = gdn.gdn_forward(*args(), A_log=to_dev(inp.A_log), dt_bias=to_dev(inp.dt_bias), initial_state=init,
+                                 capacity=4, plan=plan, write_final_state=False)
+    torch.cuda.synchronize()
+    assert f2 is None
+    assert torch.equal(o1, o2) and torch.equal(c1, c2)
+    assert torch.equal(init, to_dev(inp.initial_state))  # the input state is untouched

@@ -21,7 +21,7 @@ R, D, Hk, Hv, d = 4, 4, 2, 6, 128
 C = 2 * Hk * d + Hv * d
 
 
-def _make(seed):
+def _make(seed, keep=False):
     from gated_delta_rule_gateddeltanet_gb300.spec_step import SpeculativeStep
     g = torch.Generator().manual_seed(seed)
     w = torch.randn((C, 4), generator=g).mul_(0.5).to(dev())
@@ -30,7 +30,8 @@ def _make(seed):
     gdn_bank = torch.randn((2 * R, Hv, d, d), generator=g).mul_(0.02).to(dev())
     A_log = torch.log(torch.empty(Hv).uniform_(1, 16, generator=g)).to(dev())
     dt_bias = torch.log(torch.expm1(torch.empty(Hv).uniform_(1e-3, 0.1, generator=g))).to(dev())
-    return SpeculativeStep(w, bias, conv_bank, A_log, dt_bias, gdn_bank, num_k_heads=Hk, drafts=D)
+    return SpeculativeStep(w, bias, conv_bank, A_log, dt_bias, gdn_bank, num_k_heads=Hk, drafts=D,
+                           keep_verify_state=keep)
 
 
 def _inputs(step):
@@ -42,8 +43,9 @@ def _inputs(step):
     return x, a, b, n
 
 
-def test_graph_step_equals_eager_over_published_steps():
-    eager, graphed = _make(7), _make(7)
+@pytest.mark.parametrize("keep", [False, True])
+def test_graph_step_equals_eager_over_published_steps(keep):
+    eager, graphed = _make(7, keep), _make(7, keep)
     graphed.capture()
     for step in range(3):
         x, a, b, n = _inputs(step)
@@ -60,7 +62,7 @@ def test_graph_step_equals_eager_over_published_steps():
 
 
 def test_all_accepted_replay_reproduces_the_verify_states():
-    s = _make(8).capture()
+    s = _make(8, keep=True).capture()
     x, a, b, _ = _inputs(9)
     s.x.copy_(x); s.a.copy_(a); s.b.copy_(b); s.accept_len.fill_(D)
     s.replay()
