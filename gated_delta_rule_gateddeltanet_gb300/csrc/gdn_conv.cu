@@ -53,9 +53,15 @@ __device__ __forceinline__ typename Vec<T>::Raw load_raw(const T *p) {
 
 template <typename T>
 __device__ __forceinline__ void unpack(const typename Vec<T>::Raw &raw, float (&v)[4]) {
-    const T *e = reinterpret_cast<const T *>(&raw);
+    if constexpr (sizeof(T) == 2) {  // two conversions of two halves each
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+        v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+    } else {
+        const T *e = reinterpret_cast<const T *>(&raw);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = to_f32(e[i]);
+        for (int i = 0; i < 4; ++i) v[i] = to_f32(e[i]);
+    }
 }
 
 template <typename T>
@@ -66,9 +72,15 @@ __device__ __forceinline__ void load_vec(const T *p, float (&v)[4]) {
 template <typename T>
 __device__ __forceinline__ void store_vec(T *p, const float (&v)[4]) {
     typename Vec<T>::Raw raw;
-    T *e = reinterpret_cast<T *>(&raw);
+    if constexpr (sizeof(T) == 2) {  // two round-to-nearest conversions of two floats each
+        const __half2 a = __floats2half2_rn(v[0], v[1]), b = __floats2half2_rn(v[2], v[3]);
+        raw.x = *reinterpret_cast<const uint32_t *>(&a);
+        raw.y = *reinterpret_cast<const uint32_t *>(&b);
+    } else {
+        T *e = reinterpret_cast<T *>(&raw);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) e[i] = from_f32<T>(v[i]);
+        for (int i = 0; i < 4; ++i) e[i] = from_f32<T>(v[i]);
+    }
     *reinterpret_cast<typename Vec<T>::Raw *>(p) = raw;
 }
 
@@ -76,6 +88,16 @@ __device__ __forceinline__ void store_vec(T *p, const float (&v)[4]) {
 // is bound by instruction issue, and the IEEE forms cost ~5x more per element.
 // For very negative x the denominator overflows and the quotient is 0.
 __device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+
+// The same through sigmoid(x) = (1 + tanh(x / 2)) / 2 with the hardware tanh
+// (one special-function operation instead of two).  Its relative error (about
+// 2^-11) is below the fp16 output rounding's, so only fp16 I/O uses it.
+__device__ __forceinline__ float silu_tanh(float x) {
+    float t;
+    const float h = 0.5f * x;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return fmaf(h, t, h);
+}
 
 // A thread's block of the state: 4 channels x (K-1) entries, contiguous, moved
 // as 8-byte (fp16) or 16-byte (fp32) words.
@@ -231,7 +253,7 @@ __global__ void __launch_bounds__(NT, sizeof(T) == 2 ? 4 : 3) conv_kernel(const 
 #pragma unroll
                 for (int j = 0; j < K - 1; ++j) acc = fmaf(w[i][j], win[j][i], acc);
                 acc = fmaf(w[i][K - 1], xt[i], acc);
-                yv[i] = p.silu ? silu(acc) : acc;
+                yv[i] = p.silu ? (sizeof(T) == 2 ? silu_tanh(acc) : silu(acc)) : acc;
             }
             store_vec<T>(y + (long long)t * p.C + c0, yv);
             const int tl = t - bos;
