@@ -235,6 +235,34 @@ __global__ void __launch_bounds__(NT, sizeof(T) == 2 ? 4 : 3) conv_kernel(const 
             for (int g = 0; g < GROUP; ++g)
                 if (tg + g < t_end) raw[g] = load_raw<T>(x + (long long)(tg + g) * p.x_stride + c0);
         }
+        // Interior group: every token inside the current sequence, none its last
+        // one, none captured -- straight-line code without the per-token checks.
+        // (The condition is the same for every thread of the CTA.)
+        if (ok && tg >= bos && tg + GROUP < eos && tg + GROUP <= t_end && (!vals || tg - bos >= ncap)) {
+            T *yp = y + (long long)tg * p.C + c0;
+#pragma unroll
+            for (int g = 0; g < GROUP; ++g) {
+                float xt[V], yv[V];
+                unpack<T>(raw[g], xt);
+#pragma unroll
+                for (int i = 0; i < V; ++i) {
+                    float acc = bias[i];
+#pragma unroll
+                    for (int j = 0; j < K - 1; ++j) acc = fmaf(w[i][j], win[j][i], acc);
+                    acc = fmaf(w[i][K - 1], xt[i], acc);
+                    yv[i] = p.silu ? (sizeof(T) == 2 ? silu_tanh(acc) : silu(acc)) : acc;
+                }
+                store_vec<T>(yp, yv);
+                yp += p.C;
+#pragma unroll
+                for (int j = 0; j + 1 < K - 1; ++j)
+#pragma unroll
+                    for (int i = 0; i < V; ++i) win[j][i] = win[j + 1][i];
+#pragma unroll
+                for (int i = 0; i < V; ++i) win[K - 2][i] = xt[i];
+            }
+            continue;
+        }
 #pragma unroll
         for (int g = 0; g < GROUP; ++g) {
             const int t = tg + g;
