@@ -143,10 +143,4 @@ __device__ __forceinline__ void gates_from(int raw, float av, float bv, float A_
     }
 }
 
-// Effective decay and beta of one (token, value head).
-__device__ __forceinline__ void gates(const ForwardParams &p, long long t, int h, float &g, float &beta) {
-    gates_from(p.gate_raw, p.a[t * p.Hv + h], p.b[t * p.Hv + h], p.gate_raw ? p.A_log[h] : 0.f,
-               p.gate_raw ? p.dt_bias[h] : 0.f, g, beta);
-}
-
 }  // namespace gdn
