@@ -20,9 +20,10 @@
 // memory, completion tracked by an mbarrier; the per-token vectors
 // (normalised q and k, k.q, gates, v) are staged meanwhile, so their
 // dependent loads overlap the tile's flight.  After the update the tile goes
-// back with one bulk store.  No state bytes live in registers while in
-// flight, so registers stay low (~63) and 5 CTAs fit per SM: up to 160 KiB of
-// state in flight per SM, enough to cover HBM latency.
+// back with one bulk store (none when the caller passes no final-state
+// buffer).  No state bytes live in registers while in flight, so registers
+// stay low (48) and 5 CTAs fit per SM: up to 160 KiB of state in flight per
+// SM, enough to cover HBM latency.
 //
 // Compute mapping: LPR = dk/16 lanes share a row, 16 floats each as four
 // float4 (lane l reads float4 j*LPR + l, so the LPR lanes of a row cover one
