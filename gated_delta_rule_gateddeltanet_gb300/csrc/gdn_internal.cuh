@@ -101,6 +101,13 @@ cudaError_t launch_chunked_wy(const ForwardParams &p, int min_len, void *workspa
 bool encode_rows_f16(CUtensorMap *map, const void *base, long long row_elems, long long stride, int T, int box_x,
                      int box_y, bool swizzle128);
 
+// Tensor map over a dense row-major FP32 [rows, row_elems] array (no gaps
+// between rows), boxes of box_y rows x box_x elements, zero fill past the
+// last row; with swizzle128 (box_x = 32) each box lands in shared memory in
+// the 128-byte swizzled layout (16-byte chunk c of row r at c ^ (r % 8)).
+bool encode_rows_f32(CUtensorMap *map, const float *base, long long row_elems, long long rows, int box_x, int box_y,
+                     bool swizzle128);
+
 // Sequences up to this many tokens stay on the recurrent kernel under the
 // automatic plan; longer ones go to the chunked kernel.
 constexpr int RECURRENT_MAX_LEN = 32;

@@ -1,8 +1,10 @@
-// Token-by-token (decode / short-span) gated delta rule kernel.
+// Token-by-token (decode / short-span) gated delta rule kernels.
 //
 // Operator: "[CUDA] Add compact GatedDeltaNet operator" (Description) -- the
-// recurrent decode path of the GatedDeltaNet operator, with the native gate
-// arithmetic and the compact state_update capsule fused in.
+// recurrent path for decode and short spans, with the native gate arithmetic
+// and the compact state_update capsule fused in.
+//
+// 1. Decode kernel (every span has at most one token) -- CUDA cores.
 //
 // With a V-major state, row i of S (dk floats, value channel i) evolves on its
 // own: for a token with unit key kn, unit query qn, decay g and beta,
@@ -30,13 +32,63 @@
 // contiguous run and the shared-memory reads are conflict-free); both dot
 // products are LPR-wide xor-shuffle reductions.  Tokens are staged TB at a
 // time; rows stay in registers across the staged tokens.
+//
+// 2. Mixed kernel (some span has several tokens: speculative verification,
+// short prefill) -- a persistent kernel of 4-warp CTAs (4 per SM at 128
+// registers), each over a contiguous range of work items (sequence, value
+// head, 64-row block).  One-token spans run the code above (the same bits as
+// the decode kernel); longer spans run the tensor-core evaluation below.  At
+// four tokens per span the CUDA-core loop is bound by instruction issue
+// (about 95 instructions per row group and token), not by HBM.
+//
+// Tokens are taken TB = 4 at a time.  Within such a group the token-by-token
+// recurrence S_t = g_t S_{t-1} + u_t k_t^T, u_t = beta_t (v_t - g_t S_{t-1} k_t),
+// o_t = scale S_t q_t (unit k_t, q_t) unrolls to a closed form in the state S0
+// at the start of the group.  With G_t = g_0 ... g_t and
+// r(t, s) = g_{s+1} ... g_t (= G_t / G_s, formed as a product, never divided):
+//     P_t = S0 k_t,  Q_t = S0 q_t                 (eight dot products per row)
+//     u_t = beta_t v_t - beta_t G_t P_t - sum_{s<t} beta_t r(t,s) (k_s.k_t) u_s
+//     o_t = scale (G_t Q_t + sum_{s<=t} r(t,s) (k_s.q_t) u_s)
+//     S   = G_n S0 + sum_s r(n,s) u_s k_s^T       (n: last token of the group)
+// The per-row work is then two dense products, S0 [rows x dk] x
+// [k_0 q_0 .. k_3 q_3] [dk x 8] and the rank-4 update [rows x 4] x [4 x dk],
+// and both run as mma.sync TF32 products.  Every FP32 operand is split into a
+// TF32 high part and the exact remainder and three products are summed
+// (hi.hi + hi.lo + lo.hi), so a product carries about 2^-21 relative error
+// (FP32-level, like the CUDA-core path) for about a quarter of its
+// instructions.
+//
+// Layout: warp w of the CTA holds tile rows 16w .. 16w + 15; lane 4 g + c
+// holds rows 16w + g and 16w + g + 8 at columns 8j + 2c and 8j + 2c + 1
+// (j < dk / 8).  That is the accumulator layout of the m16n8 products, so
+// the rows stay in registers for the whole span and the update product
+// accumulates into them directly.  The dot products use the same registers
+// as their A operand with the k index permuted inside each 8-column block
+// (k = c <-> column 2c, k = c + 4 <-> column 2c + 1); the staged vectors are
+// read with the same permutation.
+//
+// Data movement: while an item computes, the next item's 64 rows arrive in
+// shared memory as dk/32 TMA tensor boxes of 64 rows x 32 floats in the
+// 128-byte swizzled layout (one tensor copy per box; one bulk copy per row
+// was issue-bound).  Fragment row g reads tile row 2g (g < 4) or 2(g - 4) + 1
+// of its 8-row group, so the swizzled 8-byte reads are conflict-free.  The
+// final rows go out from registers with 8-byte stores whose 32-byte sectors
+// are fully written (four lanes cover one row's 8-column block).  Items of
+// one (sequence, key head) are adjacent, so a CTA keeps the key-side staging
+// (unit q and k, their TF32 parts, k.k and k.q) and redoes only the gates and
+// v of each value head.
+#include <algorithm>
+#include <cstring>
+
+#include "chunk_tiles.cuh"
 #include "gdn_internal.cuh"
 #include "ptx.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int NT = 256;    // threads per CTA
+constexpr int NT = 256;    // threads per CTA of the decode kernel
+constexpr int NTM = 128;   // threads per CTA of the mixed kernel (4 warps x 16 rows on the tensor-core path)
 constexpr int TB = 4;      // tokens staged per round (one warp normalises one token)
 constexpr int ROWS = 64;   // state rows per CTA tile
 constexpr float EPS = 1e-6f;
@@ -44,13 +96,55 @@ constexpr float EPS = 1e-6f;
 // GDN_DEVERR_TIMEOUT and leaves its tile unwritten.
 constexpr long long WAIT_LIMIT = 4000000000LL;
 
-template <typename TIO, int DK>
-__global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p) {
+// Per-group staging of both span evaluations (a CTA runs one at a time): the
+// staged tokens' v entries for the tile's rows, their gates, and the outputs
+// and deltas before they are stored.
+
+// One CTA's unit of work: ROWS consecutive state rows of one (sequence, value head).
+struct Span {
+    int b, h, rb, bos, eos, kh, rows_here;
+    size_t off;  // first float of the tile in the state arrays
+};
+
+// Resolves and checks the work item (sequence b, value head h, row block
+// rb): its span and state slot.  False when there is nothing to do (a bad
+// descriptor, which is flagged, or a span longer than max_len, which the
+// chunked kernel owns).
+__device__ __forceinline__ bool resolve_span(const ForwardParams &p, int b, int h, int rb, Span &sp) {
+    sp.rb = rb;
+    sp.h = h;
+    sp.b = b;
+    const bool leader = (sp.rb == 0 && sp.h == 0 && threadIdx.x == 0);
+    if (p.cu && sp.b == 0 && leader && (p.cu[0] != 0 || p.cu[p.B] != p.T)) flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
+    sp.bos = seq_start(p.cu, p.dense_S, sp.b);
+    sp.eos = seq_start(p.cu, p.dense_S, sp.b + 1);
+    if (sp.bos < 0 || sp.eos < sp.bos || sp.eos > p.T) {
+        if (leader) flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
+        return false;
+    }
+    if (sp.eos - sp.bos > p.max_len) return false;
+    const int slot = p.slots ? p.slots[sp.b] : sp.b;
+    if (slot < 0 || slot >= p.num_slots) {
+        if (leader) flag_error(p.status, GDN_DEVERR_STATE_SLOT);
+        return false;
+    }
+    sp.kh = sp.h / p.r;
+    sp.rows_here = min(ROWS, p.dv - sp.rb * ROWS);
+    sp.off = (((size_t)slot * p.Hv + sp.h) * (size_t)p.dv + (size_t)sp.rb * ROWS) * p.dk;
+    return true;
+}
+
+// The CUDA-core evaluation of one span with NTH threads.  Every row's
+// arithmetic is independent of NTH, so both kernels that use it give
+// bit-identical results for the spans they share.
+template <typename TIO, int DK, int NTH>
+__device__ __forceinline__ void span_cuda_cores(const ForwardParams &p, const Span &sp) {
     constexpr int LPR = DK / 16;             // lanes per state row
     constexpr int GPW = 32 / LPR;            // rows per warp per pass
-    constexpr int ROWS_PASS = (NT / 32) * GPW;
+    constexpr int ROWS_PASS = (NTH / 32) * GPW;
     constexpr int NPASS = (ROWS + ROWS_PASS - 1) / ROWS_PASS;
     constexpr int EPL = DK / 32;             // q/k elements per lane when normalising
+    static_assert(NTH / 32 >= TB, "one warp normalises one staged token");
 
     extern __shared__ __align__(128) float tile[];  // [ROWS][DK]
     __shared__ __align__(16) float kn_s[TB][DK];
@@ -59,30 +153,11 @@ __global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p)
     __shared__ float v_s[TB][ROWS], o_s[TB][ROWS], u_s[TB][ROWS];
     __shared__ __align__(8) uint64_t bar;
 
-    const int nrb = (p.dv + ROWS - 1) / ROWS;
-    const int rb = blockIdx.x % nrb;
-    const int h = blockIdx.x / nrb;
-    const int b = blockIdx.y;
+    const int rb = sp.rb, h = sp.h, b = sp.b, bos = sp.bos, eos = sp.eos, kh = sp.kh, rows_here = sp.rows_here;
+    const size_t off = sp.off;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int l = lane % LPR, grp = lane / LPR;
-    const bool leader = (rb == 0 && h == 0 && tid == 0);
-
-    if (p.cu && b == 0 && leader && (p.cu[0] != 0 || p.cu[p.B] != p.T)) flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
-    const int bos = seq_start(p.cu, p.dense_S, b), eos = seq_start(p.cu, p.dense_S, b + 1);
-    if (bos < 0 || eos < bos || eos > p.T) {
-        if (leader) flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
-        return;
-    }
-    if (eos - bos > p.max_len) return;  // long span: the chunked kernel owns it
-    const int slot = p.slots ? p.slots[b] : b;
-    if (slot < 0 || slot >= p.num_slots) {
-        if (leader) flag_error(p.status, GDN_DEVERR_STATE_SLOT);
-        return;
-    }
-    const int kh = h / p.r;
-    const int rows_here = min(ROWS, p.dv - rb * ROWS);
     const uint32_t bytes = (uint32_t)rows_here * DK * 4;
-    const size_t off = (((size_t)slot * p.Hv + h) * (size_t)p.dv + (size_t)rb * ROWS) * DK;
 
     // ---- the state tile: one bulk copy in flight while the tokens are staged
     if (tid == 0) {
@@ -97,7 +172,7 @@ __global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p)
         }
     } else {
         float4 *t4 = reinterpret_cast<float4 *>(tile);
-        for (int i = tid; i < rows_here * DK / 4; i += NT) t4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = tid; i < rows_here * DK / 4; i += NTH) t4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     bool tile_pending = p.init != nullptr;
 
@@ -112,11 +187,11 @@ __global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p)
         // ---- stage: every global load of the round is issued first (v entries of
         //      the tile's rows, q and k rows, gate inputs), then the normalised q
         //      and k, k.q and the gates (one warp per token)
-        constexpr int VPT = (TB * ROWS + NT - 1) / NT;
+        constexpr int VPT = (TB * ROWS + NTH - 1) / NTH;
         float vreg[VPT];
 #pragma unroll
         for (int m = 0; m < VPT; ++m) {
-            const int i = tid + m * NT, tt = i / ROWS, rr = i % ROWS;
+            const int i = tid + m * NTH, tt = i / ROWS, rr = i % ROWS;
             vreg[m] = (i < nt * ROWS && rr < rows_here)
                           ? to_f32(vg[(long long)(t0 + tt) * p.v_stride + (long long)h * p.dv + rb * ROWS + rr])
                           : 0.f;
@@ -144,7 +219,7 @@ __global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p)
         }
 #pragma unroll
         for (int m = 0; m < VPT; ++m) {
-            const int i = tid + m * NT;
+            const int i = tid + m * NTH;
             if (i < nt * ROWS) v_s[i / ROWS][i % ROWS] = vreg[m];
         }
         if (stager) {
@@ -244,7 +319,7 @@ __global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p)
         __syncthreads();
 
         // ---- outputs and capsules of the staged tokens
-        for (int i = tid; i < nt * ROWS; i += NT) {
+        for (int i = tid; i < nt * ROWS; i += NTH) {
             const int tt = i / ROWS, rr = i % ROWS;
             if (rr >= rows_here) continue;
             const int row = rb * ROWS + rr;
@@ -255,7 +330,7 @@ __global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p)
                 p.caps[((long long)b * p.cap + tl) * p.W + ubase + (long long)h * p.dv + row] = u_s[tt][rr];
         }
         if (p.caps && rb == 0) {
-            for (int i = tid; i < nt * (DK + 1); i += NT) {
+            for (int i = tid; i < nt * (DK + 1); i += NTH) {
                 const int tt = i / (DK + 1), e = i % (DK + 1);
                 const int tl = t0 + tt - bos;
                 if (tl >= p.cap) continue;
@@ -291,14 +366,465 @@ __global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p)
 }
 
 template <typename TIO, int DK>
+__global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p) {
+    Span sp;
+    const int nrb = (p.dv + ROWS - 1) / ROWS;
+    if (!resolve_span(p, blockIdx.y, blockIdx.x / nrb, blockIdx.x % nrb, sp)) return;
+    span_cuda_cores<TIO, DK, NT>(p, sp);
+}
+
+using ct::mma_tf32;
+using ct::to_tf32;
+
+// D += A B, m16n8k4 TF32: A (rows g, g + 8; k = c), B (k = c; n = g).
+__device__ __forceinline__ void mma_k4(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k4.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// x = hi + lo exactly: hi is x rounded to TF32, lo the remainder (the tensor
+// core reads lo's top 19 bits).
+__device__ __forceinline__ void split(float x, uint32_t &hi, uint32_t &lo) {
+    hi = to_tf32(x);
+    lo = __float_as_uint(x - __uint_as_float(hi));
+}
+
+// Thread 0: the item's ROWS rows into shared memory as DK/32 tensor copies
+// of [ROWS rows x 32 floats] boxes, each in the 128-byte swizzled layout
+// (box j holds columns 32j .. 32j + 31; rows past the array read as zeros,
+// rows past the tile belong to the next head and are ignored).  Earlier
+// generic writes to the buffer must have been fenced to the async proxy
+// before the barrier that precedes this call.
+template <int DK>
+__device__ __forceinline__ void issue_rows(const Span &sp, const CUtensorMap *map, float *rows_s, uint64_t *bar) {
+    ptx::mbar_arrive_expect_tx(bar, (uint32_t)ROWS * DK * 4);
+    const int row0 = (int)(sp.off / DK);
+#pragma unroll
+    for (int j = 0; j < DK / 32; ++j) ptx::tma_load_2d(rows_s + j * 32 * ROWS, map, 32 * j, row0, bar);
+}
+
+// Float offset of element (r, col) in the swizzled boxes written by issue_rows.
+__device__ __forceinline__ int rows_at(int r, int col) {
+    const int cb = col & 31;
+    return (col >> 5) * (32 * ROWS) + r * 32 + ((((cb >> 2) ^ (r & 7)) << 2) | (cb & 3));
+}
+
+// One multi-token span.  Its rows are in flight into rows_s (when the call
+// has an initial state); once every lane holds its rows the buffer is
+// refilled with those of `next` (if given).  With `reuse` the key-side
+// staging of the first group (unit q and k, their TF32 parts and the k.k,
+// k.q products) is still in shared memory from the previous item, which had
+// the same sequence and key head.  False if the copy never landed (flagged;
+// the caller stops).
+template <typename TIO, int DK>
+__device__ __forceinline__ bool span_tensor_cores(const ForwardParams &p, const Span &sp, const CUtensorMap *map,
+                                                  float *rows_s, uint64_t *bar, uint32_t &parity, const Span *next,
+                                                  bool reuse) {
+    constexpr int NJ = DK / 8;       // 8-column blocks per row
+    constexpr int VS = DK + 8;       // row stride of the staged vectors (bank-conflict free reads)
+    constexpr int EPL = DK / 32;     // q/k elements per lane when normalising
+
+    // vector n < TB: k_n, n >= TB: q_{n - TB} (unit vectors), TF32 high parts and remainders
+    __shared__ __align__(16) float vh_s[2 * TB][VS];
+    __shared__ __align__(16) float vl_s[2 * TB][VS];
+    // per token t: beta_t, beta_t G_t, scale G_t, r(n, t); and the pair coefficients
+    __shared__ float bt_s[TB], bG_s[TB], sG_s[TB], eG_s[TB];
+    __shared__ float v_s[TB][ROWS], o_s[TB][ROWS], u_s[TB][ROWS];
+    __shared__ float g_s[TB], beta_s[TB];
+    __shared__ float mkk_s[TB][TB], mq_s[TB][TB];  // beta_t r(t,s) k_s.k_t (s < t); scale r(t,s) k_s.q_t (s <= t)
+    __shared__ float dkk_s[TB][TB], dkq_s[TB][TB];  // k_s.k_t and k_s.q_t (s <= t), kept for reuse
+    __shared__ float Gn_s;
+
+    const int rb = sp.rb, h = sp.h, b = sp.b, bos = sp.bos, eos = sp.eos, kh = sp.kh, rows_here = sp.rows_here;
+    const size_t off = sp.off;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    // tile-local rows of this lane: fragment row g is row 2g (g < 4) or 2(g - 4) + 1 of the
+    // warp's first 8 (and the same + 8), so that the swizzled reads below are conflict-free
+    const int r0 = warp * 16 + (g < 4 ? 2 * g : 2 * g - 7), r1 = r0 + 8;
+    const bool a0 = r0 < rows_here, a1 = r1 < rows_here;
+
+    // ---- the rows, from the swizzled copy in shared memory (conflict-free 8-byte reads)
+    float2 sa[NJ], sb[NJ];
+    if (p.init) {
+        const bool ok = ptx::mbar_wait_bounded(bar, parity, WAIT_LIMIT);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                flag_error(p.status, GDN_DEVERR_TIMEOUT);
+                ptx::mbar_wait_bounded(bar, parity, WAIT_LIMIT);  // let the copies land before exit
+            }
+            return false;
+        }
+        parity ^= 1u;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            sa[j] = a0 ? *reinterpret_cast<const float2 *>(rows_s + rows_at(r0, 8 * j + 2 * c)) : make_float2(0.f, 0.f);
+            sb[j] = a1 ? *reinterpret_cast<const float2 *>(rows_s + rows_at(r1, 8 * j + 2 * c)) : make_float2(0.f, 0.f);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) sa[j] = sb[j] = make_float2(0.f, 0.f);
+    }
+    __syncthreads();  // every lane holds its rows: the buffer takes the next item's
+    if (next && tid == 0) issue_rows<DK>(*next, map, rows_s, bar);
+
+    const TIO *qg = static_cast<const TIO *>(p.q);
+    const TIO *kg = static_cast<const TIO *>(p.k);
+    const TIO *vg = static_cast<const TIO *>(p.v);
+    TIO *og = static_cast<TIO *>(p.out);
+    const long long ubase = (long long)p.Hv + (long long)p.Hk * DK;
+
+    for (int t0 = bos; t0 < eos; t0 += TB) {
+        const int nt = min(TB, eos - t0);
+        // ---- stage 1: v entries of the tile's rows; warp t normalises token t's q and k
+        //      and computes its gates (tokens past the span become zero vectors, g = 1, beta = 0)
+        constexpr int VPT = TB * ROWS / NTM;
+        float vreg[VPT];
+#pragma unroll
+        for (int m = 0; m < VPT; ++m) {
+            const int i = tid + m * NTM, tt = i / ROWS, rr = i % ROWS;
+            vreg[m] = (tt < nt && rr < rows_here)
+                          ? to_f32(vg[(long long)(t0 + tt) * p.v_stride + (long long)h * p.dv + rb * ROWS + rr])
+                          : 0.f;
+        }
+        const int tw = warp;  // this warp's token
+        const bool live = tw < nt;
+        const bool keep = reuse && t0 == bos;  // the key-side staging is already in place
+        float kv[EPL], qv[EPL];
+        float ga = 0.f, gb = 0.f, gA = 0.f, gd = 0.f;
+        if (live) {
+            const long long t = t0 + tw;
+            if (!keep) {
+                const TIO *qp = qg + t * p.q_stride + (long long)kh * DK + lane * EPL;
+                const TIO *kp = kg + t * p.k_stride + (long long)kh * DK + lane * EPL;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) {
+                    qv[e] = to_f32(qp[e]);
+                    kv[e] = to_f32(kp[e]);
+                }
+            }
+            if (lane == 0) {
+                ga = p.a[t * p.Hv + h];
+                gb = p.b[t * p.Hv + h];
+                if (p.gate_raw) {
+                    gA = p.A_log[h];
+                    gd = p.dt_bias[h];
+                }
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) qv[e] = kv[e] = 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < VPT; ++m) {
+            const int i = tid + m * NTM;
+            v_s[i / ROWS][i % ROWS] = vreg[m];
+        }
+        if (!keep) {
+            float sq = 0.f, sk = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                sq = fmaf(qv[e], qv[e], sq);
+                sk = fmaf(kv[e], kv[e], sk);
+            }
+            sq = warp_sum(sq);
+            sk = warp_sum(sk);
+            const float iq = 1.f / fmaxf(sqrtf(sq), EPS), ik = 1.f / fmaxf(sqrtf(sk), EPS);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                qv[e] *= iq;
+                kv[e] *= ik;
+                const int col = lane * EPL + e;
+                uint32_t kh_, kl_, qh_, ql_;
+                split(kv[e], kh_, kl_);
+                split(qv[e], qh_, ql_);
+                vh_s[tw][col] = __uint_as_float(kh_);
+                vl_s[tw][col] = __uint_as_float(kl_);
+                vh_s[TB + tw][col] = __uint_as_float(qh_);
+                vl_s[TB + tw][col] = __uint_as_float(ql_);
+            }
+        }
+        if (lane == 0) {
+            float gt = 1.f, bt = 0.f;
+            if (live) gates_from(p.gate_raw, ga, gb, gA, gd, gt, bt);
+            g_s[tw] = gt;
+            beta_s[tw] = bt;
+        }
+        __syncthreads();
+
+        // ---- stage 2: warp t forms row t of the pair coefficients (k_s.k_t, k_s.q_t
+        //      for s <= t) and its per-token factors
+        {
+            if (!keep) {
+                float dkk[TB], dkq[TB];
+#pragma unroll
+                for (int s = 0; s < TB; ++s) {
+                    float xk = 0.f, xq = 0.f;
+                    if (s <= tw) {
+#pragma unroll
+                        for (int e = 0; e < EPL; ++e) {
+                            const int col = lane * EPL + e;
+                            const float ks = vh_s[s][col] + vl_s[s][col];
+                            xk = fmaf(ks, kv[e], xk);
+                            xq = fmaf(ks, qv[e], xq);
+                        }
+                    }
+                    dkk[s] = warp_sum(xk);
+                    dkq[s] = warp_sum(xq);
+                }
+#pragma unroll
+                for (int m = 0; m < TB; ++m)
+                    if (lane == m) dkk_s[tw][m] = dkk[m], dkq_s[tw][m] = dkq[m];
+                __syncwarp();
+            }
+            if (lane < TB) {
+                // lane s: r(t, s) = g_{s+1} .. g_t for s <= t
+                const int s = lane;
+                float rts = 1.f;
+                for (int j = s + 1; j <= tw; ++j) rts *= g_s[j];
+                const float kk = dkk_s[tw][s], kq = dkq_s[tw][s];
+                const float bt = beta_s[tw];
+                mkk_s[tw][s] = (s < tw) ? bt * rts * kk : 0.f;
+                mq_s[tw][s] = (s <= tw && live) ? p.scale * rts * kq : 0.f;
+                if (s == 0) {
+                    const float Gt = rts * g_s[0];  // G_t = g_0 r(t, 0)
+                    bt_s[tw] = bt;
+                    bG_s[tw] = bt * Gt;
+                    sG_s[tw] = live ? p.scale * Gt : 0.f;
+                    if (tw == nt - 1) Gn_s = Gt;
+                }
+                if (s == 1) {
+                    // r(n, t) for this warp's token (zero past the span)
+                    float e = 1.f;
+                    for (int j = tw + 1; j < nt; ++j) e *= g_s[j];
+                    eG_s[tw] = live ? e : 0.f;
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- the eight dot products per row: D[row][n] = S0[row] . vec_n (split TF32)
+        // three accumulators: hi.hi, hi.lo, lo.hi (independent chains)
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            uint32_t ah[4], al[4];
+            split(sa[j].x, ah[0], al[0]);
+            split(sb[j].x, ah[1], al[1]);
+            split(sa[j].y, ah[2], al[2]);
+            split(sb[j].y, ah[3], al[3]);
+            const float2 bh = *reinterpret_cast<const float2 *>(&vh_s[g][8 * j + 2 * c]);
+            const float2 bl = *reinterpret_cast<const float2 *>(&vl_s[g][8 * j + 2 * c]);
+            const uint32_t bhh[2] = {__float_as_uint(bh.x), __float_as_uint(bh.y)};
+            const uint32_t bll[2] = {__float_as_uint(bl.x), __float_as_uint(bl.y)};
+            mma_tf32(d0, ah, bhh);
+            mma_tf32(d1, ah, bll);
+            mma_tf32(d2, al, bhh);
+        }
+        // lane c holds vectors 2c and 2c + 1 of rows r0 (x0, x1) and r1 (x2, x3):
+        // P_0, P_1 in lane 0, P_2, P_3 in lane 1, Q_0, Q_1 in lane 2, Q_2, Q_3 in lane 3
+        const float x0 = d0[0] + (d1[0] + d2[0]), x1 = d0[1] + (d1[1] + d2[1]);
+        const float x2 = d0[2] + (d1[2] + d2[2]), x3 = d0[3] + (d1[3] + d2[3]);
+        const int quad = lane & ~3;
+        float Pa[TB], Pb[TB];
+#pragma unroll
+        for (int s2 = 0; s2 < TB / 2; ++s2) {
+            Pa[2 * s2] = __shfl_sync(0xffffffffu, x0, quad | s2);
+            Pa[2 * s2 + 1] = __shfl_sync(0xffffffffu, x1, quad | s2);
+            Pb[2 * s2] = __shfl_sync(0xffffffffu, x2, quad | s2);
+            Pb[2 * s2 + 1] = __shfl_sync(0xffffffffu, x3, quad | s2);
+        }
+        // Q_c of both rows for this lane's token c
+        const int qsrc = quad | (2 + (c >> 1));
+        const float qa0 = __shfl_sync(0xffffffffu, x0, qsrc), qa1 = __shfl_sync(0xffffffffu, x1, qsrc);
+        const float qb0 = __shfl_sync(0xffffffffu, x2, qsrc), qb1 = __shfl_sync(0xffffffffu, x3, qsrc);
+        const float Q0 = (c & 1) ? qa1 : qa0, Q1 = (c & 1) ? qb1 : qb0;
+
+        // ---- the deltas u_t of both rows (every lane of the quad forms all of them)
+        float ua[TB], ub[TB];
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+            const float pa = Pa[t], pb = Pb[t];
+            const float bt = bt_s[t], bG = bG_s[t];
+            float xa = fmaf(bt, v_s[t][r0], -bG * pa);
+            float xb = fmaf(bt, v_s[t][r1], -bG * pb);
+#pragma unroll
+            for (int s = 0; s < t; ++s) {
+                const float m = mkk_s[t][s];
+                xa = fmaf(-m, ua[s], xa);
+                xb = fmaf(-m, ub[s], xb);
+            }
+            ua[t] = xa;
+            ub[t] = xb;
+        }
+        // ---- token c's outputs and deltas of both rows
+        if (c < nt) {
+            float oa = sG_s[c] * Q0, ob = sG_s[c] * Q1, uc_a = 0.f, uc_b = 0.f;
+#pragma unroll
+            for (int s = 0; s < TB; ++s) {
+                const float m = mq_s[c][s];
+                oa = fmaf(m, ua[s], oa);
+                ob = fmaf(m, ub[s], ob);
+                if (s == c) uc_a = ua[s], uc_b = ub[s];
+            }
+            o_s[c][r0] = oa;
+            o_s[c][r1] = ob;
+            u_s[c][r0] = uc_a;
+            u_s[c][r1] = uc_b;
+        }
+
+        // ---- S = G_n S0 + [r(n, t) u_t] [k_t]: the rank-4 update accumulates into the rows
+        {
+            float xa = 0.f, xb = 0.f;
+#pragma unroll
+            for (int s = 0; s < TB; ++s)
+                if (s == c) xa = ua[s], xb = ub[s];
+            const float e = eG_s[c];
+            uint32_t a0h, a0l, a1h, a1l;
+            split(e * xa, a0h, a0l);
+            split(e * xb, a1h, a1l);
+            const float Gn = Gn_s;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                // B[k = c][n = g] = k_c[8j + g]
+                const uint32_t kbh = __float_as_uint(vh_s[c][8 * j + g]), kbl = __float_as_uint(vl_s[c][8 * j + g]);
+                float dd[4] = {Gn * sa[j].x, Gn * sa[j].y, Gn * sb[j].x, Gn * sb[j].y};
+                mma_k4(dd, a0h, a1h, kbh);
+                mma_k4(dd, a0h, a1h, kbl);
+                mma_k4(dd, a0l, a1l, kbh);
+                sa[j] = make_float2(dd[0], dd[1]);
+                sb[j] = make_float2(dd[2], dd[3]);
+            }
+        }
+        __syncthreads();
+
+        // ---- outputs and capsules of the group
+        for (int i = tid; i < nt * ROWS; i += NTM) {
+            const int tt = i / ROWS, rr = i % ROWS;
+            if (rr >= rows_here) continue;
+            const int row = rb * ROWS + rr;
+            const long long t = t0 + tt;
+            og[(t * p.Hv + h) * p.dv + row] = from_f32<TIO>(o_s[tt][rr]);
+            const int tl = (int)(t - bos);
+            if (p.caps && tl < p.cap)
+                p.caps[((long long)b * p.cap + tl) * p.W + ubase + (long long)h * p.dv + row] = u_s[tt][rr];
+        }
+        if (p.caps && rb == 0) {
+            for (int i = tid; i < nt * (DK + 1); i += NTM) {
+                const int tt = i / (DK + 1), e = i % (DK + 1);
+                const int tl = t0 + tt - bos;
+                if (tl >= p.cap) continue;
+                float *row = p.caps + ((long long)b * p.cap + tl) * p.W;
+                if (e == DK)
+                    row[h] = g_s[tt];
+                else if (h % p.r == 0)
+                    row[p.Hv + (long long)kh * DK + e] = vh_s[tt][e] + vl_s[tt][e];
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- the rows go back (none when the caller asked for no final state)
+    if (!p.final_state) return true;
+    float *d0p = p.final_state + off + (size_t)r0 * DK + 2 * c;
+    float *d1p = d0p + 8 * DK;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        if (a0) *reinterpret_cast<float2 *>(d0p + 8 * j) = sa[j];
+        if (a1) *reinterpret_cast<float2 *>(d1p + 8 * j) = sb[j];
+    }
+    return true;
+}
+
+// Batches with multi-token spans: a persistent kernel, each CTA over a
+// contiguous range of work items.  Spans of one token (and empty ones) take the
+// CUDA-core path, so a decode request gets the same bits whichever batch it
+// is packed in; longer spans take the tensor-core path, and the next item's
+// rows are copied into shared memory while the current one computes (a wave
+// of one-shot CTAs would instead pay the full load latency in every wave).
+template <typename TIO, int DK>
+__global__ void __launch_bounds__(NTM, 4)
+    recurrent_mixed_kernel(const ForwardParams p, int items, const __grid_constant__ CUtensorMap rows_map) {
+    extern __shared__ __align__(128) float dyn_s[];  // the CUDA-core path's tile, or (1024-aligned) the swizzled rows
+    float *rows_s = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(dyn_s) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t rows_bar;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&rows_bar, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    uint32_t parity = 0;
+    // a contiguous range of items per CTA: consecutive items share the sequence
+    // and key head (item order b, h, rb), so their key-side staging is reused
+    const int stop = (int)((long long)(blockIdx.x + 1) * items / gridDim.x);
+    int it = (int)((long long)blockIdx.x * items / gridDim.x);
+    int staged = -1;  // b Hk + kh whose single-group staging is in shared memory, or -1
+    Span cur;
+    const int nrb = (p.dv + ROWS - 1) / ROWS;
+    // item = (b Hv + h) nrb + rb
+    auto resolve_item = [&](int item, Span &sp) {
+        return resolve_span(p, item / (nrb * p.Hv), (item / nrb) % p.Hv, item % nrb, sp);
+    };
+    bool cur_ok = it < stop && resolve_item(it, cur);
+    if (cur_ok && cur.eos - cur.bos > 1 && p.init && threadIdx.x == 0) issue_rows<DK>(cur, &rows_map, rows_s, &rows_bar);
+    while (it < stop) {
+        const int nx = it + 1;
+        Span nxt;
+        const bool nxt_ok = nx < stop && resolve_item(nx, nxt);
+        const bool nxt_rows = nxt_ok && nxt.eos - nxt.bos > 1 && p.init;  // the next item wants its rows copied
+        bool issued = false;
+        if (cur_ok) {
+            if (cur.eos - cur.bos > 1) {
+                const int key = cur.b * p.Hk + cur.kh;
+                const bool single = cur.eos - cur.bos <= TB;
+                if (!span_tensor_cores<TIO, DK>(p, cur, &rows_map, rows_s, &rows_bar, parity, nxt_rows ? &nxt : nullptr,
+                                                single && staged == key))
+                    return;
+                staged = single ? key : -1;
+                issued = nxt_rows;
+            } else {
+                span_cuda_cores<TIO, DK, NTM>(p, cur);
+            }
+        }
+        ptx::fence_proxy_async_smem();  // the CUDA-core path's tile writes, before copies overwrite them
+        __syncthreads();
+        if (nxt_rows && !issued && threadIdx.x == 0) issue_rows<DK>(nxt, &rows_map, rows_s, &rows_bar);
+        cur = nxt;
+        cur_ok = nxt_ok;
+        it = nx;
+    }
+}
+
+template <typename TIO, int DK>
 cudaError_t launch_dk(const ForwardParams &p, cudaStream_t stream) {
     const int nrb = (p.dv + ROWS - 1) / ROWS;
-    dim3 grid((unsigned)(nrb * p.Hv), (unsigned)p.B);
-    const int smem = ROWS * DK * 4;
-    auto kern = recurrent_kernel<TIO, DK>;
+    if (p.T == p.B) {  // every span has at most one token: the decode kernel
+        const int smem = ROWS * DK * 4;
+        auto kern = recurrent_kernel<TIO, DK>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        kern<<<dim3((unsigned)(nrb * p.Hv), (unsigned)p.B), NT, smem, stream>>>(p);
+        return cudaGetLastError();
+    }
+    // some span has several tokens: the persistent mixed kernel, as many CTAs as fit at once
+    const int smem = ROWS * DK * 4 + 1024;
+    CUtensorMap rows_map;
+    memset(&rows_map, 0, sizeof(rows_map));
+    if (p.init && !encode_rows_f32(&rows_map, p.init, DK, (long long)p.num_slots * p.Hv * p.dv, 32, ROWS, true))
+        return cudaErrorInvalidValue;
+    auto kern = recurrent_mixed_kernel<TIO, DK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NT, smem, stream>>>(p);
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NTM, smem)) != cudaSuccess) return e;
+    const long long items = (long long)p.B * p.Hv * nrb;
+    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const int grid = (int)std::min<long long>(items, (long long)std::max(per_sm, 1) * sms);
+    kern<<<grid, NTM, smem, stream>>>(p, (int)items, rows_map);
     return cudaGetLastError();
 }
 
