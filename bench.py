@@ -520,13 +520,15 @@ def run_spec(dev, stream, lib, sh):
         d["args_ns"], d["keep_ns"] = args_ns, keep_ns
         pools.append(d)
 
+    cur = [sh]  # the stream the calls go to (the graph capture uses a side stream)
+
     def verify(i):
-        rc = lib.gdn_forward(ctypes.byref(pools[i % NBUF]["args"]), sh)
+        rc = lib.gdn_forward(ctypes.byref(pools[i % NBUF]["args"]), cur[0])
         if rc:
             raise gdn.GdnError(rc, "gdn_forward")
 
     def verify_no_state(i):
-        rc = lib.gdn_forward(ctypes.byref(pools[i % NBUF]["args_ns"]), sh)
+        rc = lib.gdn_forward(ctypes.byref(pools[i % NBUF]["args_ns"]), cur[0])
         if rc:
             raise gdn.GdnError(rc, "gdn_forward")
 
@@ -535,36 +537,67 @@ def run_spec(dev, stream, lib, sh):
         rc = lib.gdn_replay_prefix(ctypes.c_void_p(d["pool"].data_ptr()), 32, 16, 16, 48, 128, 128,
                                    ctypes.c_void_p(d["src"].data_ptr()), ctypes.c_void_p(d["dst"].data_ptr()),
                                    ctypes.c_void_p(d["caps"].data_ptr()), 4, ctypes.c_void_p(d["n"].data_ptr()),
-                                   None, sh)
+                                   None, cur[0])
         if rc:
             raise gdn.GdnError(rc, "gdn_replay_prefix")
 
-    res = {}
+    res, host = {}, {}
     for name, fn in (("verify", verify), ("verify_no_state", verify_no_state), ("replay", replay)):
         for i in range(20):
             fn(i)
         torch.cuda.synchronize()
-        n = 400
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # device time: 40 launches captured in one CUDA graph, replayed 10 times (median)
+        n = 40
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        cur[0] = ctypes.c_void_p(side.cuda_stream)
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(n):
+                fn(i)
+        cur[0] = sh
+        graph.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(10):
+            with torch.cuda.stream(side):
+                e0.record()
+                graph.replay()
+                e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / n)
+        res[name] = statistics.median(ts)
+        del graph
+        # the same calls launched one by one from the host (adds the per-call host time)
+        m = 400
         e0.record(stream)
-        for i in range(n):
+        for i in range(m):
             fn(i)
         e1.record(stream)
         torch.cuda.synchronize()
-        res[name] = e0.elapsed_time(e1) / n
+        host[name] = e0.elapsed_time(e1) / m
     hbm_peak, _, kind = measured_peaks()
     state_bytes = 2 * 16 * 48 * 128 * 128 * 4
     cap_bytes = gdn.capsule_width(16, 48, 128, 128) * 4
     rep_bytes = state_bytes + statistics.mean(d["acc"] for d in pools) * cap_bytes
     ver_bytes = state_bytes + 64 * (33152 + cap_bytes)
+    ver_ns_bytes = state_bytes // 2 + 64 * (33152 + cap_bytes)
     return {"workload": "spec verify + replay: 16 requests x 4 draft tokens, Hk=16, Hv=48, d=128, fp16, "
                         "capsules for all tokens, replay of U{0..4} accepted into the inactive bank",
+            "timing": "device time: 40 launches in one CUDA graph, median of 10 replays; *_host_loop_us: the "
+                      "same calls launched one by one through the C ABI",
             "verify_us": round(res["verify"] * 1e3, 2), "replay_us": round(res["replay"] * 1e3, 2),
             "verify_no_final_state_us": round(res["verify_no_state"] * 1e3, 2),
+            "verify_host_loop_us": round(host["verify"] * 1e3, 2),
+            "verify_no_final_state_host_loop_us": round(host["verify_no_state"] * 1e3, 2),
+            "replay_host_loop_us": round(host["replay"] * 1e3, 2),
             "verify_tokens_per_s": round(64 / (res["verify"] / 1e3), 1),
             "replay_gbs": round(rep_bytes / (res["replay"] / 1e3) / 1e9, 1),
             "replay_frac_hbm": round(rep_bytes / (res["replay"] / 1e3) / 1e9 / hbm_peak, 4),
             "verify_gbs": round(ver_bytes / (res["verify"] / 1e3) / 1e9, 1),
+            "verify_frac_hbm": round(ver_bytes / (res["verify"] / 1e3) / 1e9 / hbm_peak, 4),
+            "verify_no_final_state_frac_hbm": round(ver_ns_bytes / (res["verify_no_state"] / 1e3) / 1e9 / hbm_peak, 4),
             "l2": f"{NBUF} rotating state pools of 96 MiB"}
 
 
