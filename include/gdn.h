@@ -60,7 +60,11 @@ enum {
 enum {
     GDN_PLAN_AUTO = 0,       /* per sequence: up to 32 tokens recurrent, longer ones chunked
                                 (chunked needs dk = dv = 128 and 16-byte aligned q, k, v) */
-    GDN_PLAN_RECURRENT = 1,  /* every sequence on the token-by-token kernel */
+    GDN_PLAN_RECURRENT = 1,  /* every sequence on the recurrent kernels: the state carried
+                                token by token (batches of one-token spans), or four
+                                tokens at a time in closed form on the warp tensor cores
+                                (batches with longer spans; one-token spans in them still
+                                take the token-by-token code, with the same bits) */
     GDN_PLAN_CHUNKED = 2     /* every sequence on the tensor-core chunked kernel
                                 (dk = dv = 128 only, else GDN_ERR_UNSUPPORTED) */
 };
