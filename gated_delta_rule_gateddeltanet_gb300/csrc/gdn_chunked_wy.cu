@@ -23,13 +23,13 @@
 // not on the state, so it leaves the sequential critical path:
 //
 //  wy_prep_kernel (one CTA per (chunk, key head), four CTAs per SM): L2-normal-
-//    ises q and k, forms the [Q;K] and K^T fp16 operand tiles, runs
-//    [Q;K] K^T on the tensor cores (P = QK^T and G = KK^T, shared by the key
-//    head's value heads), and for each of its value heads computes the gates,
-//    A, P o D and the triangular inverse T.  It writes byte images of the
-//    operand tiles, already in the swizzled shared-memory layout the MMAs
-//    read, to the caller's workspace (one 48 KiB record per (chunk, key head),
-//    one 17 KiB record per (chunk, value head)), plus the capsule's k and g.
+//    ises q and k into the [Q;K] fp16 operand tile, runs [Q;K] K^T on the
+//    tensor cores (P = QK^T and G = KK^T, shared by the key head's value
+//    heads), and for each of its value heads computes the gates, A, P o D and
+//    the triangular inverse T.  It writes byte images of the operand tiles,
+//    already in the swizzled shared-memory layout the MMAs read, to the
+//    caller's workspace (one 32 KiB record per (chunk, key head), one 17 KiB
+//    record per (chunk, value head)), plus the capsule's k and g.
 //
 //  wy_scan_kernel (persistent, one CTA per SM, chains longest-first): keeps the
 //    FP32 state in tensor memory and, per chunk, loads the two records with
@@ -43,8 +43,10 @@
 //    decayed copy, capsule deltas, outputs) done by all 16 warps.
 //
 // Every MMA is kind::f16 (fp16 operands, FP32 accumulation in tensor memory)
-// with both operands K-major in the 128-byte swizzled layout and the value
-// dimension dv = 128 as M.  Numerics are those of the single-kernel chunked
+// with the value dimension dv = 128 as M and both operands in the 128-byte
+// swizzled layout, K-major except K in MMA5: its B operand is the [Q;K]
+// tile's k rows read as an MN-major operand (dk along the 128-byte rows), so
+// no transposed copy of K exists.  Numerics are those of the single-kernel chunked
 // evaluation (same fp16 operand roundings), except that gamma scales the
 // FP32 MMA result O' instead of an fp16 copy of Q.
 #include <cuda.h>
@@ -66,8 +68,7 @@ constexpr float LOG_DECAY_FLOOR = -200.f;  // exp(-200) is 0 in fp32; keeps Gamm
 constexpr long long WAIT_LIMIT = 4000000000LL;
 
 // Workspace records (byte images of shared-memory operand tiles).
-constexpr int KREC_BYTES = 49152;  // [Q;K] tile (2 K-blocks x 128 rows x 128 B) + K^T tile (128 rows x 128 B)
-constexpr int KREC_KT = 32768;
+constexpr int KREC_BYTES = 32768;  // [Q;K] tile: 2 K-blocks (dk 0-63, 64-127) x 128 rows (64 q, 64 k) x 128 B
 constexpr int VREC_T = 0;          // T, [64][64] fp16
 constexpr int VREC_PD = 8192;      // P o D, [64][64] fp16
 constexpr int VREC_F = 16384;      // per-token factors (fp32, 64 each): beta, beta*gamma, gamma, exp(Gamma_last - Gamma)
@@ -318,8 +319,9 @@ constexpr int GH = 8;    // value heads whose gates are computed together (one w
 constexpr int P_AT = 0;                    // [64][AS] fp32
 constexpr int P_M = 64 * AS * 4;           // [32][MS] fp32
 constexpr int P_TPD = 23552;               // T and P o D tiles (1024-byte aligned), 16 KiB
-constexpr int PREP_SMEM = KREC_BYTES + 1024;
-static_assert(P_M + 32 * MS * 4 <= P_TPD && P_TPD + VREC_F <= KREC_BYTES, "prep shared-memory layout");
+constexpr int PREP_BYTES = P_TPD + VREC_F;  // the value-head phase's scratch (the record image is smaller)
+constexpr int PREP_SMEM = PREP_BYTES + 1024;
+static_assert(P_M + 32 * MS * 4 <= P_TPD && KREC_BYTES <= PREP_BYTES, "prep shared-memory layout");
 
 template <typename TIO>
 __global__ void __launch_bounds__(PT, 4)
@@ -480,20 +482,6 @@ __global__ void __launch_bounds__(PT, 4)
         }
     }
     __syncthreads();
-    // ---- K^T tile (row j = feature, 64 token columns) from the K rows: 128
-    //      8 x 8 blocks moved by transposing matrix loads and matrix stores, four
-    //      blocks per instruction, four instructions per warp
-    if (ok) {
-        const int m = lane >> 3, rr = lane & 7;
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int tile = (warp * 4 + it) * 4 + m;  // 0..127: 8 token blocks x 16 feature blocks
-            const int s0 = (tile & 7) * 8, j0 = (tile >> 3) * 8;
-            uint32_t r[4];
-            ptx::ldmatrix_x4_trans(r, ptx::smem_u32(sm + sw(64 + s0 + rr, j0, 128)));
-            ptx::stmatrix_x4(ptx::smem_u32(sm + KREC_KT + sw(j0 + rr, s0, 128)), r);
-        }
-    }
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncthreads();
@@ -620,7 +608,7 @@ constexpr uint32_t TM_Y = 448;   // U^T (P o D)^T
 
 // Shared memory (offsets from a 1024-byte aligned base): two stages holding
 // one chunk's inputs each, then the fp16 state copy and the R^T / U^T tile.
-constexpr int S_KREC = 0;                   // key-head record: [Q;K] tile, K^T tile at S_KREC + KREC_KT
+constexpr int S_KREC = 0;                   // key-head record: [Q;K] tile (k rows from byte 64 * 128 of each K-block)
 constexpr int S_VREC = KREC_BYTES;          // value-head record: T, P o D, per-token factors
 constexpr int S_V = S_VREC + VREC_BYTES;    // fp16 v rows of the chunk [64][128]; then U^T diag(decay) tile
 constexpr int STAGE_BYTES = S_V + 16384;
@@ -673,6 +661,7 @@ __global__ void __launch_bounds__(NT, 1)
     const uint64_t d_S16 = ptx::sdesc_k_sw128(ptx::smem_u32(sm + OFF_S16));
     const uint64_t d_RT = ptx::sdesc_k_sw128(ptx::smem_u32(sm + OFF_RT));
     constexpr uint32_t I64 = ptx::idesc_f16_f32(128, 64), I128 = ptx::idesc_f16_f32(128, 128);
+    constexpr uint32_t I128_BMN = ptx::idesc_f16_f32(128, 128, true);  // B MN-major
 
     auto mma_wait = [&]() -> bool {
         const bool ok = ptx::mbar_wait_bounded(&bar, phase, WAIT_LIMIT);
@@ -851,10 +840,11 @@ __global__ void __launch_bounds__(NT, 1)
             if (tid == 0) {
                 ptx::tc_fence_after();
                 const uint64_t ud = ptx::sdesc_k_sw128(a_st + S_V), pd = ptx::sdesc_k_sw128(a_st + S_VREC + VREC_PD);
-                const uint64_t kt = ptx::sdesc_k_sw128(a_st + S_KREC + KREC_KT);
+                // K as MN-major B: 16 tokens per step = 16 rows of 128 B = 2048 B
+                const uint64_t kt = ptx::sdesc_mn_sw128(a_st + S_KREC + 64 * 128, 16384);
                 for (int ks = 0; ks < CH / 16; ++ks) {
                     ptx::mma_f16(tm + TM_Y, d_RT + 2 * ks, pd + 2 * ks, I64, ks > 0);
-                    ptx::mma_f16(tm + TM_S, ud + 2 * ks, kt + 2 * ks, I128, (state_live || ks > 0) ? 1u : 0u);
+                    ptx::mma_f16(tm + TM_S, ud + 2 * ks, kt + 128 * ks, I128_BMN, (state_live || ks > 0) ? 1u : 0u);
                 }
                 ptx::mma_commit(&bar);
             }

@@ -86,7 +86,7 @@ cudaError_t launch_chunked(const ForwardParams &p, int min_len, void *workspace,
 
 // Two-phase chunked path (a parallel per-chunk kernel, then the sequential
 // state-passing kernel): faster, and needs chunked_wy_workspace_bytes of
-// workspace for the per-chunk records (about 1.6 MB per 64 tokens at
+// workspace for the per-chunk records (about 1.36 MB per 64 tokens at
 // Hk = 16, Hv = 48, d = 128).
 size_t chunked_wy_workspace_bytes(int B, int T, int Hk, int Hv);
 // Workspace of the single-kernel chunked evaluation for these arguments (0 if

@@ -112,26 +112,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // ---------------------------------------------------------------- 8 x 8 b16 matrix moves (warp-wide)
 
-// Four 8 x 8 b16 matrices from shared memory, transposed: lanes 8i .. 8i+7
-// give the addresses of the eight 16-byte rows of matrix i; thread t receives
-// in r[i] the elements (2(t%4), t/4) and (2(t%4)+1, t/4) of matrix i.
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t row_addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(row_addr)
-                 : "memory");
-}
-
-// Four 8 x 8 b16 matrices to shared memory: lanes 8i .. 8i+7 give the row
-// addresses of matrix i; thread t holds in r[i] the elements (t/4, 2(t%4)) and
-// (t/4, 2(t%4)+1) of matrix i.  After ldmatrix_x4_trans this stores the
-// transposes.
-__device__ __forceinline__ void stmatrix_x4(uint32_t row_addr, const uint32_t (&r)[4]) {
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(row_addr), "r"(r[0]),
-                 "r"(r[1]), "r"(r[2]), "r"(r[3])
-                 : "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05 (5th-generation tensor cores)
 
 // Tensor-memory allocation: executed by one full warp.  The allocated base
@@ -260,10 +240,11 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // Instruction descriptor of kind::f16 with fp16 A and B (both K-major) and an
 // fp32 accumulator, for an M x N tile.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major = false) {
     return (1u << 4)                          // D format: f32
            | (0u << 7) | (0u << 10)           // A, B format: f16
-           | (0u << 15) | (0u << 16)          // A, B K-major
+           | (0u << 15)                       // A K-major
+           | ((b_mn_major ? 1u : 0u) << 16)   // B K-major, or MN-major
            | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
@@ -278,6 +259,21 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t smem_addr) {
     d |= (uint64_t)((1024u >> 4) & 0x3FFF) << 32;  // stride byte offset: 8 rows x 128 B
     d |= (uint64_t)1 << 46;                    // descriptor version for sm_100 family
     d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+    return d;
+}
+
+// Shared-memory matrix descriptor for an MN-major operand in the 128-byte
+// swizzled layout: each 128-byte row holds 64 consecutive fp16 elements along
+// MN for one K index, 8-row groups (8 K indices) are 1024 bytes apart, and
+// the next 64 MN elements start `mn_stride` bytes further.  A step of 16 along
+// K adds 16 rows = 2048 bytes to the start (128 in the address field).
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t smem_addr, uint32_t mn_stride) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFF);
+    d |= (uint64_t)((mn_stride >> 4) & 0x3FFF) << 16;  // leading byte offset: between 64-element MN blocks
+    d |= (uint64_t)((1024u >> 4) & 0x3FFF) << 32;      // stride byte offset: 8 K rows x 128 B
+    d |= (uint64_t)1 << 46;                            // descriptor version for sm_100 family
+    d |= (uint64_t)2 << 61;                            // 128-byte swizzle
     return d;
 }
 

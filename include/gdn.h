@@ -168,8 +168,8 @@ typedef struct gdn_forward_args {
  * (tensor-core) kernel may run.  The size is that of the two-phase chunked
  * evaluation: a header (work counter, the longest-first list of sequences,
  * each sequence's first chunk) plus one record per (64-token chunk, key head)
- * of 48 KiB and one per (chunk, value head) of 17,408 bytes, for at most
- * T/64 + B chunks -- about 1.6 MB per 64 tokens at Hk = 16, Hv = 48.
+ * of 32 KiB and one per (chunk, value head) of 17,408 bytes, for at most
+ * T/64 + B chunks -- about 1.36 MB per 64 tokens at Hk = 16, Hv = 48.
  *
  * gdn_forward also accepts a smaller workspace of at least (B + 2) int32
  * (rounded up to 256 bytes): it then runs the single-kernel chunked

@@ -137,9 +137,9 @@ def test_workspace_size_follows_the_plan(lib):
     assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 0
     # long batch at d = 128: the two-phase chunked evaluation may run -> a header
     # ((3 + 2B) int32 rounded up to 1 KiB) plus, for each of at most T/64 + B
-    # chunks, a 48 KiB record per key head and a 17,408-byte record per value head
+    # chunks, a 32 KiB record per key head and a 17,408-byte record per value head
     def two_phase(B, T, Hk, Hv):
-        return ((3 + 2 * B) * 4 + 1023) // 1024 * 1024 + (T // 64 + B) * (Hk * 49152 + Hv * 17408)
+        return ((3 + 2 * B) * 4 + 1023) // 1024 * 1024 + (T // 64 + B) * (Hk * 32768 + Hv * 17408)
     a = _args(num_seqs=8, total_tokens=17000, num_state_slots=8)
     assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0
     assert n.value == two_phase(8, 17000, a.num_k_heads, a.num_v_heads)
@@ -149,7 +149,7 @@ def test_workspace_size_follows_the_plan(lib):
     # the varlen prefill geometry (8 sequences, 15,991 tokens, Hk=16, Hv=48): ~414 MB
     a = _args(num_seqs=8, total_tokens=15991, num_state_slots=8, num_k_heads=16, num_v_heads=48)
     assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0
-    assert n.value == 1024 + 257 * (16 * 49152 + 48 * 17408)
+    assert n.value == 1024 + 257 * (16 * 32768 + 48 * 17408)
     # a max_seqlen hint of at most 32 keeps the batch recurrent
     a = _args(num_seqs=64, total_tokens=64, num_state_slots=64, max_seqlen=1)
     assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 0
