@@ -18,8 +18,9 @@
 // Gamma_s with r >= s are exponentiated (never exp(-Gamma)).
 //
 // Every product is an M = 128 tcgen05.mma (kind::f16, fp16 operands, fp32
-// accumulators in tensor memory) with both operands K-major in the 128-byte
-// swizzled layout, the value dimension (dv = 128) as M:
+// accumulators in tensor memory) with the operands in the 128-byte swizzled
+// layout, K-major except K in MMA5 (read from the tile's K rows as an MN-major
+// operand), and the value dimension (dv = 128) as M:
 //   MMA1  [Q;K] K^T            -> P = Q K^T, G = K K^T      (128 x 64, K = dk)
 //   MMA2  S0 [K ; gamma Q]^T   -> X^T = S0 K^T, S0 (gamma Q)^T (128 x 128, K = dk)
 // Q, K and gamma Q are the three 64-row bands of one 192-row tile, so MMA1
@@ -75,7 +76,7 @@ constexpr uint32_t TM_O = 320;   // S0 (gamma Q)^T + U^T (P o D)^T, 64 columns
 constexpr int OFF_QKG = 0;                 // [192][128]: rows 0-63 Q, 64-127 K, 128-191 gamma Q  48 KiB
 constexpr int QKG_ROWS = 192;
 constexpr int QKG_KB = QKG_ROWS * 128;     // bytes between its two 64-element K blocks
-constexpr int OFF_KT = OFF_QKG + 49152;    // [128][64]: K^T (dk rows, token columns)  16 KiB
+constexpr int OFF_KT = OFF_QKG + 49152;    // 16 KiB, unused (K is read from the K rows as an MN-major operand)
 constexpr int OFF_S16 = OFF_KT + 16384;    // [128][128]: S0 in fp16                    32 KiB
 constexpr int OFF_A32 = OFF_S16 + 32768;   //   (R^T/U^T tiles, idle until R^T is built): A in fp32 [64][65]
 constexpr int OFF_RT = OFF_S16 + 32768;    // [128][64]: R^T, then U^T                  16 KiB
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(NT, 1)
     float *T32 = reinterpret_cast<float *>(sm + OFF_T32);
     float *Mws = reinterpret_cast<float *>(sm + OFF_M);
     const uint32_t a_QKG = ptx::smem_u32(sm + OFF_QKG);
-    const uint32_t a_KT = ptx::smem_u32(sm + OFF_KT), a_S16 = ptx::smem_u32(sm + OFF_S16);
+    const uint32_t a_S16 = ptx::smem_u32(sm + OFF_S16);
     const uint32_t a_RT = ptx::smem_u32(sm + OFF_RT), a_UD = ptx::smem_u32(sm + OFF_UD);
     const uint32_t a_T = ptx::smem_u32(sm + OFF_T), a_PD = ptx::smem_u32(sm + OFF_PD);
 
@@ -425,22 +426,10 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
             __syncthreads();
-            // ---- A4: K^T (thread: one dk row, 16 tokens) and gamma Q (from the fp16 Q rows)
+            // ---- A4: gamma Q (from the fp16 Q rows); the state update reads K from the
+            //      K rows as an MN-major operand, so no transposed copy is built
             {
-                const int j = tid >> 2, sg = (tid & 3) * 16;
                 const uint8_t *kq = sm + OFF_QKG;
-#pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s = sg + 8 * m + 2 * e;
-                        const unsigned short lo = *reinterpret_cast<const unsigned short *>(kq + sw(64 + s, j, QKG_ROWS));
-                        const unsigned short hi = *reinterpret_cast<const unsigned short *>(kq + sw(65 + s, j, QKG_ROWS));
-                        w[e] = (uint32_t)lo | ((uint32_t)hi << 16);
-                    }
-                    *reinterpret_cast<uint4 *>(sm + OFF_KT + sw(j, sg + 8 * m, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
 #pragma unroll
                 for (int it = 0; it < 2; ++it) {
                     const int e = tid + NT * it;       // 64 rows x 16 pieces of 8 elements
@@ -599,12 +588,14 @@ __global__ void __launch_bounds__(NT, 1)
             // ---- G: MMA4 (output) and MMA5 (state)
             if (tid == 0) {
                 ptx::tc_fence_after();
-                const uint32_t i64 = ptx::idesc_f16_f32(128, 64), i128 = ptx::idesc_f16_f32(128, 128);
+                const uint32_t i64 = ptx::idesc_f16_f32(128, 64), i128_bmn = ptx::idesc_f16_f32(128, 128, true);
                 for (int ks = 0; ks < CH / 16; ++ks) {
                     ptx::mma_f16(tm + TM_O, ptx::sdesc_k_sw128(a_RT + ks * 32), ptx::sdesc_k_sw128(a_PD + ks * 32),
                                  i64, 1u);
-                    ptx::mma_f16(tm + TM_S, ptx::sdesc_k_sw128(a_UD + ks * 32), ptx::sdesc_k_sw128(a_KT + ks * 32),
-                                 i128, (state_live || ks > 0) ? 1u : 0u);
+                    // K rows (64..127) of the [Q;K;gamma Q] tile as MN-major B: 16 tokens = 2048 B per step
+                    ptx::mma_f16(tm + TM_S, ptx::sdesc_k_sw128(a_UD + ks * 32),
+                                 ptx::sdesc_mn_sw128(a_QKG + 64 * 128 + ks * 2048, QKG_KB),
+                                 i128_bmn, (state_live || ks > 0) ? 1u : 0u);
                 }
                 ptx::mma_commit(&sh.bar);
             }
