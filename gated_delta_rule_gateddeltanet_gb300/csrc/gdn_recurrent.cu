@@ -817,10 +817,14 @@ cudaError_t launch_dk(const ForwardParams &p, cudaStream_t stream) {
     auto kern = recurrent_mixed_kernel<TIO, DK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
+    int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NTM, smem)) != cudaSuccess) return e;
+    // CTAs per SM depend on the kernel only: asked once (0 if the query fails: one per SM)
+    static const int per_sm = [&] {
+        int n = 0;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NTM, smem) == cudaSuccess ? n : 0;
+    }();
     const long long items = (long long)p.B * p.Hv * nrb;
     if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
     const int grid = (int)std::min<long long>(items, (long long)std::max(per_sm, 1) * sms);
