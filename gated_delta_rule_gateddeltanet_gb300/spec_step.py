@@ -11,8 +11,8 @@ the conv side: capture of the appended inputs, [batch, capacity, channels].
 
 At the Qwen decode geometry the four kernels of a step run for tens of
 microseconds in total, so host launch overhead is a large part of a step.
-Here the step is four C-ABI calls on one stream with arguments built once,
-recorded into a CUDA graph:
+Here the step is four C-ABI calls with arguments built once, recorded into a
+CUDA graph:
 
   1. varlen_causal_conv_with_state: x -> y = silu(conv(x)), from the committed
      conv states (slots ``src``), capturing every draft token's input;
@@ -22,6 +22,10 @@ recorded into a CUDA graph:
   3. causal_conv_replay_prefix and 4. gdn_replay_prefix: the accepted prefix
      (``accept_len``, device data the caller writes before each replay) into
      the inactive slots ``dst`` of both banks.
+
+The conv replay needs only the conv call's capture, so it runs on a side
+stream while the GDN forward (latency-bound, HBM mostly idle) runs on the
+main one; the main stream waits for it at the end of the step.
 
 Every per-step quantity is device memory read at replay time (inputs, gate
 inputs, slot lists, accepted lengths), so one graph serves every step: the
@@ -36,8 +40,7 @@ import ctypes
 
 import torch
 
-from . import (DTYPE, GdnError, build_conv_args, build_forward_args, capsule_width, load_library, workspace_size,
-               _stream_handle)
+from . import DTYPE, GdnError, build_conv_args, build_forward_args, capsule_width, load_library, workspace_size
 
 
 class SpeculativeStep:
@@ -106,28 +109,36 @@ class SpeculativeStep:
         self._keep = (k1, k2, q, k, v, conv_weight, conv_bias, A_log, dt_bias)
         self.lib = load_library()
         self.graph = None
+        self._side = torch.cuda.Stream(dev)
+        self._conv_done, self._side_done = torch.cuda.Event(), torch.cuda.Event()
 
     def run_eager(self, stream=None):
-        """The four calls, launched one by one on ``stream`` (default: current)."""
-        s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream_handle(self.dev)
+        """The four calls on ``stream`` (default: current), the conv replay
+        forked onto a side stream after the conv call and joined at the end."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.dev)
+        s = ctypes.c_void_p(main.cuda_stream)
         lib = self.lib
         p = lambda t: ctypes.c_void_p(t.data_ptr())
         rc = lib.varlen_causal_conv_with_state(ctypes.byref(self.conv_args), s)
         if rc:
             raise GdnError(rc, "varlen_causal_conv_with_state")
-        rc = lib.gdn_forward(ctypes.byref(self.fwd_args), s)
-        if rc:
-            raise GdnError(rc, "gdn_forward")
+        self._conv_done.record(main)
+        self._side.wait_event(self._conv_done)
         two_r, C, km1 = self.conv_bank.shape
         rc = lib.causal_conv_replay_prefix(p(self.conv_bank), two_r, self.R, C, km1 + 1, DTYPE[self.conv_bank.dtype],
                                            p(self.src), p(self.dst), p(self.conv_values), self.D, p(self.accept_len),
-                                           p(self.status), s)
+                                           p(self.status), ctypes.c_void_p(self._side.cuda_stream))
         if rc:
             raise GdnError(rc, "causal_conv_replay_prefix")
+        self._side_done.record(self._side)
+        rc = lib.gdn_forward(ctypes.byref(self.fwd_args), s)
+        if rc:
+            raise GdnError(rc, "gdn_forward")
         rc = lib.gdn_replay_prefix(p(self.gdn_bank), two_r, self.R, self.Hk, self.Hv, self.d, self.d, p(self.src),
                                    p(self.dst), p(self.capsules), self.D, p(self.accept_len), p(self.status), s)
         if rc:
             raise GdnError(rc, "gdn_replay_prefix")
+        main.wait_event(self._side_done)
 
     def capture(self):
         """Records the step into a CUDA graph, after one eager warm-up step on
