@@ -72,6 +72,10 @@ struct ConvReplayParams {
 cudaError_t launch_conv(const ConvParams &p, cudaStream_t stream);
 cudaError_t launch_conv_replay(const ConvReplayParams &p, cudaStream_t stream);
 
+// Spans of at most p.max_len tokens: the CUDA-core decode kernel when every
+// span has at most one token (T == B), else the persistent mixed kernel
+// (one-token spans on the same CUDA-core code, longer ones on the warp
+// tensor cores four tokens at a time).
 cudaError_t launch_recurrent(const ForwardParams &p, cudaStream_t stream);
 // dst[m] = src[m]^T for `num` row-major rows x cols FP32 matrices.
 cudaError_t launch_transpose(const float *src, float *dst, long long num, int rows, int cols, cudaStream_t stream);
