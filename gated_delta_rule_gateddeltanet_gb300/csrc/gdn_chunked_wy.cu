@@ -227,7 +227,8 @@ __device__ void tri_inverse_inplace(float *AT, float *M, int tid) {
 // per lane).  Raw mode: g = exp(-exp(A_log) softplus(a + dt_bias)),
 // beta = sigmoid(b); precomputed mode: g = a, beta = b.  Log decays are
 // floored at LOG_DECAY_FLOOR; tokens at or past `n` get g = 1, beta = 0 (no
-// effect).  Writes the within-chunk cumulative log decay Gamma and beta to
+// effect).  Writes the within-chunk cumulative log decay Gamma (in log2
+// units, for the exponentials of A and P o D) and beta to
 // shared memory, the scan kernel's per-token factors (beta, beta gamma,
 // gamma = exp(Gamma), exp(Gamma_last - Gamma)) to the record at `fdst`, and
 // the capsule decays.
@@ -273,7 +274,7 @@ __device__ __forceinline__ void chunk_gates(const ForwardParams &p, int t0, int 
     for (int u = 0; u < 2; ++u) {
         const int s = lane + 32 * u;
         const float gm = expf(c[u]);
-        Gam[s] = c[u];
+        Gam[s] = c[u] * 1.4426950408889634f;  // log2 units: the A and P o D exponentials are bare ex2
         Beta[s] = bt[u];
         fdst[F_BETA + s] = bt[u];
         fdst[F_BG + s] = bt[u] * gm;
@@ -282,6 +283,15 @@ __device__ __forceinline__ void chunk_gates(const ForwardParams &p, int t0, int 
         const int tl = t0 + s - bos;
         if (p.caps && s < n && tl < p.cap) p.caps[((long long)b * p.cap + tl) * p.W + h] = gt[u];
     }
+}
+
+// 2^x on the special-function unit (relative error about 2^-22; flushes
+// subnormal results to zero, which only the masked-out or negligible decay
+// products reach).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // N consecutive floats (N a multiple of 4) from 16-byte aligned shared memory.
@@ -331,7 +341,8 @@ __global__ void __launch_bounds__(PT, 4)
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bar, lbar;
     __shared__ uint32_t tmem_base;
-    __shared__ float Gam_s[GH][CH], Beta_s[GH][CH];
+    __shared__ __align__(16) float Gam_s[GH][CH];  // within-chunk cumulative log2 decay per value head
+    __shared__ float Beta_s[GH][CH];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr bool STAGED = sizeof(TIO) == 2;
 
@@ -533,23 +544,29 @@ __global__ void __launch_bounds__(PT, 4)
             float v[32];
             ptx::tmem_ld32(tm + lane_sel + c32, v);
             const int r = row & 63;
-            const float *Gm = Gam_s[wi];
+            const float *Gm = Gam_s[wi];  // cumulative log2 decays: columns read 8 at a time (broadcast)
             const float Gr = Gm[r];
             if (quarter >= 2) {  // lanes 64-127: G = K K^T -> A (strictly lower)
                 const float br = Beta_s[wi][r];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int s = c32 + j;
-                    AT[r * AS + s] = (s < r) ? br * __expf(Gr - Gm[s]) * v[j] : 0.f;
+                for (int j = 0; j < 32; j += 8) {
+                    float gc[8];
+                    ld_fn<8>(Gm + c32 + j, gc);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int s = c32 + j + e;
+                        AT[r * AS + s] = (s < r) ? br * ex2_approx(Gr - gc[e]) * v[j + e] : 0.f;
+                    }
                 }
             } else {  // lanes 0-63: P = Q K^T -> P o D (lower, diagonal included)
 #pragma unroll
                 for (int j = 0; j < 32; j += 8) {
-                    float w[8];
+                    float w[8], gc[8];
+                    ld_fn<8>(Gm + c32 + j, gc);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int s = c32 + j + e;
-                        w[e] = (s <= r) ? v[j + e] * __expf(Gr - Gm[s]) : 0.f;
+                        w[e] = (s <= r) ? v[j + e] * ex2_approx(Gr - gc[e]) : 0.f;
                     }
                     st_h8(tpd + VREC_PD, sw(r, c32 + j, 64), w);
                 }
