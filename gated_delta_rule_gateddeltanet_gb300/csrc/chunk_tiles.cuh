@@ -46,6 +46,18 @@ __device__ __forceinline__ void ld4<__half>(const __half *p, float (&v)[4]) {
 }
 
 
+// 2^x on the special-function unit (relative error about 2^-22; flushes
+// subnormal results to zero, which only negligible decay products reach).
+// The chunked kernels keep cumulative log decays in log2 units so that each
+// decay factor of A, P o D and the decayed deltas is one such instruction.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+constexpr float LOG2E = 1.4426950408889634f;
+
 // ---- Small products on the warp-level tensor cores
 //
 // The block products of the triangular inverse are 16 x 16 and 32 x 32: too

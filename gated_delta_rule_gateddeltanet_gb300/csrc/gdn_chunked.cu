@@ -159,7 +159,7 @@ __device__ void tri_inverse(const float *A, float *T32, float *M, int tid) {
 }
 
 struct Shared {
-    float Gam[CH], gam[CH], beta[CH], gate[CH];
+    float Gam[CH], gam[CH], beta[CH], gate[CH];  // Gam: cumulative log decay in log2 units
     uint64_t bar;   // MMA completion
     uint64_t bar1;  // MMA1 completion (its own barrier: two commits on one barrier before a wait would alias phases)
     uint64_t lbar;  // staged rows of the next chunk
@@ -310,8 +310,8 @@ __global__ void __launch_bounds__(NT, 1)
                 if (lane >= o) { c0 += y0; c1 += y1; }
             }
             c1 += __shfl_sync(0xffffffffu, c0, 31);
-            sh.Gam[lane] = c0;
-            sh.Gam[lane + 32] = c1;
+            sh.Gam[lane] = c0 * LOG2E;  // log2 units: every decay factor below is one ex2
+            sh.Gam[lane + 32] = c1 * LOG2E;
             sh.gam[lane] = expf(c0);
             sh.gam[lane + 32] = expf(c1);
             sh.beta[lane] = bt[0];
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int s = c16 + j;
-                        A32[r * AS + s] = (s < r) ? br * __expf(Gr - sh.Gam[s]) * v[j] : 0.f;
+                        A32[r * AS + s] = (s < r) ? br * ex2_approx(Gr - sh.Gam[s]) * v[j] : 0.f;
                     }
                 } else {  // lanes 0-63: P
 #pragma unroll
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int s = c16 + j + e;
-                            w[e] = (s <= r) ? v[j + e] * __expf(Gr - sh.Gam[s]) : 0.f;
+                            w[e] = (s <= r) ? v[j + e] * ex2_approx(Gr - sh.Gam[s]) : 0.f;
                         }
                         st_h4(sm + OFF_PD, sw(r, c16 + j, 64), w[0], w[1], w[2], w[3]);
                     }
@@ -571,7 +571,7 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int j = 0; j < 16; j += 4) {
                     float w[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) w[e] = __expf(Gl - sh.Gam[c16 + j + e]) * v[j + e];
+                    for (int e = 0; e < 4; ++e) w[e] = ex2_approx(Gl - sh.Gam[c16 + j + e]) * v[j + e];
                     st_h4(sm + OFF_RT, sw(row, c16 + j, 128), v[j], v[j + 1], v[j + 2], v[j + 3]);
                     st_h4(sm + OFF_UD, sw(row, c16 + j, 128), w[0], w[1], w[2], w[3]);
                 }

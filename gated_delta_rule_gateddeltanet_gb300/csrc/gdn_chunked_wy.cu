@@ -274,7 +274,7 @@ __device__ __forceinline__ void chunk_gates(const ForwardParams &p, int t0, int 
     for (int u = 0; u < 2; ++u) {
         const int s = lane + 32 * u;
         const float gm = expf(c[u]);
-        Gam[s] = c[u] * 1.4426950408889634f;  // log2 units: the A and P o D exponentials are bare ex2
+        Gam[s] = c[u] * LOG2E;  // log2 units: the A and P o D exponentials are bare ex2
         Beta[s] = bt[u];
         fdst[F_BETA + s] = bt[u];
         fdst[F_BG + s] = bt[u] * gm;
@@ -283,15 +283,6 @@ __device__ __forceinline__ void chunk_gates(const ForwardParams &p, int t0, int 
         const int tl = t0 + s - bos;
         if (p.caps && s < n && tl < p.cap) p.caps[((long long)b * p.cap + tl) * p.W + h] = gt[u];
     }
-}
-
-// 2^x on the special-function unit (relative error about 2^-22; flushes
-// subnormal results to zero, which only the masked-out or negligible decay
-// products reach).
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
 }
 
 // N consecutive floats (N a multiple of 4) from 16-byte aligned shared memory.
