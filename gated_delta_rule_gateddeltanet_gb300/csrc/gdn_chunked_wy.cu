@@ -525,7 +525,8 @@ __global__ void __launch_bounds__(PT, 4)
             const int r = row & 63;
             if (quarter >= 2) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) AT[r * AS + c32 + j] = 0.f;
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(AT + r * AS + c32 + j) = make_float4(0.f, 0.f, 0.f, 0.f);
             } else {
                 const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -541,13 +542,18 @@ __global__ void __launch_bounds__(PT, 4)
                 const float br = Beta_s[wi][r];
 #pragma unroll
                 for (int j = 0; j < 32; j += 8) {
-                    float gc[8];
+                    float gc[8], w[8];
                     ld_fn<8>(Gm + c32 + j, gc);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int s = c32 + j + e;
-                        AT[r * AS + s] = (s < r) ? br * ex2_approx(Gr - gc[e]) * v[j + e] : 0.f;
+                        w[e] = (s < r) ? br * ex2_approx(Gr - gc[e]) * v[j + e] : 0.f;
                     }
+                    // 16-byte stores: with the 68-float row stride a quarter-warp's 8 rows
+                    // cover all 32 banks (single-float stores of one column hit 8)
+                    float4 *dst = reinterpret_cast<float4 *>(AT + r * AS + c32 + j);
+                    dst[0] = make_float4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_float4(w[4], w[5], w[6], w[7]);
                 }
             } else {  // lanes 0-63: P = Q K^T -> P o D (lower, diagonal included)
 #pragma unroll
