@@ -628,14 +628,15 @@ constexpr int S_V = S_VREC + VREC_BYTES;    // fp16 v rows of the chunk [64][128
 constexpr int STAGE_BYTES = S_V + 16384;
 constexpr int OFF_S16 = 2 * STAGE_BYTES;    // [128][128] fp16 S0 (two K-blocks)
 constexpr int OFF_RT = OFF_S16 + 32768;     // [128][64] fp16 R^T, then U^T
-constexpr int SCAN_SMEM = OFF_RT + 16384 + 1024;  // + slack for the 1024-byte alignment
+constexpr int OFF_OT = OFF_RT + 16384;      // fp16 I/O: a full chunk's outputs [64 tokens][128] for one tensor store
+constexpr int SCAN_SMEM = OFF_OT + 16384 + 1024;  // + slack for the 1024-byte alignment
 static_assert(S_V % 1024 == 0 && STAGE_BYTES % 1024 == 0, "stage layout");
 static_assert(SCAN_SMEM + 1024 <= 227 * 1024, "shared memory budget (dynamic + static)");
 
 template <typename TIO>
 __global__ void __launch_bounds__(NT, 1)
     wy_scan_kernel(const ForwardParams p, int32_t *ws, const uint8_t *krec, const uint8_t *vrec,
-                   const __grid_constant__ CUtensorMap map_v) {
+                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o, int out_tma) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bar;      // MMA completion
@@ -749,12 +750,20 @@ __global__ void __launch_bounds__(NT, 1)
                 ptx::tmem_st_wait();
             }
         };
-        // outputs of the chunk starting at tp (n tokens): o = scale (gamma O' + Y)
-        auto write_outputs = [&](int tp, int n, uint32_t ox) {
+        // outputs of the chunk starting at tp (n tokens): o = scale (gamma O' + Y).  With
+        // `tile` (fp16, a full chunk) they go to the output tile for one tensor store.
+        auto write_outputs = [&](int tp, int n, uint32_t ox, bool tile) {
             float o1[CW], y[CW], gm[CW];
             ptx::tmem_ld<CW>(tm + lane_sel + ox + c16, o1);
             ptx::tmem_ld<CW>(tm + lane_sel + TM_Y + c16, y);
             ld_fn<CW>(gam_prev + c16, gm);
+            if (tile) {
+                __half *ot = reinterpret_cast<__half *>(sm + OFF_OT);
+#pragma unroll
+                for (int j = 0; j < CW; ++j) ot[(c16 + j) * DH + row] = __float2half_rn(p.scale * fmaf(gm[j], o1[j], y[j]));
+                ptx::fence_proxy_async_smem();  // visible to the tensor store after the next barrier
+                return;
+            }
 #pragma unroll
             for (int j = 0; j < CW; ++j) {
                 const int s = c16 + j;
@@ -762,6 +771,7 @@ __global__ void __launch_bounds__(NT, 1)
                     og[((long long)(tp + s) * p.Hv + h) * DH + row] = from_f32<TIO>(p.scale * fmaf(gm[j], o1[j], y[j]));
             }
         };
+        const bool out_tile = STAGED && out_tma;
 
         // ---- chain start: the initial state into tensor memory, chunk 0's inputs
         if (state_live) {
@@ -801,8 +811,12 @@ __global__ void __launch_bounds__(NT, 1)
                 ptx::mma_commit(&bar);
             }
             // ---- while MMA2 runs: the outputs of chunk c - 1
-            if (c > 0) write_outputs(t0 - CH, CH, TM_OX + 128u * (uint32_t)(st ^ 1));
+            if (c > 0) write_outputs(t0 - CH, CH, TM_OX + 128u * (uint32_t)(st ^ 1), out_tile);
             if (!mma_wait()) { failed = true; break; }
+            if (c > 0 && out_tile && tid == 0) {  // chunk c - 1's outputs, one tensor store
+                ptx::tma_store_2d(&map_o, sm + OFF_OT, h * DH, t0 - CH);
+                ptx::bulk_commit();
+            }
             // ---- R^T = diag(beta) V - diag(beta gamma) X^T, transposed; this chunk's gamma for its outputs
             {
                 float x[CW];
@@ -881,8 +895,9 @@ __global__ void __launch_bounds__(NT, 1)
                 build_s16(reinterpret_cast<const float *>(sm + (st ^ 1) * STAGE_BYTES + S_VREC + VREC_F),
                           min(CH, eos - t0 - CH));
             } else {
-                write_outputs(t0, n, ox);  // the last chunk's outputs: no MMA left to overlap
+                write_outputs(t0, n, ox, false);  // the last chunk's outputs: no MMA left to overlap
             }
+            if (out_tile && tid == 0) ptx::bulk_wait_read_all();  // the output tile is free again
             mma_ready();
         }
         if (failed) break;
@@ -913,6 +928,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int st = 0; st < 2; ++st)  // and the staged copies
             if (pending[st]) ptx::mbar_wait_bounded(&lbar[st], lph[st], WAIT_LIMIT);
     }
+    if (tid == 0) ptx::bulk_wait_all();  // the output tensor stores are complete
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -964,7 +980,11 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, uint8_t *ws, cudaStre
     if (e != cudaSuccess) return e;
     const long long chains = (long long)p.B * p.Hv;
     const int grid = (int)(chains < num_sms() ? chains : num_sms());
-    scan<<<grid, NT, SCAN_SMEM, stream>>>(p, hdr, krec, vrec, mv);
+    // outputs: fp16 chunks go out as 64-token x 128-feature tensor stores when the map encodes
+    CUtensorMap mo{};
+    const int out_tma = sizeof(TIO) == 2 &&
+                        encode_rows_f16(&mo, p.out, (long long)p.Hv * DH, (long long)p.Hv * DH, p.T, DH, CH, false);
+    scan<<<grid, NT, SCAN_SMEM, stream>>>(p, hdr, krec, vrec, mv, mo, out_tma);
     return cudaGetLastError();
 }
 

@@ -80,6 +80,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tensor_m
         : "memory");
 }
 
+// Shared -> global 2-D tensor store of one box from a tensor map, tracked by
+// the issuing thread's bulk async-groups (coordinates must not be negative).
+__device__ __forceinline__ void tma_store_2d(const void *tensor_map, const void *src_smem, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tensor_map),
+                 "r"(smem_u32(src_smem)), "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Shared -> global, tracked by the issuing thread's bulk async-groups.
 __device__ __forceinline__ void bulk_s2g(void *dst_gmem, const void *src_smem, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst_gmem),
