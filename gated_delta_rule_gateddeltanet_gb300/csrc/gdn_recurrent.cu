@@ -106,6 +106,14 @@ struct Span {
     size_t off;  // first float of the tile in the state arrays
 };
 
+// Tensor maps for the tensor path's output stores: outputs [T, Hv dv] and
+// capsules [B cap, W], boxes of TB rows x ROWS elements; ok = 0 when a map
+// could not be encoded or a box coordinate would not be 16-byte aligned.
+struct OutMaps {
+    CUtensorMap out, caps;
+    int ok;
+};
+
 // Resolves and checks the work item (sequence b, value head h, row block
 // rb): its span and state slot.  False when there is nothing to do (a bad
 // descriptor, which is flagged, or a span longer than max_len, which the
@@ -421,7 +429,7 @@ __device__ __forceinline__ int rows_at(int r, int col) {
 template <typename TIO, int DK>
 __device__ __forceinline__ bool span_tensor_cores(const ForwardParams &p, const Span &sp, const CUtensorMap *map,
                                                   float *rows_s, uint64_t *bar, uint32_t &parity, const Span *next,
-                                                  bool reuse) {
+                                                  bool reuse, const OutMaps &om) {
     constexpr int NJ = DK / 8;       // 8-column blocks per row
     constexpr int VS = DK + 8;       // row stride of the staged vectors (bank-conflict free reads)
     constexpr int EPL = DK / 32;     // q/k elements per lane when normalising
@@ -431,7 +439,9 @@ __device__ __forceinline__ bool span_tensor_cores(const ForwardParams &p, const 
     __shared__ __align__(16) float vl_s[2 * TB][VS];
     // per token t: beta_t, beta_t G_t, scale G_t, r(n, t); and the pair coefficients
     __shared__ float bt_s[TB], bG_s[TB], sG_s[TB], eG_s[TB];
-    __shared__ float v_s[TB][ROWS], o_s[TB][ROWS], u_s[TB][ROWS];
+    __shared__ float v_s[TB][ROWS];
+    __shared__ __align__(128) TIO o_s[TB][ROWS];   // the group's outputs (I/O type): one tensor-store box
+    __shared__ __align__(128) float u_s[TB][ROWS]; // the group's deltas: one tensor-store box
     __shared__ float g_s[TB], beta_s[TB];
     __shared__ float mkk_s[TB][TB], mq_s[TB][TB];  // beta_t r(t,s) k_s.k_t (s < t); scale r(t,s) k_s.q_t (s <= t)
     __shared__ float dkk_s[TB][TB], dkq_s[TB][TB];  // k_s.k_t and k_s.q_t (s <= t), kept for reuse
@@ -554,6 +564,7 @@ __device__ __forceinline__ bool span_tensor_cores(const ForwardParams &p, const 
         }
         __syncthreads();
 
+        if (om.ok && tid == 0) ptx::bulk_wait_read_all();  // the previous group's stores have read o_s, u_s
         // ---- stage 2: warp t forms row t of the pair coefficients (k_s.k_t, k_s.q_t
         //      for s <= t) and its per-token factors
         {
@@ -669,11 +680,14 @@ __device__ __forceinline__ bool span_tensor_cores(const ForwardParams &p, const 
                 ob = fmaf(m, ub[s], ob);
                 if (s == c) uc_a = ua[s], uc_b = ub[s];
             }
-            o_s[c][r0] = oa;
-            o_s[c][r1] = ob;
+            o_s[c][r0] = from_f32<TIO>(oa);
+            o_s[c][r1] = from_f32<TIO>(ob);
             u_s[c][r0] = uc_a;
             u_s[c][r1] = uc_b;
         }
+        // a full group whose outputs and deltas all land inside this span and block: two tensor stores
+        const bool tma_group = om.ok && nt == TB && rows_here == ROWS && (!p.caps || t0 - bos + TB <= p.cap);
+        if (tma_group) ptx::fence_proxy_async_smem();
 
         // ---- S = G_n S0 + [r(n, t) u_t] [k_t]: the rank-4 update accumulates into the rows
         {
@@ -701,15 +715,24 @@ __device__ __forceinline__ bool span_tensor_cores(const ForwardParams &p, const 
         __syncthreads();
 
         // ---- outputs and capsules of the group
-        for (int i = tid; i < nt * ROWS; i += NTM) {
-            const int tt = i / ROWS, rr = i % ROWS;
-            if (rr >= rows_here) continue;
-            const int row = rb * ROWS + rr;
-            const long long t = t0 + tt;
-            og[(t * p.Hv + h) * p.dv + row] = from_f32<TIO>(o_s[tt][rr]);
-            const int tl = (int)(t - bos);
-            if (p.caps && tl < p.cap)
-                p.caps[((long long)b * p.cap + tl) * p.W + ubase + (long long)h * p.dv + row] = u_s[tt][rr];
+        if (tma_group) {
+            if (tid == 0) {
+                ptx::tma_store_2d(&om.out, &o_s[0][0], h * p.dv + rb * ROWS, t0);
+                if (p.caps)
+                    ptx::tma_store_2d(&om.caps, &u_s[0][0], (int)ubase + h * p.dv + rb * ROWS, b * p.cap + (t0 - bos));
+                ptx::bulk_commit();
+            }
+        } else {
+            for (int i = tid; i < nt * ROWS; i += NTM) {
+                const int tt = i / ROWS, rr = i % ROWS;
+                if (rr >= rows_here) continue;
+                const int row = rb * ROWS + rr;
+                const long long t = t0 + tt;
+                og[(t * p.Hv + h) * p.dv + row] = o_s[tt][rr];
+                const int tl = (int)(t - bos);
+                if (p.caps && tl < p.cap)
+                    p.caps[((long long)b * p.cap + tl) * p.W + ubase + (long long)h * p.dv + row] = u_s[tt][rr];
+            }
         }
         if (p.caps && rb == 0) {
             for (int i = tid; i < nt * (DK + 1); i += NTM) {
@@ -746,7 +769,8 @@ __device__ __forceinline__ bool span_tensor_cores(const ForwardParams &p, const 
 // of one-shot CTAs would instead pay the full load latency in every wave).
 template <typename TIO, int DK>
 __global__ void __launch_bounds__(NTM, 4)
-    recurrent_mixed_kernel(const ForwardParams p, int items, const __grid_constant__ CUtensorMap rows_map) {
+    recurrent_mixed_kernel(const ForwardParams p, int items, const __grid_constant__ CUtensorMap rows_map,
+                           const __grid_constant__ OutMaps out_maps) {
     extern __shared__ __align__(128) float dyn_s[];  // the CUDA-core path's tile, or (1024-aligned) the swizzled rows
     float *rows_s = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(dyn_s) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t rows_bar;
@@ -780,8 +804,10 @@ __global__ void __launch_bounds__(NTM, 4)
                 const int key = cur.b * p.Hk + cur.kh;
                 const bool single = cur.eos - cur.bos <= TB;
                 if (!span_tensor_cores<TIO, DK>(p, cur, &rows_map, rows_s, &rows_bar, parity, nxt_rows ? &nxt : nullptr,
-                                                single && staged == key))
+                                                single && staged == key, out_maps)) {
+                    if (out_maps.ok && threadIdx.x == 0) ptx::bulk_wait_all();
                     return;
+                }
                 staged = single ? key : -1;
                 issued = nxt_rows;
             } else {
@@ -795,6 +821,7 @@ __global__ void __launch_bounds__(NTM, 4)
         cur_ok = nxt_ok;
         it = nx;
     }
+    if (out_maps.ok && threadIdx.x == 0) ptx::bulk_wait_all();  // the output tensor stores are complete
 }
 
 template <typename TIO, int DK>
@@ -814,6 +841,21 @@ cudaError_t launch_dk(const ForwardParams &p, cudaStream_t stream) {
     memset(&rows_map, 0, sizeof(rows_map));
     if (p.init && !encode_rows_f32(&rows_map, p.init, DK, (long long)p.num_slots * p.Hv * p.dv, 32, ROWS, true))
         return cudaErrorInvalidValue;
+    // outputs and capsule deltas of full groups as tensor stores: box coordinates must be
+    // 16-byte aligned (capsule deltas start at float Hv + Hk dk of a row)
+    OutMaps out_maps;
+    memset(&out_maps, 0, sizeof(out_maps));
+    {
+        const long long ubase = (long long)p.Hv + (long long)p.Hk * DK;
+        bool ok = !p.caps || (ubase % 4 == 0 && p.W % 4 == 0);
+        if (ok)
+            ok = p.io_f16 ? encode_rows_f16(&out_maps.out, p.out, (long long)p.Hv * p.dv, (long long)p.Hv * p.dv, p.T,
+                                            ROWS, TB, false)
+                          : encode_rows_f32(&out_maps.out, static_cast<const float *>(p.out), (long long)p.Hv * p.dv, p.T,
+                                            ROWS, TB, false);
+        if (ok && p.caps) ok = encode_rows_f32(&out_maps.caps, p.caps, p.W, (long long)p.B * p.cap, ROWS, TB, false);
+        out_maps.ok = ok ? 1 : 0;
+    }
     auto kern = recurrent_mixed_kernel<TIO, DK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -828,7 +870,7 @@ cudaError_t launch_dk(const ForwardParams &p, cudaStream_t stream) {
     const long long items = (long long)p.B * p.Hv * nrb;
     if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
     const int grid = (int)std::min<long long>(items, (long long)std::max(per_sm, 1) * sms);
-    kern<<<grid, NTM, smem, stream>>>(p, (int)items, rows_map);
+    kern<<<grid, NTM, smem, stream>>>(p, (int)items, rows_map, out_maps);
     return cudaGetLastError();
 }
 
