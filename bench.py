@@ -129,8 +129,17 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
+        with open(self.path) as fh:
+            lines = fh.readlines()
+        os.unlink(self.path)
+        return self.summarise(lines)
+
+    @staticmethod
+    def summarise(lines):
+        """Median and maximum SM clock and the throttle reasons seen in
+        ``nvidia-smi --format=csv,noheader,nounits`` lines of FIELDS."""
         rows = []
-        for line in open(self.path):
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -138,7 +147,6 @@ class ClockSampler:
                 rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
-        os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -831,6 +839,10 @@ def run_cpu_baseline(inp, budget_s=12.0):
                       f"with OpenMP over (request, head) chains"}
 
 
+# seconds of oracle work the reference arm spreads over its warm-up and timed steps
+REFERENCE_BUDGET_S = 150.0
+
+
 def run_reference(a, dist: Dist):
     if dist.rank != 0:
         return
@@ -840,8 +852,7 @@ def run_reference(a, dist: Dist):
     inp = wl.decode_step()
     full = oracle_decode_sample(inp, inp.B)
     t_full = time_oracle_step(full)
-    budget = 150.0
-    per_step = budget / max(1, a.steps + a.warmup)
+    per_step = REFERENCE_BUDGET_S / max(1, a.steps + a.warmup)
     req = int(max(1, min(inp.B, math.floor(inp.B * per_step / max(t_full, 1e-6)))))
     s = oracle_decode_sample(inp, req)
     for _ in range(a.warmup):
