@@ -253,8 +253,8 @@ gdn_status gdn_replay_prefix(float *state_banks, int32_t num_slots, int32_t num_
                              int32_t *status, gdn_stream_t stream);
 
 /*
- * gdn_forward for callers that cannot allocate device memory.  The paper has
- * no counterpart to this entry point.
+ * gdn_forward for callers that cannot allocate device memory.  The onnxruntime
+ * pull requests that define the operator have no counterpart to this call.
  *
  * Some hosts own all device memory through their own allocator and give an
  * operator only its declared inputs and outputs (an inference runtime's

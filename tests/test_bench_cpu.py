@@ -90,3 +90,22 @@ def test_reference_arm_prints_one_contract_line(monkeypatch):
     with redirect_stdout(buf):
         bench.run_reference(args, types.SimpleNamespace(rank=1))
     assert buf.getvalue() == ""
+
+
+def test_clock_sampler_reads_its_process_output(tmp_path, monkeypatch):
+    """The sampler's own start / stop path, with a stand-in for nvidia-smi
+    that prints two samples and then waits to be stopped."""
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    "echo '0, 2070, 2070, 800.0, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "echo '0, 2040, 2070, 900.0, 0x4, Not Active, Not Active, Not Active, Active'\n"
+                    "exec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setattr(bench.shutil, "which", lambda name: str(fake))
+    s = bench.ClockSampler()
+    import time
+    time.sleep(0.5)
+    c = s.stop()
+    assert c["samples"] == 2 and c["sm_mhz"] == 2055 and c["reasons"] == ["sw_power_cap"]
+    monkeypatch.setattr(bench.shutil, "which", lambda name: None)
+    assert bench.ClockSampler().stop() is None
