@@ -272,6 +272,7 @@ def run_gdn(a, dist: Dist):
         extra["serving_mix"] = run_serving_mix(dev, stream, lib, sh)
         extra["state_transpose"] = run_transpose(dev, stream, lib, sh)
         extra["spec_step_graph"] = run_spec_step(dev, stream)
+        extra["long_prefill"] = run_long_prefill(dev, stream)
 
     cpu = None
     if not a.no_cpu and dist.rank == 0 and dist.world == 1:
@@ -477,6 +478,60 @@ def run_prefill(dev, stream):
                          "traffic": recorded_traffic(os.path.join(ROOT, "gated_delta_rule_gateddeltanet_gb300", "csrc",
                                                                   "gdn_chunked_wy.cu"),
                                                      "varlen_prefill.wy_kernels.ncu.md")}}
+
+
+def run_long_prefill(dev, stream):
+    """One 262,144-token sequence (the pages' 256k context), Hk=16, Hv=48,
+    d=128, fp16, zero initial state, under the chunked plan (48 chains) and
+    the sequence-parallel split plan (144 chains + the combining kernels).
+    Inputs are drawn on the device from a seeded generator (5.4 GB, far
+    larger than L2)."""
+    import torch
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    from gated_delta_rule_gateddeltanet_gb300 import workloads as wl
+    T, Hk, Hv, d = 262144, 16, 48, 128
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1006)
+    rnd = lambda shape, dt: torch.randn(shape, generator=gen, device=dev, dtype=dt)
+    q, k, v = rnd((T, Hk, d), torch.float16), rnd((T, Hk, d), torch.float16), rnd((T, Hv, d), torch.float16)
+    aa, bb = rnd((T, Hv), torch.float32), rnd((T, Hv), torch.float32)
+    A_log, dt_bias = (torch.from_numpy(x).to(dev) for x in wl.gate_params(np.random.default_rng(1006), Hv))
+    cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    final = torch.zeros((1, Hv, d, d), dtype=torch.float32, device=dev)
+    out = torch.empty((T, Hv, d), dtype=torch.float16, device=dev)
+    res = {}
+    for plan in ("chunked", "chunked_split"):
+        args, _, _ = gdn.build_forward_args(q, k, v, aa, bb, cu, A_log=A_log, dt_bias=dt_bias, final_state=final,
+                                            output=out, plan=plan)
+        ws = torch.empty(gdn.workspace_size(args), dtype=torch.uint8, device=dev)
+        run = lambda: gdn.gdn_forward(q, k, v, aa, bb, cu, A_log=A_log, dt_bias=dt_bias, final_state=final,
+                                      output=out, plan=plan, workspace=ws)
+        run()
+        times = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        res[plan] = (statistics.median(times), int(ws.numel()))
+        del ws
+        torch.cuda.empty_cache()
+    _, tc_peak, kind = measured_peaks()
+    flops = prefill_algorithmic_flops(T)
+    ms_seq, ws_seq = res["chunked"]
+    ms_split, ws_split = res["chunked_split"]
+    tflops = flops / (ms_split / 1e3) / 1e12
+    return {"workload": "long prefill: 1 sequence of 262,144 tokens, Hk=16, Hv=48, d=128, fp16, zero initial state "
+                        "(inputs drawn on the device, seed 1006)", "tokens": T,
+            "chunked_ms": round(ms_seq, 3), "chunked_split_ms": round(ms_split, 3),
+            "speedup": round(ms_seq / ms_split, 3), "tokens_per_s": round(T / (ms_split / 1e3), 1),
+            "workspace_bytes": {"chunked": ws_seq, "chunked_split": ws_split},
+            "roofline": {"bound": "tensor", "kernel": "split plan: prep + scan (144 chains) + correction + final",
+                         "achieved": round(tflops, 2), "peak": tc_peak,
+                         "peak_kind": f"{kind} dense bf16 burst (fp16 runs at the bf16 rate)", "unit": "TFLOP/s",
+                         "frac": round(tflops / tc_peak, 4), "algorithmic_flops": flops}}
 
 
 # Algorithmic FLOPs of the chunked evaluation per token and value head (chunk

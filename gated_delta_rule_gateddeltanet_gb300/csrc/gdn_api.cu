@@ -17,13 +17,25 @@ bool valid_head_dim(int d) { return d == 32 || d == 64 || d == 128; }
 
 bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+// Plans that put every sequence on a chunked kernel.
+bool forced_chunked(const gdn_forward_args *a) {
+    return a->plan == GDN_PLAN_CHUNKED || a->plan == GDN_PLAN_CHUNKED_SPLIT;
+}
+
+// Workspace of the two-phase chunked evaluation for these arguments.
+size_t two_phase_bytes(const gdn_forward_args *a) {
+    return gdn::chunked_wy_workspace_bytes(a->num_seqs, a->total_tokens, a->num_k_heads, a->num_v_heads,
+                                           a->plan == GDN_PLAN_CHUNKED_SPLIT, a->io_dtype == GDN_F16 ? 2 : 4);
+}
+
 // Host-side checks shared by gdn_forward and gdn_forward_workspace_size.
 gdn_status check_sizes(const gdn_forward_args *a) {
     if (!a) return GDN_ERR_NULL;
     if (a->io_dtype == GDN_BF16) return GDN_ERR_DTYPE;
     if (a->io_dtype != GDN_F32 && a->io_dtype != GDN_F16) return GDN_ERR_DTYPE;
     if (a->gate_mode != GDN_GATES_RAW && a->gate_mode != GDN_GATES_PRECOMPUTED) return GDN_ERR_ARG;
-    if (a->plan != GDN_PLAN_AUTO && a->plan != GDN_PLAN_RECURRENT && a->plan != GDN_PLAN_CHUNKED)
+    if (a->plan != GDN_PLAN_AUTO && a->plan != GDN_PLAN_RECURRENT && a->plan != GDN_PLAN_CHUNKED &&
+        a->plan != GDN_PLAN_CHUNKED_SPLIT)
         return GDN_ERR_ARG;
     if (a->num_seqs < 0 || a->num_seqs > 65535 || a->total_tokens < 0) return GDN_ERR_SHAPE;
     if (a->num_k_heads <= 0 || a->num_v_heads <= 0 || a->num_v_heads % a->num_k_heads != 0)
@@ -38,8 +50,8 @@ gdn_status check_sizes(const gdn_forward_args *a) {
         (a->v_stride != 0 && a->v_stride < v_min))
         return GDN_ERR_SHAPE;
     if (!(a->scale >= 0.f) || isinf(a->scale)) return GDN_ERR_SHAPE;
-    if (a->plan == GDN_PLAN_CHUNKED && !gdn::chunked_supported(a->head_dim_k, a->head_dim_v))
-        return GDN_ERR_UNSUPPORTED;
+    if (forced_chunked(a) && !gdn::chunked_supported(a->head_dim_k, a->head_dim_v)) return GDN_ERR_UNSUPPORTED;
+    if (a->plan == GDN_PLAN_CHUNKED_SPLIT && a->state_update_capacity > 0) return GDN_ERR_UNSUPPORTED;
     return GDN_OK;
 }
 
@@ -48,7 +60,7 @@ bool wants_chunked(const gdn_forward_args *a) {
     if (a->num_seqs == 0 || a->plan == GDN_PLAN_RECURRENT) return false;
     if (!gdn::chunked_supported(a->head_dim_k, a->head_dim_v)) return false;
     const int longest = a->max_seqlen > 0 && a->max_seqlen < a->total_tokens ? a->max_seqlen : a->total_tokens;
-    return a->plan == GDN_PLAN_CHUNKED || longest > gdn::RECURRENT_MAX_LEN;
+    return forced_chunked(a) || longest > gdn::RECURRENT_MAX_LEN;
 }
 
 // The chunked kernel moves q, k, v rows with bulk copies and writes output
@@ -136,22 +148,24 @@ gdn_status forward_impl(const gdn_forward_args *a, int dense_S, gdn_stream_t str
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     bool chunked = wants_chunked(a);
     if (chunked && !chunked_aligned(a, p)) {
-        if (a->plan == GDN_PLAN_CHUNKED) return GDN_ERR_ALIGN;
+        if (forced_chunked(a)) return GDN_ERR_ALIGN;
         chunked = false;  // the automatic plan keeps every sequence on the recurrent kernel
     }
     if (chunked) {
         // A workspace of gdn_forward_workspace_size bytes runs the two-phase
         // chunked evaluation; one that only holds the chain list runs the
         // single-kernel one (same results up to rounding, slower).
+        // The split plan has no single-kernel form.
         if (!a->workspace || (reinterpret_cast<uintptr_t>(a->workspace) & 15u)) return GDN_ERR_WORKSPACE;
-        const bool two_phase = a->workspace_bytes >= gdn::chunked_wy_workspace_bytes(a->num_seqs, a->total_tokens,
-                                                                                   a->num_k_heads, a->num_v_heads);
-        if (!two_phase && a->workspace_bytes < gdn::chunked_workspace_bytes(a->num_seqs)) return GDN_ERR_WORKSPACE;
-        const int min_len = a->plan == GDN_PLAN_CHUNKED ? -1 : gdn::RECURRENT_MAX_LEN;
-        const cudaError_t e = two_phase ? gdn::launch_chunked_wy(p, min_len, a->workspace, s)
+        const bool split = a->plan == GDN_PLAN_CHUNKED_SPLIT;
+        const bool two_phase = a->workspace_bytes >= two_phase_bytes(a);
+        if (!two_phase && (split || a->workspace_bytes < gdn::chunked_workspace_bytes(a->num_seqs)))
+            return GDN_ERR_WORKSPACE;
+        const int min_len = forced_chunked(a) ? -1 : gdn::RECURRENT_MAX_LEN;
+        const cudaError_t e = two_phase ? gdn::launch_chunked_wy(p, min_len, split, a->workspace, s)
                                         : gdn::launch_chunked(p, min_len, a->workspace, s);
         if (e != cudaSuccess) return GDN_ERR_CUDA;
-        if (a->plan == GDN_PLAN_CHUNKED) return GDN_OK;
+        if (forced_chunked(a)) return GDN_OK;
         p.max_len = gdn::RECURRENT_MAX_LEN;
     }
     if (gdn::launch_recurrent(p, s) != cudaSuccess) return GDN_ERR_CUDA;
@@ -181,9 +195,7 @@ gdn_status gdn_forward_workspace_size(const gdn_forward_args *args, size_t *byte
     if (!bytes) return GDN_ERR_NULL;
     const gdn_status st = check_sizes(args);
     if (st != GDN_OK) return st;
-    *bytes = wants_chunked(args) ? gdn::chunked_wy_workspace_bytes(args->num_seqs, args->total_tokens,
-                                                                   args->num_k_heads, args->num_v_heads)
-                                 : 0;
+    *bytes = wants_chunked(args) ? two_phase_bytes(args) : 0;
     return GDN_OK;
 }
 

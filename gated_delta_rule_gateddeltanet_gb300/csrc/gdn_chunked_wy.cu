@@ -52,6 +52,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "chunk_tiles.cuh"
 #include "gdn_internal.cuh"
 #include "ptx.cuh"
@@ -76,38 +78,119 @@ constexpr int F_BETA = 0, F_BG = CH, F_GAMMA = 2 * CH, F_DECAY = 3 * CH;
 constexpr int VREC_BYTES = VREC_F + 4 * CH * 4;
 static_assert(VREC_BYTES % 128 == 0, "records stay 128-byte aligned");
 
-size_t header_bytes(int B) { return ((size_t)(3 + 2 * (size_t)B) * 4 + 1023) & ~size_t(1023); }
 long long max_chunks(int B, int T) { return (long long)T / CH + B; }
 
 // ---------------------------------------------------------------- plan
 
-// Workspace header: ws[0] = work counter, ws[1] = number of sequences on this
-// path, ws[2 .. 2+B) = those sequences longest-first (counting sort on the
-// number of chunks), ws[2+B .. 3+2B) = chunk_base: the index of each
-// sequence's first chunk in the record arrays (sequences not on this path
-// own no chunks); chunk_base[B] = total chunks.  Chunk counts above 1022 share
-// the first bin (they are all scheduled first).  Sequences with a bad packing
-// are left out (the recurrent kernel reports them).
+// Sequence-parallel evaluation (split plan).  A sequence of at least
+// SPLIT_MIN chunks is cut at chunk c1 = ceil(nc / 2) into two segments whose
+// chains run at the same time.  Per value head the state after token t of
+// the second segment is affine in the state S1 entering it,
+//     S_t = S1 A_t + B_t,
+// because each token maps S -> S g (I - beta k k^T) + beta v k^T.  B_t is
+// the chain run from a zero state, A_t the chain run from the identity with
+// the v term removed (dk = dv), and the outputs inherit the same split:
+//     o_t = o_t(zero) + S1 o_t(identity),   final = S1 A_last + B_last.
+// So the second segment runs twice, from zero (its outputs go straight to the
+// output buffer) and from the identity (outputs to a workspace buffer),
+// while the first segment runs from the true initial state; two short
+// kernels then add S1 o_t(identity) to the outputs and form the final state.
+// Chain kinds in the work list:
+constexpr int K_WHOLE = 0, K_FIRST = 1, K_ZERO = 2, K_IDENT = 3;
+constexpr int SPLIT_MIN = 32;  // chunks: sequences of more than 31 * 64 tokens are split
+constexpr int OC_ROWS = 128;   // tokens per tile of the output correction
+
+// Workspace header (int32 words, B sequences):
+//   [0] work counter of the scan, [1] E = work-list entries, [2] NS = split sequences
+//   list[3B]    work entries, longest chain first: b * 4 + kind
+//   cbase[B+1]  index of each sequence's first chunk in the record arrays
+//   sidx[B]     split index of each sequence, or -1
+//   sseq[B]     the sequence of each split index
+//   tbase[B+1]  first correction tile of each split sequence (prefix over split indices)
+//   obase[B+1]  first row of each split sequence's identity-run outputs
+struct Header {
+    int32_t *w, *list, *cbase, *sidx, *sseq, *tbase, *obase;
+    __host__ __device__ Header(int32_t *ws, int B)
+        : w(ws), list(ws + 4), cbase(ws + 4 + 3 * B), sidx(ws + 5 + 4 * B), sseq(ws + 5 + 5 * B),
+          tbase(ws + 5 + 6 * B), obase(ws + 6 + 7 * B) {}
+};
+size_t header_bytes(int B) { return ((size_t)(7 + 8 * (size_t)B) * 4 + 1023) & ~size_t(1023); }
+// Split sequences and their identity-run output rows that a workspace must hold.
+long long max_split(int B, int T) { return std::min<long long>(B, (long long)T / (CH * (SPLIT_MIN - 1) + 1)); }
+long long max_split_rows(int T) { return (long long)T / 2 + CH; }
+constexpr size_t STATE_BYTES = (size_t)DH * DH * 4;
+
+// Exclusive prefix over sequences b = 0 .. B-1 of value(b), in sequence
+// order: put(b, prefix) for every b; returns the total.  All PLAN_NT threads
+// call it; thread t owns the contiguous sequences [t * per, (t + 1) * per).
 constexpr int PLAN_BINS = 1024;
 constexpr int PLAN_NT = 1024;
-__global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int dense_S, int B, int T, int min_len,
-                                                          int32_t *ws) {
-    __shared__ int hist[PLAN_BINS];
-    __shared__ int warp_sum[PLAN_NT / 32];
-    __shared__ int total;
+template <typename V, typename P>
+__device__ long long scan_sequences(int B, V value, P put, long long *wsum) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // chunks of sequence b on this path (an empty sequence has none but is still
-    // listed: its final state is its initial state), or -1 when it is not
+    const int per = (B + PLAN_NT - 1) / PLAN_NT;
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    long long local = 0;
+    for (int b = b0; b < b1; ++b) local += value(b);
+    long long incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        long long w = wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        wsum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    long long run = incl - local + (warp > 0 ? wsum[warp - 1] : 0);
+    for (int b = b0; b < b1; ++b) {
+        put(b, run);
+        run += value(b);
+    }
+    const long long total = wsum[PLAN_NT / 32 - 1];
+    __syncthreads();  // every thread has read wsum before the next scan reuses it
+    return total;
+}
+
+// Builds the header.  The work list is a counting sort of the chains on
+// their length in chunks (lengths above 1022 share the first bin and are all
+// scheduled first).  Sequences with a bad packing are left out (the recurrent
+// kernel reports them); an empty sequence is listed (its final state is its
+// initial state).  split = false: no sequence is split.
+__global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int dense_S, int B, int T, int min_len,
+                                                          bool split, int32_t *ws) {
+    __shared__ int hist[PLAN_BINS];
+    __shared__ long long wsum[PLAN_NT / 32];
+    __shared__ int total;
+    const int tid = threadIdx.x;
+    const Header hd(ws, B);
+    // chunks of sequence b on this path, or -1 when it is not
     auto chunks_of = [&](int b) -> int {
         const int lo = seq_start(cu, dense_S, b), hi = seq_start(cu, dense_S, b + 1);
         if (lo < 0 || hi < lo || hi > T || hi - lo <= min_len) return -1;
         return (hi - lo + CH - 1) / CH;
     };
+    auto is_split = [&](int c) { return split && c >= SPLIT_MIN; };
+    auto bin = [&](int c) { return PLAN_BINS - 1 - min(c, PLAN_BINS - 1); };
     for (int i = tid; i < PLAN_BINS; i += PLAN_NT) hist[i] = 0;
     __syncthreads();
     for (int b = tid; b < B; b += PLAN_NT) {
         const int c = chunks_of(b);
-        if (c >= 0) atomicAdd(&hist[PLAN_BINS - 1 - min(c, PLAN_BINS - 1)], 1);
+        if (c < 0) continue;
+        if (is_split(c)) {
+            atomicAdd(&hist[bin((c + 1) / 2)], 1);
+            atomicAdd(&hist[bin(c - (c + 1) / 2)], 2);
+        } else {
+            atomicAdd(&hist[bin(c)], 1);
+        }
     }
     __syncthreads();
     if (tid == 0) {
@@ -122,42 +205,53 @@ __global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int
     __syncthreads();
     for (int b = tid; b < B; b += PLAN_NT) {
         const int c = chunks_of(b);
-        if (c >= 0) ws[2 + atomicAdd(&hist[PLAN_BINS - 1 - min(c, PLAN_BINS - 1)], 1)] = b;
-    }
-    // chunk_base: exclusive prefix sum of the chunk counts in sequence order;
-    // thread t owns the contiguous sequences [t * per, (t + 1) * per)
-    int32_t *cbase = ws + 2 + B;
-    const int per = (B + PLAN_NT - 1) / PLAN_NT;
-    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
-    int local = 0;
-    for (int b = b0; b < b1; ++b) local += max(chunks_of(b), 0);
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) warp_sum[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int w = warp_sum[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
+        if (c < 0) continue;
+        if (is_split(c)) {
+            const int c1 = (c + 1) / 2;
+            hd.list[atomicAdd(&hist[bin(c1)], 1)] = b * 4 + K_FIRST;
+            hd.list[atomicAdd(&hist[bin(c - c1)], 1)] = b * 4 + K_ZERO;
+            hd.list[atomicAdd(&hist[bin(c - c1)], 1)] = b * 4 + K_IDENT;
+        } else {
+            hd.list[atomicAdd(&hist[bin(c)], 1)] = b * 4 + K_WHOLE;
         }
-        warp_sum[lane] = w;  // inclusive over warps
     }
-    __syncthreads();
-    int run = incl - local + (warp > 0 ? warp_sum[warp - 1] : 0);
-    for (int b = b0; b < b1; ++b) {
-        cbase[b] = run;
-        run += max(chunks_of(b), 0);
-    }
-    if (tid == PLAN_NT - 1) cbase[B] = warp_sum[31];
+    // per-sequence offsets (sequence order)
+    const long long nch = scan_sequences(
+        B, [&](int b) -> long long { return max(chunks_of(b), 0); },
+        [&](int b, long long run) { hd.cbase[b] = (int32_t)run; }, wsum);
+    const long long ns = scan_sequences(
+        B, [&](int b) -> long long { return is_split(chunks_of(b)) ? 1 : 0; },
+        [&](int b, long long run) {
+            const bool sp = is_split(chunks_of(b));
+            hd.sidx[b] = sp ? (int32_t)run : -1;
+            if (sp) hd.sseq[run] = b;
+        },
+        wsum);
+    // tokens of each split sequence's second segment (from chunk c1 on)
+    auto seg2 = [&](int b) -> long long {
+        const int c = chunks_of(b);
+        if (!is_split(c)) return 0;
+        return (long long)seq_start(cu, dense_S, b + 1) - seq_start(cu, dense_S, b) - (long long)CH * ((c + 1) / 2);
+    };
+    const long long ntile = scan_sequences(
+        B, [&](int b) -> long long { return (seg2(b) + OC_ROWS - 1) / OC_ROWS; },
+        [&](int b, long long run) {
+            if (hd.sidx[b] >= 0) hd.tbase[hd.sidx[b]] = (int32_t)run;
+        },
+        wsum);
+    const long long nrow = scan_sequences(
+        B, [&](int b) -> long long { return seg2(b); },
+        [&](int b, long long run) {
+            if (hd.sidx[b] >= 0) hd.obase[hd.sidx[b]] = (int32_t)run;
+        },
+        wsum);
     if (tid == 0) {
-        ws[0] = 0;
-        ws[1] = total;
+        hd.cbase[B] = (int32_t)nch;
+        hd.tbase[ns] = (int32_t)ntile;
+        hd.obase[ns] = (int32_t)nrow;
+        hd.w[0] = 0;
+        hd.w[1] = total;
+        hd.w[2] = (int32_t)ns;
     }
 }
 
@@ -338,7 +432,7 @@ __global__ void __launch_bounds__(PT, 4)
     constexpr bool STAGED = sizeof(TIO) == 2;
 
     const int g = blockIdx.x / p.Hk, kh = blockIdx.x % p.Hk;
-    const int32_t *cbase = ws + 2 + p.B;
+    const int32_t *cbase = Header(const_cast<int32_t *>(ws), p.B).cbase;
     if (g >= cbase[p.B]) return;  // past the last chunk (the grid is sized by an upper bound)
     int lo = 0, hi = p.B;         // the sequence b with cbase[b] <= g < cbase[b + 1]
     while (hi - lo > 1) {
@@ -635,8 +729,9 @@ static_assert(SCAN_SMEM + 1024 <= 227 * 1024, "shared memory budget (dynamic + s
 
 template <typename TIO>
 __global__ void __launch_bounds__(NT, 1)
-    wy_scan_kernel(const ForwardParams p, int32_t *ws, const uint8_t *krec, const uint8_t *vrec,
-                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o, int out_tma) {
+    wy_scan_kernel(const ForwardParams p, int32_t *ws, const uint8_t *krec, const uint8_t *vrec, float *split_states,
+                   TIO *oid, const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+                   const __grid_constant__ CUtensorMap map_oi, int out_tma) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bar;      // MMA completion
@@ -696,28 +791,44 @@ __global__ void __launch_bounds__(NT, 1)
         return __syncthreads_and(ok);
     };
 
-    const int n_items = ws[1] * p.Hv;
-    const int32_t *cbase = ws + 2 + p.B;
+    const Header hd(ws, p.B);
+    const int n_items = hd.w[1] * p.Hv;
+    const int32_t *cbase = hd.cbase;
     const TIO *vg = static_cast<const TIO *>(p.v);
-    TIO *og = static_cast<TIO *>(p.out);
     const long long ubase = (long long)p.Hv + (long long)p.Hk * DH;
 
     while (!failed) {
-        if (tid == 0) item_s = atomicAdd(&ws[0], 1);
+        if (tid == 0) item_s = atomicAdd(&hd.w[0], 1);
         __syncthreads();
         const int item = item_s;
         __syncthreads();
         if (item >= n_items) break;
-        const int b = ws[2 + item / p.Hv], h = item % p.Hv, kh = h / p.r;
+        const int e = hd.list[item / p.Hv], h = item % p.Hv, kh = h / p.r;
+        const int b = e >> 2, kind = e & 3;
         const int bos = seq_start(p.cu, p.dense_S, b), eos = seq_start(p.cu, p.dense_S, b + 1);
         const int nc = (eos - bos + CH - 1) / CH;
+        // the chunks of this chain: a whole sequence, or one segment of a split one
+        const int c1 = (nc + 1) / 2;
+        const int c_lo = kind >= K_ZERO ? c1 : 0, c_hi = kind == K_FIRST ? c1 : nc;
         const long long gbase = cbase[b];
         const int slot = p.slots ? p.slots[b] : b;
         if (slot < 0 || slot >= p.num_slots) {
-            if (tid == 0 && h == 0) flag_error(p.status, GDN_DEVERR_STATE_SLOT);
+            if (tid == 0 && h == 0 && kind <= K_FIRST) flag_error(p.status, GDN_DEVERR_STATE_SLOT);
             continue;
         }
         const size_t head_off = ((size_t)slot * p.Hv + h) * (size_t)DH * DH;
+        // where the outputs and the final state go: a split sequence's first segment
+        // leaves its state S1 in the workspace, the second segment's zero run writes
+        // the outputs (corrected later) and B, the identity run its outputs to the
+        // workspace rows of this sequence and A
+        float *sstate = nullptr;
+        if (kind != K_WHOLE) sstate = split_states + ((size_t)(hd.sidx[b] * 3 + kind - 1) * p.Hv + h) * (DH * DH);
+        TIO *const og = kind == K_IDENT ? oid : static_cast<TIO *>(p.out);
+        const long long orow = kind == K_IDENT ? (long long)hd.obase[hd.sidx[b]] - (bos + CH * c1) : 0;
+        const CUtensorMap *const mo = kind == K_IDENT ? &map_oi : &map_o;
+        float *const fdst = kind == K_FIRST ? sstate
+                                            : (p.final_state ? (kind == K_WHOLE ? p.final_state + head_off : sstate)
+                                                             : nullptr);
 
         // chunk c's records (and fp16 v rows) into stage st
         auto stage_load = [&](int c, int st) {
@@ -731,7 +842,7 @@ __global__ void __launch_bounds__(NT, 1)
             pending[st] = true;
         };
         // S0 -> fp16 operand tile; the tensor-memory state becomes gamma_last S0
-        bool state_live = p.init != nullptr;
+        bool state_live = kind == K_IDENT || (kind != K_ZERO && p.init != nullptr);
         auto build_s16 = [&](const float *F, int n) {
             const float gl = F[F_GAMMA + n - 1];
             float v[CS];
@@ -768,13 +879,20 @@ __global__ void __launch_bounds__(NT, 1)
             for (int j = 0; j < CW; ++j) {
                 const int s = c16 + j;
                 if (s < n)
-                    og[((long long)(tp + s) * p.Hv + h) * DH + row] = from_f32<TIO>(p.scale * fmaf(gm[j], o1[j], y[j]));
+                    og[((long long)(tp + s) + orow) * p.Hv * DH + (long long)h * DH + row] =
+                        from_f32<TIO>(p.scale * fmaf(gm[j], o1[j], y[j]));
             }
         };
         const bool out_tile = STAGED && out_tma;
 
-        // ---- chain start: the initial state into tensor memory, chunk 0's inputs
-        if (state_live) {
+        // ---- chain start: the initial state into tensor memory, the first chunk's inputs
+        if (kind == K_IDENT) {
+            float v[CS];
+#pragma unroll
+            for (int j = 0; j < CS; ++j) v[j] = c32 + j == row ? 1.f : 0.f;
+            ptx::tmem_st<CS>(tm + lane_sel + TM_S + c32, v);
+            ptx::tmem_st_wait();
+        } else if (state_live) {
             const float *src = p.init + head_off + (size_t)row * DH + c32;
             float v[CS];
 #pragma unroll
@@ -785,16 +903,16 @@ __global__ void __launch_bounds__(NT, 1)
             ptx::tmem_st<CS>(tm + lane_sel + TM_S + c32, v);
             ptx::tmem_st_wait();
         }
-        if (nc > 0) {
-            stage_load(0, 0);
-            if (nc > 1) stage_load(1, 1);
+        if (c_hi > c_lo) {
+            stage_load(c_lo, 0);
+            if (c_hi > c_lo + 1) stage_load(c_lo + 1, 1);
             if (!stage_wait(0)) { failed = true; break; }
-            build_s16(reinterpret_cast<const float *>(sm + S_VREC + VREC_F), min(CH, eos - bos));
+            build_s16(reinterpret_cast<const float *>(sm + S_VREC + VREC_F), min(CH, eos - bos - CH * c_lo));
         }
         mma_ready();
 
-        for (int c = 0; c < nc && !failed; ++c) {
-            const int st = c & 1;
+        for (int c = c_lo; c < c_hi && !failed; ++c) {
+            const int st = (c - c_lo) & 1;
             uint8_t *stage = sm + st * STAGE_BYTES;
             const float *F = reinterpret_cast<const float *>(stage + S_VREC + VREC_F);
             const int t0 = bos + CH * c, n = min(CH, eos - t0);
@@ -811,10 +929,10 @@ __global__ void __launch_bounds__(NT, 1)
                 ptx::mma_commit(&bar);
             }
             // ---- while MMA2 runs: the outputs of chunk c - 1
-            if (c > 0) write_outputs(t0 - CH, CH, TM_OX + 128u * (uint32_t)(st ^ 1), out_tile);
+            if (c > c_lo) write_outputs(t0 - CH, CH, TM_OX + 128u * (uint32_t)(st ^ 1), out_tile);
             if (!mma_wait()) { failed = true; break; }
-            if (c > 0 && out_tile && tid == 0) {  // chunk c - 1's outputs, one tensor store
-                ptx::tma_store_2d(&map_o, sm + OFF_OT, h * DH, t0 - CH);
+            if (c > c_lo && out_tile && tid == 0) {  // chunk c - 1's outputs, one tensor store
+                ptx::tma_store_2d(mo, sm + OFF_OT, h * DH, (int)(t0 - CH + orow));
                 ptx::bulk_commit();
             }
             // ---- R^T = diag(beta) V - diag(beta gamma) X^T, transposed; this chunk's gamma for its outputs
@@ -824,6 +942,10 @@ __global__ void __launch_bounds__(NT, 1)
                 float be[CW], bg[CW];
                 ld_fn<CW>(F + F_BETA + c16, be);
                 ld_fn<CW>(F + F_BG + c16, bg);
+                if (kind == K_IDENT) {  // the identity run has no v term
+#pragma unroll
+                    for (int j = 0; j < CW; ++j) be[j] = 0.f;
+                }
 #pragma unroll
                 for (int j = 0; j < CW; j += 8) {
                     float w[8];
@@ -888,9 +1010,9 @@ __global__ void __launch_bounds__(NT, 1)
             if (!mma_wait()) { failed = true; break; }
             state_live = true;
             // this stage is free now (its gamma was copied to gam_prev): chunk c + 2 goes there
-            if (c + 2 < nc) stage_load(c + 2, st);
+            if (c + 2 < c_hi) stage_load(c + 2, st);
             // ---- the next chunk's fp16 state copy (its inputs first)
-            if (c + 1 < nc) {
+            if (c + 1 < c_hi) {
                 if (!stage_wait(st ^ 1)) { failed = true; break; }
                 build_s16(reinterpret_cast<const float *>(sm + (st ^ 1) * STAGE_BYTES + S_VREC + VREC_F),
                           min(CH, eos - t0 - CH));
@@ -902,9 +1024,9 @@ __global__ void __launch_bounds__(NT, 1)
         }
         if (failed) break;
         // ---- chain end: the final state (unless the caller asked for none)
-        if (p.final_state) {
+        if (fdst) {
             ptx::tc_fence_after();
-            float *dst = p.final_state + head_off + (size_t)row * DH + c32;
+            float *dst = fdst + (size_t)row * DH + c32;
             float v[CS];
             if (state_live) {
                 ptx::tmem_ld<CS>(tm + lane_sel + TM_S + c32, v);
@@ -937,6 +1059,246 @@ __global__ void __launch_bounds__(NT, 1)
     }
 }
 
+// ---------------------------------------------------------------- split plan: combining the segments
+
+// Outputs of each split sequence's second segment: o_t += S1 o_t(identity),
+// over tiles of OC_ROWS tokens of one (split sequence, value head).  Per tile
+// one tcgen05 product [OC_ROWS tokens x dk] x [dk x dv] (the identity-run
+// rows and the fp16 copy of S1, both K-major in the 128-byte swizzled
+// layout) accumulates in tensor memory; the epilogue thread of token t adds
+// its row to the output already there (the zero run's) and rounds once.
+// Persistent over contiguous ranges of tiles, so consecutive tiles share
+// (sequence, head) and S1 is converted once per range piece.
+constexpr int OC_NT = 128;
+constexpr int OC_SMEM = 2 * OC_ROWS * DH * 2 + 1024;
+
+// dst[0 .. 32) += c, rounded once to the I/O type (16-byte accesses).
+__device__ __forceinline__ void add_row32(float *dst, const float (&c)[32]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        float4 v = reinterpret_cast<float4 *>(dst)[q];
+        v.x += c[4 * q];
+        v.y += c[4 * q + 1];
+        v.z += c[4 * q + 2];
+        v.w += c[4 * q + 3];
+        reinterpret_cast<float4 *>(dst)[q] = v;
+    }
+}
+__device__ __forceinline__ void add_row32(__half *dst, const float (&c)[32]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 v = reinterpret_cast<uint4 *>(dst)[q];
+        __half2 *hv = reinterpret_cast<__half2 *>(&v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(hv[e]);
+            hv[e] = __floats2half2_rn(f.x + c[8 * q + 2 * e], f.y + c[8 * q + 2 * e + 1]);
+        }
+        reinterpret_cast<uint4 *>(dst)[q] = v;
+    }
+}
+
+template <typename TIO>
+__global__ void __launch_bounds__(OC_NT, 1)
+    wy_out_correction_kernel(const ForwardParams p, int32_t *ws, const float *split_states, const TIO *oid,
+                             const __grid_constant__ CUtensorMap map_oa, int a_tma) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *a_t = sm;                    // identity-run outputs: [OC_ROWS][dk] fp16, two K-blocks
+    uint8_t *b_t = sm + OC_ROWS * DH * 2;  // S1 (dv rows) as fp16, two K-blocks
+    __shared__ __align__(8) uint64_t bar, lbar;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const Header hd(ws, p.B);
+    const int ns = hd.w[2];
+    const long long ntiles = (long long)hd.tbase[ns] * p.Hv;
+    const long long u0 = (long long)blockIdx.x * ntiles / gridDim.x;
+    const long long u1 = (long long)(blockIdx.x + 1) * ntiles / gridDim.x;
+    if (u0 >= u1) return;
+    if (warp == 0) {
+        ptx::tmem_alloc(&tmem_base, 128);
+        ptx::tmem_relinquish();
+    }
+    if (tid == 0) {
+        ptx::mbar_init(&bar, 1);
+        ptx::mbar_init(&lbar, 1);
+        ptx::fence_mbar_init();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tm = tmem_base;
+    const uint32_t lane_sel = (uint32_t)(warp * 32) << 16;
+    constexpr uint32_t I128 = ptx::idesc_f16_f32(128, 128);
+    uint32_t ph = 0, lph = 0;
+    bool ok = true, mma_out = false, load_out = false;
+    int cur = -1;  // (split index, head) whose S1 is in b_t
+    TIO *og = static_cast<TIO *>(p.out);
+    for (long long u = u0; u < u1 && ok; ++u) {
+        // tile u -> split index j (tiles of j: [Hv tbase[j], Hv tbase[j + 1]), head-major), head h, tile k
+        int lo = 0, hi = ns;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if ((long long)hd.tbase[mid] * p.Hv <= u) lo = mid;
+            else hi = mid;
+        }
+        const int j = lo;
+        const long long nt = hd.tbase[j + 1] - hd.tbase[j];
+        const long long rel = u - (long long)hd.tbase[j] * p.Hv;
+        const int h = (int)(rel / nt), k = (int)(rel % nt);
+        const int b = hd.sseq[j];
+        const int bos = seq_start(p.cu, p.dense_S, b), eos = seq_start(p.cu, p.dense_S, b + 1);
+        const int c1 = ((eos - bos + CH - 1) / CH + 1) / 2;
+        const int t0 = bos + CH * c1 + OC_ROWS * k;      // first token of the tile
+        const long long r0 = hd.obase[j] + (long long)OC_ROWS * k;  // its first identity-run row
+        const int slot = p.slots ? p.slots[b] : b;
+        if (slot < 0 || slot >= p.num_slots) continue;  // flagged by the scan; nothing was computed
+        if (a_tma && tid == 0) {
+            ptx::mbar_arrive_expect_tx(&lbar, OC_ROWS * DH * 2);
+            ptx::tma_load_2d(a_t, &map_oa, h * DH, (int)r0, &lbar);
+            ptx::tma_load_2d(a_t + OC_ROWS * 128, &map_oa, h * DH + 64, (int)r0, &lbar);
+            load_out = true;
+        }
+        if (!a_tma) {  // FP32 rows: converted here, zero past the segment
+            const bool live = t0 + tid < eos;
+            const TIO *src = oid + ((r0 + tid) * p.Hv + h) * DH;
+#pragma unroll 4
+            for (int col = 0; col < DH; col += 8) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = live ? to_f32(src[col + e]) : 0.f;
+                st_h8(a_t, sw(tid, col, OC_ROWS), x);
+            }
+        }
+        if (j * p.Hv + h != cur) {  // S1 of this (sequence, head) -> fp16 operand
+            cur = j * p.Hv + h;
+            const float *s1 = split_states + ((size_t)j * 3 * p.Hv + h) * (DH * DH) + (size_t)tid * DH;
+#pragma unroll 4
+            for (int col = 0; col < DH; col += 8) {
+                const float4 x0 = *reinterpret_cast<const float4 *>(s1 + col);
+                const float4 x1 = *reinterpret_cast<const float4 *>(s1 + col + 4);
+                const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                st_h8(b_t, sw(tid, col, DH), x);
+            }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (a_tma) {
+            const bool got = ptx::mbar_wait_bounded(&lbar, lph, WAIT_LIMIT);
+            if (got) {
+                lph ^= 1u;
+                load_out = false;
+            }
+            ok = __syncthreads_and(got);
+            if (!ok) break;
+        }
+        if (tid == 0) {
+            ptx::tc_fence_after();
+            const uint64_t ad = ptx::sdesc_k_sw128(ptx::smem_u32(a_t)), bd = ptx::sdesc_k_sw128(ptx::smem_u32(b_t));
+            for (int ks = 0; ks < DH / 16; ++ks) {
+                const uint32_t ko = ((ks >> 2) * (OC_ROWS * 128) + (ks & 3) * 32) >> 4;
+                ptx::mma_f16(tm, ad + ko, bd + ko, I128, ks > 0);
+            }
+            ptx::mma_commit(&bar);
+        }
+        mma_out = true;
+        const bool done = ptx::mbar_wait_bounded(&bar, ph, WAIT_LIMIT);
+        if (done) {
+            ph ^= 1u;
+            mma_out = false;
+        }
+        ptx::tc_fence_after();
+        ok = __syncthreads_and(done);
+        if (!ok) break;
+        // epilogue: token t0 + tid, dv = 128 columns
+        const int t = t0 + tid;
+#pragma unroll 1
+        for (int q = 0; q < DH / 32; ++q) {
+            float c[32];
+            ptx::tmem_ld32(tm + lane_sel + 32 * q, c);
+            if (t < eos) add_row32(og + ((long long)t * p.Hv + h) * DH + 32 * q, c);
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+    }
+    if (!ok && tid == 0) {
+        flag_error(p.status, GDN_DEVERR_TIMEOUT);
+        if (mma_out) ptx::mbar_wait_bounded(&bar, ph, WAIT_LIMIT);   // let the MMA drain before tensor memory is freed
+        if (load_out) ptx::mbar_wait_bounded(&lbar, lph, WAIT_LIMIT);  // and the row copies
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tm, 128);
+    }
+}
+
+// Final state of each split sequence: S1 A + B (FP32, CUDA cores), one CTA
+// per (split sequence, value head); 8 x 8 outputs per thread.
+constexpr int FS_NT = 256;
+constexpr int FS_LD = DH + 1;  // row stride of S1 in shared memory (column reads conflict-free)
+constexpr int FS_SMEM = (DH * FS_LD + DH * DH) * 4;
+
+__global__ void __launch_bounds__(FS_NT, 1)
+    wy_split_final_kernel(const ForwardParams p, const int32_t *ws, const float *split_states) {
+    extern __shared__ float fs_smem[];
+    float *s1 = fs_smem;           // [dv][FS_LD]
+    float *am = fs_smem + DH * FS_LD;  // [dk][dk]
+    const Header hd(const_cast<int32_t *>(ws), p.B);
+    const int j = blockIdx.x / p.Hv, h = blockIdx.x % p.Hv;
+    if (j >= hd.w[2]) return;
+    const int b = hd.sseq[j];
+    const int slot = p.slots ? p.slots[b] : b;
+    if (slot < 0 || slot >= p.num_slots) return;
+    const int tid = threadIdx.x;
+    const float *S1 = split_states + ((size_t)(j * 3 + 0) * p.Hv + h) * (DH * DH);
+    const float *Bm = split_states + ((size_t)(j * 3 + 1) * p.Hv + h) * (DH * DH);
+    const float *Am = split_states + ((size_t)(j * 3 + 2) * p.Hv + h) * (DH * DH);
+    for (int i = tid; i < DH * DH / 4; i += FS_NT) {
+        const float4 x = reinterpret_cast<const float4 *>(S1)[i];
+        const int r = (4 * i) / DH, c = (4 * i) % DH;
+        s1[r * FS_LD + c] = x.x;
+        s1[r * FS_LD + c + 1] = x.y;
+        s1[r * FS_LD + c + 2] = x.z;
+        s1[r * FS_LD + c + 3] = x.w;
+        reinterpret_cast<float4 *>(am)[i] = reinterpret_cast<const float4 *>(Am)[i];
+    }
+    __syncthreads();
+    const int i0 = (tid >> 4) * 8, m0 = (tid & 15) * 4;  // rows i0 .. i0+7; columns m0 .. m0+3 and 64 + m0 ..
+    float acc[8][8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+#pragma unroll 4
+    for (int kk = 0; kk < DH; ++kk) {
+        const float4 a0 = *reinterpret_cast<const float4 *>(am + kk * DH + m0);
+        const float4 a1 = *reinterpret_cast<const float4 *>(am + kk * DH + 64 + m0);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const float sv = s1[(i0 + r) * FS_LD + kk];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(sv, av[c], acc[r][c]);
+        }
+    }
+    float *dst = p.final_state + ((size_t)slot * p.Hv + h) * (DH * DH);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const size_t row = (size_t)(i0 + r) * DH;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int m = m0 + 64 * half;
+            const float4 bb = *reinterpret_cast<const float4 *>(Bm + row + m);
+            *reinterpret_cast<float4 *>(dst + row + m) =
+                make_float4(acc[r][4 * half] + bb.x, acc[r][4 * half + 1] + bb.y, acc[r][4 * half + 2] + bb.z,
+                            acc[r][4 * half + 3] + bb.w);
+        }
+    }
+}
+
 int num_sms() {
     static int cached = 0;
     if (cached == 0) {
@@ -950,7 +1312,7 @@ int num_sms() {
 }
 
 template <typename TIO>
-cudaError_t launch_io(const ForwardParams &p, int min_len, uint8_t *ws, cudaStream_t stream) {
+cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *ws, cudaStream_t stream) {
     CUtensorMap mq{}, mk{}, mv{};
     if (sizeof(TIO) == 2) {
         // q, k: 64-token x 64-feature boxes in the 128-byte swizzle of the MMA operand tiles;
@@ -964,7 +1326,12 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, uint8_t *ws, cudaStre
     const long long maxch = max_chunks(p.B, p.T);
     uint8_t *krec = ws + header_bytes(p.B);
     uint8_t *vrec = krec + (size_t)maxch * p.Hk * KREC_BYTES;
-    wy_plan_kernel<<<1, PLAN_NT, 0, stream>>>(p.cu, p.dense_S, p.B, p.T, min_len, hdr);
+    float *split_states = reinterpret_cast<float *>(vrec + (size_t)maxch * p.Hv * VREC_BYTES);
+    const long long nsplit = split ? max_split(p.B, p.T) : 0;
+    TIO *oid = reinterpret_cast<TIO *>(reinterpret_cast<uint8_t *>(split_states) +
+                                       (size_t)nsplit * 3 * p.Hv * STATE_BYTES);
+    const long long oid_rows = max_split_rows(p.T);
+    wy_plan_kernel<<<1, PLAN_NT, 0, stream>>>(p.cu, p.dense_S, p.B, p.T, min_len, nsplit > 0, hdr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long prep_ctas = maxch * p.Hk;
@@ -978,27 +1345,51 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, uint8_t *ws, cudaStre
     auto scan = wy_scan_kernel<TIO>;
     e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, SCAN_SMEM);
     if (e != cudaSuccess) return e;
-    const long long chains = (long long)p.B * p.Hv;
+    const long long chains = (long long)p.B * p.Hv * (nsplit > 0 ? 3 : 1);
     const int grid = (int)(chains < num_sms() ? chains : num_sms());
-    // outputs: fp16 chunks go out as 64-token x 128-feature tensor stores when the map encodes
-    CUtensorMap mo{};
-    const int out_tma = sizeof(TIO) == 2 &&
-                        encode_rows_f16(&mo, p.out, (long long)p.Hv * DH, (long long)p.Hv * DH, p.T, DH, CH, false);
-    scan<<<grid, NT, SCAN_SMEM, stream>>>(p, hdr, krec, vrec, mv, mo, out_tma);
+    // outputs: fp16 chunks go out as 64-token x 128-feature tensor stores when the maps encode
+    // (the identity runs of split sequences write their rows of the workspace buffer)
+    CUtensorMap mo{}, moi{};
+    const int out_tma =
+        sizeof(TIO) == 2 &&
+        encode_rows_f16(&mo, p.out, (long long)p.Hv * DH, (long long)p.Hv * DH, p.T, DH, CH, false) &&
+        (nsplit == 0 || encode_rows_f16(&moi, oid, (long long)p.Hv * DH, (long long)p.Hv * DH, (int)oid_rows, DH,
+                                        CH, false));
+    scan<<<grid, NT, SCAN_SMEM, stream>>>(p, hdr, krec, vrec, split_states, oid, mv, mo, moi, out_tma);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || nsplit == 0) return e;
+    // split sequences: outputs of the second segments, then their final states
+    CUtensorMap moa{};
+    const int a_tma = sizeof(TIO) == 2 && encode_rows_f16(&moa, oid, (long long)p.Hv * DH, (long long)p.Hv * DH,
+                                                          (int)oid_rows, 64, OC_ROWS, true);
+    auto corr = wy_out_correction_kernel<TIO>;
+    e = cudaFuncSetAttribute(corr, cudaFuncAttributeMaxDynamicSharedMemorySize, OC_SMEM);
+    if (e != cudaSuccess) return e;
+    corr<<<3 * num_sms(), OC_NT, OC_SMEM, stream>>>(p, hdr, split_states, oid, moa, a_tma);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !p.final_state) return e;
+    e = cudaFuncSetAttribute(wy_split_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FS_SMEM);
+    if (e != cudaSuccess) return e;
+    wy_split_final_kernel<<<(unsigned)(nsplit * p.Hv), FS_NT, FS_SMEM, stream>>>(p, hdr, split_states);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t chunked_wy_workspace_bytes(int B, int T, int Hk, int Hv) {
+size_t chunked_wy_workspace_bytes(int B, int T, int Hk, int Hv, bool split, int io_bytes) {
     const long long maxch = max_chunks(B, T);
-    return header_bytes(B) + (size_t)maxch * ((size_t)Hk * KREC_BYTES + (size_t)Hv * VREC_BYTES);
+    size_t n = header_bytes(B) + (size_t)maxch * ((size_t)Hk * KREC_BYTES + (size_t)Hv * VREC_BYTES);
+    if (split && max_split(B, T) > 0)
+        n += (size_t)max_split(B, T) * 3 * Hv * STATE_BYTES + (size_t)max_split_rows(T) * Hv * DH * io_bytes;
+    return n;
 }
 
-cudaError_t launch_chunked_wy(const ForwardParams &p, int min_len, void *workspace, cudaStream_t stream) {
+cudaError_t launch_chunked_wy(const ForwardParams &p, int min_len, bool split, void *workspace,
+                              cudaStream_t stream) {
     if (p.B == 0) return cudaSuccess;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    return p.io_f16 ? launch_io<__half>(p, min_len, ws, stream) : launch_io<float>(p, min_len, ws, stream);
+    return p.io_f16 ? launch_io<__half>(p, min_len, split, ws, stream)
+                    : launch_io<float>(p, min_len, split, ws, stream);
 }
 
 }  // namespace gdn

@@ -91,12 +91,16 @@ cudaError_t launch_chunked(const ForwardParams &p, int min_len, void *workspace,
 // Two-phase chunked path (a parallel per-chunk kernel, then the sequential
 // state-passing kernel): faster, and needs chunked_wy_workspace_bytes of
 // workspace for the per-chunk records (about 1.36 MB per 64 tokens at
-// Hk = 16, Hv = 48, d = 128).
-size_t chunked_wy_workspace_bytes(int B, int T, int Hk, int Hv);
+// Hk = 16, Hv = 48, d = 128).  With `split`, every sequence of more than
+// 31 * 64 tokens is evaluated as two segments at once (see
+// gdn_chunked_wy.cu), which needs room for three states per split sequence
+// and head and for the identity-run outputs (io_bytes per element).
+size_t chunked_wy_workspace_bytes(int B, int T, int Hk, int Hv, bool split, int io_bytes);
 // Workspace of the single-kernel chunked evaluation for these arguments (0 if
 // no chunked kernel can run); argument errors as gdn_forward_workspace_size.
 gdn_status single_kernel_workspace_size(const gdn_forward_args *args, size_t *bytes);
-cudaError_t launch_chunked_wy(const ForwardParams &p, int min_len, void *workspace, cudaStream_t stream);
+cudaError_t launch_chunked_wy(const ForwardParams &p, int min_len, bool split, void *workspace,
+                              cudaStream_t stream);
 
 // Tensor map over a packed fp16 [T, row_elems] array with `stride` elements
 // between tokens, boxes of box_y tokens x box_x elements, zero fill past T;

@@ -65,8 +65,13 @@ enum {
                                 tokens at a time in closed form on the warp tensor cores
                                 (batches with longer spans; one-token spans in them still
                                 take the token-by-token code, with the same bits) */
-    GDN_PLAN_CHUNKED = 2     /* every sequence on the tensor-core chunked kernel
+    GDN_PLAN_CHUNKED = 2,    /* every sequence on the tensor-core chunked kernel
                                 (dk = dv = 128 only, else GDN_ERR_UNSUPPORTED) */
+    GDN_PLAN_CHUNKED_SPLIT = 3 /* GDN_PLAN_CHUNKED, and every sequence of more than
+                                1984 tokens (31 chunks) is evaluated as two halves at
+                                once: for batches of a few long sequences, whose
+                                (sequence, head) chains would leave most SMs idle.
+                                See "Sequence-parallel evaluation" below. */
 };
 
 /* Bits of the device status word. */
@@ -163,13 +168,41 @@ typedef struct gdn_forward_args {
 } gdn_forward_args;
 
 /*
+ * Sequence-parallel evaluation (GDN_PLAN_CHUNKED_SPLIT).
+ *
+ * The pages' operator evaluates each (sequence, value head) chain in order,
+ * chunk after chunk ("[CUDA] Add compact GatedDeltaNet operator",
+ * Description); a single long prompt then has only Hv chains, fewer than the
+ * GPU's SMs.  Per value head, each token maps the state affinely,
+ * S -> S g (I - beta kn kn^T) + beta v kn^T, so over the second half of a
+ * sequence S_t = S1 A_t + B_t, with S1 the state entering that half.  The
+ * split plan runs, at the same time, the first half from the initial state
+ * (giving S1), and the second half twice: from a zero state (giving B_t and
+ * the outputs scale B_t qn) and from the identity with v removed (giving A_t
+ * and scale A_t qn; dk = dv).  Two further kernels add S1 (scale A_t qn) to the
+ * second half's outputs and write S1 A + B as the final state.  The results
+ * equal those of GDN_PLAN_CHUNKED up to floating-point rounding (the
+ * correction is a tensor-core product with fp16 operands and FP32
+ * accumulation, and second-half outputs are rounded twice to the I/O type).
+ * Whether a sequence is split depends only on its own length, so a packed
+ * batch still gives bitwise the results of its sequences run one at a time.
+ * Restrictions: state_update_capacity must be 0 (GDN_ERR_UNSUPPORTED
+ * otherwise), the workspace must be the one gdn_forward_workspace_size
+ * reports for this plan (there is no single-kernel form; smaller workspaces
+ * and gdn_forward_no_alloc give GDN_ERR_WORKSPACE).
+ */
+
+/*
  * Bytes of device workspace gdn_forward needs for these arguments (sizes,
- * plan and max_seqlen only are read).  Non-zero exactly when a chunked
+ * plan, io_dtype and max_seqlen only are read).  Non-zero exactly when a chunked
  * (tensor-core) kernel may run.  The size is that of the two-phase chunked
  * evaluation: a header (work counter, the longest-first list of sequences,
  * each sequence's first chunk) plus one record per (64-token chunk, key head)
  * of 32 KiB and one per (chunk, value head) of 17,408 bytes, for at most
  * T/64 + B chunks -- about 1.36 MB per 64 tokens at Hk = 16, Hv = 48.
+ * GDN_PLAN_CHUNKED_SPLIT adds three FP32 states per value head for each
+ * sequence that can be split (at most min(B, T / 1985)) and T/2 + 64 rows of
+ * Hv * dv io_dtype elements for the second halves' identity-run outputs.
  *
  * gdn_forward also accepts a smaller workspace of at least (B + 2) int32
  * (rounded up to 256 bytes): it then runs the single-kernel chunked

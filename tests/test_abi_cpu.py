@@ -136,10 +136,10 @@ def test_workspace_size_follows_the_plan(lib):
     a = _args(num_seqs=16, total_tokens=16, num_state_slots=16)
     assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 0
     # long batch at d = 128: the two-phase chunked evaluation may run -> a header
-    # ((3 + 2B) int32 rounded up to 1 KiB) plus, for each of at most T/64 + B
+    # ((7 + 8B) int32 rounded up to 1 KiB) plus, for each of at most T/64 + B
     # chunks, a 32 KiB record per key head and a 17,408-byte record per value head
     def two_phase(B, T, Hk, Hv):
-        return ((3 + 2 * B) * 4 + 1023) // 1024 * 1024 + (T // 64 + B) * (Hk * 32768 + Hv * 17408)
+        return ((7 + 8 * B) * 4 + 1023) // 1024 * 1024 + (T // 64 + B) * (Hk * 32768 + Hv * 17408)
     a = _args(num_seqs=8, total_tokens=17000, num_state_slots=8)
     assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0
     assert n.value == two_phase(8, 17000, a.num_k_heads, a.num_v_heads)
@@ -158,6 +158,25 @@ def test_workspace_size_follows_the_plan(lib):
     assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 0
     a = _args(num_seqs=8, total_tokens=17000, num_state_slots=8, head_dim_k=64)
     assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 0
+
+
+def test_split_plan_workspace_and_restrictions(lib):
+    n = ctypes.c_size_t(0)
+    base = ((7 + 8 * 8) * 4 + 1023) // 1024 * 1024 + (17000 // 64 + 8) * (16 * 32768 + 48 * 17408)
+    # + three FP32 states per value head for each sequence that can be split
+    # (at most min(B, T / 1985)) + T/2 + 64 rows of identity-run outputs
+    for io, esz in ((1, 2), (0, 4)):
+        a = _args(num_seqs=8, total_tokens=17000, num_state_slots=8, plan=3, io_dtype=io)
+        assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0
+        assert n.value == base + 8 * 3 * 48 * 128 * 128 * 4 + (17000 // 2 + 64) * 48 * 128 * esz
+    # too short to split anything: the plain two-phase size
+    a = _args(num_seqs=2, total_tokens=1984, num_state_slots=2, plan=3)
+    assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0
+    assert n.value == 1024 + (1984 // 64 + 2) * (16 * 32768 + 48 * 17408)
+    assert lib.gdn_forward(ctypes.byref(_args(plan=3, head_dim_k=64)), None) == 7
+    assert lib.gdn_forward(ctypes.byref(_args(plan=3, state_update_capacity=4)), None) == 7  # no capsules
+    assert lib.gdn_forward(ctypes.byref(_args(plan=3)), None) == 5                            # no workspace
+    assert lib.gdn_forward(ctypes.byref(_args(plan=4)), None) == 8
 
 
 def test_forced_chunked_plan_needs_d128_and_workspace(lib):
