@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-extra", action="store_true", help="skip the prefill / verify+replay sub-measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
+    ap.add_argument("--only", choices=sorted(SUB_MEASUREMENTS),
+                    help="run one sub-measurement alone on GPU 0 and print its JSON (for profiling)")
     return ap.parse_args()
 
 
@@ -927,8 +929,32 @@ def run_reference(a, dist: Dist):
     print(json.dumps(line), flush=True)
 
 
+# The sub-measurements reported beside the headline (see run_gdn), by name.
+SUB_MEASUREMENTS = {"prefill": run_prefill, "spec_verify_replay": run_spec, "causal_conv": run_conv,
+                    "serving_mix": run_serving_mix, "state_transpose": run_transpose,
+                    "spec_step_graph": run_spec_step, "long_prefill": run_long_prefill}
+NEEDS_LIB = {"spec_verify_replay", "serving_mix", "state_transpose"}
+
+
+def run_only(name):
+    """One sub-measurement alone (e.g. under a profiler), printed as JSON."""
+    import torch
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib = gdn.load_library()
+    stream = torch.cuda.current_stream(dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    fn = SUB_MEASUREMENTS[name]
+    res = fn(dev, stream, lib, sh) if name in NEEDS_LIB else fn(dev, stream)
+    print(json.dumps({"only": name, name: res}), flush=True)
+
+
 def main():
     a = parse()
+    if a.only:
+        run_only(a.only)
+        return
     dist = Dist()
     try:
         if a.impl == "reference":
