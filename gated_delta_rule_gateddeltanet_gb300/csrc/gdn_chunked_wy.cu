@@ -1068,7 +1068,10 @@ __global__ void __launch_bounds__(NT, 1)
 // layout) accumulates in tensor memory; the epilogue thread of token t adds
 // its row to the output already there (the zero run's) and rounds once.
 // Persistent over contiguous ranges of tiles, so consecutive tiles share
-// (sequence, head) and S1 is converted once per range piece.
+// (sequence, head) and S1 is converted once per range piece.  HBM-bound: the
+// fp16 path loads the next tile's identity-run rows (TMA) as soon as the
+// current product has read its operand, and each thread loads its output
+// row before the product, so the copies overlap the product and epilogue.
 constexpr int OC_NT = 128;
 constexpr int OC_SMEM = 2 * OC_ROWS * DH * 2 + 1024;
 
@@ -1084,24 +1087,28 @@ __device__ __forceinline__ void add_row32(float *dst, const float (&c)[32]) {
         reinterpret_cast<float4 *>(dst)[q] = v;
     }
 }
-__device__ __forceinline__ void add_row32(__half *dst, const float (&c)[32]) {
+
+// Eight fp16 values (one 16-byte piece of a row) plus c[0 .. 8), rounded once.
+__device__ __forceinline__ uint4 add_h8(uint4 v, const float *c) {
+    __half2 *hv = reinterpret_cast<__half2 *>(&v);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 v = reinterpret_cast<uint4 *>(dst)[q];
-        __half2 *hv = reinterpret_cast<__half2 *>(&v);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(hv[e]);
-            hv[e] = __floats2half2_rn(f.x + c[8 * q + 2 * e], f.y + c[8 * q + 2 * e + 1]);
-        }
-        reinterpret_cast<uint4 *>(dst)[q] = v;
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(hv[e]);
+        hv[e] = __floats2half2_rn(f.x + c[2 * e], f.y + c[2 * e + 1]);
     }
+    return v;
 }
+
+struct OcTile {
+    int j, h, b, eos, t0, slot;
+    long long r0;  // first identity-run row of the tile
+};
 
 template <typename TIO>
 __global__ void __launch_bounds__(OC_NT, 1)
     wy_out_correction_kernel(const ForwardParams p, int32_t *ws, const float *split_states, const TIO *oid,
                              const __grid_constant__ CUtensorMap map_oa, int a_tma) {
+    constexpr bool F16 = sizeof(TIO) == 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *a_t = sm;                    // identity-run outputs: [OC_ROWS][dk] fp16, two K-blocks
@@ -1115,6 +1122,34 @@ __global__ void __launch_bounds__(OC_NT, 1)
     const long long u0 = (long long)blockIdx.x * ntiles / gridDim.x;
     const long long u1 = (long long)(blockIdx.x + 1) * ntiles / gridDim.x;
     if (u0 >= u1) return;
+    // tile u -> split index j (tiles of j: [Hv tbase[j], Hv tbase[j + 1]), head-major), head, position
+    auto resolve = [&](long long u) {
+        int lo = 0, hi = ns;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if ((long long)hd.tbase[mid] * p.Hv <= u) lo = mid;
+            else hi = mid;
+        }
+        OcTile x;
+        x.j = lo;
+        const long long nt = hd.tbase[lo + 1] - hd.tbase[lo];
+        const long long rel = u - (long long)hd.tbase[lo] * p.Hv;
+        x.h = (int)(rel / nt);
+        const int k = (int)(rel % nt);
+        x.b = hd.sseq[lo];
+        const int bos = seq_start(p.cu, p.dense_S, x.b);
+        x.eos = seq_start(p.cu, p.dense_S, x.b + 1);
+        const int c1 = ((x.eos - bos + CH - 1) / CH + 1) / 2;
+        x.t0 = bos + CH * c1 + OC_ROWS * k;
+        x.r0 = hd.obase[lo] + (long long)OC_ROWS * k;
+        x.slot = p.slots ? p.slots[x.b] : x.b;
+        return x;
+    };
+    auto load_a = [&](const OcTile &x) {  // thread 0: the tile's identity-run rows, two swizzled boxes
+        ptx::mbar_arrive_expect_tx(&lbar, OC_ROWS * DH * 2);
+        ptx::tma_load_2d(a_t, &map_oa, x.h * DH, (int)x.r0, &lbar);
+        ptx::tma_load_2d(a_t + OC_ROWS * 128, &map_oa, x.h * DH + 64, (int)x.r0, &lbar);
+    };
     if (warp == 0) {
         ptx::tmem_alloc(&tmem_base, 128);
         ptx::tmem_relinquish();
@@ -1134,51 +1169,42 @@ __global__ void __launch_bounds__(OC_NT, 1)
     bool ok = true, mma_out = false, load_out = false;
     int cur = -1;  // (split index, head) whose S1 is in b_t
     TIO *og = static_cast<TIO *>(p.out);
+    OcTile x = resolve(u0);
+    if (a_tma && tid == 0) {
+        load_a(x);
+        load_out = true;
+    }
     for (long long u = u0; u < u1 && ok; ++u) {
-        // tile u -> split index j (tiles of j: [Hv tbase[j], Hv tbase[j + 1]), head-major), head h, tile k
-        int lo = 0, hi = ns;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if ((long long)hd.tbase[mid] * p.Hv <= u) lo = mid;
-            else hi = mid;
-        }
-        const int j = lo;
-        const long long nt = hd.tbase[j + 1] - hd.tbase[j];
-        const long long rel = u - (long long)hd.tbase[j] * p.Hv;
-        const int h = (int)(rel / nt), k = (int)(rel % nt);
-        const int b = hd.sseq[j];
-        const int bos = seq_start(p.cu, p.dense_S, b), eos = seq_start(p.cu, p.dense_S, b + 1);
-        const int c1 = ((eos - bos + CH - 1) / CH + 1) / 2;
-        const int t0 = bos + CH * c1 + OC_ROWS * k;      // first token of the tile
-        const long long r0 = hd.obase[j] + (long long)OC_ROWS * k;  // its first identity-run row
-        const int slot = p.slots ? p.slots[b] : b;
-        if (slot < 0 || slot >= p.num_slots) continue;  // flagged by the scan; nothing was computed
-        if (a_tma && tid == 0) {
-            ptx::mbar_arrive_expect_tx(&lbar, OC_ROWS * DH * 2);
-            ptx::tma_load_2d(a_t, &map_oa, h * DH, (int)r0, &lbar);
-            ptx::tma_load_2d(a_t + OC_ROWS * 128, &map_oa, h * DH + 64, (int)r0, &lbar);
-            load_out = true;
+        // Tiles of a sequence whose slot is out of range run like the others but
+        // write nothing (the scan flagged the slot and computed nothing for it).
+        const bool live_seq = x.slot >= 0 && x.slot < p.num_slots;
+        const int t = x.t0 + tid;
+        const bool live = live_seq && t < x.eos;
+        TIO *dst = og + ((long long)t * p.Hv + x.h) * DH;
+        uint4 orow[F16 ? 16 : 1];  // fp16: this thread's output row, loaded before the product
+        if (F16 && live) {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) orow[q] = reinterpret_cast<const uint4 *>(dst)[q];
         }
         if (!a_tma) {  // FP32 rows: converted here, zero past the segment
-            const bool live = t0 + tid < eos;
-            const TIO *src = oid + ((r0 + tid) * p.Hv + h) * DH;
+            const TIO *src = oid + ((x.r0 + tid) * p.Hv + x.h) * DH;
 #pragma unroll 4
             for (int col = 0; col < DH; col += 8) {
-                float x[8];
+                float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = live ? to_f32(src[col + e]) : 0.f;
-                st_h8(a_t, sw(tid, col, OC_ROWS), x);
+                for (int e = 0; e < 8; ++e) v[e] = live ? to_f32(src[col + e]) : 0.f;
+                st_h8(a_t, sw(tid, col, OC_ROWS), v);
             }
         }
-        if (j * p.Hv + h != cur) {  // S1 of this (sequence, head) -> fp16 operand
-            cur = j * p.Hv + h;
-            const float *s1 = split_states + ((size_t)j * 3 * p.Hv + h) * (DH * DH) + (size_t)tid * DH;
+        if (x.j * p.Hv + x.h != cur) {  // S1 of this (sequence, head) -> fp16 operand
+            cur = x.j * p.Hv + x.h;
+            const float *s1 = split_states + ((size_t)x.j * 3 * p.Hv + x.h) * (DH * DH) + (size_t)tid * DH;
 #pragma unroll 4
             for (int col = 0; col < DH; col += 8) {
                 const float4 x0 = *reinterpret_cast<const float4 *>(s1 + col);
                 const float4 x1 = *reinterpret_cast<const float4 *>(s1 + col + 4);
-                const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-                st_h8(b_t, sw(tid, col, DH), x);
+                const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                st_h8(b_t, sw(tid, col, DH), v);
             }
         }
         ptx::fence_proxy_async_smem();
@@ -1211,20 +1237,34 @@ __global__ void __launch_bounds__(OC_NT, 1)
         ptx::tc_fence_after();
         ok = __syncthreads_and(done);
         if (!ok) break;
-        // epilogue: token t0 + tid, dv = 128 columns
-        const int t = t0 + tid;
-#pragma unroll 1
+        // the operand tile is free: the next tile's rows are on their way during this epilogue
+        if (u + 1 < u1) {
+            x = resolve(u + 1);
+            if (a_tma && tid == 0) {
+                load_a(x);
+                load_out = true;
+            }
+        }
+        // epilogue: token t, dv = 128 columns (unrolled: the row stays in registers)
+#pragma unroll
         for (int q = 0; q < DH / 32; ++q) {
             float c[32];
             ptx::tmem_ld32(tm + lane_sel + 32 * q, c);
-            if (t < eos) add_row32(og + ((long long)t * p.Hv + h) * DH + 32 * q, c);
+            if (!live) continue;
+            if constexpr (F16) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    reinterpret_cast<uint4 *>(dst)[4 * q + m] = add_h8(orow[4 * q + m], c + 8 * m);
+            } else {
+                add_row32(reinterpret_cast<float *>(dst) + 32 * q, c);
+            }
         }
         ptx::tc_fence_before();
         __syncthreads();
     }
-    if (!ok && tid == 0) {
-        flag_error(p.status, GDN_DEVERR_TIMEOUT);
-        if (mma_out) ptx::mbar_wait_bounded(&bar, ph, WAIT_LIMIT);   // let the MMA drain before tensor memory is freed
+    if (tid == 0) {
+        if (!ok) flag_error(p.status, GDN_DEVERR_TIMEOUT);
+        if (mma_out) ptx::mbar_wait_bounded(&bar, ph, WAIT_LIMIT);    // let the MMA drain before tensor memory is freed
         if (load_out) ptx::mbar_wait_bounded(&lbar, lph, WAIT_LIMIT);  // and the row copies
     }
     ptx::tc_fence_before();
