@@ -219,6 +219,15 @@ __global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int
     const long long nch = scan_sequences(
         B, [&](int b) -> long long { return max(chunks_of(b), 0); },
         [&](int b, long long run) { hd.cbase[b] = (int32_t)run; }, wsum);
+    if (!split) {  // nothing below is read when no sequence is split
+        if (tid == 0) {
+            hd.cbase[B] = (int32_t)nch;
+            hd.w[0] = 0;
+            hd.w[1] = total;
+            hd.w[2] = 0;
+        }
+        return;
+    }
     const long long ns = scan_sequences(
         B, [&](int b) -> long long { return is_split(chunks_of(b)) ? 1 : 0; },
         [&](int b, long long run) {
@@ -727,7 +736,9 @@ constexpr int SCAN_SMEM = OFF_OT + 16384 + 1024;  // + slack for the 1024-byte a
 static_assert(S_V % 1024 == 0 && STAGE_BYTES % 1024 == 0, "stage layout");
 static_assert(SCAN_SMEM + 1024 <= 227 * 1024, "shared memory budget (dynamic + static)");
 
-template <typename TIO>
+// SPLIT = false: every chain is a whole sequence (the work list holds no
+// other kind), and the split-plan code is compiled out.
+template <typename TIO, bool SPLIT>
 __global__ void __launch_bounds__(NT, 1)
     wy_scan_kernel(const ForwardParams p, int32_t *ws, const uint8_t *krec, const uint8_t *vrec, float *split_states,
                    TIO *oid, const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -804,7 +815,7 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
         if (item >= n_items) break;
         const int e = hd.list[item / p.Hv], h = item % p.Hv, kh = h / p.r;
-        const int b = e >> 2, kind = e & 3;
+        const int b = e >> 2, kind = SPLIT ? (e & 3) : K_WHOLE;
         const int bos = seq_start(p.cu, p.dense_S, b), eos = seq_start(p.cu, p.dense_S, b + 1);
         const int nc = (eos - bos + CH - 1) / CH;
         // the chunks of this chain: a whole sequence, or one segment of a split one
@@ -1068,14 +1079,21 @@ __global__ void __launch_bounds__(NT, 1)
 // layout) accumulates in tensor memory; the epilogue thread of token t adds
 // its row to the output already there (the zero run's) and rounds once.
 // Persistent over contiguous ranges of tiles, so consecutive tiles share
-// (sequence, head) and S1 is converted once per range piece.  HBM-bound: the
-// fp16 path loads the next tile's identity-run rows (TMA) as soon as the
-// current product has read its operand, and each thread loads its output
-// row before the product, so the copies overlap the product and epilogue.
+// (sequence, head) and S1 is converted once per range piece.
+//
+// HBM-bound (per token and head, fp16: 256 B of identity-run rows and 256 B
+// of output read, 256 B written).  With fp16 I/O every copy is a tensor copy
+// that overlaps other work: the next tile's identity-run rows load as soon as
+// the product has read the current ones, the tile's output rows load (into a
+// third swizzled tile) while S1 is converted and the product runs, and a full
+// tile's updated rows leave by tensor stores that complete during the next
+// tile.  A tile that ends past its sequence is written row by row by its
+// threads instead, so rows of the next sequence are never stored.
 constexpr int OC_NT = 128;
-constexpr int OC_SMEM = 2 * OC_ROWS * DH * 2 + 1024;
+constexpr int OC_TILE = OC_ROWS * DH * 2;  // one fp16 [OC_ROWS][128] tile, two K-blocks
+constexpr int OC_SMEM = 3 * OC_TILE + 1024;
 
-// dst[0 .. 32) += c, rounded once to the I/O type (16-byte accesses).
+// dst[0 .. 32) += c (FP32 I/O; 16-byte accesses).
 __device__ __forceinline__ void add_row32(float *dst, const float (&c)[32]) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -1107,13 +1125,15 @@ struct OcTile {
 template <typename TIO>
 __global__ void __launch_bounds__(OC_NT, 1)
     wy_out_correction_kernel(const ForwardParams p, int32_t *ws, const float *split_states, const TIO *oid,
-                             const __grid_constant__ CUtensorMap map_oa, int a_tma) {
+                             const __grid_constant__ CUtensorMap map_oa, const __grid_constant__ CUtensorMap map_out,
+                             int tma) {
     constexpr bool F16 = sizeof(TIO) == 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *a_t = sm;                    // identity-run outputs: [OC_ROWS][dk] fp16, two K-blocks
-    uint8_t *b_t = sm + OC_ROWS * DH * 2;  // S1 (dv rows) as fp16, two K-blocks
-    __shared__ __align__(8) uint64_t bar, lbar;
+    uint8_t *a_t = sm;                // identity-run outputs: [OC_ROWS][dk] fp16
+    uint8_t *b_t = sm + OC_TILE;      // S1 (dv rows) as fp16
+    uint8_t *o_t = sm + 2 * OC_TILE;  // the tile's output rows (fp16 I/O with tensor copies)
+    __shared__ __align__(8) uint64_t bar, lbar, obar;
     __shared__ uint32_t tmem_base;
     const int tid = threadIdx.x, warp = tid >> 5;
     const Header hd(ws, p.B);
@@ -1122,6 +1142,7 @@ __global__ void __launch_bounds__(OC_NT, 1)
     const long long u0 = (long long)blockIdx.x * ntiles / gridDim.x;
     const long long u1 = (long long)(blockIdx.x + 1) * ntiles / gridDim.x;
     if (u0 >= u1) return;
+    const bool use_tma = F16 && tma;
     // tile u -> split index j (tiles of j: [Hv tbase[j], Hv tbase[j + 1]), head-major), head, position
     auto resolve = [&](long long u) {
         int lo = 0, hi = ns;
@@ -1145,10 +1166,11 @@ __global__ void __launch_bounds__(OC_NT, 1)
         x.slot = p.slots ? p.slots[x.b] : x.b;
         return x;
     };
-    auto load_a = [&](const OcTile &x) {  // thread 0: the tile's identity-run rows, two swizzled boxes
-        ptx::mbar_arrive_expect_tx(&lbar, OC_ROWS * DH * 2);
-        ptx::tma_load_2d(a_t, &map_oa, x.h * DH, (int)x.r0, &lbar);
-        ptx::tma_load_2d(a_t + OC_ROWS * 128, &map_oa, x.h * DH + 64, (int)x.r0, &lbar);
+    // thread 0: a tile's rows as two swizzled boxes of 64 columns
+    auto load_tile = [&](uint8_t *dst, const CUtensorMap *map, int x0, int y0, uint64_t *mb) {
+        ptx::mbar_arrive_expect_tx(mb, OC_TILE);
+        ptx::tma_load_2d(dst, map, x0, y0, mb);
+        ptx::tma_load_2d(dst + OC_ROWS * 128, map, x0 + 64, y0, mb);
     };
     if (warp == 0) {
         ptx::tmem_alloc(&tmem_base, 128);
@@ -1157,6 +1179,7 @@ __global__ void __launch_bounds__(OC_NT, 1)
     if (tid == 0) {
         ptx::mbar_init(&bar, 1);
         ptx::mbar_init(&lbar, 1);
+        ptx::mbar_init(&obar, 1);
         ptx::fence_mbar_init();
     }
     ptx::tc_fence_before();
@@ -1165,28 +1188,38 @@ __global__ void __launch_bounds__(OC_NT, 1)
     const uint32_t tm = tmem_base;
     const uint32_t lane_sel = (uint32_t)(warp * 32) << 16;
     constexpr uint32_t I128 = ptx::idesc_f16_f32(128, 128);
-    uint32_t ph = 0, lph = 0;
-    bool ok = true, mma_out = false, load_out = false;
+    uint32_t ph = 0, lph = 0, oph = 0;
+    bool ok = true, mma_out = false, a_out = false, o_out = false;
     int cur = -1;  // (split index, head) whose S1 is in b_t
     TIO *og = static_cast<TIO *>(p.out);
     OcTile x = resolve(u0);
-    if (a_tma && tid == 0) {
-        load_a(x);
-        load_out = true;
+    if (use_tma && tid == 0) {
+        load_tile(a_t, &map_oa, x.h * DH, (int)x.r0, &lbar);
+        a_out = true;
     }
+    // a bounded wait on one of this CTA's barriers (false: flagged by the caller)
+    auto wait_on = [&](uint64_t *mb, uint32_t &par, bool &outstanding) -> bool {
+        const bool got = ptx::mbar_wait_bounded(mb, par, WAIT_LIMIT);
+        if (got) {
+            par ^= 1u;
+            outstanding = false;
+        }
+        return __syncthreads_and(got);
+    };
     for (long long u = u0; u < u1 && ok; ++u) {
         // Tiles of a sequence whose slot is out of range run like the others but
         // write nothing (the scan flagged the slot and computed nothing for it).
         const bool live_seq = x.slot >= 0 && x.slot < p.num_slots;
         const int t = x.t0 + tid;
         const bool live = live_seq && t < x.eos;
+        const bool full = live_seq && x.t0 + OC_ROWS <= x.eos;  // every row of the tile is this sequence's
         TIO *dst = og + ((long long)t * p.Hv + x.h) * DH;
-        uint4 orow[F16 ? 16 : 1];  // fp16: this thread's output row, loaded before the product
-        if (F16 && live) {
-#pragma unroll
-            for (int q = 0; q < 16; ++q) orow[q] = reinterpret_cast<const uint4 *>(dst)[q];
+        if (use_tma && tid == 0) {  // the output rows; the buffer's previous tensor store has read it
+            ptx::bulk_wait_read_all();
+            load_tile(o_t, &map_out, x.h * DH, x.t0, &obar);
+            o_out = true;
         }
-        if (!a_tma) {  // FP32 rows: converted here, zero past the segment
+        if (!use_tma) {  // rows converted here, zero past the segment
             const TIO *src = oid + ((x.r0 + tid) * p.Hv + x.h) * DH;
 #pragma unroll 4
             for (int col = 0; col < DH; col += 8) {
@@ -1210,15 +1243,7 @@ __global__ void __launch_bounds__(OC_NT, 1)
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncthreads();
-        if (a_tma) {
-            const bool got = ptx::mbar_wait_bounded(&lbar, lph, WAIT_LIMIT);
-            if (got) {
-                lph ^= 1u;
-                load_out = false;
-            }
-            ok = __syncthreads_and(got);
-            if (!ok) break;
-        }
+        if (use_tma && !(ok = wait_on(&lbar, lph, a_out))) break;
         if (tid == 0) {
             ptx::tc_fence_after();
             const uint64_t ad = ptx::sdesc_k_sw128(ptx::smem_u32(a_t)), bd = ptx::sdesc_k_sw128(ptx::smem_u32(b_t));
@@ -1229,34 +1254,53 @@ __global__ void __launch_bounds__(OC_NT, 1)
             ptx::mma_commit(&bar);
         }
         mma_out = true;
-        const bool done = ptx::mbar_wait_bounded(&bar, ph, WAIT_LIMIT);
-        if (done) {
-            ph ^= 1u;
-            mma_out = false;
-        }
+        if (!(ok = wait_on(&bar, ph, mma_out))) break;
         ptx::tc_fence_after();
-        ok = __syncthreads_and(done);
-        if (!ok) break;
         // the operand tile is free: the next tile's rows are on their way during this epilogue
+        const OcTile cx = x;
         if (u + 1 < u1) {
             x = resolve(u + 1);
-            if (a_tma && tid == 0) {
-                load_a(x);
-                load_out = true;
+            if (use_tma && tid == 0) {
+                load_tile(a_t, &map_oa, x.h * DH, (int)x.r0, &lbar);
+                a_out = true;
             }
         }
-        // epilogue: token t, dv = 128 columns (unrolled: the row stays in registers)
+        if (use_tma) {
+            if (!(ok = wait_on(&obar, oph, o_out))) break;
+            // token t's row: TMEM columns 32q .. 32q + 31 onto the swizzled output tile
 #pragma unroll
-        for (int q = 0; q < DH / 32; ++q) {
-            float c[32];
-            ptx::tmem_ld32(tm + lane_sel + 32 * q, c);
-            if (!live) continue;
-            if constexpr (F16) {
+            for (int q = 0; q < DH / 32; ++q) {
+                float c[32];
+                ptx::tmem_ld32(tm + lane_sel + 32 * q, c);
 #pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    reinterpret_cast<uint4 *>(dst)[4 * q + m] = add_h8(orow[4 * q + m], c + 8 * m);
-            } else {
-                add_row32(reinterpret_cast<float *>(dst) + 32 * q, c);
+                for (int m = 0; m < 4; ++m) {
+                    uint4 *pv = reinterpret_cast<uint4 *>(o_t + sw(tid, 32 * q + 8 * m, OC_ROWS));
+                    const uint4 r = add_h8(*pv, c + 8 * m);
+                    if (full) *pv = r;
+                    else if (live) reinterpret_cast<uint4 *>(dst)[4 * q + m] = r;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            __syncthreads();
+            if (full && tid == 0) {
+                ptx::tma_store_2d(&map_out, o_t, cx.h * DH, cx.t0);
+                ptx::tma_store_2d(&map_out, o_t + OC_ROWS * 128, cx.h * DH + 64, cx.t0);
+                ptx::bulk_commit();
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < DH / 32; ++q) {
+                float c[32];
+                ptx::tmem_ld32(tm + lane_sel + 32 * q, c);
+                if (!live) continue;
+                if constexpr (F16) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        reinterpret_cast<uint4 *>(dst)[4 * q + m] =
+                            add_h8(reinterpret_cast<const uint4 *>(dst)[4 * q + m], c + 8 * m);
+                } else {
+                    add_row32(reinterpret_cast<float *>(dst) + 32 * q, c);
+                }
             }
         }
         ptx::tc_fence_before();
@@ -1264,8 +1308,10 @@ __global__ void __launch_bounds__(OC_NT, 1)
     }
     if (tid == 0) {
         if (!ok) flag_error(p.status, GDN_DEVERR_TIMEOUT);
-        if (mma_out) ptx::mbar_wait_bounded(&bar, ph, WAIT_LIMIT);    // let the MMA drain before tensor memory is freed
-        if (load_out) ptx::mbar_wait_bounded(&lbar, lph, WAIT_LIMIT);  // and the row copies
+        if (mma_out) ptx::mbar_wait_bounded(&bar, ph, WAIT_LIMIT);  // let the MMA drain before tensor memory is freed
+        if (a_out) ptx::mbar_wait_bounded(&lbar, lph, WAIT_LIMIT);  // and the copies in flight
+        if (o_out) ptx::mbar_wait_bounded(&obar, oph, WAIT_LIMIT);
+        ptx::bulk_wait_all();  // the tensor stores are complete
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -1382,7 +1428,7 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *
     if (prep_ctas > 0) prep<<<(unsigned)prep_ctas, PT, PREP_SMEM, stream>>>(p, hdr, krec, vrec, mq, mk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto scan = wy_scan_kernel<TIO>;
+    auto scan = nsplit > 0 ? wy_scan_kernel<TIO, true> : wy_scan_kernel<TIO, false>;
     e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, SCAN_SMEM);
     if (e != cudaSuccess) return e;
     const long long chains = (long long)p.B * p.Hv * (nsplit > 0 ? 3 : 1);
@@ -1399,13 +1445,15 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *
     e = cudaGetLastError();
     if (e != cudaSuccess || nsplit == 0) return e;
     // split sequences: outputs of the second segments, then their final states
-    CUtensorMap moa{};
-    const int a_tma = sizeof(TIO) == 2 && encode_rows_f16(&moa, oid, (long long)p.Hv * DH, (long long)p.Hv * DH,
-                                                          (int)oid_rows, 64, OC_ROWS, true);
+    CUtensorMap moa{}, mout{};
+    const int oc_tma =
+        sizeof(TIO) == 2 &&
+        encode_rows_f16(&moa, oid, (long long)p.Hv * DH, (long long)p.Hv * DH, (int)oid_rows, 64, OC_ROWS, true) &&
+        encode_rows_f16(&mout, p.out, (long long)p.Hv * DH, (long long)p.Hv * DH, p.T, 64, OC_ROWS, true);
     auto corr = wy_out_correction_kernel<TIO>;
     e = cudaFuncSetAttribute(corr, cudaFuncAttributeMaxDynamicSharedMemorySize, OC_SMEM);
     if (e != cudaSuccess) return e;
-    corr<<<3 * num_sms(), OC_NT, OC_SMEM, stream>>>(p, hdr, split_states, oid, moa, a_tma);
+    corr<<<2 * num_sms(), OC_NT, OC_SMEM, stream>>>(p, hdr, split_states, oid, moa, mout, oc_tma);
     e = cudaGetLastError();
     if (e != cudaSuccess || !p.final_state) return e;
     e = cudaFuncSetAttribute(wy_split_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FS_SMEM);
