@@ -42,6 +42,12 @@
 //    with the CUDA-core work between them (fp16 state copy, R^T, U^T and its
 //    decayed copy, capsule deltas, outputs) done by all 16 warps.
 //
+//  Split plan (sequence-parallel, for few long sequences): the scan runs each
+//    long sequence as three chains per head (first half; second half from a
+//    zero state; second half from the identity), and wy_out_correction_kernel
+//    and wy_split_final_kernel combine them (see "Sequence-parallel
+//    evaluation" below).
+//
 // Every MMA is kind::f16 (fp16 operands, FP32 accumulation in tensor memory)
 // with the value dimension dv = 128 as M and both operands in the 128-byte
 // swizzled layout, K-major except K in MMA5: its B operand is the [Q;K]
@@ -104,7 +110,7 @@ constexpr int OC_ROWS = 128;   // tokens per tile of the output correction
 //   [0] work counter of the scan, [1] E = work-list entries, [2] NS = split sequences
 //   list[3B]    work entries, longest chain first: b * 4 + kind
 //   cbase[B+1]  index of each sequence's first chunk in the record arrays
-//   sidx[B]     split index of each sequence, or -1
+//   sidx[B]     split index of each sequence, or -1      (these four: split plan only)
 //   sseq[B]     the sequence of each split index
 //   tbase[B+1]  first correction tile of each split sequence (prefix over split indices)
 //   obase[B+1]  first row of each split sequence's identity-run outputs
