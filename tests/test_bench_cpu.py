@@ -109,3 +109,14 @@ def test_clock_sampler_reads_its_process_output(tmp_path, monkeypatch):
     assert c["samples"] == 2 and c["sm_mhz"] == 2055 and c["reasons"] == ["sw_power_cap"]
     monkeypatch.setattr(bench.shutil, "which", lambda name: None)
     assert bench.ClockSampler().stop() is None
+
+
+def test_only_names_every_sub_measurement():
+    """--only accepts exactly the sub-measurements the full run reports."""
+    import inspect
+    import re
+    src = inspect.getsource(bench.run_gdn)
+    reported = set(re.findall(r'extra\["(\w+)"\]', src))
+    assert reported == set(bench.SUB_MEASUREMENTS)
+    for name, fn in bench.SUB_MEASUREMENTS.items():
+        assert (len(inspect.signature(fn).parameters) == 4) == (name in bench.NEEDS_LIB), name

@@ -44,7 +44,7 @@ def _run_both(inp, B, S, plan, workspace=None):
 
 
 @pytest.mark.parametrize("B,S,plan,tol", [(6, 4, "auto", 1e-5), (3, 200, "auto", 2e-3), (2, 130, "chunked", 2e-3),
-                                          (5, 1, "recurrent", 1e-5)])
+                                          (5, 1, "recurrent", 1e-5), (2, 2100, "chunked_split", 2e-3)])
 def test_dense_equals_packed_and_oracle(B, S, plan, tol):
     io = np.float32 if tol == 1e-5 else np.float16
     inp = _dense_inputs(301 + S, B, S, 2, 6, 128, io)
