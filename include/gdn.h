@@ -170,9 +170,10 @@ typedef struct gdn_forward_args {
 /*
  * Sequence-parallel evaluation (GDN_PLAN_CHUNKED_SPLIT).
  *
- * The pages' operator evaluates each (sequence, value head) chain in order,
- * chunk after chunk ("[CUDA] Add compact GatedDeltaNet operator",
- * Description); a single long prompt then has only Hv chains, fewer than the
+ * The chunked evaluation of the operator ("[CUDA] Add compact GatedDeltaNet
+ * operator", Description: the tensor-core chunked-prefill path) passes the
+ * state from chunk to chunk, so each (sequence, value head) chain is
+ * sequential, and a single long prompt has only Hv chains, fewer than the
  * GPU's SMs.  Per value head, each token maps the state affinely,
  * S -> S g (I - beta kn kn^T) + beta v kn^T, so over the second half of a
  * sequence S_t = S1 A_t + B_t, with S1 the state entering that half.  The
@@ -196,9 +197,10 @@ typedef struct gdn_forward_args {
  * Bytes of device workspace gdn_forward needs for these arguments (sizes,
  * plan, io_dtype and max_seqlen only are read).  Non-zero exactly when a chunked
  * (tensor-core) kernel may run.  The size is that of the two-phase chunked
- * evaluation: a header (work counter, the longest-first list of sequences,
- * each sequence's first chunk) plus one record per (64-token chunk, key head)
- * of 32 KiB and one per (chunk, value head) of 17,408 bytes, for at most
+ * evaluation: a header (work counter, the longest-first work list and
+ * per-sequence offsets: 4 (7 + 8B) bytes rounded up to 1 KiB) plus one record
+ * per (64-token chunk, key head) of 32 KiB and one per (chunk, value head) of
+ * 17,408 bytes, for at most
  * T/64 + B chunks -- about 1.36 MB per 64 tokens at Hk = 16, Hv = 48.
  * GDN_PLAN_CHUNKED_SPLIT adds three FP32 states per value head for each
  * sequence that can be split (at most min(B, T / 1985)) and T/2 + 64 rows of
