@@ -482,6 +482,22 @@ def run_prefill(dev, stream):
                                                      "varlen_prefill.wy_kernels.ncu.md")}}
 
 
+def long_prefill_inputs(dev, T=262144, Hk=16, Hv=48, d=128, seed=1006):
+    """The long-prefill batch (one sequence of T tokens), drawn on the device
+    from a seeded generator: q, k, v ~ N(0,1) fp16, raw a, b ~ N(0,1), and the
+    gate parameters of the other workloads."""
+    import torch
+    from gated_delta_rule_gateddeltanet_gb300 import workloads as wl
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    rnd = lambda shape, dt: torch.randn(shape, generator=gen, device=dev, dtype=dt)
+    q, k, v = rnd((T, Hk, d), torch.float16), rnd((T, Hk, d), torch.float16), rnd((T, Hv, d), torch.float16)
+    aa, bb = rnd((T, Hv), torch.float32), rnd((T, Hv), torch.float32)
+    A_log, dt_bias = (torch.from_numpy(x).to(dev) for x in wl.gate_params(np.random.default_rng(seed), Hv))
+    cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    return q, k, v, aa, bb, A_log, dt_bias, cu
+
+
 def run_long_prefill(dev, stream):
     """One 262,144-token sequence (the pages' 256k context), Hk=16, Hv=48,
     d=128, fp16, zero initial state, under the chunked plan (48 chains) and
@@ -490,15 +506,9 @@ def run_long_prefill(dev, stream):
     larger than L2)."""
     import torch
     import gated_delta_rule_gateddeltanet_gb300 as gdn
-    from gated_delta_rule_gateddeltanet_gb300 import workloads as wl
-    T, Hk, Hv, d = 262144, 16, 48, 128
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(1006)
-    rnd = lambda shape, dt: torch.randn(shape, generator=gen, device=dev, dtype=dt)
-    q, k, v = rnd((T, Hk, d), torch.float16), rnd((T, Hk, d), torch.float16), rnd((T, Hv, d), torch.float16)
-    aa, bb = rnd((T, Hv), torch.float32), rnd((T, Hv), torch.float32)
-    A_log, dt_bias = (torch.from_numpy(x).to(dev) for x in wl.gate_params(np.random.default_rng(1006), Hv))
-    cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    q, k, v, aa, bb, A_log, dt_bias, cu = long_prefill_inputs(dev)
+    T, Hk, d = q.shape
+    Hv = v.shape[1]
     final = torch.zeros((1, Hv, d, d), dtype=torch.float32, device=dev)
     out = torch.empty((T, Hv, d), dtype=torch.float16, device=dev)
     res = {}

@@ -139,3 +139,26 @@ def test_split_full_heads_sampled():
     o_ref, f_ref, _ = run_oracle(sub)
     assert max_rel(out[:, hs], o_ref) <= TOL
     assert max_rel(final[:, hs], f_ref) <= TOL
+
+
+def test_long_prefill_full_size_sampled():
+    """The long-prefill measurement itself: one 262,144-token sequence at
+    Hk = 16, Hv = 48, d = 128, fp16, zero initial state, the bench's own
+    inputs and launch (split plan).  The oracle runs key head 5 and its
+    value heads 15-17 over all 262,144 tokens (each chain is independent of
+    the other heads)."""
+    import bench
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    q, k, v, aa, bb, A_log, dt_bias, cu = bench.long_prefill_inputs(dev())
+    Hv = v.shape[1]
+    final = torch.zeros((1, Hv, 128, 128), dtype=torch.float32, device=dev())
+    out, final, _ = gdn.gdn_forward(q, k, v, aa, bb, cu, A_log=A_log, dt_bias=dt_bias, final_state=final,
+                                    plan="chunked_split")
+    torch.cuda.synchronize()
+    kh, hs = 5, slice(15, 18)
+    h = lambda x: np.ascontiguousarray(x.cpu().numpy())
+    sub = wl.GdnInputs(h(q[:, kh:kh + 1]), h(k[:, kh:kh + 1]), h(v[:, hs]), h(aa[:, hs]), h(bb[:, hs]),
+                       h(A_log[hs]), h(dt_bias[hs]), h(cu), None)
+    o_ref, f_ref, _ = run_oracle(sub)
+    assert max_rel(out[:, hs].double().cpu().numpy(), o_ref) <= TOL
+    assert max_rel(final[:, hs].double().cpu().numpy(), f_ref) <= TOL
