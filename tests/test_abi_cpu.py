@@ -268,3 +268,31 @@ def test_dense_and_transpose_reject_bad_arguments_before_launch(lib):
     assert lib.gdn_state_transpose(None, P(0x100000), 4, 128, 128, None) == 1
     # 4 matrices of 128 x 128 floats = 256 KiB: destinations inside that range overlap the source
     assert lib.gdn_state_transpose(P(0x100000), P(0x100000 + 4096), 4, 128, 128, None) == 8
+
+
+def test_split_workspace_bounds_hold_for_any_lengths(lib):
+    """The split plan's workspace holds three states per head for at most
+    min(B, T / 1985) split sequences and T/2 + 64 identity-run rows: for any
+    mix of lengths, the sequences the rule splits (32 or more chunks, cut
+    after ceil(chunks / 2)) stay within both, and gdn_forward_workspace_size
+    reports exactly that room."""
+    rng = __import__("numpy").random.default_rng(17)
+    n = ctypes.c_size_t(0)
+    cases = [[1985] * 7, [1984] * 9, [64 * 33 + 1, 1985, 3], [262144], [4096, 4095, 4097, 1]]
+    cases += [list(rng.integers(0, 9000, rng.integers(1, 40))) for _ in range(200)]
+    for lengths in cases:
+        B, T = len(lengths), int(sum(lengths))
+        if T == 0:
+            continue
+        chunks = [(L + 63) // 64 for L in lengths]
+        split = [c >= 32 for c in chunks]
+        seg2 = sum(L - 64 * ((c + 1) // 2) for L, c, s in zip(lengths, chunks, split) if s)
+        nsplit = sum(split)
+        max_split = min(B, T // (64 * 31 + 1))
+        assert nsplit <= max_split, lengths
+        assert seg2 <= T // 2 + 64, lengths
+        a = _args(num_seqs=B, total_tokens=T, num_state_slots=B, plan=3)
+        assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0
+        base = ((7 + 8 * B) * 4 + 1023) // 1024 * 1024 + (T // 64 + B) * (16 * 32768 + 48 * 17408)
+        extra = max_split * 3 * 48 * 128 * 128 * 4 + (T // 2 + 64) * 48 * 128 * 2 if max_split > 0 else 0
+        assert n.value == base + extra, lengths
