@@ -218,3 +218,23 @@ def test_chunked_many_sequences(path):
     inp = wl.make_inputs(215, lengths, Hk=1, Hv=1, dk=128, dv=128, io_dtype=np.float16, state_std=0.02,
                          capacity=2)
     _check(inp, run_gpu(inp, plan="chunked", in_place=False, workspace=_ws(path, inp)), run_oracle(inp))
+
+
+def test_pages_ragged_batch_is_bitwise_the_prompts_alone():
+    """The validation case of "Add GatedDeltaNet evaluation export for Qwen
+    hybrid models" (reviewer validation): a batch of 17-, 512- and 1993-token
+    prompts gives bit-identical outputs to the same prompts run alone.  Under
+    the automatic plan the 17-token prompt takes the tensor-core short-span
+    kernel and the others the chunked kernels, in the batch and alone."""
+    lengths = [17, 512, 1993]
+    inp = wl.make_inputs(216, lengths, Hk=2, Hv=6, dk=128, dv=128, io_dtype=np.float16, state_std=0.02)
+    out, final, _ = run_gpu(inp, in_place=False)
+    cu = inp.cu_seqlens
+    for s, L in enumerate(lengths):
+        t0, t1 = cu[s], cu[s + 1]
+        one = wl.GdnInputs(inp.q[t0:t1], inp.k[t0:t1], inp.v[t0:t1], inp.a[t0:t1], inp.b[t0:t1], inp.A_log,
+                           inp.dt_bias, np.array([0, L], np.int32), inp.initial_state[s:s + 1], None)
+        o1, f1, _ = run_gpu(one, in_place=False)
+        assert np.array_equal(out[t0:t1], o1)
+        assert np.array_equal(final[s], f1[0])
+    _check(inp, (out, final, None), run_oracle(inp))
