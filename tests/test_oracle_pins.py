@@ -167,6 +167,131 @@ def test_raw_gates_stable_at_extremes():
     assert caps[0, 0, 0] == 1.0 and caps[0, 0, 1] == 0.0
 
 
+# ------------------------------------------------------- L2-norm clamp (eps)
+#
+# The pages fuse the Qwen q/k normalisation into the operator ("[CUDA] Add
+# compact GatedDeltaNet operator", Description) without printing it; the
+# reading taken is x / max(|x|, 1e-6).  These cases fix that reading by hand:
+# a zero key gives kn = 0, so u = beta v and the state is only decayed; a zero
+# query gives a zero output; a vector shorter than eps is divided by eps (a
+# non-unit direction, exact in rationals up to the one rounding of the
+# division); a vector just longer than eps is normalised as usual.  A missing
+# clamp (NaN), eps added to the norm, eps on the squared norm, or another eps
+# each change one of the expected values below.
+
+EPS = Fr(1e-6)  # the double nearest 1e-6, exactly
+
+
+def _exact_unit(x):
+    """x / max(|x|, eps) in rationals for integer-times-power-of-two vectors
+    whose norm is rational (so sqrt is exact)."""
+    xs = [Fr(float(e)) for e in x]
+    ss = sum(e * e for e in xs)
+    if ss == 0:
+        return [Fr(0)] * len(xs)
+    n_num, n_den = math.isqrt(ss.numerator), math.isqrt(ss.denominator)
+    assert Fr(n_num, n_den) ** 2 == ss, "test vector must have a rational norm"
+    nrm = Fr(n_num, n_den)
+    return [e / max(nrm, EPS) for e in xs]
+
+
+def _brute_units(qns, kns, vs, gs, bs, S0, scale):
+    """The unrolled transition S_t = g S (I - beta kn kn^T) + beta v kn^T with
+    the normalised vectors given (any length), read-out o = scale S_t qn."""
+    dv, dk = len(S0), len(S0[0])
+    S = [row[:] for row in S0]
+    outs, us = [], []
+    for qn, kn, v, g, beta in zip(qns, kns, vs, gs, bs):
+        P = [[(1 if i == j else 0) - beta * kn[i] * kn[j] for j in range(dk)] for i in range(dk)]
+        Snew = [[g * sum(S[a][m] * P[m][j] for m in range(dk)) + beta * v[a] * kn[j] for j in range(dk)]
+                for a in range(dv)]
+        u = [beta * (v[a] - g * sum(S[a][j] * kn[j] for j in range(dk))) for a in range(dv)]
+        outs.append([scale * sum(Snew[a][j] * qn[j] for j in range(dk)) for a in range(dv)])
+        us.append(u)
+        S = Snew
+    return outs, S, us
+
+
+def test_l2_norm_clamp_zero_and_tiny_vectors():
+    Hk, Hv, dk, dv = 1, 2, 4, 3
+    e23, e22 = 2.0 ** -23, 2.0 ** -22
+    normal_q, normal_k = [1, 2, 2, 4], [2, 4, 1, 2]           # norms 5 and 5
+    rows = [  # (q, k) per token
+        (normal_q, normal_k),
+        (normal_q, [0, 0, 0, 0]),                               # zero key
+        ([0, 0, 0, 0], normal_k),                               # zero query
+        (normal_q, [3 * e23, 4 * e23, 0, 0]),                   # |k| = 5.96e-7 < eps
+        ([0, 3 * e23, 0, 4 * e23], normal_k),                   # |q| = 5.96e-7 < eps
+        (normal_q, [3 * e22, 0, 4 * e22, 0]),                   # |k| = 1.19e-6 > eps
+        ([0, 0, 0, 0], [0, 0, 0, 0]),                           # both zero
+        ([e23, e23, e23, e23], [-e23, e23, -e23, e23]),         # |x| = 2.4e-7, both tiny
+        (normal_q, normal_k),
+    ]
+    T = len(rows)
+    q = np.array([r[0] for r in rows], np.float64).reshape(T, Hk, dk)
+    k = np.array([r[1] for r in rows], np.float64).reshape(T, Hk, dk)
+    rng = np.random.default_rng(17)
+    v = rng.integers(-4, 5, (T, Hv, dv)) / 2.0
+    g = rng.choice([0.5, 0.75, 1.0], (T, Hv))
+    beta = rng.choice([0.25, 0.5, 1.0], (T, Hv))
+    S0 = rng.integers(-3, 4, (1, Hv, dv, dk)) / 4.0
+    cu = np.array([0, T], np.int32)
+    out, final, caps = oracle.gdn_forward(q, k, v, g, beta, cu, gate_mode="precomputed", initial_state=S0,
+                                          capacity=T)
+    W = oracle.capsule_width(Hk, Hv, dk, dv)
+    kn_caps = caps[0, :, Hv:Hv + Hk * dk]
+    u_caps = caps[0, :, Hv + Hk * dk:W].reshape(T, Hv, dv)
+
+    # by hand: the clamp's effect on the normalised key
+    assert np.array_equal(kn_caps[1], np.zeros(dk)) and np.array_equal(kn_caps[6], np.zeros(dk))
+    np.testing.assert_allclose(kn_caps[3], np.array([3, 4, 0, 0]) * e23 / 1e-6, rtol=1e-15)
+    np.testing.assert_allclose(kn_caps[5], np.array([3, 0, 4, 0]) / 5.0, rtol=1e-15)
+    np.testing.assert_allclose(kn_caps[7], np.array([-1, 1, -1, 1]) * e23 / 1e-6, rtol=1e-15)
+    # zero key: the delta is beta v exactly, and the state is only decayed
+    assert np.array_equal(u_caps[1], beta[1][:, None] * v[1])
+    _, s0, _ = oracle.gdn_forward(q[:1], k[:1], v[:1], g[:1], beta[:1], np.array([0, 1]),
+                                  gate_mode="precomputed", initial_state=S0)
+    _, s1, _ = oracle.gdn_forward(q[:2], k[:2], v[:2], g[:2], beta[:2], np.array([0, 2]),
+                                  gate_mode="precomputed", initial_state=S0)
+    assert np.array_equal(s1[0], g[1][:, None, None] * s0[0])
+    # zero query: a zero output
+    assert np.array_equal(out[2], np.zeros((Hv, dv))) and np.array_equal(out[6], np.zeros((Hv, dv)))
+
+    # everything against the exact rational evaluation with the clamped vectors
+    qns = [_exact_unit(q[t, 0]) for t in range(T)]
+    kns = [_exact_unit(k[t, 0]) for t in range(T)]
+    for h in range(Hv):
+        outs, Sx, us = _brute_units(qns, kns, [[Fr(x) for x in v[t, h]] for t in range(T)],
+                                    [Fr(g[t, h]) for t in range(T)], [Fr(beta[t, h]) for t in range(T)],
+                                    [[Fr(x) for x in row] for row in S0[0, h]], Fr(1, 2))
+        assert max_rel(final[0, h], np.array([[float(x) for x in r] for r in Sx])) <= 1e-13
+        for t in range(T):
+            ex_o = np.array([float(x) for x in outs[t]])
+            assert np.max(np.abs(out[t, h] - ex_o)) <= 1e-13 * max(1.0, np.max(np.abs(ex_o)))
+            assert np.max(np.abs(u_caps[t, h] - np.array([float(x) for x in us[t]]))) <= 1e-13
+
+
+def test_chunked_evaluator_clamps_like_the_sequential_oracle():
+    """The chunked (WY) evaluator with runs of zero and sub-eps keys and queries
+    inside and across chunks equals the sequential oracle."""
+    lengths = [40, 23]
+    q, k, v, a, b, A_log, dt_bias, S0, cu = _rand_batch(33, lengths, 1, 2, 16, 8)
+    k[3] = 0.0
+    k[10:14] = 0.0
+    q[5:9] = 0.0
+    k[20] *= 1e-8 / np.linalg.norm(k[20])
+    q[21] *= 3e-7 / np.linalg.norm(q[21])
+    k[41] *= 5e-7 / np.linalg.norm(k[41])
+    out, final, caps = oracle.gdn_forward(q, k, v, a, b, cu, A_log=A_log, dt_bias=dt_bias,
+                                          initial_state=S0, capacity=max(lengths))
+    for chunk in (1, 8, 64):
+        o2, f2, u2 = chunked.chunked_forward(q, k, v, a, b, cu, A_log=A_log, dt_bias=dt_bias,
+                                             initial_state=S0, chunk=chunk)
+        assert max_rel(o2, out) <= 1e-10
+        assert max_rel(f2, final) <= 1e-10
+    assert np.array_equal(out[5:9], np.zeros_like(out[5:9]))
+
+
 # ---------------------------------------------------------------- invariants
 
 def _rand_batch(seed, lengths, Hk, Hv, dk, dv, state=True):
