@@ -80,8 +80,9 @@ def test_reference_arm_prints_one_contract_line(monkeypatch):
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
     assert d["value"] > 0 and d["higher_is_better"] is True and d["steps"] == 1 and d["warmup"] == 1
+    # the same config object as the GPU arm's line
+    assert d["config"] == bench.workload_config(64, 16, 48, 128, 128, 1)
     assert d["config"]["workload"] == bench.WORKLOAD
-    assert 1 <= d["config"]["requests_per_step_sampled"] <= 64
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
