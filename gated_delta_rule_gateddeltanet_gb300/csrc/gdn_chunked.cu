@@ -701,17 +701,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *cu, int dense
     }
 }
 
-int num_sms() {
-    static int cached = 0;
-    if (cached == 0) {
-        int dev = 0, n = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-            cached = n;
-        else
-            cached = 148;
-    }
-    return cached;
-}
+int num_sms() { return current_device_sms(); }
 
 template <typename TIO>
 cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStream_t stream) {

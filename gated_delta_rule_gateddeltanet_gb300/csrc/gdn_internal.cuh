@@ -34,6 +34,21 @@ struct ForwardParams {
     int dense_S;
 };
 
+// Streaming multiprocessors of the current device, looked up once per device
+// ordinal (persistent grids are sized from it; a process may drive GPUs with
+// different SM counts).
+inline int current_device_sms() {
+    constexpr int kMaxDevices = 128;
+    static int cached[kMaxDevices] = {};
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+    if (dev < kMaxDevices && __atomic_load_n(&cached[dev], __ATOMIC_RELAXED) > 0)
+        return __atomic_load_n(&cached[dev], __ATOMIC_RELAXED);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    if (dev < kMaxDevices) __atomic_store_n(&cached[dev], n, __ATOMIC_RELAXED);
+    return n;
+}
+
 // First token of sequence b (b may be B: one past the last sequence).
 __host__ __device__ __forceinline__ int seq_start(const int32_t *cu, int dense_S, int b) {
     return cu ? cu[b] : b * dense_S;
