@@ -19,6 +19,14 @@
 // current) and caches it; make that first call before any stream capture.
 // Nothing here calls cudaMalloc, cudaFree or any allocating routine.
 //
+// The cached address belongs to the device's primary context as it was at the
+// first call: after cudaDeviceReset (or anything else that tears that context
+// down) it is stale, so the library must not be used across a device reset.
+//
+// The sequence-parallel split plan has no single-kernel form (it needs
+// per-sequence states and identity-run rows that grow with the batch), so it
+// is refused here with GDN_ERR_UNSUPPORTED before anything else is looked at.
+//
 // All calls share the one array.  Everything the kernels need from it (the
 // work counter and the chain list) is rewritten at the start of every call,
 // so what an earlier call left there does not matter; but calls that overlap
@@ -54,6 +62,7 @@ gdn_status scratch_address(void **out) {
 
 extern "C" gdn_status gdn_forward_no_alloc(const gdn_forward_args *args, gdn_stream_t stream) {
     if (!args) return GDN_ERR_NULL;
+    if (args->plan == GDN_PLAN_CHUNKED_SPLIT) return GDN_ERR_UNSUPPORTED;
     size_t need = 0;
     gdn_status st = gdn::single_kernel_workspace_size(args, &need);
     if (st != GDN_OK) return st;

@@ -190,7 +190,7 @@ typedef struct gdn_forward_args {
  * Restrictions: state_update_capacity must be 0 (GDN_ERR_UNSUPPORTED
  * otherwise), the workspace must be the one gdn_forward_workspace_size
  * reports for this plan (there is no single-kernel form; smaller workspaces
- * and gdn_forward_no_alloc give GDN_ERR_WORKSPACE).
+ * give GDN_ERR_WORKSPACE and gdn_forward_no_alloc GDN_ERR_UNSUPPORTED).
  */
 
 /*
@@ -302,8 +302,14 @@ gdn_status gdn_replay_prefix(float *state_banks, int32_t num_slots, int32_t num_
  *
  *  - Batches of more than GDN_NO_ALLOC_MAX_SEQS sequences that need a
  *    workspace are rejected with GDN_ERR_WORKSPACE before anything runs.
+ *  - plan = GDN_PLAN_CHUNKED_SPLIT is rejected with GDN_ERR_UNSUPPORTED: the
+ *    split plan's workspace grows with the batch and it has no single-kernel
+ *    form.
  *  - The first call on each device looks up the array's device address with
  *    that device current; make that first call before any stream capture.
+ *    The address is kept for the life of the process, so the library must not
+ *    be used after a cudaDeviceReset (or any other teardown of the device's
+ *    primary context) in the same process.
  *  - All calls share the array (each call rewrites what it uses), so calls
  *    that overlap on the GPU, e.g. on two streams, race and must not be made.
  *  - No cudaMalloc, cudaFree or other allocating routine is called.

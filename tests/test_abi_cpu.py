@@ -177,6 +177,10 @@ def test_split_plan_workspace_and_restrictions(lib):
     assert lib.gdn_forward(ctypes.byref(_args(plan=3, state_update_capacity=4)), None) == 7  # no capsules
     assert lib.gdn_forward(ctypes.byref(_args(plan=3)), None) == 5                            # no workspace
     assert lib.gdn_forward(ctypes.byref(_args(plan=4)), None) == 8
+    # the no-alloc entry has no form of the split plan: refused before any lookup or launch
+    assert lib.gdn_forward_no_alloc(ctypes.byref(_args(plan=3)), None) == 7
+    assert lib.gdn_forward_no_alloc(ctypes.byref(_args(plan=3, num_seqs=1, total_tokens=3000,
+                                                       num_state_slots=1)), None) == 7
 
 
 def test_forced_chunked_plan_needs_d128_and_workspace(lib):

@@ -63,6 +63,36 @@ def test_no_alloc_matches_gdn_forward_on_consecutive_calls():
         assert np.all(np.isfinite(got[0]))
 
 
+def test_no_alloc_all_short_batch_needs_no_scratch():
+    # every sequence takes the recurrent kernels, which use no workspace: the
+    # call must not look the scratch array up and must match gdn_forward
+    inp = wl.make_inputs(303, [1, 4, 32, 0, 17, 2], Hk=2, Hv=6, dk=128, dv=128, io_dtype=np.float16,
+                         state_std=0.02, capacity=4)
+    for _ in range(2):
+        want = _run("gdn_forward", inp, use_workspace=True)
+        got = _run("gdn_forward_no_alloc", inp, use_workspace=False)
+        for g, w in zip(got, want):
+            assert max_rel(g, w) <= TOL
+
+
+def test_no_alloc_python_wrapper_matches_gdn_forward():
+    # the binding's wrapper: it drops any workspace argument and lets the
+    # argument builder allocate the outputs, then calls the no-alloc entry
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    inp = wl.make_inputs(304, [150, 3, 90], Hk=2, Hv=6, dk=128, dv=128, io_dtype=np.float16, state_std=0.02,
+                         capacity=5)
+    kw = dict(A_log=to_dev(inp.A_log), dt_bias=to_dev(inp.dt_bias), capacity=inp.capacity)
+    ins = [to_dev(x) for x in (inp.q, inp.k, inp.v, inp.a, inp.b, inp.cu_seqlens)]
+    for _ in range(2):
+        s0, s1 = to_dev(inp.initial_state), to_dev(inp.initial_state)
+        want = gdn.gdn_forward(*ins, initial_state=s0, final_state=s0, **kw)
+        got = gdn.gdn_forward_no_alloc(*ins, initial_state=s1, final_state=s1,
+                                       workspace=torch.empty(16, dtype=torch.uint8, device=dev()), **kw)
+        torch.cuda.synchronize()
+        for g, w in zip(got, want):
+            assert max_rel(g.double().cpu().numpy(), w.double().cpu().numpy()) <= TOL
+
+
 def test_no_alloc_rejects_batches_beyond_its_scratch():
     import gated_delta_rule_gateddeltanet_gb300 as gdn
     lib = gdn.load_library()
