@@ -51,7 +51,6 @@ gdn_status check_sizes(const gdn_forward_args *a) {
         return GDN_ERR_SHAPE;
     if (!(a->scale >= 0.f) || isinf(a->scale)) return GDN_ERR_SHAPE;
     if (forced_chunked(a) && !gdn::chunked_supported(a->head_dim_k, a->head_dim_v)) return GDN_ERR_UNSUPPORTED;
-    if (a->plan == GDN_PLAN_CHUNKED_SPLIT && a->state_update_capacity > 0) return GDN_ERR_UNSUPPORTED;
     return GDN_OK;
 }
 

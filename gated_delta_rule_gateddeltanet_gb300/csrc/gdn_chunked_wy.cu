@@ -170,9 +170,11 @@ __device__ long long scan_sequences(int B, V value, P put, long long *wsum) {
 // their length in chunks (lengths above 1022 share the first bin and are all
 // scheduled first).  Sequences with a bad packing are left out (the recurrent
 // kernel reports them); an empty sequence is listed (its final state is its
-// initial state).  split = false: no sequence is split.
+// initial state).  split = false: no sequence is split.  A sequence is split
+// only when the tokens it captures (the first `cap`) all lie in its first
+// segment, which runs from the true state and so yields the exact deltas.
 __global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int dense_S, int B, int T, int min_len,
-                                                          bool split, int32_t *ws) {
+                                                          bool split, int cap, int32_t *ws) {
     __shared__ int hist[PLAN_BINS];
     __shared__ long long wsum[PLAN_NT / 32];
     __shared__ int total;
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int
         if (lo < 0 || hi < lo || hi > T || hi - lo <= min_len) return -1;
         return (hi - lo + CH - 1) / CH;
     };
-    auto is_split = [&](int c) { return split && c >= SPLIT_MIN; };
+    auto is_split = [&](int c) { return split && c >= SPLIT_MIN && cap <= CH * ((c + 1) / 2); };
     auto bin = [&](int c) { return PLAN_BINS - 1 - min(c, PLAN_BINS - 1); };
     for (int i = tid; i < PLAN_BINS; i += PLAN_NT) hist[i] = 0;
     __syncthreads();
@@ -846,6 +848,9 @@ __global__ void __launch_bounds__(NT, 1)
         float *const fdst = kind == K_FIRST ? sstate
                                             : (p.final_state ? (kind == K_WHOLE ? p.final_state + head_off : sstate)
                                                              : nullptr);
+        // capsule deltas come from chains that run from the true state (a split
+        // sequence's captured tokens all lie in its first segment)
+        const bool caps_here = p.caps != nullptr && kind <= K_FIRST;
 
         // chunk c's records (and fp16 v rows) into stage st
         auto stage_load = [&](int c, int st) {
@@ -1016,7 +1021,7 @@ __global__ void __launch_bounds__(NT, 1)
                 ptx::mma_commit(&bar);
             }
             // the capsule deltas while MMA4/5 run
-            if (p.caps) {
+            if (caps_here) {
 #pragma unroll
                 for (int j = 0; j < CW; ++j) {
                     const int s = c16 + j, tl = t0 + s - bos;
@@ -1413,7 +1418,7 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *
     TIO *oid = reinterpret_cast<TIO *>(reinterpret_cast<uint8_t *>(split_states) +
                                        (size_t)nsplit * 3 * p.Hv * STATE_BYTES);
     const long long oid_rows = max_split_rows(p.T);
-    wy_plan_kernel<<<1, PLAN_NT, 0, stream>>>(p.cu, p.dense_S, p.B, p.T, min_len, nsplit > 0, hdr);
+    wy_plan_kernel<<<1, PLAN_NT, 0, stream>>>(p.cu, p.dense_S, p.B, p.T, min_len, nsplit > 0, p.cap, hdr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long prep_ctas = maxch * p.Hk;

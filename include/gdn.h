@@ -68,8 +68,8 @@ enum {
     GDN_PLAN_CHUNKED = 2,    /* every sequence on the tensor-core chunked kernel
                                 (dk = dv = 128 only, else GDN_ERR_UNSUPPORTED) */
     GDN_PLAN_CHUNKED_SPLIT = 3 /* GDN_PLAN_CHUNKED, and every sequence of more than
-                                1984 tokens (31 chunks) is evaluated as two halves at
-                                once: for batches of a few long sequences, whose
+                                1984 tokens (31 chunks) whose captured tokens lie in
+                                its first half is evaluated as two halves at once: for batches of a few long sequences, whose
                                 (sequence, head) chains would leave most SMs idle.
                                 See "Sequence-parallel evaluation" below. */
 };
@@ -185,10 +185,14 @@ typedef struct gdn_forward_args {
  * equal those of GDN_PLAN_CHUNKED up to floating-point rounding (the
  * correction is a tensor-core product with fp16 operands and FP32
  * accumulation, and second-half outputs are rounded twice to the I/O type).
- * Whether a sequence is split depends only on its own length, so a packed
- * batch still gives bitwise the results of its sequences run one at a time.
- * Restrictions: state_update_capacity must be 0 (GDN_ERR_UNSUPPORTED
- * otherwise), the workspace must be the one gdn_forward_workspace_size
+ * Capsules: only tokens whose state is known exactly have a delta, so a
+ * sequence is split only when its captured tokens (the first
+ * state_update_capacity) all lie in the first half, which runs from the true
+ * initial state; otherwise it runs whole.  A sequence of more than 1984
+ * tokens is split when that holds, so whether it is split depends only on
+ * its own length and the capacity, and a packed batch still gives bitwise
+ * the results of its sequences run one at a time.
+ * Restrictions: the workspace must be the one gdn_forward_workspace_size
  * reports for this plan (there is no single-kernel form; smaller workspaces
  * give GDN_ERR_WORKSPACE and gdn_forward_no_alloc GDN_ERR_UNSUPPORTED).
  */

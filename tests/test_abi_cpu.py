@@ -174,7 +174,9 @@ def test_split_plan_workspace_and_restrictions(lib):
     assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0
     assert n.value == 1024 + (1984 // 64 + 2) * (16 * 32768 + 48 * 17408)
     assert lib.gdn_forward(ctypes.byref(_args(plan=3, head_dim_k=64)), None) == 7
-    assert lib.gdn_forward(ctypes.byref(_args(plan=3, state_update_capacity=4)), None) == 7  # no capsules
+    # capsules are allowed (captured tokens come from first halves); this call has no workspace
+    assert lib.gdn_forward(ctypes.byref(_args(plan=3, state_update_capacity=4, state_update=ctypes.c_void_p(0x1000))),
+                           None) == 5
     assert lib.gdn_forward(ctypes.byref(_args(plan=3)), None) == 5                            # no workspace
     assert lib.gdn_forward(ctypes.byref(_args(plan=4)), None) == 8
     # the no-alloc entry has no form of the split plan: refused before any lookup or launch

@@ -162,3 +162,33 @@ def test_long_prefill_full_size_sampled():
     o_ref, f_ref, _ = run_oracle(sub)
     assert max_rel(out[:, hs].double().cpu().numpy(), o_ref) <= TOL
     assert max_rel(final[:, hs].double().cpu().numpy(), f_ref) <= TOL
+
+
+@pytest.mark.parametrize("cap", [1000, 1500])
+def test_split_plan_with_capsules(cap):
+    """Capsules under the split plan.  Only tokens whose state is exact have a
+    delta, so a sequence is split only when its captured tokens (the first
+    `cap`) lie in its first half: with cap = 1000 both long sequences (first
+    halves of 1088 and 2112 tokens) are split; with cap = 1500 the
+    2100-token one runs whole and gives bitwise the chunked plan's results."""
+    from gpu_common import capsule_parts
+    lengths = [2100, 300, 4217]
+    inp = wl.make_inputs(908, lengths, Hk=2, Hv=4, dk=128, dv=128, io_dtype=np.float16, state_std=0.05,
+                         capacity=cap)
+    gpu = run_gpu(inp, plan="chunked_split", in_place=False)
+    ref = run_oracle(inp)
+    _check(inp, gpu, ref)
+    Hk, Hv, dk, dv = inp.dims
+    g, kn, u = capsule_parts(gpu[2], Hk, Hv, dk, dv)
+    gr, knr, ur = capsule_parts(ref[2], Hk, Hv, dk, dv)
+    for s, L in enumerate(lengths):
+        n = min(L, cap)
+        assert max_rel(g[s, :n], gr[s, :n]) <= 1e-5
+        assert max_rel(kn[s, :n], knr[s, :n]) <= 1e-5
+        assert max_rel(u[s, :n], ur[s, :n]) <= TOL, (s, max_rel(u[s, :n], ur[s, :n]))
+    if cap == 1500:  # the first sequence was not split: the chunked plan's bits
+        whole = run_gpu(inp, plan="chunked", in_place=False)
+        n0 = inp.cu_seqlens[1]
+        assert np.array_equal(gpu[0][:n0], whole[0][:n0])
+        assert np.array_equal(gpu[1][0], whole[1][0])
+        assert np.array_equal(gpu[2][0], whole[2][0])
