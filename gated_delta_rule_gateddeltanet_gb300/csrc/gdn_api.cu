@@ -22,10 +22,15 @@ bool forced_chunked(const gdn_forward_args *a) {
     return a->plan == GDN_PLAN_CHUNKED || a->plan == GDN_PLAN_CHUNKED_SPLIT;
 }
 
+// Whether the split plan splits anything at these head sizes.
+bool splits(const gdn_forward_args *a) {
+    return a->plan == GDN_PLAN_CHUNKED_SPLIT && gdn::chunked_wy_splits(a->head_dim_k, a->head_dim_v);
+}
+
 // Workspace of the two-phase chunked evaluation for these arguments.
 size_t two_phase_bytes(const gdn_forward_args *a) {
-    return gdn::chunked_wy_workspace_bytes(a->num_seqs, a->total_tokens, a->num_k_heads, a->num_v_heads,
-                                           a->plan == GDN_PLAN_CHUNKED_SPLIT, a->io_dtype == GDN_F16 ? 2 : 4);
+    return gdn::chunked_wy_workspace_bytes(a->num_seqs, a->total_tokens, a->num_k_heads, a->num_v_heads, splits(a),
+                                           a->io_dtype == GDN_F16 ? 2 : 4);
 }
 
 // Host-side checks shared by gdn_forward and gdn_forward_workspace_size.
@@ -50,16 +55,16 @@ gdn_status check_sizes(const gdn_forward_args *a) {
         (a->v_stride != 0 && a->v_stride < v_min))
         return GDN_ERR_SHAPE;
     if (!(a->scale >= 0.f) || isinf(a->scale)) return GDN_ERR_SHAPE;
-    if (forced_chunked(a) && !gdn::chunked_supported(a->head_dim_k, a->head_dim_v)) return GDN_ERR_UNSUPPORTED;
+    if (forced_chunked(a) && !gdn::chunked_wy_supported(a->head_dim_k, a->head_dim_v)) return GDN_ERR_UNSUPPORTED;
     return GDN_OK;
 }
 
 // Whether these sizes may use the chunked kernel (and so need workspace).
 bool wants_chunked(const gdn_forward_args *a) {
     if (a->num_seqs == 0 || a->plan == GDN_PLAN_RECURRENT) return false;
-    if (!gdn::chunked_supported(a->head_dim_k, a->head_dim_v)) return false;
+    if (!gdn::chunked_wy_supported(a->head_dim_k, a->head_dim_v)) return false;
     const int longest = a->max_seqlen > 0 && a->max_seqlen < a->total_tokens ? a->max_seqlen : a->total_tokens;
-    return forced_chunked(a) || longest > gdn::RECURRENT_MAX_LEN;
+    return forced_chunked(a) || longest > gdn::recurrent_max_len(a->head_dim_k, a->head_dim_v);
 }
 
 // The chunked kernel moves q, k, v rows with bulk copies and writes output
@@ -133,7 +138,8 @@ gdn_status single_kernel_workspace_size(const gdn_forward_args *args, size_t *by
     if (!bytes) return GDN_ERR_NULL;
     const gdn_status st = check_sizes(args);
     if (st != GDN_OK) return st;
-    *bytes = wants_chunked(args) ? chunked_workspace_bytes(args->num_seqs) : 0;
+    const bool single = chunked_supported(args->head_dim_k, args->head_dim_v);
+    *bytes = wants_chunked(args) && single ? chunked_workspace_bytes(args->num_seqs) : 0;
     return GDN_OK;
 }
 }  // namespace gdn
@@ -150,22 +156,29 @@ gdn_status forward_impl(const gdn_forward_args *a, int dense_S, gdn_stream_t str
         if (forced_chunked(a)) return GDN_ERR_ALIGN;
         chunked = false;  // the automatic plan keeps every sequence on the recurrent kernel
     }
+    const bool d128 = gdn::chunked_supported(a->head_dim_k, a->head_dim_v);
+    if (chunked && !d128 && !forced_chunked(a) &&
+        (!a->workspace || (reinterpret_cast<uintptr_t>(a->workspace) & 15u) || a->workspace_bytes < two_phase_bytes(a)))
+        chunked = false;  // head sizes 32 / 64 have only the two-phase form: without its workspace
+                          // the automatic plan keeps every sequence on the recurrent kernels
     if (chunked) {
         // A workspace of gdn_forward_workspace_size bytes runs the two-phase
         // chunked evaluation; one that only holds the chain list runs the
-        // single-kernel one (same results up to rounding, slower).
+        // single-kernel one (same results up to rounding, slower; dk = dv = 128).
         // The split plan has no single-kernel form.
         if (!a->workspace || (reinterpret_cast<uintptr_t>(a->workspace) & 15u)) return GDN_ERR_WORKSPACE;
-        const bool split = a->plan == GDN_PLAN_CHUNKED_SPLIT;
+        const bool split = splits(a);
         const bool two_phase = a->workspace_bytes >= two_phase_bytes(a);
-        if (!two_phase && (split || a->workspace_bytes < gdn::chunked_workspace_bytes(a->num_seqs)))
+        if (!two_phase && (a->plan == GDN_PLAN_CHUNKED_SPLIT || !d128 ||
+                           a->workspace_bytes < gdn::chunked_workspace_bytes(a->num_seqs)))
             return GDN_ERR_WORKSPACE;
-        const int min_len = forced_chunked(a) ? -1 : gdn::RECURRENT_MAX_LEN;
+        const int auto_max = gdn::recurrent_max_len(a->head_dim_k, a->head_dim_v);
+        const int min_len = forced_chunked(a) ? -1 : auto_max;
         const cudaError_t e = two_phase ? gdn::launch_chunked_wy(p, min_len, split, a->workspace, s)
                                         : gdn::launch_chunked(p, min_len, a->workspace, s);
         if (e != cudaSuccess) return GDN_ERR_CUDA;
         if (forced_chunked(a)) return GDN_OK;
-        p.max_len = gdn::RECURRENT_MAX_LEN;
+        p.max_len = auto_max;
     }
     if (gdn::launch_recurrent(p, s) != cudaSuccess) return GDN_ERR_CUDA;
     return GDN_OK;

@@ -70,7 +70,12 @@ namespace {
 using namespace ct;
 
 constexpr int CH = 64;   // chunk length
-constexpr int DH = 128;  // dk = dv on this path
+// Operand tiles are sized for dk = dv = DH = 128.  Smaller head sizes (32, 64)
+// run on the same tiles zero-padded: features past dk and state rows past dv
+// are zero in every operand and in the tensor-memory state, so they add
+// nothing to any product, and only the first dk / dv entries are read from
+// or written to memory.
+constexpr int DH = 128;
 constexpr float EPS = 1e-6f;
 constexpr float LOG_DECAY_FLOOR = -200.f;  // exp(-200) is 0 in fp32; keeps Gamma well-conditioned
 constexpr long long WAIT_LIMIT = 4000000000LL;
@@ -435,7 +440,7 @@ constexpr int PREP_BYTES = P_TPD + VREC_F;  // the value-head phase's scratch (t
 constexpr int PREP_SMEM = PREP_BYTES + 1024;
 static_assert(P_M + 32 * MS * 4 <= P_TPD && KREC_BYTES <= PREP_BYTES, "prep shared-memory layout");
 
-template <typename TIO>
+template <typename TIO, bool PAD>
 __global__ void __launch_bounds__(PT, 4)
     wy_prep_kernel(const ForwardParams p, const int32_t *ws, uint8_t *krec, uint8_t *vrec,
                    const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k) {
@@ -447,6 +452,7 @@ __global__ void __launch_bounds__(PT, 4)
     __shared__ float Beta_s[GH][CH];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr bool STAGED = sizeof(TIO) == 2;
+    const int dk_ = PAD ? p.dk : DH;  // PAD: head size 32 or 64 on the zero-padded tiles
 
     const int g = blockIdx.x / p.Hk, kh = blockIdx.x % p.Hk;
     const int32_t *cbase = Header(const_cast<int32_t *>(ws), p.B).cbase;
@@ -470,11 +476,13 @@ __global__ void __launch_bounds__(PT, 4)
         ptx::mbar_init(&lbar, 1);
         ptx::fence_mbar_init();
         if (STAGED) {
-            ptx::mbar_arrive_expect_tx(&lbar, 2 * CH * DH * 2);
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
-                ptx::tma_load_2d(sm + kb * 16384, &map_q, kh * DH + kb * 64, t0, &lbar);
-                ptx::tma_load_2d(sm + kb * 16384 + CH * 128, &map_k, kh * DH + kb * 64, t0, &lbar);
+            // one 64-feature box per K-block that holds features of this head (the
+            // features past dk that a box brings are zeroed when normalising)
+            const int nkb = (dk_ + 63) / 64;
+            ptx::mbar_arrive_expect_tx(&lbar, (uint32_t)(nkb * 2 * CH * 64 * 2));
+            for (int kb = 0; kb < nkb; ++kb) {
+                ptx::tma_load_2d(sm + kb * 16384, &map_q, kh * dk_ + kb * 64, t0, &lbar);
+                ptx::tma_load_2d(sm + kb * 16384 + CH * 128, &map_k, kh * dk_ + kb * 64, t0, &lbar);
             }
         }
     }
@@ -516,11 +524,12 @@ __global__ void __launch_bounds__(PT, 4)
             for (int m = 0; m < 4; ++m) {
                 const uint4 raw = *reinterpret_cast<const uint4 *>(sm + sw(rrow, 32 * qp + 8 * m, 128));
                 const __half2 *hv = reinterpret_cast<const __half2 *>(&raw);
+                const bool in_head = 32 * qp + 8 * m < dk_;  // dk is a multiple of 32
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 f = __half22float2(hv[e]);
-                    x[8 * m + 2 * e] = f.x;
-                    x[8 * m + 2 * e + 1] = f.y;
+                    x[8 * m + 2 * e] = in_head ? f.x : 0.f;
+                    x[8 * m + 2 * e + 1] = in_head ? f.y : 0.f;
                 }
             }
 #pragma unroll
@@ -532,8 +541,8 @@ __global__ void __launch_bounds__(PT, 4)
             for (int e = 0; e < 32; ++e) x[e] = s < n ? x[e] * inv : 0.f;  // rows past the sequence become zero
 #pragma unroll
             for (int m = 0; m < 4; ++m) st_h8(sm, sw(rrow, 32 * qp + 8 * m, 128), x + 8 * m);
-            if (which == 1 && p.caps && s < n && tl < p.cap) {
-                float *dst = p.caps + ((long long)b * p.cap + tl) * p.W + p.Hv + (long long)kh * DH + 32 * qp;
+            if (which == 1 && p.caps && s < n && tl < p.cap && 32 * qp < dk_) {
+                float *dst = p.caps + ((long long)b * p.cap + tl) * p.W + p.Hv + (long long)kh * dk_ + 32 * qp;
 #pragma unroll
                 for (int e = 0; e < 32; ++e) dst[e] = x[e];  // rows need not be 16-byte aligned
             }
@@ -550,10 +559,10 @@ __global__ void __launch_bounds__(PT, 4)
                 const int s = warp + 8 * (u + 4 * round);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) qv[u][e] = kv[u][e] = 0.f;
-                if (s < n) {
+                if (s < n && lane * 4 < dk_) {
                     const long long t = (long long)t0 + s;
-                    ld4<TIO>(qg + t * p.q_stride + (long long)kh * DH + lane * 4, qv[u]);
-                    ld4<TIO>(kg + t * p.k_stride + (long long)kh * DH + lane * 4, kv[u]);
+                    ld4<TIO>(qg + t * p.q_stride + (long long)kh * dk_ + lane * 4, qv[u]);
+                    ld4<TIO>(kg + t * p.k_stride + (long long)kh * dk_ + lane * 4, kv[u]);
                 }
             }
 #pragma unroll
@@ -586,8 +595,8 @@ __global__ void __launch_bounds__(PT, 4)
                 st_h4(sm, sw(s, c, 128), qv[u][0], qv[u][1], qv[u][2], qv[u][3]);
                 st_h4(sm, sw(64 + s, c, 128), kv[u][0], kv[u][1], kv[u][2], kv[u][3]);
                 const int tl = t0 + s - bos;
-                if (p.caps && s < n && tl < p.cap) {
-                    float *dst = p.caps + ((long long)b * p.cap + tl) * p.W + p.Hv + (long long)kh * DH + c;
+                if (p.caps && s < n && tl < p.cap && c < dk_) {
+                    float *dst = p.caps + ((long long)b * p.cap + tl) * p.W + p.Hv + (long long)kh * dk_ + c;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) dst[e] = kv[u][e];  // rows need not be 16-byte aligned
                 }
@@ -604,7 +613,7 @@ __global__ void __launch_bounds__(PT, 4)
         ptx::tc_fence_after();
         const uint32_t a_qk = ptx::smem_u32(sm);
         const uint32_t i64 = ptx::idesc_f16_f32(128, 64);
-        for (int ks = 0; ks < DH / 16; ++ks) {
+        for (int ks = 0; ks < dk_ / 16; ++ks) {  // features past dk are zero
             const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
             ptx::mma_f16(tm, ptx::sdesc_k_sw128(a_qk + ko), ptx::sdesc_k_sw128(a_qk + 64 * 128 + ko), i64, ks > 0);
         }
@@ -746,7 +755,7 @@ static_assert(SCAN_SMEM + 1024 <= 227 * 1024, "shared memory budget (dynamic + s
 
 // SPLIT = false: every chain is a whole sequence (the work list holds no
 // other kind), and the split-plan code is compiled out.
-template <typename TIO, bool SPLIT>
+template <typename TIO, bool SPLIT, bool PAD>
 __global__ void __launch_bounds__(NT, 1)
     wy_scan_kernel(const ForwardParams p, int32_t *ws, const uint8_t *krec, const uint8_t *vrec, float *split_states,
                    TIO *oid, const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -814,7 +823,11 @@ __global__ void __launch_bounds__(NT, 1)
     const int n_items = hd.w[1] * p.Hv;
     const int32_t *cbase = hd.cbase;
     const TIO *vg = static_cast<const TIO *>(p.v);
-    const long long ubase = (long long)p.Hv + (long long)p.Hk * DH;
+    // PAD: head sizes 32 / 64 on the zero-padded tiles (otherwise 128, known at compile time)
+    const int dk_ = PAD ? p.dk : DH, dv_ = PAD ? p.dv : DH;
+    const long long ubase = (long long)p.Hv + (long long)p.Hk * dk_;
+    // this thread's state row and 32-column block hold data (the rest is zero padding)
+    const bool row_in = !PAD || row < dv_, cols_in = !PAD || c32 < dk_;
 
     while (!failed) {
         if (tid == 0) item_s = atomicAdd(&hd.w[0], 1);
@@ -835,7 +848,7 @@ __global__ void __launch_bounds__(NT, 1)
             if (tid == 0 && h == 0 && kind <= K_FIRST) flag_error(p.status, GDN_DEVERR_STATE_SLOT);
             continue;
         }
-        const size_t head_off = ((size_t)slot * p.Hv + h) * (size_t)DH * DH;
+        const size_t head_off = ((size_t)slot * p.Hv + h) * (size_t)dv_ * dk_;
         // where the outputs and the final state go: a split sequence's first segment
         // leaves its state S1 in the workspace, the second segment's zero run writes
         // the outputs (corrected later) and B, the identity run its outputs to the
@@ -859,7 +872,7 @@ __global__ void __launch_bounds__(NT, 1)
                 ptx::mbar_arrive_expect_tx(&lbar[st], (uint32_t)(KREC_BYTES + VREC_BYTES + (STAGED ? CH * DH * 2 : 0)));
                 ptx::bulk_g2s(stage + S_KREC, krec + ((gbase + c) * p.Hk + kh) * KREC_BYTES, KREC_BYTES, &lbar[st]);
                 ptx::bulk_g2s(stage + S_VREC, vrec + ((gbase + c) * p.Hv + h) * VREC_BYTES, VREC_BYTES, &lbar[st]);
-                if (STAGED) ptx::tma_load_2d(stage + S_V, &map_v, h * DH, bos + CH * c, &lbar[st]);
+                if (STAGED) ptx::tma_load_2d(stage + S_V, &map_v, h * dv_, bos + CH * c, &lbar[st]);
             }
             pending[st] = true;
         };
@@ -893,15 +906,16 @@ __global__ void __launch_bounds__(NT, 1)
             if (tile) {
                 __half *ot = reinterpret_cast<__half *>(sm + OFF_OT);
 #pragma unroll
-                for (int j = 0; j < CW; ++j) ot[(c16 + j) * DH + row] = __float2half_rn(p.scale * fmaf(gm[j], o1[j], y[j]));
+                for (int j = 0; j < CW; ++j)
+                    if (row_in) ot[(c16 + j) * dv_ + row] = __float2half_rn(p.scale * fmaf(gm[j], o1[j], y[j]));
                 ptx::fence_proxy_async_smem();  // visible to the tensor store after the next barrier
                 return;
             }
 #pragma unroll
             for (int j = 0; j < CW; ++j) {
                 const int s = c16 + j;
-                if (s < n)
-                    og[((long long)(tp + s) + orow) * p.Hv * DH + (long long)h * DH + row] =
+                if (s < n && row_in)
+                    og[((long long)(tp + s) + orow) * p.Hv * dv_ + (long long)h * dv_ + row] =
                         from_f32<TIO>(p.scale * fmaf(gm[j], o1[j], y[j]));
             }
         };
@@ -915,11 +929,12 @@ __global__ void __launch_bounds__(NT, 1)
             ptx::tmem_st<CS>(tm + lane_sel + TM_S + c32, v);
             ptx::tmem_st_wait();
         } else if (state_live) {
-            const float *src = p.init + head_off + (size_t)row * DH + c32;
+            const float *src = p.init + head_off + (size_t)row * dk_ + c32;
             float v[CS];
 #pragma unroll
             for (int j = 0; j < CS; j += 4) {
-                const float4 x = *reinterpret_cast<const float4 *>(src + j);
+                const float4 x = row_in && cols_in ? *reinterpret_cast<const float4 *>(src + j)
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
                 v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
             }
             ptx::tmem_st<CS>(tm + lane_sel + TM_S + c32, v);
@@ -944,7 +959,7 @@ __global__ void __launch_bounds__(NT, 1)
             if (tid == 0) {
                 ptx::tc_fence_after();
                 const uint64_t bd = ptx::sdesc_k_sw128(a_st + S_KREC);
-                for (int ks = 0; ks < DH / 16; ++ks) {
+                for (int ks = 0; ks < dk_ / 16; ++ks) {  // state columns past dk are zero
                     const uint32_t ko = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
                     ptx::mma_f16(tm + ox, d_S16 + ko, bd + ko, I128, ks > 0);
                 }
@@ -954,7 +969,7 @@ __global__ void __launch_bounds__(NT, 1)
             if (c > c_lo) write_outputs(t0 - CH, CH, TM_OX + 128u * (uint32_t)(st ^ 1), out_tile);
             if (!mma_wait()) { failed = true; break; }
             if (c > c_lo && out_tile && tid == 0) {  // chunk c - 1's outputs, one tensor store
-                ptx::tma_store_2d(mo, sm + OFF_OT, h * DH, (int)(t0 - CH + orow));
+                ptx::tma_store_2d(mo, sm + OFF_OT, h * dv_, (int)(t0 - CH + orow));
                 ptx::bulk_commit();
             }
             // ---- R^T = diag(beta) V - diag(beta gamma) X^T, transposed; this chunk's gamma for its outputs
@@ -975,10 +990,12 @@ __global__ void __launch_bounds__(NT, 1)
                     for (int e = 0; e < 8; ++e) {
                         const int s = c16 + j + e;
                         float vv;
-                        if (STAGED)
+                        if (!row_in)
+                            vv = 0.f;  // the tile's rows past dv hold the next head's features
+                        else if (STAGED)
                             vv = to_f32(reinterpret_cast<const TIO *>(stage + S_V)[s * DH + row]);
                         else
-                            vv = s < n ? to_f32(vg[(long long)(t0 + s) * p.v_stride + (long long)h * DH + row]) : 0.f;
+                            vv = s < n ? to_f32(vg[(long long)(t0 + s) * p.v_stride + (long long)h * dv_ + row]) : 0.f;
                         w[e] = fmaf(be[j + e], vv, -bg[j + e] * x[j + e]);
                     }
                     st_h8(sm + OFF_RT, sw(row, c16 + j, 128), w);
@@ -1025,8 +1042,8 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int j = 0; j < CW; ++j) {
                     const int s = c16 + j, tl = t0 + s - bos;
-                    if (s < n && tl < p.cap)
-                        p.caps[((long long)b * p.cap + tl) * p.W + ubase + (long long)h * DH + row] = u[j];
+                    if (s < n && tl < p.cap && row_in)
+                        p.caps[((long long)b * p.cap + tl) * p.W + ubase + (long long)h * dv_ + row] = u[j];
                 }
             }
             if (!mma_wait()) { failed = true; break; }
@@ -1048,7 +1065,7 @@ __global__ void __launch_bounds__(NT, 1)
         // ---- chain end: the final state (unless the caller asked for none)
         if (fdst) {
             ptx::tc_fence_after();
-            float *dst = fdst + (size_t)row * DH + c32;
+            float *dst = fdst + (size_t)row * (kind == K_WHOLE ? dk_ : DH) + c32;
             float v[CS];
             if (state_live) {
                 ptx::tmem_ld<CS>(tm + lane_sel + TM_S + c32, v);
@@ -1056,9 +1073,11 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int j = 0; j < CS; ++j) v[j] = 0.f;
             }
+            if (row_in && cols_in) {
 #pragma unroll
-            for (int j = 0; j < CS; j += 4)
-                *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                for (int j = 0; j < CS; j += 4)
+                    *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
         }
         ptx::tc_fence_before();
         __syncthreads();
@@ -1404,9 +1423,9 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *
     if (sizeof(TIO) == 2) {
         // q, k: 64-token x 64-feature boxes in the 128-byte swizzle of the MMA operand tiles;
         // v: 64-token x 128-feature rows as they are
-        if (!encode_rows_f16(&mq, p.q, (long long)p.Hk * DH, p.q_stride, p.T, 64, CH, true) ||
-            !encode_rows_f16(&mk, p.k, (long long)p.Hk * DH, p.k_stride, p.T, 64, CH, true) ||
-            !encode_rows_f16(&mv, p.v, (long long)p.Hv * DH, p.v_stride, p.T, DH, CH, false))
+        if (!encode_rows_f16(&mq, p.q, (long long)p.Hk * p.dk, p.q_stride, p.T, 64, CH, true) ||
+            !encode_rows_f16(&mk, p.k, (long long)p.Hk * p.dk, p.k_stride, p.T, 64, CH, true) ||
+            !encode_rows_f16(&mv, p.v, (long long)p.Hv * p.dv, p.v_stride, p.T, DH, CH, false))
             return cudaErrorInvalidValue;
     }
     int32_t *hdr = reinterpret_cast<int32_t *>(ws);
@@ -1414,7 +1433,8 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *
     uint8_t *krec = ws + header_bytes(p.B);
     uint8_t *vrec = krec + (size_t)maxch * p.Hk * KREC_BYTES;
     float *split_states = reinterpret_cast<float *>(vrec + (size_t)maxch * p.Hv * VREC_BYTES);
-    const long long nsplit = split ? max_split(p.B, p.T) : 0;
+    // the split plan's identity run needs dk = dv; it is built for 128
+    const long long nsplit = split && p.dk == DH && p.dv == DH ? max_split(p.B, p.T) : 0;
     TIO *oid = reinterpret_cast<TIO *>(reinterpret_cast<uint8_t *>(split_states) +
                                        (size_t)nsplit * 3 * p.Hv * STATE_BYTES);
     const long long oid_rows = max_split_rows(p.T);
@@ -1423,13 +1443,15 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *
     if (e != cudaSuccess) return e;
     const long long prep_ctas = maxch * p.Hk;
     if (prep_ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    auto prep = wy_prep_kernel<TIO>;
+    const bool pad = p.dk != DH || p.dv != DH;
+    auto prep = pad ? wy_prep_kernel<TIO, true> : wy_prep_kernel<TIO, false>;
     e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
     if (e != cudaSuccess) return e;
     if (prep_ctas > 0) prep<<<(unsigned)prep_ctas, PT, PREP_SMEM, stream>>>(p, hdr, krec, vrec, mq, mk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto scan = nsplit > 0 ? wy_scan_kernel<TIO, true> : wy_scan_kernel<TIO, false>;
+    auto scan = pad ? wy_scan_kernel<TIO, false, true>
+                    : (nsplit > 0 ? wy_scan_kernel<TIO, true, false> : wy_scan_kernel<TIO, false, false>);
     e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, SCAN_SMEM);
     if (e != cudaSuccess) return e;
     const long long chains = (long long)p.B * p.Hv * (nsplit > 0 ? 3 : 1);
@@ -1439,7 +1461,7 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *
     CUtensorMap mo{}, moi{};
     const int out_tma =
         sizeof(TIO) == 2 &&
-        encode_rows_f16(&mo, p.out, (long long)p.Hv * DH, (long long)p.Hv * DH, p.T, DH, CH, false) &&
+        encode_rows_f16(&mo, p.out, (long long)p.Hv * p.dv, (long long)p.Hv * p.dv, p.T, p.dv, CH, false) &&
         (nsplit == 0 || encode_rows_f16(&moi, oid, (long long)p.Hv * DH, (long long)p.Hv * DH, (int)oid_rows, DH,
                                         CH, false));
     scan<<<grid, NT, SCAN_SMEM, stream>>>(p, hdr, krec, vrec, split_states, oid, mv, mo, moi, out_tma);
@@ -1464,6 +1486,12 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *
 }
 
 }  // namespace
+
+bool chunked_wy_supported(int dk, int dv) {
+    auto ok = [](int d) { return d == 32 || d == 64 || d == DH; };
+    return ok(dk) && ok(dv);
+}
+bool chunked_wy_splits(int dk, int dv) { return dk == DH && dv == DH; }
 
 size_t chunked_wy_workspace_bytes(int B, int T, int Hk, int Hv, bool split, int io_bytes) {
     const long long maxch = max_chunks(B, T);

@@ -98,7 +98,8 @@ cudaError_t launch_replay(const ReplayParams &p, cudaStream_t stream);
 
 // Chunked tensor-core path: sequences with more than `min_len` tokens
 // (min_len < 0: every sequence).  Needs chunked_workspace_bytes(B) of
-// device workspace (the chain list and its work counter).
+// device workspace (the chain list and its work counter).  Single-kernel
+// form: dk = dv = 128 only.
 bool chunked_supported(int dk, int dv);
 size_t chunked_workspace_bytes(int B);
 cudaError_t launch_chunked(const ForwardParams &p, int min_len, void *workspace, cudaStream_t stream);
@@ -109,7 +110,11 @@ cudaError_t launch_chunked(const ForwardParams &p, int min_len, void *workspace,
 // Hk = 16, Hv = 48, d = 128).  With `split`, every sequence of more than
 // 31 * 64 tokens is evaluated as two segments at once (see
 // gdn_chunked_wy.cu), which needs room for three states per split sequence
-// and head and for the identity-run outputs (io_bytes per element).
+// and head and for the identity-run outputs (io_bytes per element); only
+// dk = dv = 128 is split (other sizes run unsplit under that plan).  Head
+// sizes 32, 64 and 128 in any combination (zero-padded operand tiles).
+bool chunked_wy_supported(int dk, int dv);
+bool chunked_wy_splits(int dk, int dv);
 size_t chunked_wy_workspace_bytes(int B, int T, int Hk, int Hv, bool split, int io_bytes);
 // Workspace of the single-kernel chunked evaluation for these arguments (0 if
 // no chunked kernel can run); argument errors as gdn_forward_workspace_size.
@@ -132,8 +137,14 @@ bool encode_rows_f32(CUtensorMap *map, const float *base, long long row_elems, l
                      bool swizzle128);
 
 // Sequences up to this many tokens stay on the recurrent kernel under the
-// automatic plan; longer ones go to the chunked kernel.
+// automatic plan; longer ones go to the chunked kernel.  Head sizes below
+// 128 run the chunked kernels on d = 128 tiles zero-padded, while the
+// recurrent kernels' cost falls with dk dv, so they keep sequences longer.
 constexpr int RECURRENT_MAX_LEN = 32;
+constexpr int RECURRENT_MAX_LEN_SMALL_HEADS = 256;
+inline int recurrent_max_len(int dk, int dv) {
+    return dk == 128 && dv == 128 ? RECURRENT_MAX_LEN : RECURRENT_MAX_LEN_SMALL_HEADS;
+}
 
 // ---------------------------------------------------------------- device helpers
 

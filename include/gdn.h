@@ -58,19 +58,24 @@ enum {
 
 /* Which kernel evaluates a sequence. */
 enum {
-    GDN_PLAN_AUTO = 0,       /* per sequence: up to 32 tokens recurrent, longer ones chunked
-                                (chunked needs dk = dv = 128 and 16-byte aligned q, k, v) */
+    GDN_PLAN_AUTO = 0,       /* per sequence: up to 32 tokens recurrent (256 when dk or dv
+                                is below 128), longer ones chunked (the chunked kernels
+                                need 16-byte aligned q, k, v and the workspace; head
+                                sizes below 128 run them on zero-padded d = 128 tiles) */
     GDN_PLAN_RECURRENT = 1,  /* every sequence on the recurrent kernels: the state carried
                                 token by token (batches of one-token spans), or four
                                 tokens at a time in closed form on the warp tensor cores
                                 (batches with longer spans; one-token spans in them still
                                 take the token-by-token code, with the same bits) */
-    GDN_PLAN_CHUNKED = 2,    /* every sequence on the tensor-core chunked kernel
-                                (dk = dv = 128 only, else GDN_ERR_UNSUPPORTED) */
-    GDN_PLAN_CHUNKED_SPLIT = 3 /* GDN_PLAN_CHUNKED, and every sequence of more than
-                                1984 tokens (31 chunks) whose captured tokens lie in
-                                its first half is evaluated as two halves at once: for batches of a few long sequences, whose
+    GDN_PLAN_CHUNKED = 2,    /* every sequence on the tensor-core chunked kernels (head
+                                sizes 32, 64, 128 in any combination; below 128 the
+                                d = 128 operand tiles are zero-padded) */
+    GDN_PLAN_CHUNKED_SPLIT = 3 /* GDN_PLAN_CHUNKED, and at dk = dv = 128 every sequence
+                                of more than 1984 tokens (31 chunks) whose captured
+                                tokens lie in its first half is evaluated as two halves
+                                at once: for batches of a few long sequences, whose
                                 (sequence, head) chains would leave most SMs idle.
+                                Other head sizes run unsplit.
                                 See "Sequence-parallel evaluation" below. */
 };
 
@@ -210,11 +215,16 @@ typedef struct gdn_forward_args {
  * sequence that can be split (at most min(B, T / 1985)) and T/2 + 64 rows of
  * Hv * dv io_dtype elements for the second halves' identity-run outputs.
  *
- * gdn_forward also accepts a smaller workspace of at least (B + 2) int32
- * (rounded up to 256 bytes): it then runs the single-kernel chunked
- * evaluation, which keeps only the sequence list and work counter there.
- * Both give the same results up to floating-point rounding; the two-phase one
- * is faster.  The workspace must be 16-byte aligned and not shared by calls
+ * The records hold d = 128 operand tiles at every head size (smaller heads
+ * are zero-padded), so the size does not depend on dk and dv.
+ *
+ * At dk = dv = 128, gdn_forward also accepts a smaller workspace of at least
+ * (B + 2) int32 (rounded up to 256 bytes): it then runs the single-kernel
+ * chunked evaluation, which keeps only the sequence list and work counter
+ * there.  Both give the same results up to floating-point rounding; the
+ * two-phase one is faster.  Other head sizes have only the two-phase form:
+ * with a smaller workspace the automatic plan runs every sequence on the
+ * recurrent kernels and a forced chunked plan returns GDN_ERR_WORKSPACE.  The workspace must be 16-byte aligned and not shared by calls
  * that overlap on the GPU.  Returns GDN_OK and writes *bytes, or an argument
  * error.
  */
@@ -309,6 +319,9 @@ gdn_status gdn_replay_prefix(float *state_banks, int32_t num_slots, int32_t num_
  *  - plan = GDN_PLAN_CHUNKED_SPLIT is rejected with GDN_ERR_UNSUPPORTED: the
  *    split plan's workspace grows with the batch and it has no single-kernel
  *    form.
+ *  - Head sizes below 128 have no single-kernel chunked form: the automatic
+ *    plan then keeps every sequence on the recurrent kernels, and
+ *    GDN_PLAN_CHUNKED returns GDN_ERR_WORKSPACE.
  *  - The first call on each device looks up the array's device address with
  *    that device current; make that first call before any stream capture.
  *    The address is kept for the life of the process, so the library must not

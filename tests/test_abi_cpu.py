@@ -153,11 +153,14 @@ def test_workspace_size_follows_the_plan(lib):
     # a max_seqlen hint of at most 32 keeps the batch recurrent
     a = _args(num_seqs=64, total_tokens=64, num_state_slots=64, max_seqlen=1)
     assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 0
-    # forced recurrent plan: none; other head dims: none (recurrent only)
+    # forced recurrent plan: none
     a = _args(num_seqs=8, total_tokens=17000, num_state_slots=8, plan=1)
     assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 0
-    a = _args(num_seqs=8, total_tokens=17000, num_state_slots=8, head_dim_k=64)
-    assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 0
+    # head sizes 32 / 64 run the same two-phase evaluation on zero-padded tiles: the same records
+    for dk, dv in ((64, 128), (32, 32), (128, 64)):
+        a = _args(num_seqs=8, total_tokens=17000, num_state_slots=8, head_dim_k=dk, head_dim_v=dv)
+        assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0
+        assert n.value == two_phase(8, 17000, a.num_k_heads, a.num_v_heads)
 
 
 def test_split_plan_workspace_and_restrictions(lib):
@@ -173,7 +176,10 @@ def test_split_plan_workspace_and_restrictions(lib):
     a = _args(num_seqs=2, total_tokens=1984, num_state_slots=2, plan=3)
     assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0
     assert n.value == 1024 + (1984 // 64 + 2) * (16 * 32768 + 48 * 17408)
-    assert lib.gdn_forward(ctypes.byref(_args(plan=3, head_dim_k=64)), None) == 7
+    assert lib.gdn_forward(ctypes.byref(_args(plan=3, head_dim_k=64)), None) == 5  # runs unsplit: needs workspace
+    # below 128 nothing is split: the plain two-phase size
+    a = _args(num_seqs=8, total_tokens=17000, num_state_slots=8, plan=3, head_dim_k=64, head_dim_v=64)
+    assert lib.gdn_forward_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == base
     # capsules are allowed (captured tokens come from first halves); this call has no workspace
     assert lib.gdn_forward(ctypes.byref(_args(plan=3, state_update_capacity=4, state_update=ctypes.c_void_p(0x1000))),
                            None) == 5
@@ -185,9 +191,10 @@ def test_split_plan_workspace_and_restrictions(lib):
                                                        num_state_slots=1)), None) == 7
 
 
-def test_forced_chunked_plan_needs_d128_and_workspace(lib):
-    assert lib.gdn_forward(ctypes.byref(_args(plan=2, head_dim_k=64)), None) == 7
-    assert lib.gdn_forward(ctypes.byref(_args(plan=2, head_dim_v=32)), None) == 7
+def test_forced_chunked_plan_needs_workspace(lib):
+    # every head size has the two-phase form; without its workspace a forced plan is refused
+    assert lib.gdn_forward(ctypes.byref(_args(plan=2, head_dim_k=64)), None) == 5
+    assert lib.gdn_forward(ctypes.byref(_args(plan=2, head_dim_v=32)), None) == 5
     assert lib.gdn_forward(ctypes.byref(_args(max_seqlen=-1)), None) == 3
     # forced chunked plan without workspace
     assert lib.gdn_forward(ctypes.byref(_args(plan=2)), None) == 5

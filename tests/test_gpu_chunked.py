@@ -238,3 +238,59 @@ def test_pages_ragged_batch_is_bitwise_the_prompts_alone():
         assert np.array_equal(out[t0:t1], o1)
         assert np.array_equal(final[s], f1[0])
     _check(inp, (out, final, None), run_oracle(inp))
+
+
+# Head sizes 32 and 64 (and mixed dk != dv) run the two-phase evaluation on the
+# d = 128 operand tiles zero-padded: features past dk and state rows past dv
+# are zero in every operand, so the same tensor-core products give the
+# smaller heads' results; only the first dk / dv entries are read or written.
+SMALL = [(64, 64), (32, 32), (64, 128), (128, 64), (32, 128), (128, 32)]
+
+
+@pytest.mark.parametrize("dk,dv", SMALL)
+@pytest.mark.parametrize("io", [np.float16, np.float32])
+def test_forced_chunked_small_head_sizes(io, dk, dv):
+    inp = wl.make_inputs(220 + dk + dv, LENGTHS, Hk=2, Hv=6, dk=dk, dv=dv, io_dtype=io, state_std=0.02,
+                         capacity=70)
+    _check(inp, run_gpu(inp, plan="chunked", in_place=False), run_oracle(inp))
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (32, 32)])
+def test_auto_plan_small_heads_takes_the_chunked_path(dk, dv):
+    """Long sequences at d = 32 / 64 under the automatic plan (the binding
+    passes the workspace gdn_forward_workspace_size asks for): short ones stay
+    on the recurrent kernels, long ones go to the chunked kernels; one key
+    head with a single value head (Hk = Hv = 1) puts the last head's boxes
+    past the end of the q / k / v rows."""
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    for Hk, Hv, seed in ((2, 4, 230), (1, 1, 231)):
+        lengths = [300, 17, 1000, 64, 2]
+        inp = wl.make_inputs(seed + dk, lengths, Hk=Hk, Hv=Hv, dk=dk, dv=dv, io_dtype=np.float16, state_std=0.02,
+                             capacity=20)
+        a = gdn.build_forward_args(to_dev(inp.q), to_dev(inp.k), to_dev(inp.v), to_dev(inp.a), to_dev(inp.b),
+                                   to_dev(inp.cu_seqlens), A_log=to_dev(inp.A_log), dt_bias=to_dev(inp.dt_bias))[0]
+        assert gdn.workspace_size(a) > 0  # the chunked kernels may run
+        _check(inp, run_gpu(inp, in_place=True), run_oracle(inp))
+        # pack = one by one, bitwise (each sequence's plan depends on its own length)
+        out, final, caps = run_gpu(inp, in_place=False)
+        cu = inp.cu_seqlens
+        for s, L in enumerate(lengths):
+            t0, t1 = cu[s], cu[s + 1]
+            one = wl.GdnInputs(inp.q[t0:t1], inp.k[t0:t1], inp.v[t0:t1], inp.a[t0:t1], inp.b[t0:t1], inp.A_log,
+                               inp.dt_bias, np.array([0, L], np.int32), inp.initial_state[s:s + 1], None, 20)
+            o1, f1, c1 = run_gpu(one, in_place=False)
+            assert np.array_equal(out[t0:t1], o1)
+            assert np.array_equal(final[s], f1[0])
+            assert np.array_equal(caps[s], c1[0])
+
+
+def test_split_plan_small_heads_runs_unsplit():
+    """Below d = 128 the split plan splits nothing (its identity run is built
+    for 128): the results are the chunked plan's, bitwise."""
+    inp = wl.make_inputs(240, [2500, 90], Hk=2, Hv=4, dk=64, dv=64, io_dtype=np.float16, state_std=0.05,
+                         capacity=8)
+    a = run_gpu(inp, plan="chunked_split", in_place=False)
+    b = run_gpu(inp, plan="chunked", in_place=False)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    _check(inp, a, run_oracle(inp))
