@@ -171,6 +171,7 @@ template <typename TIO>
 __global__ void __launch_bounds__(NT, 1)
     chunked_kernel(const ForwardParams p, int32_t *ws, const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v) {
+    dependent_prologue();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ Shared sh;
@@ -665,6 +666,7 @@ __global__ void __launch_bounds__(NT, 1)
 constexpr int PLAN_BINS = 1024;
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *cu, int dense_S, int B, int T, int min_len,
                                                     int32_t *ws) {
+    dependent_prologue();
     __shared__ int hist[PLAN_BINS];
     __shared__ int total;
     const int tid = threadIdx.x;
@@ -712,8 +714,7 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStre
             !encode_rows_f16(&mv, p.v, (long long)p.Hv * DH, p.v_stride, p.T, DH, CH, false))
             return cudaErrorInvalidValue;
     }
-    plan_kernel<<<1, 1024, 0, stream>>>(p.cu, p.dense_S, p.B, p.T, min_len, ws);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(plan_kernel, dim3(1), dim3(1024), 0, stream, p.cu, p.dense_S, p.B, p.T, min_len, ws);
     if (e != cudaSuccess) return e;
     auto kern = chunked_kernel<TIO>;
     constexpr int smem = SMEM_ALLOC;
@@ -721,8 +722,7 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStre
     if (e != cudaSuccess) return e;
     const long long chains = (long long)p.B * p.Hv;
     const int grid = (int)(chains < num_sms() ? chains : num_sms());
-    kern<<<grid, NT, smem, stream>>>(p, ws, mq, mk, mv);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(grid), dim3(NT), smem, stream, p, ws, mq, mk, mv);
 }
 
 }  // namespace

@@ -180,6 +180,7 @@ __device__ long long scan_sequences(int B, V value, P put, long long *wsum) {
 // segment, which runs from the true state and so yields the exact deltas.
 __global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int dense_S, int B, int T, int min_len,
                                                           bool split, int cap, int32_t *ws) {
+    dependent_prologue();
     __shared__ int hist[PLAN_BINS];
     __shared__ long long wsum[PLAN_NT / 32];
     __shared__ int total;
@@ -444,6 +445,7 @@ template <typename TIO, bool PAD>
 __global__ void __launch_bounds__(PT, 4)
     wy_prep_kernel(const ForwardParams p, const int32_t *ws, uint8_t *krec, uint8_t *vrec,
                    const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k) {
+    dependent_prologue();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bar, lbar;
@@ -760,6 +762,7 @@ __global__ void __launch_bounds__(NT, 1)
     wy_scan_kernel(const ForwardParams p, int32_t *ws, const uint8_t *krec, const uint8_t *vrec, float *split_states,
                    TIO *oid, const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
                    const __grid_constant__ CUtensorMap map_oi, int out_tma) {
+    dependent_prologue();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bar;      // MMA completion
@@ -1157,6 +1160,7 @@ __global__ void __launch_bounds__(OC_NT, 1)
     wy_out_correction_kernel(const ForwardParams p, int32_t *ws, const float *split_states, const TIO *oid,
                              const __grid_constant__ CUtensorMap map_oa, const __grid_constant__ CUtensorMap map_out,
                              int tma) {
+    dependent_prologue();
     constexpr bool F16 = sizeof(TIO) == 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1359,6 +1363,7 @@ constexpr int FS_SMEM = (DH * FS_LD + DH * DH) * 4;
 
 __global__ void __launch_bounds__(FS_NT, 1)
     wy_split_final_kernel(const ForwardParams p, const int32_t *ws, const float *split_states) {
+    dependent_prologue();
     extern __shared__ float fs_smem[];
     float *s1 = fs_smem;           // [dv][FS_LD]
     float *am = fs_smem + DH * FS_LD;  // [dk][dk]
@@ -1438,8 +1443,8 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *
     TIO *oid = reinterpret_cast<TIO *>(reinterpret_cast<uint8_t *>(split_states) +
                                        (size_t)nsplit * 3 * p.Hv * STATE_BYTES);
     const long long oid_rows = max_split_rows(p.T);
-    wy_plan_kernel<<<1, PLAN_NT, 0, stream>>>(p.cu, p.dense_S, p.B, p.T, min_len, nsplit > 0, p.cap, hdr);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(wy_plan_kernel, dim3(1), dim3(PLAN_NT), 0, stream, p.cu, p.dense_S, p.B, p.T,
+                                     min_len, nsplit > 0, p.cap, hdr);
     if (e != cudaSuccess) return e;
     const long long prep_ctas = maxch * p.Hk;
     if (prep_ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -1447,8 +1452,7 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *
     auto prep = pad ? wy_prep_kernel<TIO, true> : wy_prep_kernel<TIO, false>;
     e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
     if (e != cudaSuccess) return e;
-    if (prep_ctas > 0) prep<<<(unsigned)prep_ctas, PT, PREP_SMEM, stream>>>(p, hdr, krec, vrec, mq, mk);
-    e = cudaGetLastError();
+    if (prep_ctas > 0) e = launch_dependent(prep, dim3((unsigned)prep_ctas), dim3(PT), PREP_SMEM, stream, p, hdr, krec, vrec, mq, mk);
     if (e != cudaSuccess) return e;
     auto scan = pad ? wy_scan_kernel<TIO, false, true>
                     : (nsplit > 0 ? wy_scan_kernel<TIO, true, false> : wy_scan_kernel<TIO, false, false>);
@@ -1464,8 +1468,8 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *
         encode_rows_f16(&mo, p.out, (long long)p.Hv * p.dv, (long long)p.Hv * p.dv, p.T, p.dv, CH, false) &&
         (nsplit == 0 || encode_rows_f16(&moi, oid, (long long)p.Hv * DH, (long long)p.Hv * DH, (int)oid_rows, DH,
                                         CH, false));
-    scan<<<grid, NT, SCAN_SMEM, stream>>>(p, hdr, krec, vrec, split_states, oid, mv, mo, moi, out_tma);
-    e = cudaGetLastError();
+    e = launch_dependent(scan, dim3(grid), dim3(NT), SCAN_SMEM, stream, p, hdr, krec, vrec, split_states, oid, mv, mo,
+                         moi, out_tma);
     if (e != cudaSuccess || nsplit == 0) return e;
     // split sequences: outputs of the second segments, then their final states
     CUtensorMap moa{}, mout{};
@@ -1476,13 +1480,13 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *
     auto corr = wy_out_correction_kernel<TIO>;
     e = cudaFuncSetAttribute(corr, cudaFuncAttributeMaxDynamicSharedMemorySize, OC_SMEM);
     if (e != cudaSuccess) return e;
-    corr<<<2 * num_sms(), OC_NT, OC_SMEM, stream>>>(p, hdr, split_states, oid, moa, mout, oc_tma);
-    e = cudaGetLastError();
+    e = launch_dependent(corr, dim3(2 * num_sms()), dim3(OC_NT), OC_SMEM, stream, p, hdr, split_states, oid, moa, mout,
+                         oc_tma);
     if (e != cudaSuccess || !p.final_state) return e;
     e = cudaFuncSetAttribute(wy_split_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FS_SMEM);
     if (e != cudaSuccess) return e;
-    wy_split_final_kernel<<<(unsigned)(nsplit * p.Hv), FS_NT, FS_SMEM, stream>>>(p, hdr, split_states);
-    return cudaGetLastError();
+    return launch_dependent(wy_split_final_kernel, dim3((unsigned)(nsplit * p.Hv)), dim3(FS_NT), FS_SMEM, stream, p,
+                            hdr, split_states);
 }
 
 }  // namespace

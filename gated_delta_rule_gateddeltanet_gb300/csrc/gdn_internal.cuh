@@ -158,6 +158,40 @@ __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
 
+// ---------------------------------------------------------------- dependent launches
+//
+// The kernels of the library (all but the causal convolution's, whose
+// one-wave decode step measured slower so) are launched as programmatic
+// dependents of the kernel before them on the stream (launch_dependent): a
+// kernel's CTAs may become
+// resident while that kernel's last CTAs finish, which hides the launch gap
+// between consecutive kernels (back-to-back decode steps, the chunked path's
+// plan -> prep -> scan, the speculative step's verify -> replay).  Every kernel
+// starts with dependent_prologue(): it waits until the previous kernel has
+// completed and its memory is visible (the ordering a plain launch gives), and
+// then lets the next kernel's CTAs be scheduled.  For a kernel launched
+// without the attribute the wait returns at once.
+__device__ __forceinline__ void dependent_prologue() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 __device__ __forceinline__ void flag_error(int32_t *status, int bit) {
     if (status) atomicOr(status, bit);
 }

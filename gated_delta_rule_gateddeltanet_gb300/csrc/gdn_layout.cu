@@ -23,6 +23,7 @@ constexpr int TILE = 32, ROWS_PER_PASS = 8;
 __global__ void __launch_bounds__(TILE * ROWS_PER_PASS) transpose_kernel(const float *__restrict__ src,
                                                                          float *__restrict__ dst, int rows, int cols,
                                                                          int tiles_c) {
+    dependent_prologue();
     __shared__ float tile[TILE][TILE + 1];
     const long long m = blockIdx.y;  // matrix index
     const int tr = blockIdx.x / tiles_c, tc = blockIdx.x % tiles_c;
@@ -53,9 +54,8 @@ cudaError_t launch_transpose(const float *src, float *dst, long long num, int ro
     for (long long m0 = 0; m0 < num; m0 += 65535) {
         const long long n = num - m0 < 65535 ? num - m0 : 65535;
         dim3 grid((unsigned)(tiles_r * tiles_c), (unsigned)n);
-        transpose_kernel<<<grid, dim3(TILE, ROWS_PER_PASS), 0, stream>>>(src + m0 * rows * cols,
-                                                                         dst + m0 * rows * cols, rows, cols, tiles_c);
-        const cudaError_t e = cudaGetLastError();
+        const cudaError_t e = launch_dependent(transpose_kernel, grid, dim3(TILE, ROWS_PER_PASS), 0, stream,
+                                               src + m0 * rows * cols, dst + m0 * rows * cols, rows, cols, tiles_c);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -375,6 +375,7 @@ __device__ __forceinline__ void span_cuda_cores(const ForwardParams &p, const Sp
 
 template <typename TIO, int DK>
 __global__ void __launch_bounds__(NT, 5) recurrent_kernel(const ForwardParams p) {
+    dependent_prologue();
     Span sp;
     const int nrb = (p.dv + ROWS - 1) / ROWS;
     if (!resolve_span(p, blockIdx.y, blockIdx.x / nrb, blockIdx.x % nrb, sp)) return;
@@ -771,6 +772,7 @@ template <typename TIO, int DK>
 __global__ void __launch_bounds__(NTM, 4)
     recurrent_mixed_kernel(const ForwardParams p, int items, const __grid_constant__ CUtensorMap rows_map,
                            const __grid_constant__ OutMaps out_maps) {
+    dependent_prologue();
     extern __shared__ __align__(128) float dyn_s[];  // the CUDA-core path's tile, or (1024-aligned) the swizzled rows
     float *rows_s = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(dyn_s) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t rows_bar;
@@ -832,8 +834,7 @@ cudaError_t launch_dk(const ForwardParams &p, cudaStream_t stream) {
         auto kern = recurrent_kernel<TIO, DK>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        kern<<<dim3((unsigned)(nrb * p.Hv), (unsigned)p.B), NT, smem, stream>>>(p);
-        return cudaGetLastError();
+        return launch_dependent(kern, dim3((unsigned)(nrb * p.Hv), (unsigned)p.B), dim3(NT), smem, stream, p);
     }
     // some span has several tokens: the persistent mixed kernel, as many CTAs as fit at once
     const int smem = ROWS * DK * 4 + 1024;
@@ -870,8 +871,7 @@ cudaError_t launch_dk(const ForwardParams &p, cudaStream_t stream) {
     const long long items = (long long)p.B * p.Hv * nrb;
     if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
     const int grid = (int)std::min<long long>(items, (long long)std::max(per_sm, 1) * sms);
-    kern<<<grid, NTM, smem, stream>>>(p, (int)items, rows_map, out_maps);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(grid), dim3(NTM), smem, stream, p, (int)items, rows_map, out_maps);
 }
 
 template <typename TIO>

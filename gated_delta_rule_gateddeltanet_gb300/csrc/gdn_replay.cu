@@ -38,6 +38,7 @@ constexpr long long WAIT_LIMIT = 4000000000LL;
 
 template <int DK>
 __global__ void __launch_bounds__(NT, MIN_CTAS) replay_kernel(const ReplayParams p, int bulk_caps) {
+    dependent_prologue();
     constexpr int LPR4 = DK / 4;                   // lanes covering one row, a float4 each
     constexpr int RPI = 32 / LPR4;                 // rows per warp instruction
     constexpr int RPT = ROWS / ((NT / 32) * RPI);  // rows per thread
@@ -176,8 +177,7 @@ cudaError_t launch_dk(const ReplayParams &p, cudaStream_t stream) {
     // the offsets of kn, u and the decay groups are multiples of four floats:
     // W = Hv + Hk dk + Hv dv is, whenever Hv is (dk, dv are multiples of 32).
     const int bulk_caps = (p.Hv % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.caps) & 15) == 0);
-    replay_kernel<DK><<<grid, NT, 0, stream>>>(p, bulk_caps);
-    return cudaGetLastError();
+    return launch_dependent(replay_kernel<DK>, grid, dim3(NT), 0, stream, p, bulk_caps);
 }
 
 }  // namespace
