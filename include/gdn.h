@@ -14,11 +14,11 @@
  * dependents of the kernel before them on the stream: their thread blocks may
  * be scheduled while that kernel finishes, but each waits for its completion
  * (and the visibility of its writes) before reading anything, so stream order
- * holds as with plain launches.  Each library kernel also allows the kernel
- * after it to be scheduled early: a caller's own kernel launched right after
- * with programmatic stream serialization must itself wait (griddepcontrol.wait
- * or cudaGridDependencySynchronize) before reading the library's outputs,
- * which is that launch mode's rule; plainly launched kernels are unaffected.
+ * holds as with plain launches.  A caller's own kernel launched right after
+ * a library call with programmatic stream serialization must itself wait
+ * (griddepcontrol.wait or cudaGridDependencySynchronize) before reading the
+ * library's outputs, which is that launch mode's rule; plainly launched
+ * kernels are unaffected.
  *
  * Errors come in two kinds.
  *  - Argument errors that the host can see (NULL pointers, bad sizes, BF16,
