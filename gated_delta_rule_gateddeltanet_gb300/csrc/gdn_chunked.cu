@@ -770,6 +770,19 @@ bool encode_rows_f32(CUtensorMap *map, const float *base, long long row_elems, l
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_rows_f32_strided(CUtensorMap *map, const float *base, long long row_elems, long long stride, int T,
+                             int box_x, int box_y) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)(T > 0 ? T : 1)};
+    const cuuint64_t strides[1] = {(cuuint64_t)stride * 4};
+    const cuuint32_t box[2] = {(cuuint32_t)box_x, (cuuint32_t)box_y};
+    const cuuint32_t estride[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t chunked_workspace_bytes(int B) { return ((size_t)(B + 2) * sizeof(int32_t) + 255) & ~size_t(255); }
 
 bool chunked_supported(int dk, int dv) { return dk == DH && dv == DH; }

@@ -88,10 +88,15 @@ cudaError_t launch_conv(const ConvParams &p, cudaStream_t stream);
 cudaError_t launch_conv_replay(const ConvReplayParams &p, cudaStream_t stream);
 
 // Spans of at most p.max_len tokens: the CUDA-core decode kernel when every
-// span has at most one token (T == B), else the persistent mixed kernel
-// (one-token spans on the same CUDA-core code, longer ones on the warp
-// tensor cores four tokens at a time).
+// span has at most one token (T == B), else at dk = dv = 128 the tcgen05
+// short-span kernel and at other head sizes the persistent mixed kernel
+// (one-token spans on the decode kernel's arithmetic in both, longer ones four
+// tokens at a time).
 cudaError_t launch_recurrent(const ForwardParams &p, cudaStream_t stream);
+// Batches with a multi-token span at dk = dv = 128: the tcgen05 short-span
+// kernel (gdn_verify.cu); one-token spans in it keep the decode kernel's bits.
+bool verify_kernel_supported(const ForwardParams &p);
+cudaError_t launch_verify(const ForwardParams &p, cudaStream_t stream);
 // dst[m] = src[m]^T for `num` row-major rows x cols FP32 matrices.
 cudaError_t launch_transpose(const float *src, float *dst, long long num, int rows, int cols, cudaStream_t stream);
 cudaError_t launch_replay(const ReplayParams &p, cudaStream_t stream);
@@ -135,6 +140,12 @@ bool encode_rows_f16(CUtensorMap *map, const void *base, long long row_elems, lo
 // the 128-byte swizzled layout (16-byte chunk c of row r at c ^ (r % 8)).
 bool encode_rows_f32(CUtensorMap *map, const float *base, long long row_elems, long long rows, int box_x, int box_y,
                      bool swizzle128);
+
+// Tensor map over a packed FP32 [T, row_elems] array with `stride` elements
+// between tokens (stride * 4 a multiple of 16), boxes of box_y tokens x box_x
+// elements, zero fill past T.
+bool encode_rows_f32_strided(CUtensorMap *map, const float *base, long long row_elems, long long stride, int T,
+                             int box_x, int box_y);
 
 // Sequences up to this many tokens stay on the recurrent kernel under the
 // automatic plan; longer ones go to the chunked kernel.  Head sizes below

@@ -34,9 +34,10 @@
 // time; rows stay in registers across the staged tokens.
 //
 // 2. Mixed kernel (some span has several tokens: speculative verification,
-// short prefill) -- a persistent kernel of 4-warp CTAs (4 per SM at 128
-// registers), each over a contiguous range of work items (sequence, value
-// head, 64-row block).  One-token spans run the code above (the same bits as
+// short prefill) at head sizes 32 and 64 (at dk = dv = 128 such batches run
+// the tcgen05 kernel of gdn_verify.cu) -- a persistent kernel of 4-warp CTAs
+// (4 per SM at 128 registers), each over a contiguous range of work items
+// (sequence, value head, 64-row block).  One-token spans run the code above (the same bits as
 // the decode kernel); longer spans run the tensor-core evaluation below.  At
 // four tokens per span the CUDA-core loop is bound by instruction issue
 // (about 95 instructions per row group and token), not by HBM.
@@ -836,6 +837,7 @@ cudaError_t launch_dk(const ForwardParams &p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         return launch_dependent(kern, dim3((unsigned)(nrb * p.Hv), (unsigned)p.B), dim3(NT), smem, stream, p);
     }
+    if (verify_kernel_supported(p)) return launch_verify(p, stream);
     // some span has several tokens: the persistent mixed kernel, as many CTAs as fit at once
     const int smem = ROWS * DK * 4 + 1024;
     CUtensorMap rows_map;

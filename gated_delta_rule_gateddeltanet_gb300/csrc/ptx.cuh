@@ -150,6 +150,31 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::tf32 (32-bit containers read as
+// TF32), one thread issues.
+__device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::tf32 (32-bit containers, TF32
+// inputs), one thread issues.  A sits in tensor memory: row i in lane i, one
+// element per column, K = 8 columns per instruction.
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // The mbarrier receives one arrival when every tcgen05 operation this thread
 // issued before has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -212,6 +237,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                 "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+                 : "memory");
+}
+
 // Loads / stores of N columns (N = 8, 16, 32) for code generic in N.
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]) {
@@ -252,6 +285,15 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_maj
     return (1u << 4)                          // D format: f32
            | (0u << 7) | (0u << 10)           // A, B format: f16
            | (0u << 15)                       // A K-major
+           | ((b_mn_major ? 1u : 0u) << 16)   // B K-major, or MN-major
+           | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor of kind::tf32 (A and B TF32, A K-major) with an fp32
+// accumulator, for an M x N tile.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N, bool b_mn_major = false) {
+    return (1u << 4)                          // D format: f32
+           | (2u << 7) | (2u << 10)           // A, B format: tf32
            | ((b_mn_major ? 1u : 0u) << 16)   // B K-major, or MN-major
            | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
