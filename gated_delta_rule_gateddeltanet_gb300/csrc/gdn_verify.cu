@@ -319,15 +319,15 @@ __global__ void __launch_bounds__(NTV, 2)
         }
     };
 
-    VCursor cur_c;  // the item after the current one
+    // the current item's position and its sequence's descriptor (loaded again only when
+    // the position moves to another sequence)
+    VCursor cur_c;
     cur_c.b = first / p.Hv;
     cur_c.h = first - cur_c.b * p.Hv;
     cur_c.kh = cur_c.h / p.r;
     cur_c.hr = cur_c.h - cur_c.kh * p.r;
-    VItem it = first < stop ? make_item(p, cur_c, load_raw(p, cur_c.b)) : no_item();
-    advance(p, cur_c);
-    VRaw rn = {0, 0, 0};  // descriptor loads of the next item
-    if (first + 1 < stop) rn = load_raw(p, cur_c.b);
+    VRaw seq = load_raw(p, cur_c.b);
+    VItem it = first < stop ? make_item(p, cur_c, seq) : no_item();
     bool loaded = load_bytes(it) != 0;
     if (tid == 0) issue_load(it);
     GateIn gc = load_gates(p, it);  // this item's first-group gate inputs
@@ -474,12 +474,9 @@ __global__ void __launch_bounds__(NTV, 2)
     };
 
     for (int i = first; i < stop; ++i) {
-        // the next item's descriptor and gate inputs (its rows are copied once this item's
-        // rows have been stored)
-        const VItem nx = i + 1 < stop ? make_item(p, cur_c, rn) : no_item();
-        advance(p, cur_c);
-        if (i + 2 < stop) rn = load_raw(p, cur_c.b);
-        const GateIn gn = load_gates(p, nx);
+        // warm the next sequence's descriptor in L2 (read when the position gets there)
+        if (tid == 0 && p.cu && cur_c.b + 2 <= p.B) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.cu + cur_c.b + 1));
+        if (tid == 0 && p.slots && cur_c.b + 1 < p.B) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.slots + cur_c.b + 1));
 
         // ---- this item's copies have landed (no copies: zeros without an initial state)
         bool bad = false;
@@ -780,6 +777,13 @@ __global__ void __launch_bounds__(NTV, 2)
             }
         }
 
+        // ---- the next item
+        advance(p, cur_c);
+        VItem nx = no_item();
+        if (i + 1 < stop) {
+            if (cur_c.h == 0) seq = load_raw(p, cur_c.b);
+            nx = make_item(p, cur_c, seq);
+        }
         // ---- the item's output boxes and rows go back; then the buffer takes the next item
         if (tid == 0) {
             if (tma_group) {
@@ -802,7 +806,7 @@ __global__ void __launch_bounds__(NTV, 2)
         }
         loaded = load_bytes(nx) != 0;
         it = nx;
-        gc = gn;
+        gc = load_gates(p, it);  // used once its copies have landed
     }
 
     if (tid == 0) {
