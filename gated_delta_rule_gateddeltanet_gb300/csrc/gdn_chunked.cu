@@ -770,6 +770,20 @@ bool encode_rows_f32(CUtensorMap *map, const float *base, long long row_elems, l
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_state_tiles(CUtensorMap *map, const float *base, int d, long long rows, int box_rows) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return false;
+    // [rows, d] viewed as (32 features, rows, d / 32 feature blocks): one box of
+    // box_rows rows lands as d / 32 consecutive 128-byte swizzled tiles
+    const cuuint64_t dims[3] = {32, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)(d / 32)};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 4, 128};
+    const cuuint32_t box[3] = {32, (cuuint32_t)box_rows, (cuuint32_t)(d / 32)};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_rows_f32_strided(CUtensorMap *map, const float *base, long long row_elems, long long stride, int T,
                              int box_x, int box_y) {
     auto encode = tensor_map_encoder();

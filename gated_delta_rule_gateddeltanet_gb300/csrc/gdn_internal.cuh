@@ -141,6 +141,12 @@ bool encode_rows_f16(CUtensorMap *map, const void *base, long long row_elems, lo
 bool encode_rows_f32(CUtensorMap *map, const float *base, long long row_elems, long long rows, int box_x, int box_y,
                      bool swizzle128);
 
+// Tensor map over a dense FP32 [rows, d] array whose boxes of box_rows rows
+// land in shared memory as d / 32 consecutive tiles of box_rows x 32 floats in
+// the 128-byte swizzled layout (one tensor copy instead of d / 32); false if
+// the driver does not accept the view.
+bool encode_state_tiles(CUtensorMap *map, const float *base, int d, long long rows, int box_rows);
+
 // Tensor map over a packed FP32 [T, row_elems] array with `stride` elements
 // between tokens (stride * 4 a multiple of 16), boxes of box_y tokens x box_x
 // elements, zero fill past T.

@@ -63,13 +63,15 @@ namespace {
 constexpr int D = 128;     // dk = dv
 constexpr int TB = 4;      // tokens per group
 constexpr int NTV = 256;   // threads per CTA (two CTAs per SM)
-constexpr int ISSUER = 128;  // the thread that issues the tensor-core products (warp 4, lane 0)
+constexpr int ISSUER_HI = 128;  // the threads that issue the tensor-core products: rows (warp 4, lane 0)
+constexpr int ISSUER_LO = 160;  // and remainders (warp 5, lane 0)
+constexpr int STAGER = 32;      // the thread that issues the q, k, v copies (warp 1, lane 0)
 constexpr float EPS = 1e-6f;
 constexpr long long WAIT_LIMIT = 4000000000LL;  // SM cycles (~2 s)
 
 // Tensor-memory columns (one allocation of 256 per CTA): the TF32 remainders of
-// the rows and the accumulator of the dot products.
-constexpr uint32_t TM_LO = 0, TM_D1 = 128, TM_COLS = 256;
+// the rows and the two accumulators of the dot products (rows, remainders).
+constexpr uint32_t TM_LO = 0, TM_D1 = 128, TM_D1L = 144, TM_COLS = 256;
 
 constexpr uint32_t TILE = D * D * 4;  // one state: 4 boxes of 128 rows x 128 bytes (128-byte swizzle)
 
@@ -88,9 +90,10 @@ struct Layout {
 // features wide and TB tokens high; output boxes TB tokens x 64 elements.
 struct VMaps {
     CUtensorMap in, fin;      // the state pools, boxes of 128 rows x 32 floats (128-byte swizzle)
+    CUtensorMap in3;          // the initial pool, one box of 128 rows x 128 floats as four such tiles
     CUtensorMap out, caps;    // outputs and capsules of full groups
     CUtensorMap q, k, v;      // the first group's q, k, v rows of an item
-    int out_ok, stg_ok;
+    int out_ok, stg_ok, in3_ok;
 };
 
 struct VItem {
@@ -176,9 +179,10 @@ __device__ __forceinline__ float tf32_trunc(float x) { return __uint_as_float(__
 __device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(ct::to_tf32(x)); }
 
 // D1 [128 x 16] = S [128 x 128] . B1^T, B1 rows k_hi(t), k_lo(t), q_hi(t),
-// q_lo(t) (t < 4), K-major: the rows themselves (shared memory, read as TF32)
-// and then their remainders (tensor memory), 16 K steps of 8 each.
-__device__ __forceinline__ void issue_mma1(uint32_t tm, uint32_t rows_base, uint32_t b1_base) {
+// q_lo(t) (t < 4), K-major, 16 K steps of 8, in two parts issued by two threads
+// into two accumulators: the rows themselves (shared memory, read as TF32) and
+// their remainders (tensor memory).
+__device__ __forceinline__ void issue_mma_rows(uint32_t tm, uint32_t rows_base, uint32_t b1_base) {
     constexpr uint32_t idesc = ptx::idesc_tf32_f32(128, 16);
 #pragma unroll 4
     for (int s = 0; s < D / 8; ++s) {
@@ -187,10 +191,14 @@ __device__ __forceinline__ void issue_mma1(uint32_t tm, uint32_t rows_base, uint
         const uint64_t bd = ptx::sdesc_k_sw128(b1_base + (uint32_t)(s >> 2) * 2048u) + (uint64_t)(2 * (s & 3));
         ptx::mma_tf32_ss(tm + TM_D1, ad, bd, idesc, s != 0);
     }
+}
+
+__device__ __forceinline__ void issue_mma_rem(uint32_t tm, uint32_t b1_base) {
+    constexpr uint32_t idesc = ptx::idesc_tf32_f32(128, 16);
 #pragma unroll 4
     for (int s = 0; s < D / 8; ++s) {
         const uint64_t bd = ptx::sdesc_k_sw128(b1_base + (uint32_t)(s >> 2) * 2048u) + (uint64_t)(2 * (s & 3));
-        ptx::mma_tf32_ts(tm + TM_D1, tm + TM_LO + 8u * s, bd, idesc, 1u);
+        ptx::mma_tf32_ts(tm + TM_D1L, tm + TM_LO + 8u * s, bd, idesc, s != 0);
     }
 }
 
@@ -277,7 +285,7 @@ __global__ void __launch_bounds__(NTV, 2)
     }
     if (tid == 0) {
         ptx::mbar_init(&full_bar, 1);
-        ptx::mbar_init(&mma_bar, 1);
+        ptx::mbar_init(&mma_bar, 2);  // one commit per issuing thread
         ptx::fence_mbar_init();
     }
     ptx::tc_fence_before();
@@ -303,15 +311,22 @@ __global__ void __launch_bounds__(NTV, 2)
         if (!it.ok) return 0u;
         return (p.init ? TILE : 0u) + (mp.stg_ok && it.eos > it.bos ? 3u * TB * D * (uint32_t)sizeof(TIO) : 0u);
     };
+    // thread 0 arms the barrier and copies the rows, thread STAGER copies the q, k, v rows
+    // (a copy may complete before the barrier is armed: its bytes are counted all the same)
     auto issue_load = [&](const VItem &it) {
         const uint32_t bytes = load_bytes(it);
         if (!bytes) return;
-        ptx::mbar_arrive_expect_tx(&full_bar, bytes);
-        if (p.init) {
+        if (tid == 0) {
+            ptx::mbar_arrive_expect_tx(&full_bar, bytes);
+            if (p.init) {
+                if (mp.in3_ok) {
+                    ptx::tma_load_3d(rows, &mp.in3, 0, it.row0, 0, &full_bar);
+                } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) ptx::tma_load_2d(rows + j * (D * 128), &mp.in, 32 * j, it.row0, &full_bar);
-        }
-        if (L::STAGE && mp.stg_ok && it.eos > it.bos) {
+                    for (int j = 0; j < 4; ++j) ptx::tma_load_2d(rows + j * (D * 128), &mp.in, 32 * j, it.row0, &full_bar);
+                }
+            }
+        } else if (tid == STAGER && L::STAGE && mp.stg_ok && it.eos > it.bos) {
             TIO *st = reinterpret_cast<TIO *>(sm + L::STG);
             ptx::tma_load_2d(st, &mp.q, it.kh * D, it.bos, &full_bar);
             ptx::tma_load_2d(st + TB * D, &mp.k, it.kh * D, it.bos, &full_bar);
@@ -329,7 +344,7 @@ __global__ void __launch_bounds__(NTV, 2)
     VRaw seq = load_raw(p, cur_c.b);
     VItem it = first < stop ? make_item(p, cur_c, seq) : no_item();
     bool loaded = load_bytes(it) != 0;
-    if (tid == 0) issue_load(it);
+    issue_load(it);
     GateIn gc = load_gates(p, it);  // this item's first-group gate inputs
 
     uint32_t full_phase = 0u, mma_phase = 0u;
@@ -529,16 +544,21 @@ __global__ void __launch_bounds__(NTV, 2)
                 // ---- the dot products: one thread of warp 4 issues them while warps 0-3 form
                 //      the gates, k_s.k_t and k_s.q_t (s <= t, unless kept) and the group
                 //      factors, and warps 5-7 write the capsule keys
-                if (tid == ISSUER) {
+                if (tid == ISSUER_HI) {
                     ptx::tc_fence_after();
-                    issue_mma1(tm, rows_base, b1_base);
+                    issue_mma_rows(tm, rows_base, b1_base);
+                    ptx::mma_commit(&mma_bar);
+                } else if (tid == ISSUER_LO) {
+                    ptx::tc_fence_after();
+                    issue_mma_rem(tm, b1_base);
                     ptx::mma_commit(&mma_bar);
                 }
                 mma_out = true;
+                if (tid == 0) ptx::bulk_wait_read_all();  // the previous output boxes have been read
                 if (warp < TB) {
                     group_factors(it, t0, nt, first_group, !keep);
-                } else if (warp > TB && p.caps && it.h % p.r == 0) {
-                    for (int x = tid - (TB + 1) * 32; x < nt * D; x += (NTV / 32 - TB - 1) * 32) {
+                } else if (warp > TB + 1 && p.caps && it.h % p.r == 0) {
+                    for (int x = tid - (TB + 2) * 32; x < nt * D; x += (NTV / 32 - TB - 2) * 32) {
                         const int tt = x >> 7, e = x & (D - 1);
                         const int tl = t0 + tt - it.bos;
                         if (tl < p.cap)
@@ -562,8 +582,11 @@ __global__ void __launch_bounds__(NTV, 2)
                     vr[t] = t >= nt ? 0.f
                             : staged ? to_f32(stv[t * D + row])
                                      : to_f32(vg[(long long)(t0 + t) * p.v_stride + (long long)it.h * D + row]);
-                float d1[16];
+                float d1[16], d1l[16];
                 ptx::tmem_ld16(tm + lane_sel + TM_D1, d1);
+                ptx::tmem_ld16(tm + lane_sel + TM_D1L, d1l);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) d1[c] += d1l[c];
                 float u[TB];
 #pragma unroll
                 for (int t = 0; t < TB; ++t) {
@@ -611,7 +634,7 @@ __global__ void __launch_bounds__(NTV, 2)
                         k2[t][1] = make_float2(k4.z, k4.w);
                     }
                     float *fin = p.final_state + (size_t)it.row0 * D + 4 * lane;
-#pragma unroll 4
+#pragma unroll 8
                     for (int rr = 0; rr < 16; ++rr) {
                         const int r = 16 * warp + rr;
                         float4 *sp = reinterpret_cast<float4 *>(rows + chunk_at(r, lane >> 3, lane & 7));
@@ -796,14 +819,15 @@ __global__ void __launch_bounds__(NTV, 2)
                                           it.b * p.cap + (t0 - it.bos));
                 }
             }
-            if (it.ok && n < 2 && p.final_state) {  // one-token and empty spans (the others are written)
+            const bool rows_out = it.ok && n < 2 && p.final_state;  // one-token and empty spans
+            if (rows_out) {                                         // (the others are written directly)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) ptx::tma_store_2d(&mp.fin, rows + j * (D * 128), 32 * j, it.row0);
             }
             ptx::bulk_commit();
-            ptx::bulk_wait_read_all();  // the stores have read the buffer and the boxes
-            issue_load(nx);
+            if (rows_out) ptx::bulk_wait_read_all();  // the stores have read the buffer
         }
+        issue_load(nx);
         loaded = load_bytes(nx) != 0;
         it = nx;
         gc = load_gates(p, it);  // used once its copies have landed
@@ -833,6 +857,7 @@ cudaError_t launch_io(const ForwardParams &p, cudaStream_t stream) {
     VMaps mp;
     memset(&mp, 0, sizeof(mp));
     if (p.init && !encode_rows_f32(&mp.in, p.init, D, rows, 32, D, true)) return cudaErrorInvalidValue;
+    mp.in3_ok = p.init && encode_state_tiles(&mp.in3, p.init, D, rows, D) ? 1 : 0;
     if (p.final_state && !encode_rows_f32(&mp.fin, p.final_state, D, rows, 32, D, true)) return cudaErrorInvalidValue;
     const bool f16 = sizeof(TIO) == 2;
     // outputs and capsule deltas of full groups as tensor stores: box coordinates must be

@@ -80,6 +80,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tensor_m
         : "memory");
 }
 
+// Global -> shared copy of one 3-D box, at element coordinates (x, y, z).
+__device__ __forceinline__ void tma_load_3d(void *dst_smem, const void *tensor_map, int x, int y, int z,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(tensor_map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Shared -> global 2-D tensor store of one box from a tensor map, tracked by
 // the issuing thread's bulk async-groups (coordinates must not be negative).
 __device__ __forceinline__ void tma_store_2d(const void *tensor_map, const void *src_smem, int x, int y) {
