@@ -74,9 +74,10 @@ enum {
                                 sizes below 128 run them on zero-padded d = 128 tiles) */
     GDN_PLAN_RECURRENT = 1,  /* every sequence on the recurrent kernels: the state carried
                                 token by token (batches of one-token spans), or four
-                                tokens at a time in closed form on the warp tensor cores
-                                (batches with longer spans; one-token spans in them still
-                                take the token-by-token code, with the same bits) */
+                                tokens at a time in closed form on the tensor cores
+                                (batches with longer spans: tcgen05 at dk = dv = 128, warp
+                                tensor cores at smaller heads; one-token spans in them
+                                still take the token-by-token arithmetic, same bits) */
     GDN_PLAN_CHUNKED = 2,    /* every sequence on the tensor-core chunked kernels (head
                                 sizes 32, 64, 128 in any combination; below 128 the
                                 d = 128 operand tiles are zero-padded) */
