@@ -60,10 +60,12 @@ constexpr float LOG2E = 1.4426950408889634f;
 
 // ---- Small products on the warp-level tensor cores
 //
-// The block products of the triangular inverse are 16 x 16 and 32 x 32: too
-// small for tcgen05 (M >= 64) and, on the CUDA cores, bound by shared-memory
-// traffic.  They run as mma.sync m16n8k8 TF32 products (10-bit mantissas, FP32
-// accumulation).  The inverse only feeds the tensor cores as an fp16 operand
+// The block products of the triangular inverse are 16 x 16 and 32 x 32: small
+// and dependent, so a tcgen05 product per level is an asynchronous round trip
+// (operand tiles, issue, mbarrier, tensor-memory read-back) -- measured, that
+// variant made the prep kernel 200.9 us against 140.6 -- and on the CUDA
+// cores they are bound by shared-memory traffic.  They run as mma.sync
+// m16n8k8 TF32 products (10-bit mantissas, FP32 accumulation).  The inverse only feeds the tensor cores as an fp16 operand
 // (also a 10-bit mantissa), and at the full varlen prefill (15,991 tokens)
 // TF32 products gave the same end-to-end error against the FP64 oracle as
 // FP32-accurate split products (output 8.10e-4, state 5.77e-4 vs 5.80e-4
