@@ -84,3 +84,37 @@ def test_zero_initial_state_multi_token_fp16():
     """No initial state: the rows start at zero (no row copies are issued)."""
     inp = wl.make_inputs(640, [4, 3, 4, 2], Hk=2, Hv=6, dk=128, dv=128, io_dtype=np.float16, capacity=4)
     _check(inp, run_gpu(inp), run_oracle(inp), fp16=True)
+
+
+@pytest.mark.parametrize("pad", [0, 3])
+def test_d128_spans_from_fused_views(pad):
+    """d = 128 (the tcgen05 short-span kernel): q, k, v as strided views of one
+    fused projection [T, 2 Hk dk + Hv dv + pad] fp16.  pad = 0: the first
+    group's q, k, v rows arrive by tensor copies from the strided views; pad = 3:
+    the row stride (in bytes) is not a multiple of 16, so they are read with
+    plain loads.  Spans: a two-group span (6 tokens, capsules for the first 4),
+    full and ragged groups, one token and empty, in place."""
+    import torch
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    from gpu_common import to_dev
+    lengths = [6, 4, 3, 1, 0, 4, 2]
+    Hk, Hv, d = 2, 4, 128
+    inp = wl.make_inputs(650 + pad, lengths, Hk=Hk, Hv=Hv, dk=d, dv=d, io_dtype=np.float16, state_std=0.02,
+                         capacity=4)
+    T = inp.T
+    width = 2 * Hk * d + Hv * d
+    fused = np.zeros((T, width + pad), np.float16)
+    fused[:, :Hk * d] = inp.q.reshape(T, -1)
+    fused[:, Hk * d:2 * Hk * d] = inp.k.reshape(T, -1)
+    fused[:, 2 * Hk * d:width] = inp.v.reshape(T, -1)
+    f = to_dev(fused)
+    q = f[:, :Hk * d].view(T, Hk, d) if pad == 0 else f[:, :Hk * d].unflatten(1, (Hk, d))
+    k = f[:, Hk * d:2 * Hk * d].unflatten(1, (Hk, d))
+    v = f[:, 2 * Hk * d:width].unflatten(1, (Hv, d))
+    state = to_dev(inp.initial_state)
+    out, final, caps = gdn.gdn_forward(q, k, v, to_dev(inp.a), to_dev(inp.b), to_dev(inp.cu_seqlens),
+                                       A_log=to_dev(inp.A_log), dt_bias=to_dev(inp.dt_bias), initial_state=state,
+                                       final_state=state, capacity=4)
+    torch.cuda.synchronize()
+    gpu = (out.double().cpu().numpy(), final.double().cpu().numpy(), caps.double().cpu().numpy())
+    _check(inp, gpu, run_oracle(inp), fp16=True)
