@@ -320,6 +320,7 @@ gdn_status varlen_causal_conv_with_state(const gdn_conv_args *a, gdn_stream_t st
     // Sequences of at most one token always lie inside one token block, where the
     // conv kernel writes their state itself; empty ones keep an in-place state.
     p.skip_state_kernel = a->max_seqlen == 1 && a->initial_state == a->final_state;
+    p.max_len_hint = a->max_seqlen;
     if (gdn::launch_conv(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
     return GDN_OK;
 }

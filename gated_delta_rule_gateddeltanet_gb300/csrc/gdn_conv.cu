@@ -25,7 +25,8 @@
 // sequence start, from the state.  The state is therefore only read by the
 // conv kernel; a second small kernel rolls each sequence's state forward
 // afterwards (same thread reads then writes), so updating the state in place
-// is race-free.
+// is race-free.  Short sequences (a max_seqlen hint of at most SHORT_MAX) run
+// conv_short_kernel instead, in which a thread carries whole sequences.
 #include <type_traits>
 
 #include "gdn_internal.cuh"
@@ -97,6 +98,34 @@ __device__ __forceinline__ float silu_tanh(float x) {
     const float h = 0.5f * x;
     asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
     return fmaf(h, t, h);
+}
+
+// One token's outputs for a thread's 4 channels: bias + the K taps over the
+// window (oldest first) and the token itself, then SiLU.  Every kernel that
+// produces outputs calls this, so the launch shape chosen for a batch never
+// changes a bit of the results.
+template <typename T, int K>
+__device__ __forceinline__ void conv_point(const float (&w)[4][K], const float (&bias)[4], const float (&win)[K - 1][4],
+                                           const float (&xt)[4], int silu_on, float (&yv)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float acc = bias[i];
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) acc = fmaf(w[i][j], win[j][i], acc);
+        acc = fmaf(w[i][K - 1], xt[i], acc);
+        yv[i] = silu_on ? (sizeof(T) == 2 ? silu_tanh(acc) : silu(acc)) : acc;
+    }
+}
+
+// The window after token xt: entries move one place older, xt becomes the newest.
+template <int K>
+__device__ __forceinline__ void window_push(float (&win)[K - 1][4], const float (&xt)[4]) {
+#pragma unroll
+    for (int j = 0; j + 1 < K - 1; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) win[j][i] = win[j + 1][i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) win[K - 2][i] = xt[i];
 }
 
 // A thread's block of the state: 4 channels x (K-1) entries, contiguous, moved
@@ -245,22 +274,10 @@ __global__ void __launch_bounds__(NT, sizeof(T) == 2 ? 4 : 3) conv_kernel(const 
             for (int g = 0; g < GROUP; ++g) {
                 float xt[V], yv[V];
                 unpack<T>(raw[g], xt);
-#pragma unroll
-                for (int i = 0; i < V; ++i) {
-                    float acc = bias[i];
-#pragma unroll
-                    for (int j = 0; j < K - 1; ++j) acc = fmaf(w[i][j], win[j][i], acc);
-                    acc = fmaf(w[i][K - 1], xt[i], acc);
-                    yv[i] = p.silu ? (sizeof(T) == 2 ? silu_tanh(acc) : silu(acc)) : acc;
-                }
+                conv_point<T, K>(w, bias, win, xt, p.silu, yv);
                 store_vec<T>(yp, yv);
                 yp += p.C;
-#pragma unroll
-                for (int j = 0; j + 1 < K - 1; ++j)
-#pragma unroll
-                    for (int i = 0; i < V; ++i) win[j][i] = win[j + 1][i];
-#pragma unroll
-                for (int i = 0; i < V; ++i) win[K - 2][i] = xt[i];
+                window_push<K>(win, xt);
             }
             continue;
         }
@@ -276,23 +293,11 @@ __global__ void __launch_bounds__(NT, sizeof(T) == 2 ? 4 : 3) conv_kernel(const 
             float xt[V];
             unpack<T>(raw[g], xt);
             float yv[V];
-#pragma unroll
-            for (int i = 0; i < V; ++i) {
-                float acc = bias[i];
-#pragma unroll
-                for (int j = 0; j < K - 1; ++j) acc = fmaf(w[i][j], win[j][i], acc);
-                acc = fmaf(w[i][K - 1], xt[i], acc);
-                yv[i] = p.silu ? (sizeof(T) == 2 ? silu_tanh(acc) : silu(acc)) : acc;
-            }
+            conv_point<T, K>(w, bias, win, xt, p.silu, yv);
             store_vec<T>(y + (long long)t * p.C + c0, yv);
             const int tl = t - bos;
             if (vals && tl < ncap) store_vec<T>(vals + ((long long)b * p.cap + tl) * p.C + c0, xt);
-#pragma unroll
-            for (int j = 0; j + 1 < K - 1; ++j)
-#pragma unroll
-                for (int i = 0; i < V; ++i) win[j][i] = win[j + 1][i];
-#pragma unroll
-            for (int i = 0; i < V; ++i) win[K - 2][i] = xt[i];
+            window_push<K>(win, xt);
             // A sequence that lies wholly inside this token block is read and
             // written by this thread only: its new state is the window now.
             if (t == eos - 1 && bos >= t_begin) {
@@ -347,6 +352,129 @@ __global__ void __launch_bounds__(NT) conv_state_kernel(const ConvParams p) {
         for (int j = 0; j < K - 1; ++j) st_out[((long long)slot * p.C + c0 + i) * (K - 1) + j] = nw[i][j];
 }
 
+// Short sequences (decode steps, speculative drafts): a max_seqlen hint of
+// 1 .. SHORT_MAX.  A thread owns 4 channels of SHORT_SEQS consecutive
+// sequences and runs each sequence's tokens itself, so its work is two
+// dependent rounds of loads: the sequence bounds, slots, capture counts and
+// weights, then the states and the first SHORT_PREFETCH input rows of its
+// sequences together.  The token-block kernel instead resolves each token's
+// sequence through a search and loads the slot and then the state per
+// sequence, one after the other (five dependent rounds for two 1-token
+// sequences per CTA).  Each thread writes its sequences' new states itself,
+// so there is no state-rolling launch.  A sequence longer than the hint
+// (a caller error) still gets exact results: its remaining rows are loaded
+// SHORT_PREFETCH at a time.
+constexpr int SHORT_MAX = 8;       // longest hint served by conv_short_kernel
+constexpr int SHORT_NT = 128;      // threads per CTA
+constexpr int SHORT_SEQS = 2;      // sequences per thread (keeps a 64 x 10240 decode step in one wave)
+constexpr int SHORT_PREFETCH = 4;  // input rows per sequence loaded with the state
+
+template <typename T, int K>
+__global__ void __launch_bounds__(SHORT_NT) conv_short_kernel(const ConvParams p) {
+    dependent_prologue();
+    constexpr int V = Vec<T>::N;
+    using Raw = typename Vec<T>::Raw;
+    const int cg = blockIdx.x * SHORT_NT + threadIdx.x;
+    const int b0 = blockIdx.y * SHORT_SEQS;
+    const bool leader = blockIdx.x == 0 && threadIdx.x == 0;  // raises the flags of its sequences
+    if (leader && blockIdx.y == 0 && (p.cu[0] != 0 || p.cu[p.B] != p.T)) flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
+    if (cg >= p.C / V) return;
+    const int c0 = cg * V;
+    const T *x = static_cast<const T *>(p.x);
+    T *y = static_cast<T *>(p.out);
+    T *vals = static_cast<T *>(p.values);
+    const T *st_in = static_cast<const T *>(p.state_in);
+    T *st_out = static_cast<T *>(p.state_out);
+
+    // ---- first round: what each sequence is, and the weights
+    int bos[SHORT_SEQS], eos[SHORT_SEQS], slot[SHORT_SEQS], cc[SHORT_SEQS];
+#pragma unroll
+    for (int u = 0; u < SHORT_SEQS; ++u) {
+        const int b = b0 + u;
+        bos[u] = eos[u] = slot[u] = 0;
+        cc[u] = p.cap;
+        if (b < p.B) {
+            bos[u] = p.cu[b];
+            eos[u] = p.cu[b + 1];
+            slot[u] = p.slots ? p.slots[b] : b;
+            if (p.capture_count) cc[u] = p.capture_count[b];
+        }
+    }
+    float w[V][K], bias[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+#pragma unroll
+        for (int j = 0; j < K; ++j) w[i][j] = p.w[(long long)(c0 + i) * K + j];
+        bias[i] = p.bias ? p.bias[c0 + i] : 0.f;
+    }
+    bool ok[SHORT_SEQS];
+    int len[SHORT_SEQS], ncap[SHORT_SEQS];
+#pragma unroll
+    for (int u = 0; u < SHORT_SEQS; ++u) {
+        const int b = b0 + u;
+        const bool slot_ok = slot[u] >= 0 && slot[u] < p.num_slots;
+        ok[u] = b < p.B && bos[u] >= 0 && eos[u] >= bos[u] && eos[u] <= p.T && slot_ok;
+        if (b < p.B && !ok[u] && leader)
+            flag_error(p.status, slot_ok ? GDN_DEVERR_CU_SEQLENS : GDN_DEVERR_STATE_SLOT);
+        ncap[u] = cc[u];
+        if (p.capture_count && (cc[u] < 0 || cc[u] > p.cap)) {
+            if (ok[u] && leader) flag_error(p.status, GDN_DEVERR_CAPTURE_COUNT);
+            ncap[u] = 0;
+        }
+        len[u] = ok[u] ? eos[u] - bos[u] : 0;
+    }
+
+    // ---- second round: the states and the first input rows of every sequence
+    StateBlock<T, K> sb[SHORT_SEQS];
+    Raw raw[SHORT_SEQS][SHORT_PREFETCH];
+#pragma unroll
+    for (int u = 0; u < SHORT_SEQS; ++u) {
+        if (ok[u] && st_in) sb[u].load(st_in + ((long long)slot[u] * p.C + c0) * (K - 1));
+#pragma unroll
+        for (int g = 0; g < SHORT_PREFETCH; ++g)
+            if (g < len[u]) raw[u][g] = load_raw<T>(x + (long long)(bos[u] + g) * p.x_stride + c0);
+    }
+
+#pragma unroll
+    for (int u = 0; u < SHORT_SEQS; ++u) {
+        if (!ok[u]) continue;
+        const int b = b0 + u;
+        float win[K - 1][V];
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j)
+#pragma unroll
+            for (int i = 0; i < V; ++i) win[j][i] = st_in ? to_f32(sb[u].at(i, j)) : 0.f;
+        for (int t0 = 0; t0 < len[u]; t0 += SHORT_PREFETCH) {
+            if (t0 > 0) {  // only past the prefetched rows (a sequence longer than the hint)
+#pragma unroll
+                for (int g = 0; g < SHORT_PREFETCH; ++g)
+                    if (t0 + g < len[u]) raw[u][g] = load_raw<T>(x + (long long)(bos[u] + t0 + g) * p.x_stride + c0);
+            }
+#pragma unroll
+            for (int g = 0; g < SHORT_PREFETCH; ++g) {
+                const int tl = t0 + g;
+                if (tl >= len[u]) break;
+                float xt[V], yv[V];
+                unpack<T>(raw[u][g], xt);
+                conv_point<T, K>(w, bias, win, xt, p.silu, yv);
+                store_vec<T>(y + (long long)(bos[u] + tl) * p.C + c0, yv);
+                if (vals && tl < ncap[u]) store_vec<T>(vals + ((long long)b * p.cap + tl) * p.C + c0, xt);
+                window_push<K>(win, xt);
+            }
+        }
+        // the new state is the window; an empty sequence keeps its state (copied when
+        // the state is not updated in place, zero when there is no initial state)
+        if (len[u] > 0 || st_out != st_in) {
+            StateBlock<T, K> nb;
+#pragma unroll
+            for (int i = 0; i < V; ++i)
+#pragma unroll
+                for (int j = 0; j < K - 1; ++j) nb.at(i, j) = from_f32<T>(win[j][i]);
+            nb.store(st_out + ((long long)slot[u] * p.C + c0) * (K - 1));
+        }
+    }
+}
+
 // Replay: state[dst] = the last K-1 entries of (state[src], values[j, 0..n))
 template <typename T, int K>
 __global__ void __launch_bounds__(NT) conv_replay_kernel(const ConvReplayParams p) {
@@ -392,6 +520,12 @@ template <typename T, int K>
 cudaError_t launch_conv_k(const ConvParams &p, cudaStream_t stream) {
     constexpr int V = Vec<T>::N;
     const int cgroups = p.C / V;
+    const long long seq_blocks = ((long long)p.B + SHORT_SEQS - 1) / SHORT_SEQS;
+    if (p.max_len_hint >= 1 && p.max_len_hint <= SHORT_MAX && seq_blocks <= 65535) {
+        dim3 grid((unsigned)((cgroups + SHORT_NT - 1) / SHORT_NT), (unsigned)seq_blocks);
+        conv_short_kernel<T, K><<<grid, SHORT_NT, 0, stream>>>(p);  // plain launch, as below
+        return cudaGetLastError();
+    }
     const int cblocks = (cgroups + NT - 1) / NT;
     if (p.T > 0) {
         dim3 grid((unsigned)((p.T + p.tokens_per_cta - 1) / p.tokens_per_cta), (unsigned)cblocks);

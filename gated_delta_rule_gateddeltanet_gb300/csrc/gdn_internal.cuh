@@ -67,6 +67,7 @@ struct ReplayParams {
 struct ConvParams {
     int B, T, C, K, num_slots, io_f16, silu, cap, tokens_per_cta;
     int skip_state_kernel;  // 1: no sequence straddles token blocks and the state is updated in place
+    int max_len_hint;       // the caller's bound on the longest sequence (0: unknown)
     long long x_stride;
     const void *x;
     const float *w, *bias;

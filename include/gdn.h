@@ -392,9 +392,10 @@ typedef struct gdn_conv_args {
     int32_t activation;            /* GDN_ACT_* */
     int32_t state_update_capacity; /* 0 = no capture */
     int32_t max_seqlen;            /* upper bound on the longest sequence, 0 = unknown.  A
-                                      performance hint: a bound of 1 (decode) with an
-                                      in-place state skips the state-rolling launch.
-                                      Results do not depend on it. */
+                                      performance hint: a bound of 1 to 8 (decode steps,
+                                      speculative drafts) runs one launch in which a thread
+                                      carries whole sequences.  Results do not depend on
+                                      it, bit for bit, even when a sequence exceeds it. */
     int64_t x_stride;
     const void *x;
     const float *weight;

@@ -99,10 +99,14 @@ def test_conv_qwen_geometry_decode_and_prefill():
     C = 10240
     x, w, bias, st, cu = _inputs(52, [1] * 64, C, 4, np.float16)
     want = _oracle(x, w, bias, st, cu, cap=1)
-    for hint in (0, 1):  # a max_seqlen hint of 1 skips the state-rolling launch
+    runs = []
+    for hint in (0, 1):  # a max_seqlen hint of 1 runs the short-sequence kernel (no state-rolling launch)
         got = _gpu(x, w, bias, st, cu, cap=1, max_seqlen=hint)
         assert max_rel(got[0], want[0]) <= 2e-3 and np.array_equal(got[1], want[1])
         assert np.array_equal(got[2], want[2])
+        runs.append(got)
+    for a, b in zip(*runs):  # the hint changes the launch shape, never a bit of the results
+        assert np.array_equal(a, b)
     lengths = wl.varlen_prefill_lengths()
     x, w, bias, st, cu = _inputs(53, lengths, C, 4, np.float16)
     got = _gpu(x, w, bias, st, cu)
@@ -151,3 +155,59 @@ def test_conv_status_flags():
     status.zero_()
     _gpu(x, w, bias, st, cu, slots=np.array([0, 7], np.int32), status=status)
     assert status.item() & gdn.DEVERR["state_slot"]
+
+
+@pytest.mark.parametrize("io", [np.float16, np.float32])
+@pytest.mark.parametrize("K", [4, 3, 2])
+@pytest.mark.parametrize("in_place", [True, False])
+def test_conv_short_sequences_kernel(io, K, in_place):
+    """max_seqlen hints of 1 .. 8 run one thread per (sequence pair, 4 channels):
+    ragged 0-8 token sequences (odd count, so the last pair is half empty),
+    scattered slots, per-request capture counts; results equal the oracle's and,
+    bit for bit, the token-block kernel's (hint 0)."""
+    lengths = [1, 0, 8, 3, 1, 5, 0, 2, 7, 4, 1]
+    S = 16
+    x, w, bias, st, cu = _inputs(70 + K, lengths, 520, K, io, num_slots=S)
+    slots = np.array([9, 2, 15, 0, 4, 11, 7, 3, 13, 6, 1], np.int32)
+    cap = 5
+    cc = np.array([1, 0, 5, 2, 1, 3, 0, 2, 4, 5, 0], np.int32)
+    want = _oracle(x, w, bias, st, cu, cap=cap, capture_count=cc, slots=slots)
+    tol = 2e-3 if io == np.float16 else 1e-5
+    runs = []
+    for hint in (8, 0):
+        got = _gpu(x, w, bias, st, cu, cap=cap, capture_count=cc, slots=slots, in_place=in_place, max_seqlen=hint)
+        assert max_rel(got[0], want[0]) <= tol
+        assert np.array_equal(got[1], want[1])  # written slots, and untouched ones
+        for s_, L in enumerate(lengths):
+            n = min(L, cap, cc[s_])
+            assert np.array_equal(got[2][s_, :n], want[2][s_, :n])
+            assert np.all(got[2][s_, n:] == 0)
+        runs.append(got)
+    for a, b in zip(*runs):
+        assert np.array_equal(a, b)
+
+
+def test_conv_short_kernel_zero_state_and_hint_exceeded():
+    """No initial state (zeros; empty sequences still get their zero state out of
+    place), and a hint that a sequence exceeds (a caller error): the short kernel
+    loads the rows past its prefetch and stays exact."""
+    lengths = [0, 2, 1, 13, 0, 6]
+    x, w, bias, _, cu = _inputs(80, lengths, 256, 4, np.float16, state=False)
+    want = _oracle(x, w, bias, None, cu, num_slots=6)
+    for hint in (2, 8):
+        got = _gpu(x, w, bias, None, cu, in_place=False, num_slots=6, max_seqlen=hint)
+        assert max_rel(got[0], want[0]) <= 2e-3
+        assert np.array_equal(got[1], want[1])
+        ref = _gpu(x, w, bias, None, cu, in_place=False, num_slots=6, max_seqlen=0)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+
+
+def test_conv_short_kernel_status_flags():
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    x, w, bias, st, cu = _inputs(81, [1, 1, 1], 64, 4, np.float32)
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    _gpu(x, w, bias, st, cu, cap=1, capture_count=np.array([1, 2, 0], np.int32), status=status, max_seqlen=1)
+    assert status.item() == gdn.DEVERR["capture_count"]
+    status.zero_()
+    _gpu(x, w, bias, st, cu, slots=np.array([0, 7, 1], np.int32), status=status, max_seqlen=1)
+    assert status.item() == gdn.DEVERR["state_slot"]
