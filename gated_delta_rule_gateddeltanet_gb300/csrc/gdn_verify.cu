@@ -273,6 +273,11 @@ __global__ void __launch_bounds__(NTV, 2)
     __shared__ __align__(8) uint64_t full_bar;
     __shared__ __align__(8) uint64_t mma_bar;
     __shared__ uint32_t tmem_base;
+    // the next item as thread 0 resolved it early (no final state: its copies start
+    // once the current item's products have read the rows)
+    __shared__ VCursor nx_cur_s;
+    __shared__ VRaw nx_seq_s;
+    __shared__ VItem nx_s;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
@@ -313,7 +318,8 @@ __global__ void __launch_bounds__(NTV, 2)
     };
     // thread 0 arms the barrier and copies the rows, thread STAGER copies the q, k, v rows
     // (a copy may complete before the barrier is armed: its bytes are counted all the same)
-    auto issue_load = [&](const VItem &it) {
+    // (with `one`, the caller is thread 0 alone and copies everything)
+    auto issue_load = [&](const VItem &it, bool one = false) {
         const uint32_t bytes = load_bytes(it);
         if (!bytes) return;
         if (tid == 0) {
@@ -326,7 +332,8 @@ __global__ void __launch_bounds__(NTV, 2)
                     for (int j = 0; j < 4; ++j) ptx::tma_load_2d(rows + j * (D * 128), &mp.in, 32 * j, it.row0, &full_bar);
                 }
             }
-        } else if (tid == STAGER && L::STAGE && mp.stg_ok && it.eos > it.bos) {
+        }
+        if ((one ? tid == 0 : tid == STAGER) && L::STAGE && mp.stg_ok && it.eos > it.bos) {
             TIO *st = reinterpret_cast<TIO *>(sm + L::STG);
             ptx::tma_load_2d(st, &mp.q, it.kh * D, it.bos, &full_bar);
             ptx::tma_load_2d(st + TB * D, &mp.k, it.kh * D, it.bos, &full_bar);
@@ -498,6 +505,7 @@ __global__ void __launch_bounds__(NTV, 2)
         if (loaded) {
             bad = !ptx::mbar_wait_bounded(&full_bar, full_phase, WAIT_LIMIT);
             full_phase ^= 1u;
+            loaded = false;  // (true again once the next item's copies are issued)
         }
         const int n = it.ok ? it.eos - it.bos : -1;
         if (it.ok && !p.init) {
@@ -508,6 +516,7 @@ __global__ void __launch_bounds__(NTV, 2)
                     *reinterpret_cast<float4 *>(rows + chunk_at(row, j, 4 * half + m)) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         bool tma_group = false;
+        bool early = false;  // the next item's copies are already on their way
 
         if (n >= 2) {
             // ================= tensor-core groups
@@ -566,6 +575,14 @@ __global__ void __launch_bounds__(NTV, 2)
                                 kn_s[tt][e];
                     }
                 }
+                // v of this row (both threads of the row form its deltas), read before the
+                // barrier so that the staged rows are free once the products are done
+                float vr[TB];
+#pragma unroll
+                for (int t = 0; t < TB; ++t)
+                    vr[t] = t >= nt ? 0.f
+                            : staged ? to_f32(stv[t * D + row])
+                                     : to_f32(vg[(long long)(t0 + t) * p.v_stride + (long long)it.h * D + row]);
                 __syncthreads();
 
                 // ---- every thread: its row's deltas from P and Q, outputs (half 0), then the
@@ -576,12 +593,31 @@ __global__ void __launch_bounds__(NTV, 2)
                 ptx::tc_fence_after();
                 const bool tg = mp.out_ok && last && nt == TB && (!p.caps || t0 - it.bos + TB <= p.cap);
                 tma_group = tg;
-                float vr[TB];  // both threads of the row form its deltas
-#pragma unroll
-                for (int t = 0; t < TB; ++t)
-                    vr[t] = t >= nt ? 0.f
-                            : staged ? to_f32(stv[t * D + row])
-                                     : to_f32(vg[(long long)(t0 + t) * p.v_stride + (long long)it.h * D + row]);
+                // Writing no final state, nothing reads this item's rows or staged q, k,
+                // v once its last group's products are done (every thread holds its v
+                // since the barrier above): thread 0 resolves the next item and starts
+                // its copies, which then overlap the deltas, the outputs and the item's
+                // end.  The other threads take the next item from shared memory after
+                // the item's last barrier; the next item's own barriers come before
+                // thread 0 writes the descriptor again.
+                early = last && !p.final_state;
+                if (early) {
+                    if (tid == 0 && !bad) {
+                        VCursor nc = cur_c;
+                        advance(p, nc);
+                        VRaw ns = seq;
+                        VItem nxe = no_item();
+                        if (i + 1 < stop) {
+                            if (nc.h == 0) ns = load_raw(p, nc.b);
+                            nxe = make_item(p, nc, ns);
+                        }
+                        nx_cur_s = nc;
+                        nx_seq_s = ns;
+                        nx_s = nxe;
+                        issue_load(nxe, true);
+                        loaded = load_bytes(nxe) != 0;  // in flight until the next item waits
+                    }
+                }
                 float d1[16], d1l[16];
                 ptx::tmem_ld16(tm + lane_sel + TM_D1, d1);
                 ptx::tmem_ld16(tm + lane_sel + TM_D1L, d1l);
@@ -800,12 +836,19 @@ __global__ void __launch_bounds__(NTV, 2)
             }
         }
 
-        // ---- the next item
-        advance(p, cur_c);
+        // ---- the next item (resolved by thread 0 already when `early`; the barrier
+        //      at the end of the item orders its shared-memory copy before these reads)
         VItem nx = no_item();
-        if (i + 1 < stop) {
-            if (cur_c.h == 0) seq = load_raw(p, cur_c.b);
-            nx = make_item(p, cur_c, seq);
+        if (early) {
+            cur_c = nx_cur_s;
+            seq = nx_seq_s;
+            nx = nx_s;
+        } else {
+            advance(p, cur_c);
+            if (i + 1 < stop) {
+                if (cur_c.h == 0) seq = load_raw(p, cur_c.b);
+                nx = make_item(p, cur_c, seq);
+            }
         }
         // ---- the item's output boxes and rows go back; then the buffer takes the next item
         if (tid == 0) {
@@ -827,7 +870,7 @@ __global__ void __launch_bounds__(NTV, 2)
             ptx::bulk_commit();
             if (rows_out) ptx::bulk_wait_read_all();  // the stores have read the buffer
         }
-        issue_load(nx);
+        if (!early) issue_load(nx);
         loaded = load_bytes(nx) != 0;
         it = nx;
         gc = load_gates(p, it);  // used once its copies have landed
