@@ -27,7 +27,7 @@ __all__ = ["gdn_forward", "ForwardCall", "gdn_forward_dense", "state_transpose",
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_DTYPE", 3: "GDN_ERR_SHAPE", 4: "GDN_ERR_ALIGN",
           5: "GDN_ERR_WORKSPACE", 6: "GDN_ERR_CUDA", 7: "GDN_ERR_UNSUPPORTED", 8: "GDN_ERR_ARG"}
 DEVERR = {"cu_seqlens": 0x1, "state_slot": 0x2, "accept_len": 0x4, "replay_slot": 0x8, "timeout": 0x10,
-          "capture_count": 0x20}
+          "capture_count": 0x20, "dup_slot": 0x40}
 ACTIVATION = {"none": 0, "silu": 1}
 PLAN = {"auto": 0, "recurrent": 1, "chunked": 2, "chunked_split": 3}
 DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}

@@ -151,6 +151,11 @@ gdn_status forward_impl(const gdn_forward_args *a, int dense_S, gdn_stream_t str
     const gdn_status st = resolve_forward(a, dense_S, &p);
     if (st != GDN_OK || a->num_seqs == 0) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+#ifdef GDN_DEBUG_CHECKS
+    if (p.final_state &&
+        gdn::debug_check_distinct_slots(p.slots, nullptr, p.B, p.num_slots, p.status, s) != cudaSuccess)
+        return GDN_ERR_CUDA;
+#endif
     bool chunked = wants_chunked(a);
     if (chunked && !chunked_aligned(a, p)) {
         if (forced_chunked(a)) return GDN_ERR_ALIGN;
@@ -266,6 +271,11 @@ gdn_status gdn_replay_prefix(float *state_banks, int32_t num_slots, int32_t num_
     p.n = accept_len;
     p.caps = state_update;
     p.status = status;
+#ifdef GDN_DEBUG_CHECKS
+    if (gdn::debug_check_distinct_slots(dst_slots, src_slots, num_requests, num_slots, status,
+                                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GDN_ERR_CUDA;
+#endif
     if (gdn::launch_replay(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
     return GDN_OK;
 }
@@ -321,6 +331,11 @@ gdn_status varlen_causal_conv_with_state(const gdn_conv_args *a, gdn_stream_t st
     // conv kernel writes their state itself; empty ones keep an in-place state.
     p.skip_state_kernel = a->max_seqlen == 1 && a->initial_state == a->final_state;
     p.max_len_hint = a->max_seqlen;
+#ifdef GDN_DEBUG_CHECKS
+    if (gdn::debug_check_distinct_slots(p.slots, nullptr, p.B, p.num_slots, p.status,
+                                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GDN_ERR_CUDA;
+#endif
     if (gdn::launch_conv(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
     return GDN_OK;
 }
@@ -352,6 +367,11 @@ gdn_status causal_conv_replay_prefix(void *conv_states, int32_t num_slots, int32
     p.dst = dst_slots;
     p.n = accept_len;
     p.status = status;
+#ifdef GDN_DEBUG_CHECKS
+    if (gdn::debug_check_distinct_slots(dst_slots, src_slots, num_requests, num_slots, status,
+                                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GDN_ERR_CUDA;
+#endif
     if (gdn::launch_conv_replay(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
     return GDN_OK;
 }

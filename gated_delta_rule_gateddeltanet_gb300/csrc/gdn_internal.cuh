@@ -86,6 +86,13 @@ struct ConvReplayParams {
 };
 
 cudaError_t launch_conv(const ConvParams &p, cudaStream_t stream);
+
+#ifdef GDN_DEBUG_CHECKS
+// Debug builds: GDN_DEVERR_DUP_SLOT when two of the n requests write the same
+// slot, or one writes a slot another reads (`read` may be null; see gdn_debug.cu).
+cudaError_t debug_check_distinct_slots(const int32_t *written, const int32_t *read, int n, int num_slots,
+                                       int32_t *status, cudaStream_t stream);
+#endif
 cudaError_t launch_conv_replay(const ConvReplayParams &p, cudaStream_t stream);
 
 // Spans of at most p.max_len tokens: the CUDA-core decode kernel when every

@@ -29,6 +29,11 @@
  *    work (a sequence or a request) and OR a GDN_DEVERR_* bit into the
  *    optional device word `status`; they never trap.  The caller zeroes that
  *    word and reads it when it chooses.
+ *  - Preconditions that cost a launch to check (the requests of one call use
+ *    distinct state slots) are checked only by the debug build of the library
+ *    (libgdn_debug.so, compiled with GDN_DEBUG_CHECKS): a small kernel ahead
+ *    of the call's work sets GDN_DEVERR_DUP_SLOT.  The release build assumes
+ *    them.
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -97,6 +102,10 @@ enum {
 #define GDN_DEVERR_REPLAY_SLOT 0x8 /* a replay source or destination slot out of range */
 #define GDN_DEVERR_TIMEOUT 0x10    /* a bounded wait inside a kernel gave up (the unit is not written) */
 #define GDN_DEVERR_CAPTURE_COUNT 0x20 /* conv: capture_count[b] outside [0, capacity] (nothing captured) */
+#define GDN_DEVERR_DUP_SLOT 0x40   /* debug builds only (GDN_DEBUG_CHECKS): two requests of one call
+                                      write the same state slot, or a replay writes a slot that
+                                      another request of the call reads; the release build does
+                                      not check this precondition (results are then undefined) */
 
 /*
  * Arguments of gdn_forward.

@@ -41,6 +41,17 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, n)
 
 
+def test_debug_library_builds_and_exports_every_declared_symbol(lib):
+    """libgdn_debug.so (the precondition checks of GDN_DEBUG_CHECKS) builds
+    from the same sources and exports the same entry points."""
+    from gated_delta_rule_gateddeltanet_gb300 import build
+    path = build.build(debug=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for n in declared_functions():
+        assert n in exported, n
+
+
 def test_forward_args_layout_matches_c(tmp_path):
     import gated_delta_rule_gateddeltanet_gb300 as g
     fields = [f for f, _ in g.ForwardArgs._fields_]
