@@ -878,7 +878,7 @@ def run_spec_step(dev, stream):
         torch.cuda.synchronize()
         res[name] = round(e0.elapsed_time(e1) / n * 1e3, 2)
     res["workload"] = ("speculative step of one layer: 16 requests x 4 drafts, conv (10240 channels, capture) + "
-                       "gdn_forward (capsules) + conv replay (on a side stream, overlapping gdn_forward) + GDN replay of "
+                       "gdn_forward (capsules) + conv replay (on a side stream, overlapping the GDN replay) + GDN replay of "
                        "U{0..4} accepted tokens; 4 launches eager (prebuilt C-ABI arguments) vs one CUDA-graph replay")
     res["tokens_per_s_graph"] = round(R * D / (res["graph_us"] / 1e6), 1)
     return res

@@ -24,8 +24,11 @@ CUDA graph:
      the inactive slots ``dst`` of both banks.
 
 The conv replay needs only the conv call's capture, so it runs on a side
-stream while the GDN forward (latency-bound, HBM mostly idle) runs on the
-main one; the main stream waits for it at the end of the step.
+stream beside the GDN replay; the main stream waits for it at the end of the
+step.  It forks after the GDN forward rather than before it: the verify
+kernel runs two register-heavy CTAs per SM, and conv-replay CTAs resident
+beside it delayed their placement (the step took 41.0 µs with the fork
+before the forward, 39.1 µs with it after).
 
 Every per-step quantity is device memory read at replay time (inputs, gate
 inputs, slot lists, accepted lengths), so one graph serves every step: the
@@ -114,7 +117,7 @@ class SpeculativeStep:
 
     def run_eager(self, stream=None):
         """The four calls on ``stream`` (default: current), the conv replay
-        forked onto a side stream after the conv call and joined at the end."""
+        forked onto a side stream after the GDN forward and joined at the end."""
         main = stream if stream is not None else torch.cuda.current_stream(self.dev)
         s = ctypes.c_void_p(main.cuda_stream)
         lib = self.lib
@@ -122,6 +125,11 @@ class SpeculativeStep:
         rc = lib.varlen_causal_conv_with_state(ctypes.byref(self.conv_args), s)
         if rc:
             raise GdnError(rc, "varlen_causal_conv_with_state")
+        rc = lib.gdn_forward(ctypes.byref(self.fwd_args), s)
+        if rc:
+            raise GdnError(rc, "gdn_forward")
+        # the conv replay forks here, beside the GDN replay: beside the verify its CTAs
+        # would take SM room the verify's two register-heavy CTAs per SM need
         self._conv_done.record(main)
         self._side.wait_event(self._conv_done)
         two_r, C, km1 = self.conv_bank.shape
@@ -131,9 +139,6 @@ class SpeculativeStep:
         if rc:
             raise GdnError(rc, "causal_conv_replay_prefix")
         self._side_done.record(self._side)
-        rc = lib.gdn_forward(ctypes.byref(self.fwd_args), s)
-        if rc:
-            raise GdnError(rc, "gdn_forward")
         rc = lib.gdn_replay_prefix(p(self.gdn_bank), two_r, self.R, self.Hk, self.Hv, self.d, self.d, p(self.src),
                                    p(self.dst), p(self.capsules), self.D, p(self.accept_len), p(self.status), s)
         if rc:
