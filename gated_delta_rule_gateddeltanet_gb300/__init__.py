@@ -137,6 +137,8 @@ def _token_stride(t, name, inner):
     dims are contiguous (allows slices of a fused qkv projection)."""
     if t.dim() != 3:
         raise ValueError(f"{name} must be [T, H, d]")
+    if t.numel() == 0:  # no tokens (every sequence empty): nothing is read, any strides do
+        return inner
     if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
         raise ValueError(f"{name}: heads and channels must be contiguous inside a token")
     return t.stride(0) if t.shape[0] > 1 else inner
@@ -379,7 +381,7 @@ def build_conv_args(x, weight, cu_seqlens, *, bias=None, initial_state=None, fin
     B = cu_seqlens.shape[0] - 1
     if x.dtype not in DTYPE:
         raise TypeError(f"unsupported dtype {x.dtype}")
-    if x.stride(1) != 1:
+    if x.numel() > 0 and x.stride(1) != 1:  # (no tokens: nothing is read)
         raise ValueError("x: channels must be contiguous")
     _check(weight, "weight", dtype=torch.float32, device=dev)
     _check(bias, "bias", dtype=torch.float32, device=dev)

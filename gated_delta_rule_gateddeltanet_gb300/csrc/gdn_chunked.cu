@@ -708,7 +708,7 @@ int num_sms() { return current_device_sms(); }
 template <typename TIO>
 cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStream_t stream) {
     CUtensorMap mq{}, mk{}, mv{};
-    if (sizeof(TIO) == 2) {
+    if (sizeof(TIO) == 2 && p.T > 0) {  // (no tokens: no chunk reads q, k or v)
         if (!encode_rows_f16(&mq, p.q, (long long)p.Hk * DH, p.q_stride, p.T, DH, CH, false) ||
             !encode_rows_f16(&mk, p.k, (long long)p.Hk * DH, p.k_stride, p.T, DH, CH, false) ||
             !encode_rows_f16(&mv, p.v, (long long)p.Hv * DH, p.v_stride, p.T, DH, CH, false))

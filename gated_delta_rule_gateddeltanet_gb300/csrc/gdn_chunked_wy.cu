@@ -1425,7 +1425,7 @@ int num_sms() { return current_device_sms(); }
 template <typename TIO>
 cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *ws, cudaStream_t stream) {
     CUtensorMap mq{}, mk{}, mv{};
-    if (sizeof(TIO) == 2) {
+    if (sizeof(TIO) == 2 && p.T > 0) {  // (no tokens: no chunk reads q, k or v)
         // q, k: 64-token x 64-feature boxes in the 128-byte swizzle of the MMA operand tiles;
         // v: 64-token x 128-feature rows as they are
         if (!encode_rows_f16(&mq, p.q, (long long)p.Hk * p.dk, p.q_stride, p.T, 64, CH, true) ||

@@ -211,3 +211,13 @@ def test_conv_short_kernel_status_flags():
     status.zero_()
     _gpu(x, w, bias, st, cu, slots=np.array([0, 7, 1], np.int32), status=status, max_seqlen=1)
     assert status.item() == gdn.DEVERR["state_slot"]
+
+
+@pytest.mark.parametrize("hint", [0, 1])
+def test_conv_all_empty_batch(hint):
+    """Every sequence empty (T = 0): no outputs, states kept (copied out of place)."""
+    x, w, bias, st, cu = _inputs(82, [0, 0, 0], 64, 4, np.float16)
+    for in_place in (True, False):
+        got = _gpu(x, w, bias, st, cu, in_place=in_place, max_seqlen=hint)
+        assert got[0].shape[0] == 0
+        assert np.array_equal(got[1], st.astype(np.float64))
