@@ -132,6 +132,14 @@ def _check(t, name, dtype=None, device=None, contiguous=True):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _shape(t, name, shape):
+    """Raise unless ``t`` (if given) has exactly ``shape``: the C ABI takes raw
+    pointers, so the binding is where a buffer's extent is checked against the
+    call's geometry, before any launch."""
+    if t is not None and tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError(f"{name} must have shape {tuple(int(x) for x in shape)}, got {tuple(t.shape)}")
+
+
 def _token_stride(t, name, inner):
     """Elements between consecutive tokens of a [T, H, d] view whose inner two
     dims are contiguous (allows slices of a fused qkv projection)."""
@@ -166,6 +174,18 @@ def build_forward_args(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, g
     _check(cu_seqlens, "cu_seqlens", dtype=torch.int32, device=dev)
     _check(state_slots, "state_slots", dtype=torch.int32, device=dev)
     _check(status, "status", dtype=torch.int32, device=dev)
+    if cu_seqlens is not None and cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be one-dimensional [B + 1]")
+    _shape(k, "k", (T, Hk, dk))
+    if v.dim() != 3 or v.shape[0] != T:
+        raise ValueError(f"v must be [T = {T}, Hv, dv], got {tuple(v.shape)}")
+    _shape(a, "a", (T, Hv))
+    _shape(b, "b", (T, Hv))
+    _shape(A_log, "A_log", (Hv,))
+    _shape(dt_bias, "dt_bias", (Hv,))
+    _shape(state_slots, "state_slots", (B,))
+    if status is not None and status.numel() < 1:
+        raise ValueError("status must hold one int32")
     if num_state_slots is None:
         if initial_state is not None:
             num_state_slots = initial_state.shape[0]
@@ -182,13 +202,18 @@ def build_forward_args(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, g
             final_state.copy_(initial_state)
     _check(initial_state, "initial_state", dtype=torch.float32, device=dev)
     _check(final_state, "final_state", dtype=torch.float32, device=dev)
+    _shape(initial_state, "initial_state", (num_state_slots, Hv, dv, dk))
+    _shape(final_state, "final_state", (num_state_slots, Hv, dv, dk))
     if output is None:
         output = torch.empty((T, Hv, dv), dtype=q.dtype, device=dev)
     _check(output, "output", dtype=q.dtype, device=dev)
+    _shape(output, "output", (T, Hv, dv))
     W = capsule_width(Hk, Hv, dk, dv)
     if capacity > 0 and state_update is None:
         state_update = torch.zeros((B, capacity, W), dtype=torch.float32, device=dev)
     _check(state_update, "state_update", dtype=torch.float32, device=dev)
+    if capacity > 0:
+        _shape(state_update, "state_update", (B, capacity, W))
 
     args = ForwardArgs()
     args.num_seqs, args.total_tokens, args.num_k_heads, args.num_v_heads = B, T, Hk, Hv
@@ -361,8 +386,12 @@ def gdn_replay_prefix(state_banks, src_slots, dst_slots, state_update, accept_le
                     ("status", status)):
         _check(t, name, dtype=torch.int32, device=dev)
     _check(state_update, "state_update", dtype=torch.float32, device=dev)
-    if state_update is not None and state_update.shape[2] != capsule_width(num_k_heads, Hv, dk, dv):
-        raise ValueError("state_update row width does not match the state geometry")
+    if src_slots.dim() != 1:
+        raise ValueError("src_slots must be one-dimensional [R]")
+    _shape(dst_slots, "dst_slots", (R,))
+    _shape(accept_len, "accept_len", (R,))
+    if state_update is not None:
+        _shape(state_update, "state_update", (R, cap, capsule_width(num_k_heads, Hv, dk, dv)))
     rc = lib.gdn_replay_prefix(_ptr(state_banks), S, R, int(num_k_heads), Hv, dk, dv, _ptr(src_slots),
                                _ptr(dst_slots), _ptr(state_update), cap, _ptr(accept_len), _ptr(status),
                                _stream_handle(dev))
@@ -388,6 +417,12 @@ def build_conv_args(x, weight, cu_seqlens, *, bias=None, initial_state=None, fin
     for name, t in (("cu_seqlens", cu_seqlens), ("state_slots", state_slots), ("capture_count", capture_count),
                     ("status", status)):
         _check(t, name, dtype=torch.int32, device=dev)
+    if cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be one-dimensional [B + 1]")
+    _shape(weight, "weight", (C, K))
+    _shape(bias, "bias", (C,))
+    _shape(state_slots, "state_slots", (B,))
+    _shape(capture_count, "capture_count", (B,))
     if num_state_slots is None:
         src = initial_state if initial_state is not None else final_state
         num_state_slots = src.shape[0] if src is not None else B
@@ -402,6 +437,11 @@ def build_conv_args(x, weight, cu_seqlens, *, bias=None, initial_state=None, fin
         state_update = torch.zeros((B, capacity, C), dtype=x.dtype, device=dev)
     _check(output, "output", dtype=x.dtype, device=dev)
     _check(state_update, "state_update", dtype=x.dtype, device=dev)
+    _shape(initial_state, "initial_state", (num_state_slots, C, K - 1))
+    _shape(final_state, "final_state", (num_state_slots, C, K - 1))
+    _shape(output, "output", (T, C))
+    if capacity > 0:
+        _shape(state_update, "state_update", (B, capacity, C))
     a = ConvArgs()
     a.num_seqs, a.total_tokens, a.channels, a.kernel_size = B, T, C, K
     a.num_state_slots, a.io_dtype = int(num_state_slots), DTYPE[x.dtype]
@@ -444,6 +484,13 @@ def causal_conv_replay_prefix(conv_states, src_slots, dst_slots, state_update, a
                     ("status", status)):
         _check(t, name, dtype=torch.int32, device=dev)
     cap = state_update.shape[1] if state_update is not None else 0
+    R = src_slots.shape[0]
+    if src_slots.dim() != 1:
+        raise ValueError("src_slots must be one-dimensional [R]")
+    _shape(dst_slots, "dst_slots", (R,))
+    _shape(accept_len, "accept_len", (R,))
+    if state_update is not None:
+        _shape(state_update, "state_update", (R, cap, C))
     rc = lib.causal_conv_replay_prefix(_ptr(conv_states), S, src_slots.shape[0], C, Km1 + 1, DTYPE[conv_states.dtype],
                                        _ptr(src_slots), _ptr(dst_slots), _ptr(state_update), cap, _ptr(accept_len),
                                        _ptr(status), _stream_handle(dev))

@@ -120,3 +120,151 @@ def test_all_empty_batch(plan, d, in_place):
     out, final, caps = run_gpu(inp, plan=plan, in_place=in_place)
     assert out.shape[0] == 0
     assert np.array_equal(final, inp.initial_state.astype(np.float64))
+
+
+# ---------------------------------------------------------------- prefix replay
+
+def _replay_case(i):
+    rng = np.random.default_rng(7000 + i)
+    dk = int(rng.choice([32, 64, 128]))
+    dv = dk if rng.random() < 0.6 else int(rng.choice([32, 64, 128]))
+    Hk = int(rng.choice([1, 2, 4]))
+    Hv = Hk * int(rng.choice([1, 2, 3]))
+    R = int(rng.integers(1, 9))
+    cap = int(rng.integers(1, 7))
+    S = 2 * R + 1 + int(rng.integers(0, 4))  # room for R + 1 candidate sources and R destinations
+    perm = rng.permutation(S)
+    src = rng.choice(perm[:R + 1], size=R).astype(np.int32)  # sources may repeat (read only)
+    dst = perm[R + 1:2 * R + 1].astype(np.int32)  # distinct, never another request's source
+    for j in range(R):
+        if rng.random() < 0.2:
+            dst[j] = src[j]  # in-place replay of a request onto its own source
+    if len(set(dst.tolist())) < R or any(dst[j] in np.delete(src, j) for j in range(R)):
+        dst = perm[R + 1:2 * R + 1].astype(np.int32)
+    n = rng.integers(0, cap + 1, size=R).astype(np.int32)
+    return dict(seed=7100 + i, dk=dk, dv=dv, Hk=Hk, Hv=Hv, R=R, cap=cap, S=S, src=src, dst=dst, n=n)
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_replay_matches_oracle(i):
+    """Random head sizes, GQA ratios, request counts, capacities, accepted
+    lengths (0 = copy) and slot layouts (sources shared, in-place replays);
+    FP32-level (1e-5) on the written slots, every other slot bit for bit."""
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    import oracle as orc
+    c = _replay_case(i)
+    rng = np.random.default_rng(c["seed"])
+    banks = (rng.standard_normal((c["S"], c["Hv"], c["dv"], c["dk"])) * 0.02).astype(np.float32)
+    W = gdn.capsule_width(c["Hk"], c["Hv"], c["dk"], c["dv"])
+    caps = np.empty((c["R"], c["cap"], W), np.float32)
+    caps[:, :, :c["Hv"]] = rng.uniform(0.5, 1.0, size=(c["R"], c["cap"], c["Hv"]))
+    caps[:, :, c["Hv"]:c["Hv"] + c["Hk"] * c["dk"]] = rng.standard_normal((c["R"], c["cap"], c["Hk"] * c["dk"])) / np.sqrt(c["dk"])
+    caps[:, :, c["Hv"] + c["Hk"] * c["dk"]:] = rng.standard_normal((c["R"], c["cap"], c["Hv"] * c["dv"])) * 0.1
+    want = orc.gdn_replay(banks, c["src"], c["dst"], caps, c["n"], num_k_heads=c["Hk"])
+    got_t = torch.from_numpy(banks.copy()).to(dev())
+    gdn.gdn_replay_prefix(got_t, torch.from_numpy(c["src"]).to(dev()), torch.from_numpy(c["dst"]).to(dev()),
+                          torch.from_numpy(caps).to(dev()), torch.from_numpy(c["n"]).to(dev()), num_k_heads=c["Hk"])
+    torch.cuda.synchronize()
+    got = got_t.double().cpu().numpy()
+    for j, d in enumerate(c["dst"]):
+        assert max_rel(got[d], want[d]) <= 1e-5, (j, max_rel(got[d], want[d]))
+    others = np.setdiff1d(np.arange(c["S"]), c["dst"])
+    assert np.array_equal(got[others], banks[others].astype(np.float64))
+
+
+# ---------------------------------------------------------------- causal conv and its replay
+
+def _conv_case(i):
+    rng = np.random.default_rng(8000 + i)
+    io = np.float16 if rng.random() < 0.6 else np.float32
+    C = int(rng.choice([8, 64, 520, 1032]))
+    K = int(rng.choice([2, 3, 4]))
+    B = int(rng.integers(1, 10))
+    kinds = rng.choice(["empty", "one", "short", "long"], size=B, p=[0.1, 0.35, 0.35, 0.2])
+    span = {"empty": (0, 1), "one": (1, 2), "short": (2, 9), "long": (9, 150)}
+    lengths = [int(rng.integers(*span[k])) for k in kinds]
+    longest = max(lengths)
+    hint = int(rng.choice([0, max(longest, 1), 8, max(longest, 1) + int(rng.integers(0, 5))]))
+    if hint and hint < longest:
+        hint = longest
+    S = B + int(rng.integers(0, 4))
+    slots = rng.permutation(S)[:B].astype(np.int32)
+    cap = int(rng.choice([0, 1, 3, 6]))
+    cc = rng.integers(0, cap + 1, size=B).astype(np.int32) if (cap and rng.random() < 0.5) else None
+    return dict(seed=8100 + i, io=io, C=C, K=K, lengths=lengths, hint=hint, S=S, slots=slots, cap=cap, cc=cc,
+                in_place=bool(rng.random() < 0.5), state=bool(rng.random() < 0.8), bias=bool(rng.random() < 0.7))
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_conv_matches_oracle(i):
+    """Random channel counts, kernel sizes, ragged batches, max_seqlen hints
+    (0, exact, 8, above), scattered slots, capture capacities and counts, in
+    place or not, with or without an initial state and bias: outputs at 2e-3
+    (fp16) / 1e-5 (FP32), states and captured inputs bit for bit, untouched
+    slots and capture rows unchanged."""
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    import oracle as orc
+    c = _conv_case(i)
+    rng = np.random.default_rng(c["seed"])
+    T = sum(c["lengths"])
+    x = rng.standard_normal((T, c["C"])).astype(c["io"])
+    w = (rng.standard_normal((c["C"], c["K"])) / 2).astype(np.float32)
+    bias = (rng.standard_normal(c["C"]) / 4).astype(np.float32) if c["bias"] else None
+    st = rng.standard_normal((c["S"], c["C"], c["K"] - 1)).astype(c["io"]) if c["state"] else None
+    cu = np.concatenate([[0], np.cumsum(c["lengths"])]).astype(np.int32)
+    st0 = st if st is not None else np.zeros((c["S"], c["C"], c["K"] - 1))
+    want = orc.conv_forward(x, w, cu, st0, bias=bias, state_slots=c["slots"], capacity=c["cap"],
+                            capture_count=c["cc"])
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    tdt = torch.float16 if c["io"] == np.float16 else torch.float32
+    init = t(st)
+    if c["in_place"] and init is not None:
+        final = init
+    else:
+        final = t(st0.astype(c["io"])) if st is None else init.clone()
+        if st is None:
+            final.fill_(float("nan"))  # only the named slots must be written
+    vals = torch.zeros((len(c["lengths"]), max(c["cap"], 1), c["C"]), dtype=tdt, device=dev()) if c["cap"] else None
+    out, fin, cap_out = gdn.varlen_causal_conv_with_state(
+        t(x), t(w), t(cu), bias=t(bias), initial_state=init, final_state=final, state_slots=t(c["slots"]),
+        capture_count=t(c["cc"]), capacity=c["cap"], state_update=vals, num_state_slots=c["S"], max_seqlen=c["hint"])
+    torch.cuda.synchronize()
+    tol = 2e-3 if c["io"] == np.float16 else 1e-5
+    assert max_rel(out.double().cpu().numpy(), want[0]) <= tol
+    fin = fin.double().cpu().numpy()
+    assert np.array_equal(fin[c["slots"]], want[1][c["slots"]])
+    others = np.setdiff1d(np.arange(c["S"]), c["slots"])
+    if st is not None and others.size:
+        assert np.array_equal(fin[others], st[others].astype(np.float64))
+    if c["cap"]:
+        got_v = cap_out.double().cpu().numpy()
+        for s_, L in enumerate(c["lengths"]):
+            m = min(L, c["cap"], c["cc"][s_] if c["cc"] is not None else c["cap"])
+            assert np.array_equal(got_v[s_, :m], want[2][s_, :m])
+            assert np.all(got_v[s_, m:] == 0)
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_random_conv_replay_matches_oracle(i):
+    """Random channel counts, kernel sizes, request counts and accepted lengths:
+    the replayed states equal the oracle's bit for bit, sources untouched."""
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    import oracle as orc
+    rng = np.random.default_rng(8500 + i)
+    io = np.float16 if i % 2 == 0 else np.float32
+    C = int(rng.choice([8, 64, 520])) if io == np.float16 else int(rng.choice([4, 64, 516]))
+    K = int(rng.choice([2, 3, 4]))
+    R = int(rng.integers(1, 9))
+    cap = int(rng.integers(1, 7))
+    S = 2 * R + 1
+    perm = rng.permutation(S)
+    src, dst = perm[:R].astype(np.int32), perm[R:2 * R].astype(np.int32)
+    n = rng.integers(0, cap + 1, size=R).astype(np.int32)
+    states = rng.standard_normal((S, C, K - 1)).astype(io)
+    vals = rng.standard_normal((R, cap, C)).astype(io)
+    want = orc.conv_replay(states, src, dst, vals, n)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    st_t = t(states)
+    gdn.causal_conv_replay_prefix(st_t, t(src), t(dst), t(vals), t(n))
+    torch.cuda.synchronize()
+    assert np.array_equal(st_t.double().cpu().numpy(), want)
