@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(NT, 1)
 // (the recurrent kernel reports them).
 constexpr int PLAN_BINS = 1024;
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *cu, int dense_S, int B, int T, int min_len,
-                                                    int32_t *ws) {
+                                                    int32_t *ws, int32_t *status) {
     dependent_prologue();
     __shared__ int hist[PLAN_BINS];
     __shared__ int total;
@@ -678,7 +678,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *cu, int dense
         const int chunks = min((hi - lo + CH - 1) / CH, PLAN_BINS - 1);
         return PLAN_BINS - 1 - chunks;  // descending length
     };
+    // a packing error is flagged here too: under the forced chunked plan no other
+    // kernel sees the batch
+    if (tid == 0 && cu && (cu[0] != 0 || cu[B] != T)) flag_error(status, GDN_DEVERR_CU_SEQLENS);
     for (int b = tid; b < B; b += blockDim.x) {
+        const int lo = seq_start(cu, dense_S, b), hi = seq_start(cu, dense_S, b + 1);
+        if (lo < 0 || hi < lo || hi > T) flag_error(status, GDN_DEVERR_CU_SEQLENS);
         const int k = key(b);
         if (k >= 0) atomicAdd(&hist[k], 1);
     }
@@ -714,7 +719,8 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, int32_t *ws, cudaStre
             !encode_rows_f16(&mv, p.v, (long long)p.Hv * DH, p.v_stride, p.T, DH, CH, false))
             return cudaErrorInvalidValue;
     }
-    cudaError_t e = launch_dependent(plan_kernel, dim3(1), dim3(1024), 0, stream, p.cu, p.dense_S, p.B, p.T, min_len, ws);
+    cudaError_t e =
+        launch_dependent(plan_kernel, dim3(1), dim3(1024), 0, stream, p.cu, p.dense_S, p.B, p.T, min_len, ws, p.status);
     if (e != cudaSuccess) return e;
     auto kern = chunked_kernel<TIO>;
     constexpr int smem = SMEM_ALLOC;

@@ -179,7 +179,7 @@ __device__ long long scan_sequences(int B, V value, P put, long long *wsum) {
 // only when the tokens it captures (the first `cap`) all lie in its first
 // segment, which runs from the true state and so yields the exact deltas.
 __global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int dense_S, int B, int T, int min_len,
-                                                          bool split, int cap, int32_t *ws) {
+                                                          bool split, int cap, int32_t *ws, int32_t *status) {
     dependent_prologue();
     __shared__ int hist[PLAN_BINS];
     __shared__ long long wsum[PLAN_NT / 32];
@@ -196,7 +196,12 @@ __global__ void __launch_bounds__(PLAN_NT) wy_plan_kernel(const int32_t *cu, int
     auto bin = [&](int c) { return PLAN_BINS - 1 - min(c, PLAN_BINS - 1); };
     for (int i = tid; i < PLAN_BINS; i += PLAN_NT) hist[i] = 0;
     __syncthreads();
+    // a packing error is flagged here too: under the forced chunked plans no other
+    // kernel sees the batch
+    if (tid == 0 && cu && (cu[0] != 0 || cu[B] != T)) flag_error(status, GDN_DEVERR_CU_SEQLENS);
     for (int b = tid; b < B; b += PLAN_NT) {
+        const int lo = seq_start(cu, dense_S, b), hi = seq_start(cu, dense_S, b + 1);
+        if (lo < 0 || hi < lo || hi > T) flag_error(status, GDN_DEVERR_CU_SEQLENS);
         const int c = chunks_of(b);
         if (c < 0) continue;
         if (is_split(c)) {
@@ -1444,7 +1449,7 @@ cudaError_t launch_io(const ForwardParams &p, int min_len, bool split, uint8_t *
                                        (size_t)nsplit * 3 * p.Hv * STATE_BYTES);
     const long long oid_rows = max_split_rows(p.T);
     cudaError_t e = launch_dependent(wy_plan_kernel, dim3(1), dim3(PLAN_NT), 0, stream, p.cu, p.dense_S, p.B, p.T,
-                                     min_len, nsplit > 0, p.cap, hdr);
+                                     min_len, nsplit > 0, p.cap, hdr, p.status);
     if (e != cudaSuccess) return e;
     const long long prep_ctas = maxch * p.Hk;
     if (prep_ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

@@ -268,3 +268,50 @@ def test_random_conv_replay_matches_oracle(i):
     gdn.causal_conv_replay_prefix(st_t, t(src), t(dst), t(vals), t(n))
     torch.cuda.synchronize()
     assert np.array_equal(st_t.double().cpu().numpy(), want)
+
+
+# ---------------------------------------------------------------- device status on every path
+
+STATUS_PATHS = {
+    "decode": dict(lengths=[1, 1, 1], d=128, plan="auto"),
+    "verify": dict(lengths=[4, 3, 6], d=128, plan="recurrent"),
+    "mixed": dict(lengths=[4, 3, 6], d=64, plan="recurrent"),
+    "two_phase": dict(lengths=[80, 70, 40], d=128, plan="chunked"),
+    "single_kernel": dict(lengths=[80, 70, 40], d=128, plan="chunked", single=True),
+    "split": dict(lengths=[2100, 70, 40], d=128, plan="chunked_split"),
+}
+
+
+@pytest.mark.parametrize("path", list(STATUS_PATHS))
+def test_status_flags_skip_only_the_bad_sequence(path):
+    """A sequence whose slot is out of range, or whose cu_seqlens entries run
+    backwards, sets its status bit and is skipped: its slot keeps the initial
+    state and the other sequences' states are those of the valid call, bit
+    for bit (each chain is evaluated alone)."""
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    from gpu_common import single_kernel_workspace
+    spec = STATUS_PATHS[path]
+    d = spec["d"]
+    inp = wl.make_inputs(6500, spec["lengths"], Hk=1, Hv=2, dk=d, dv=d, io_dtype=np.float16, state_std=0.02,
+                         num_slots=4, state_slots=[0, 1, 2])
+    ws = (lambda x: single_kernel_workspace(x)) if spec.get("single") else (lambda x: None)
+    _, good, _ = run_gpu(inp, plan=spec["plan"], in_place=False, workspace=ws(inp))
+    init = inp.initial_state.astype(np.float64)
+
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    bad_slot = wl.GdnInputs(inp.q, inp.k, inp.v, inp.a, inp.b, inp.A_log, inp.dt_bias, inp.cu_seqlens,
+                            inp.initial_state, np.array([0, 9, 2], np.int32))
+    _, fin, _ = run_gpu(bad_slot, plan=spec["plan"], in_place=False, status=status, workspace=ws(bad_slot))
+    assert status.item() == gdn.DEVERR["state_slot"]
+    assert np.array_equal(fin[0], good[0]) and np.array_equal(fin[2], good[2])
+    assert np.array_equal(fin[1], init[1]) and np.array_equal(fin[3], init[3])
+
+    status.zero_()
+    cu = inp.cu_seqlens.copy()
+    cu[2] = cu[1] - 1  # sequence 1 ends before it starts; sequence 2 starts one token early
+    bad_cu = wl.GdnInputs(inp.q, inp.k, inp.v, inp.a, inp.b, inp.A_log, inp.dt_bias, cu, inp.initial_state,
+                          inp.state_slots)
+    _, fin, _ = run_gpu(bad_cu, plan=spec["plan"], in_place=False, status=status, workspace=ws(bad_cu))
+    assert status.item() & gdn.DEVERR["cu_seqlens"]
+    assert np.array_equal(fin[0], good[0])
+    assert np.array_equal(fin[1], init[1])
