@@ -322,7 +322,12 @@ __global__ void __launch_bounds__(NT) conv_state_kernel(const ConvParams p) {
     if (cg >= p.C / V) return;
     const int bos = p.cu[b], eos = p.cu[b + 1];
     const int slot = p.slots ? p.slots[b] : b;
-    if (bos < 0 || eos < bos || eos > p.T || slot < 0 || slot >= p.num_slots) return;  // flagged by conv_kernel
+    if (bos < 0 || eos < bos || eos > p.T || slot < 0 || slot >= p.num_slots) {
+        // flagged here as well: conv_kernel only sees sequences that own tokens
+        if (blockIdx.x == 0 && threadIdx.x == 0)
+            flag_error(p.status, slot < 0 || slot >= p.num_slots ? GDN_DEVERR_STATE_SLOT : GDN_DEVERR_CU_SEQLENS);
+        return;
+    }
     if (eos > bos && bos / p.tokens_per_cta == (eos - 1) / p.tokens_per_cta) return;  // written by conv_kernel
     const int c0 = cg * V;
     const T *x = static_cast<const T *>(p.x);

@@ -221,3 +221,52 @@ def test_conv_all_empty_batch(hint):
         got = _gpu(x, w, bias, st, cu, in_place=in_place, max_seqlen=hint)
         assert got[0].shape[0] == 0
         assert np.array_equal(got[1], st.astype(np.float64))
+
+
+@pytest.mark.parametrize("hint", [0, 4])
+def test_conv_bad_sequence_flagged_and_skipped(hint):
+    """A backwards cu_seqlens entry: the bit is set, that sequence's slot keeps
+    its state, and the valid sequences match the valid call bit for bit (token-
+    block kernel and short-sequence kernel)."""
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    x, w, bias, st, cu = _inputs(83, [3, 2, 4], 64, 4, np.float16)
+    good = _gpu(x, w, bias, st, cu, in_place=False, max_seqlen=hint)
+    bad_cu = cu.copy()
+    bad_cu[2] = bad_cu[1] - 1  # sequence 1 ends before it starts
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    got = _gpu(x, w, bias, st, bad_cu, in_place=False, status=status, max_seqlen=hint)
+    assert status.item() & gdn.DEVERR["cu_seqlens"]
+    assert np.array_equal(got[1][0], good[1][0])
+    assert np.array_equal(got[1][1], st[1].astype(np.float64))
+
+
+def test_conv_replay_status_flags():
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    rng = np.random.default_rng(84)
+    C, K = 64, 4
+    states = to_dev(rng.standard_normal((4, C, K - 1)).astype(np.float16))
+    before = states.clone()
+    vals = to_dev(rng.standard_normal((2, 3, C)).astype(np.float16))
+    i32 = lambda *v: to_dev(np.array(v, np.int32))
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    gdn.causal_conv_replay_prefix(states, i32(0, 1), i32(2, 3), vals, i32(4, 1), status=status)  # n > capacity
+    torch.cuda.synchronize()
+    assert status.item() == gdn.DEVERR["accept_len"]
+    assert torch.equal(states[2], before[2])  # the bad request is skipped
+    status.zero_()
+    before = states.clone()
+    gdn.causal_conv_replay_prefix(states, i32(0, 7), i32(2, 3), vals, i32(1, 1), status=status)  # source out of range
+    torch.cuda.synchronize()
+    assert status.item() == gdn.DEVERR["replay_slot"]
+    assert torch.equal(states[3], before[3])
+
+
+@pytest.mark.parametrize("hint", [0, 2])
+def test_conv_empty_sequence_with_bad_slot_flagged(hint):
+    """An empty sequence (no tokens for the token-block kernel to visit) whose
+    slot is out of range still sets the bit."""
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    x, w, bias, st, cu = _inputs(85, [2, 0, 2], 64, 4, np.float16)
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    _gpu(x, w, bias, st, cu, slots=np.array([0, 7, 2], np.int32), in_place=False, status=status, max_seqlen=hint)
+    assert status.item() == gdn.DEVERR["state_slot"]
