@@ -315,3 +315,20 @@ def test_status_flags_skip_only_the_bad_sequence(path):
     assert status.item() & gdn.DEVERR["cu_seqlens"]
     assert np.array_equal(fin[0], good[0])
     assert np.array_equal(fin[1], init[1])
+
+
+@pytest.mark.parametrize("path", list(STATUS_PATHS))
+def test_empty_sequence_with_bad_slot_flagged(path):
+    """An empty sequence whose slot is out of range sets the bit on every path
+    (no kernel may rely on visiting a sequence through its tokens)."""
+    import gated_delta_rule_gateddeltanet_gb300 as gdn
+    from gpu_common import single_kernel_workspace
+    spec = STATUS_PATHS[path]
+    d = spec["d"]
+    inp = wl.make_inputs(6600, spec["lengths"] + [0], Hk=1, Hv=2, dk=d, dv=d, io_dtype=np.float16, state_std=0.02,
+                         num_slots=4, state_slots=[0, 1, 2, 7])
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    ws = single_kernel_workspace(inp) if spec.get("single") else None
+    _, fin, _ = run_gpu(inp, plan=spec["plan"], in_place=False, status=status, workspace=ws)
+    assert status.item() == gdn.DEVERR["state_slot"]
+    assert np.array_equal(fin[3], inp.initial_state[3].astype(np.float64))
