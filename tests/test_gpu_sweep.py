@@ -332,3 +332,39 @@ def test_empty_sequence_with_bad_slot_flagged(path):
     _, fin, _ = run_gpu(inp, plan=spec["plan"], in_place=False, status=status, workspace=ws)
     assert status.item() == gdn.DEVERR["state_slot"]
     assert np.array_equal(fin[3], inp.initial_state[3].astype(np.float64))
+
+
+@pytest.mark.parametrize("path", list(STATUS_PATHS))
+def test_extreme_raw_gates_match_oracle(path):
+    """Raw gate inputs far out in both tails (a, b in {-60, -5, 0, 5, 60} with
+    A_log up to log 16): decays that underflow to exactly 0 (the state
+    restarts), decays of 1 - 1e-27, betas of 0 and 1, on every path, against
+    the oracle at the path's tolerance; nothing becomes NaN."""
+    from gpu_common import single_kernel_workspace
+    import oracle as orc
+    spec = STATUS_PATHS[path]
+    d = spec["d"]
+    inp = wl.make_inputs(6700, spec["lengths"], Hk=1, Hv=2, dk=d, dv=d, io_dtype=np.float16, state_std=0.02,
+                         capacity=8)
+    rng = np.random.default_rng(6701)
+    vals = np.array([-60.0, -5.0, 0.0, 5.0, 60.0], np.float32)
+    a = rng.choice(vals, size=inp.a.shape).astype(np.float32)
+    b = rng.choice(vals, size=inp.b.shape).astype(np.float32)
+    A_log = np.log(np.array([1.0, 16.0], np.float32)).astype(np.float32)
+    extreme = wl.GdnInputs(inp.q, inp.k, inp.v, a, b, A_log, inp.dt_bias, inp.cu_seqlens, inp.initial_state,
+                           inp.state_slots, inp.capacity)
+    ws = single_kernel_workspace(extreme) if spec.get("single") else None
+    out, fin, caps = run_gpu(extreme, plan=spec["plan"], in_place=False, workspace=ws)
+    ref = orc.gdn_forward(extreme.q, extreme.k, extreme.v, a, b, extreme.cu_seqlens, A_log=A_log,
+                          dt_bias=extreme.dt_bias, initial_state=extreme.initial_state, capacity=8)
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(fin))
+    tensor_cores = spec["plan"] not in ("recurrent", "auto")  # the auto plan here runs the decode kernel
+    assert max_rel(out, ref[0]) <= 2e-3, max_rel(out, ref[0])  # fp16 outputs: one fp16 rounding
+    tol_state = 2e-3 if tensor_cores else 1e-5
+    assert max_rel(fin, ref[1]) <= tol_state, max_rel(fin, ref[1])
+    g, kn, u = capsule_parts(caps, 1, 2, d, d)
+    gr, knr, ur = capsule_parts(ref[2], 1, 2, d, d)
+    for s_, L in enumerate(spec["lengths"]):
+        n = min(L, 8)
+        assert max_rel(g[s_, :n], gr[s_, :n]) <= 1e-5
+        assert max_rel(u[s_, :n], ur[s_, :n]) <= tol_state
