@@ -151,7 +151,8 @@ enum {
  *   status        device int32 or NULL (see above)
  *   workspace     device scratch of workspace_bytes (may be NULL when
  *                 gdn_forward_workspace_size reports 0)
- * Sequences in one call must use distinct state slots.
+ * Sequences in one call must use distinct state slots (checked by the debug
+ * build: GDN_DEVERR_DUP_SLOT).
  */
 typedef struct gdn_forward_args {
     int32_t num_seqs;              /* B >= 0 (at most 65535) */
@@ -313,7 +314,8 @@ gdn_status gdn_state_transpose(const float *src, float *dst, int64_t num_matrice
  *   status       device int32 or NULL: GDN_DEVERR_REPLAY_SLOT,
  *                GDN_DEVERR_ACCEPT_LEN (the request is skipped)
  * A destination may equal its own source (in place) but must not be any other
- * request's source or destination.
+ * request's source or destination (the debug build checks this and sets
+ * GDN_DEVERR_DUP_SLOT).
  */
 gdn_status gdn_replay_prefix(float *state_banks, int32_t num_slots, int32_t num_requests,
                              int32_t num_k_heads, int32_t num_v_heads, int32_t head_dim_k,
