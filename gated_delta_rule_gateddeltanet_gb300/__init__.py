@@ -132,12 +132,21 @@ def _check(t, name, dtype=None, device=None, contiguous=True):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _shape(t, name, shape):
-    """Raise unless ``t`` (if given) has exactly ``shape``: the C ABI takes raw
+def _shape(t, name, shape, leading_at_least=False):
+    """Raise unless ``t`` (if given) has ``shape``: the C ABI takes raw
     pointers, so the binding is where a buffer's extent is checked against the
-    call's geometry, before any launch."""
-    if t is not None and tuple(t.shape) != tuple(int(x) for x in shape):
-        raise ValueError(f"{name} must have shape {tuple(int(x) for x in shape)}, got {tuple(t.shape)}")
+    call's geometry, before any launch.  With ``leading_at_least`` the first
+    extent may be larger (a state pool or output buffer with more rows than the
+    call addresses); the inner extents must match."""
+    if t is None:
+        return
+    want = tuple(int(x) for x in shape)
+    got = tuple(t.shape)
+    ok = (len(got) == len(want) and got[1:] == want[1:] and
+          (got[0] >= want[0] if leading_at_least else got[0] == want[0]))
+    if not ok:
+        lead = "at least " if leading_at_least else ""
+        raise ValueError(f"{name} must have shape {want} ({lead}{want[0]} rows), got {got}")
 
 
 def _token_stride(t, name, inner):
@@ -202,18 +211,18 @@ def build_forward_args(q, k, v, a, b, cu_seqlens, *, A_log=None, dt_bias=None, g
             final_state.copy_(initial_state)
     _check(initial_state, "initial_state", dtype=torch.float32, device=dev)
     _check(final_state, "final_state", dtype=torch.float32, device=dev)
-    _shape(initial_state, "initial_state", (num_state_slots, Hv, dv, dk))
-    _shape(final_state, "final_state", (num_state_slots, Hv, dv, dk))
+    _shape(initial_state, "initial_state", (num_state_slots, Hv, dv, dk), leading_at_least=True)
+    _shape(final_state, "final_state", (num_state_slots, Hv, dv, dk), leading_at_least=True)
     if output is None:
         output = torch.empty((T, Hv, dv), dtype=q.dtype, device=dev)
     _check(output, "output", dtype=q.dtype, device=dev)
-    _shape(output, "output", (T, Hv, dv))
+    _shape(output, "output", (T, Hv, dv), leading_at_least=True)
     W = capsule_width(Hk, Hv, dk, dv)
     if capacity > 0 and state_update is None:
         state_update = torch.zeros((B, capacity, W), dtype=torch.float32, device=dev)
     _check(state_update, "state_update", dtype=torch.float32, device=dev)
     if capacity > 0:
-        _shape(state_update, "state_update", (B, capacity, W))
+        _shape(state_update, "state_update", (B, capacity, W), leading_at_least=True)
 
     args = ForwardArgs()
     args.num_seqs, args.total_tokens, args.num_k_heads, args.num_v_heads = B, T, Hk, Hv
@@ -391,7 +400,7 @@ def gdn_replay_prefix(state_banks, src_slots, dst_slots, state_update, accept_le
     _shape(dst_slots, "dst_slots", (R,))
     _shape(accept_len, "accept_len", (R,))
     if state_update is not None:
-        _shape(state_update, "state_update", (R, cap, capsule_width(num_k_heads, Hv, dk, dv)))
+        _shape(state_update, "state_update", (R, cap, capsule_width(num_k_heads, Hv, dk, dv)), leading_at_least=True)
     rc = lib.gdn_replay_prefix(_ptr(state_banks), S, R, int(num_k_heads), Hv, dk, dv, _ptr(src_slots),
                                _ptr(dst_slots), _ptr(state_update), cap, _ptr(accept_len), _ptr(status),
                                _stream_handle(dev))
@@ -437,11 +446,11 @@ def build_conv_args(x, weight, cu_seqlens, *, bias=None, initial_state=None, fin
         state_update = torch.zeros((B, capacity, C), dtype=x.dtype, device=dev)
     _check(output, "output", dtype=x.dtype, device=dev)
     _check(state_update, "state_update", dtype=x.dtype, device=dev)
-    _shape(initial_state, "initial_state", (num_state_slots, C, K - 1))
-    _shape(final_state, "final_state", (num_state_slots, C, K - 1))
-    _shape(output, "output", (T, C))
+    _shape(initial_state, "initial_state", (num_state_slots, C, K - 1), leading_at_least=True)
+    _shape(final_state, "final_state", (num_state_slots, C, K - 1), leading_at_least=True)
+    _shape(output, "output", (T, C), leading_at_least=True)
     if capacity > 0:
-        _shape(state_update, "state_update", (B, capacity, C))
+        _shape(state_update, "state_update", (B, capacity, C), leading_at_least=True)
     a = ConvArgs()
     a.num_seqs, a.total_tokens, a.channels, a.kernel_size = B, T, C, K
     a.num_state_slots, a.io_dtype = int(num_state_slots), DTYPE[x.dtype]
@@ -490,7 +499,7 @@ def causal_conv_replay_prefix(conv_states, src_slots, dst_slots, state_update, a
     _shape(dst_slots, "dst_slots", (R,))
     _shape(accept_len, "accept_len", (R,))
     if state_update is not None:
-        _shape(state_update, "state_update", (R, cap, C))
+        _shape(state_update, "state_update", (R, cap, C), leading_at_least=True)
     rc = lib.causal_conv_replay_prefix(_ptr(conv_states), S, src_slots.shape[0], C, Km1 + 1, DTYPE[conv_states.dtype],
                                        _ptr(src_slots), _ptr(dst_slots), _ptr(state_update), cap, _ptr(accept_len),
                                        _ptr(status), _stream_handle(dev))

@@ -32,7 +32,7 @@ def _fwd(**over):
     ("dt_bias", torch.zeros(Hv - 1)),
     ("state_slots", torch.tensor([0], dtype=torch.int32)),
     ("initial_state", torch.zeros(S, Hv, d, d + 32)),
-    ("final_state", torch.zeros(S + 1, Hv, d, d)),
+    ("final_state", torch.zeros(S - 1, Hv, d, d)),
     ("output", torch.zeros(T - 1, Hv, d, dtype=torch.float16)),
     ("state_update", torch.zeros(B, 3, gdn.capsule_width(Hk, Hv, d, d))),
 ])
@@ -40,6 +40,16 @@ def test_forward_rejects_wrong_shapes(name, bad):
     _fwd()  # the consistent call resolves
     with pytest.raises(ValueError, match=name):
         _fwd(**{name: bad})
+
+
+def test_forward_accepts_larger_pools_and_buffers():
+    """A state pool with more slots than the call addresses (e.g. both banks of
+    a speculative step) and an output or capsule buffer with spare rows are
+    valid: only their leading extent may exceed the call's."""
+    W = gdn.capsule_width(Hk, Hv, d, d)
+    _fwd(initial_state=torch.zeros(2 * S, Hv, d, d), final_state=torch.zeros(S + 1, Hv, d, d),
+         output=torch.zeros(T + 2, Hv, d, dtype=torch.float16), state_update=torch.zeros(B + 1, 2, W),
+         num_state_slots=S)
 
 
 def test_forward_rejects_two_dimensional_cu_seqlens():
@@ -70,8 +80,8 @@ def _conv(**over):
     ("capture_count", torch.tensor([1], dtype=torch.int32)),
     ("initial_state", torch.zeros(S, C, K, dtype=torch.float16)),
     ("final_state", torch.zeros(S, C + 8, K - 1, dtype=torch.float16)),
-    ("output", torch.zeros(T + 1, C, dtype=torch.float16)),
-    ("state_update", torch.zeros(B + 1, 2, C, dtype=torch.float16)),
+    ("output", torch.zeros(T - 1, C, dtype=torch.float16)),
+    ("state_update", torch.zeros(B - 1, 2, C, dtype=torch.float16)),
 ])
 def test_conv_rejects_wrong_shapes(name, bad):
     _conv()
