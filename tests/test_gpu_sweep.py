@@ -368,3 +368,59 @@ def test_extreme_raw_gates_match_oracle(path):
         n = min(L, 8)
         assert max_rel(g[s_, :n], gr[s_, :n]) <= 1e-5
         assert max_rel(u[s_, :n], ur[s_, :n]) <= tol_state
+
+
+# ---------------------------------------------------------------- dense rank-4 inputs and the split plan
+
+@pytest.mark.parametrize("i", range(8))
+def test_random_dense_equals_packed_and_oracle(i):
+    """gdn_forward_dense on random batch and sequence sizes, head sizes and
+    plans: bit for bit the packed call on the same tokens, and the oracle at
+    the plan's tolerance."""
+    from test_gpu_dense import _run_both
+    rng = np.random.default_rng(9000 + i)
+    dk = int(rng.choice([32, 64, 128]))
+    dv = dk if rng.random() < 0.7 else int(rng.choice([32, 64, 128]))
+    B = int(rng.integers(1, 5))
+    S = int(rng.choice([1, 3, 17, 70, 130]))
+    plan = str(rng.choice(["auto", "recurrent", "chunked"]))
+    io = np.float16 if rng.random() < 0.6 else np.float32
+    Hk = int(rng.choice([1, 2]))
+    inp = wl.make_inputs(9100 + i, [S] * B, Hk=Hk, Hv=Hk * int(rng.choice([1, 3])), dk=dk, dv=dv, io_dtype=io,
+                         state_std=0.02 if rng.random() < 0.8 else None)
+    od, fd, op, fp = _run_both(inp, B, S, plan)
+    assert np.array_equal(od, op) and np.array_equal(fd, fp)
+    o_ref, f_ref, _ = oracle.gdn_forward(inp.q, inp.k, inp.v, inp.a, inp.b, inp.cu_seqlens, A_log=inp.A_log,
+                                         dt_bias=inp.dt_bias, initial_state=inp.initial_state,
+                                         num_state_slots=B)
+    limit = 32 if dk == dv == 128 else 256
+    tc = plan == "chunked" or (plan == "auto" and S > limit)
+    assert max_rel(od, o_ref) <= (2e-3 if (tc or io == np.float16) else 1e-5)
+    assert max_rel(fd, f_ref) <= (2e-3 if tc else 1e-5)
+
+
+@pytest.mark.parametrize("i", range(4))
+def test_random_split_plan_matches_oracle(i):
+    """The sequence-parallel split plan on random batches: one or two
+    sequences around and past the split threshold (1984 tokens) among short
+    ones, fp16 or FP32, a capture capacity that allows the split or forbids it
+    (captured tokens past the first half), at 2e-3 against the oracle."""
+    rng = np.random.default_rng(9500 + i)
+    longs = [int(rng.integers(1900, 2700)) for _ in range(int(rng.integers(1, 3)))]
+    shorts = [int(rng.integers(0, 200)) for _ in range(int(rng.integers(0, 3)))]
+    lengths = list(rng.permutation(longs + shorts))
+    io = np.float16 if rng.random() < 0.5 else np.float32
+    cap = int(rng.choice([0, 4, 1500]))
+    inp = wl.make_inputs(9600 + i, lengths, Hk=1, Hv=2, dk=128, dv=128, io_dtype=io, state_std=0.02, capacity=cap)
+    out, fin, caps = run_gpu(inp, plan="chunked_split", in_place=bool(i % 2))
+    o_ref, f_ref, c_ref = oracle.gdn_forward(inp.q, inp.k, inp.v, inp.a, inp.b, inp.cu_seqlens, A_log=inp.A_log,
+                                             dt_bias=inp.dt_bias, initial_state=inp.initial_state, capacity=cap)
+    assert max_rel(out, o_ref) <= 2e-3, max_rel(out, o_ref)
+    assert max_rel(fin, f_ref) <= 2e-3, max_rel(fin, f_ref)
+    if cap:
+        _, _, u = capsule_parts(caps, 1, 2, 128, 128)
+        _, _, ur = capsule_parts(c_ref, 1, 2, 128, 128)
+        for s_, L in enumerate(lengths):
+            n = min(L, cap)
+            if n:
+                assert max_rel(u[s_, :n], ur[s_, :n]) <= 2e-3
