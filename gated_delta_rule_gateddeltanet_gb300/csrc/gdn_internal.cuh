@@ -185,8 +185,8 @@ __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2hal
 
 // ---------------------------------------------------------------- dependent launches
 //
-// The kernels of the library (all but the causal convolution's, whose
-// one-wave decode step measured slower so) are launched as programmatic
+// The kernels of the library (all but the causal convolution's token-block
+// kernels, whose one-wave decode step measured slower so) are launched as programmatic
 // dependents of the kernel before them on the stream (launch_dependent): a
 // kernel's CTAs may become
 // resident while that kernel's last CTAs finish, which hides the launch gap
