@@ -13,7 +13,10 @@
 // copies give.  Two CTAs of 8 warps per SM, each persistent over a
 // contiguous range of items (consecutive value heads of one key head reuse
 // the key-side staging); while one CTA waits for its next item's copies the
-// other computes.  For the row-local work thread (warp w, lane l) owns state
+// other computes.  CTAs with fewer items than the fullest ones start a few
+// microseconds later, so that the first copies do not all land in one burst,
+// and without a final state an item's successor is copied in as soon as its
+// last products have read the rows.  For the row-local work thread (warp w, lane l) owns state
 // row r = 32 (w % 4) + l -- the tensor-memory lane its warp can reach -- and
 // half w / 4 of the row's columns, as 16 float4 chunks at columns
 // 32 j + 16 (w / 4) + 4 m (j, m < 4).
