@@ -124,6 +124,8 @@ gdn_status resolve_forward(const gdn_forward_args *a, int dense_S, gdn::ForwardP
     p.caps = p.cap > 0 ? a->state_update : nullptr;
     p.status = a->status;
     p.max_len = 0x7fffffff;
+    p.min_len = 0;
+    p.max_len_hint = a->max_seqlen;
 
     *out = p;
     return GDN_OK;

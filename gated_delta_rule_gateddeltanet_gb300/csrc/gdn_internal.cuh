@@ -29,6 +29,11 @@ struct ForwardParams {
     int32_t *status;
     // Sequences with more tokens than this are left to the chunked kernel.
     int max_len;
+    // Sequences with fewer tokens than this are left to another kernel of the
+    // same call (0: none); see launch_recurrent.
+    int min_len;
+    // The caller's bound on the longest sequence (gdn_forward_args.max_seqlen, 0: unknown).
+    int max_len_hint;
     // Rank-4 [B, S, H, D] inputs: cu is null and sequence b owns tokens
     // [b S, (b + 1) S) with S = dense_S.  0 for packed inputs.
     int dense_S;
@@ -95,11 +100,14 @@ cudaError_t debug_check_distinct_slots(const int32_t *written, const int32_t *re
 #endif
 cudaError_t launch_conv_replay(const ConvReplayParams &p, cudaStream_t stream);
 
-// Spans of at most p.max_len tokens: the CUDA-core decode kernel when every
-// span has at most one token (T == B), else at dk = dv = 128 the tcgen05
-// short-span kernel and at other head sizes the persistent mixed kernel
-// (one-token spans on the decode kernel's arithmetic in both, longer ones four
-// tokens at a time).
+// Spans of at most p.max_len tokens: the CUDA-core decode kernel when the
+// caller bounds every span to one token (a max_seqlen hint of 1), else at
+// dk = dv = 128 the tcgen05 short-span kernel and at other head sizes the
+// persistent mixed kernel (one-token spans on the decode kernel's arithmetic
+// in both, longer ones four tokens at a time).  Without the hint, a batch with
+// as many tokens as sequences may still hold multi-token spans next to empty
+// ones: the decode kernel then takes the spans of at most one token and the
+// short-span kernel the others, so that no span's bits depend on its batch.
 cudaError_t launch_recurrent(const ForwardParams &p, cudaStream_t stream);
 // Batches with a multi-token span at dk = dv = 128: the tcgen05 short-span
 // kernel (gdn_verify.cu); one-token spans in it keep the decode kernel's bits.

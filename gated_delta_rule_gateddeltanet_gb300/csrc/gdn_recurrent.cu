@@ -131,7 +131,7 @@ __device__ __forceinline__ bool resolve_span(const ForwardParams &p, int b, int 
         if (leader) flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
         return false;
     }
-    if (sp.eos - sp.bos > p.max_len) return false;
+    if (sp.eos - sp.bos > p.max_len || sp.eos - sp.bos < p.min_len) return false;  // another kernel's
     const int slot = p.slots ? p.slots[sp.b] : sp.b;
     if (slot < 0 || slot >= p.num_slots) {
         if (leader) flag_error(p.status, GDN_DEVERR_STATE_SLOT);
@@ -828,17 +828,35 @@ __global__ void __launch_bounds__(NTM, 4)
 }
 
 template <typename TIO, int DK>
+cudaError_t launch_mixed(const ForwardParams &p, cudaStream_t stream);
+
+template <typename TIO, int DK>
 cudaError_t launch_dk(const ForwardParams &p, cudaStream_t stream) {
     const int nrb = (p.dv + ROWS - 1) / ROWS;
-    if (p.T == p.B) {  // every span has at most one token: the decode kernel
+    const bool promised = p.max_len_hint == 1;  // the caller bounds every span to one token
+    if (promised || p.T == p.B) {
+        // the decode kernel; without the promise only for spans of at most one token
+        // (T == B allows multi-token spans next to empty ones), the rest below
+        ForwardParams pd = p;
+        if (!promised) pd.max_len = std::min(p.max_len, 1);
         const int smem = ROWS * DK * 4;
         auto kern = recurrent_kernel<TIO, DK>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        return launch_dependent(kern, dim3((unsigned)(nrb * p.Hv), (unsigned)p.B), dim3(NT), smem, stream, p);
+        if (e == cudaSuccess)
+            e = launch_dependent(kern, dim3((unsigned)(nrb * p.Hv), (unsigned)p.B), dim3(NT), smem, stream, pd);
+        if (e != cudaSuccess || promised || p.max_len < 2) return e;
+        ForwardParams pm = p;
+        pm.min_len = 2;
+        return verify_kernel_supported(pm) ? launch_verify(pm, stream) : launch_mixed<TIO, DK>(pm, stream);
     }
     if (verify_kernel_supported(p)) return launch_verify(p, stream);
-    // some span has several tokens: the persistent mixed kernel, as many CTAs as fit at once
+    return launch_mixed<TIO, DK>(p, stream);
+}
+
+// Some span has several tokens: the persistent mixed kernel, as many CTAs as fit at once.
+template <typename TIO, int DK>
+cudaError_t launch_mixed(const ForwardParams &p, cudaStream_t stream) {
+    const int nrb = (p.dv + ROWS - 1) / ROWS;
     const int smem = ROWS * DK * 4 + 1024;
     CUtensorMap rows_map;
     memset(&rows_map, 0, sizeof(rows_map));

@@ -151,7 +151,7 @@ __device__ __forceinline__ VItem make_item(const ForwardParams &p, const VCursor
         if (leader) flag_error(p.status, GDN_DEVERR_CU_SEQLENS);
         return it;
     }
-    if (it.eos - it.bos > p.max_len) return it;
+    if (it.eos - it.bos > p.max_len || it.eos - it.bos < p.min_len) return it;  // another kernel's
     if (r.slot < 0 || r.slot >= p.num_slots) {
         if (leader) flag_error(p.status, GDN_DEVERR_STATE_SLOT);
         return it;

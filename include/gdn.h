@@ -170,8 +170,9 @@ typedef struct gdn_forward_args {
     int32_t max_seqlen;            /* upper bound on the longest sequence, 0 = unknown (T).
                                       A performance hint: under GDN_PLAN_AUTO a bound of
                                       at most 32 keeps every sequence on the recurrent
-                                      kernel and skips the chunked launches.  Results do
-                                      not depend on it. */
+                                      kernel and skips the chunked launches, and a bound
+                                      of 1 (decode) runs the decode kernel alone.  Results
+                                      do not depend on it as long as it is a true bound. */
     int64_t q_stride;
     int64_t k_stride;
     int64_t v_stride;

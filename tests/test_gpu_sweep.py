@@ -424,3 +424,27 @@ def test_random_split_plan_matches_oracle(i):
             n = min(L, cap)
             if n:
                 assert max_rel(u[s_, :n], ur[s_, :n]) <= 2e-3
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_as_many_tokens_as_sequences_with_multi_token_spans(d):
+    """T == B does not mean one token per span: with empty sequences beside
+    multi-token ones, every span must still get the bits it gets alone (the
+    decode kernel takes the spans of at most one token, the short-span kernel
+    the others), and the results match the oracle."""
+    lengths = [2, 0, 3, 0, 1, 0]  # T = 6 = B
+    inp = wl.make_inputs(6800 + d, lengths, Hk=1, Hv=2, dk=d, dv=d, io_dtype=np.float16, state_std=0.02,
+                         capacity=4)
+    out, fin, caps = run_gpu(inp, in_place=False)
+    o_ref, f_ref, _ = oracle.gdn_forward(inp.q, inp.k, inp.v, inp.a, inp.b, inp.cu_seqlens, A_log=inp.A_log,
+                                         dt_bias=inp.dt_bias, initial_state=inp.initial_state, capacity=4)
+    assert max_rel(out, o_ref) <= 2e-3 and max_rel(fin, f_ref) <= 1e-5
+    cu = inp.cu_seqlens
+    for s_, L in enumerate(lengths):
+        one = wl.GdnInputs(inp.q[cu[s_]:cu[s_ + 1]], inp.k[cu[s_]:cu[s_ + 1]], inp.v[cu[s_]:cu[s_ + 1]],
+                           inp.a[cu[s_]:cu[s_ + 1]], inp.b[cu[s_]:cu[s_ + 1]], inp.A_log, inp.dt_bias,
+                           np.array([0, L], np.int32), inp.initial_state[s_:s_ + 1], None, 4)
+        o1, f1, c1 = run_gpu(one, in_place=False)
+        assert np.array_equal(out[cu[s_]:cu[s_ + 1]], o1), s_
+        assert np.array_equal(fin[s_], f1[0]), s_
+        assert np.array_equal(caps[s_, :min(L, 4)], c1[0, :min(L, 4)]), s_
