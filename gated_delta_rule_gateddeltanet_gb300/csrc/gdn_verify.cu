@@ -358,8 +358,10 @@ __global__ void __launch_bounds__(NTV, 2)
     // copies about 3 us later: the fullest CTAs then have the memory system to
     // themselves while their first rows arrive, instead of every CTA's first copy
     // landing in one burst (16 x 4 verify: 27.5 vs 29.3 us, 18.4 vs 19.9 writing no
-    // final state).  Costs nothing when every CTA has the same number of items.
-    if (stop - first < (int)(((long long)items + gridDim.x - 1) / gridDim.x)) __nanosleep(3000);
+    // final state).  Costs nothing when every CTA has the same number of items, and
+    // a CTA whose first item has no work (another kernel's span, or a bad one) does
+    // not wait.
+    if (it.ok && stop - first < (int)(((long long)items + gridDim.x - 1) / gridDim.x)) __nanosleep(3000);
     issue_load(it);
     GateIn gc = load_gates(p, it);  // this item's first-group gate inputs
 
