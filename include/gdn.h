@@ -77,12 +77,13 @@ enum {
                                 is below 128), longer ones chunked (the chunked kernels
                                 need 16-byte aligned q, k, v and the workspace; head
                                 sizes below 128 run them on zero-padded d = 128 tiles) */
-    GDN_PLAN_RECURRENT = 1,  /* every sequence on the recurrent kernels: the state carried
-                                token by token (batches of one-token spans), or four
-                                tokens at a time in closed form on the tensor cores
-                                (batches with longer spans: tcgen05 at dk = dv = 128, warp
-                                tensor cores at smaller heads; one-token spans in them
-                                still take the token-by-token arithmetic, same bits) */
+    GDN_PLAN_RECURRENT = 1,  /* every sequence on the recurrent kernels: a one-token span
+                                carries the state token by token, a longer span goes
+                                four tokens at a time in closed form on the tensor cores
+                                (tcgen05 at dk = dv = 128, warp tensor cores at smaller
+                                heads), whatever else the batch holds, so a span gets
+                                the same bits in any batch (a max_seqlen hint of 1
+                                promises one-token spans: only the decode kernel runs) */
     GDN_PLAN_CHUNKED = 2,    /* every sequence on the tensor-core chunked kernels (head
                                 sizes 32, 64, 128 in any combination; below 128 the
                                 d = 128 operand tiles are zero-padded) */
